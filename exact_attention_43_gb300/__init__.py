@@ -1,0 +1,21 @@
+"""Fused exact attention for one NVIDIA GB300 (sm_103a).
+
+``attn_fwd`` (prefill, causal or not, grouped-query heads, per-row LSE) and
+``attn_decode`` (flash-decoding: split-KV chunk partials merged by an
+LSE-rescaling reduce) run in hand-written CUDA kernels behind the C ABI of
+``include/attn.h``; this package is the thin PyTorch-facing binding.
+"""
+
+from .binding import (  # noqa: F401
+    AttnError,
+    ExtensionMissing,
+    attn_decode,
+    attn_fwd,
+    check_device_status,
+    debug_set,
+    decode_chunk,
+    decode_workspace_bytes,
+    load,
+    status_string,
+    version,
+)

@@ -1,0 +1,166 @@
+"""ctypes binding to the C ABI in include/attn.h: argument marshalling only.
+
+Every step of the attention path runs in the CUDA library; this module only
+turns PyTorch tensors into pointers and sizes, passes the current CUDA stream
+and raises on a non-zero status.  There is no fallback: if the library is not
+built, every call raises ``ExtensionMissing``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libexact_attention.so")
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_CUDA = 3
+ATTN_ERR_DEVICE_TIMEOUT = 4
+ATTN_BF16 = 0
+ATTN_FP16 = 1
+
+EXPORTS = ("attn_fwd", "attn_decode", "attn_decode_workspace_bytes", "attn_decode_chunk",
+           "attn_check_device_status", "attn_debug_set", "attn_status_string", "attn_version")
+
+
+class ExtensionMissing(RuntimeError):
+    pass
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{msg} (status {status})")
+        self.status = status
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the shared library and declare the C signatures (no CUDA call is made)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ExtensionMissing(
+            f"{path} is not built; run `python -m exact_attention_43_gb300.build` "
+            "(or __graft_entry__.build())")
+    lib = ctypes.CDLL(path)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
+    lib.attn_fwd.restype = i
+    lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
+    lib.attn_decode.restype = i
+    lib.attn_decode_workspace_bytes.argtypes = [i, i, i, i, i]
+    lib.attn_decode_workspace_bytes.restype = sz
+    lib.attn_decode_chunk.argtypes = [i, i]
+    lib.attn_decode_chunk.restype = i
+    lib.attn_check_device_status.argtypes = [vp]
+    lib.attn_check_device_status.restype = i
+    lib.attn_debug_set.argtypes = [i, ctypes.c_uint]
+    lib.attn_debug_set.restype = i
+    lib.attn_status_string.argtypes = [i]
+    lib.attn_status_string.restype = ctypes.c_char_p
+    lib.attn_version.argtypes = []
+    lib.attn_version.restype = i
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().attn_status_string(status).decode()
+
+
+def _check(status: int, what: str):
+    if status != ATTN_OK:
+        raise AttnError(status, f"{what}: {status_string(status)}")
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return ATTN_BF16
+    if t.dtype == torch.float16:
+        return ATTN_FP16
+    raise TypeError(f"unsupported dtype {t.dtype}: bf16 or fp16")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def attn_fwd(q, k, v, *, causal: bool, scale: float | None = None, out=None, lse=None,
+             return_lse: bool = True, stream=None):
+    """Prefill attention: q [B,Hq,Sq,D], k/v [B,Hkv,Skv,D] (contiguous CUDA tensors).
+
+    Returns (O, LSE) with O like q and LSE [B,Hq,Sq] float32 (None when
+    return_lse is False and no lse buffer was given).
+    """
+    lib = load()
+    B, Hq, Sq, D = q.shape
+    Hkv, Skv = k.shape[1], k.shape[2]
+    for t in (q, k, v):
+        if not t.is_contiguous():
+            raise ValueError("q, k and v must be contiguous")
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != D:
+        raise ValueError("k and v must be [B, Hkv, Skv, D] matching q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    st = lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Skv, D,
+                      1 if causal else 0, float(scale), _dtype_code(q), _stream(stream))
+    _check(st, "attn_fwd")
+    return out, lse
+
+
+def attn_decode(q, k_cache, v_cache, seq_lens, *, num_splits: int = 0, out=None, stream=None):
+    """Flash-decoding: q [B,Hq,D], caches [B,Hkv,max_S,D], seq_lens [B] int32 (all CUDA)."""
+    lib = load()
+    B, Hq, D = q.shape
+    Hkv, max_S = k_cache.shape[1], k_cache.shape[2]
+    for t in (q, k_cache, v_cache, seq_lens):
+        if not t.is_contiguous():
+            raise ValueError("decode inputs must be contiguous")
+    if seq_lens.dtype != torch.int32:
+        raise TypeError("seq_lens must be int32")
+    if out is None:
+        out = torch.empty_like(q)
+    st = lib.attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), _ptr(out), B, Hq,
+                         Hkv, max_S, D, num_splits, _dtype_code(q), _stream(stream))
+    _check(st, "attn_decode")
+    return out
+
+
+def decode_chunk(max_S: int, num_splits: int) -> int:
+    return load().attn_decode_chunk(max_S, num_splits)
+
+
+def decode_workspace_bytes(B, Hq, max_S, D, num_splits) -> int:
+    return load().attn_decode_workspace_bytes(B, Hq, max_S, D, num_splits)
+
+
+def check_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the library's device status."""
+    return load().attn_check_device_status(_stream(stream))
+
+
+def debug_set(fault: int, wait_limit_us: int = 0) -> int:
+    return load().attn_debug_set(fault, wait_limit_us)
+
+
+def version() -> int:
+    return load().attn_version()

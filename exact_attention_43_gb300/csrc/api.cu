@@ -1,0 +1,238 @@
+// C-ABI entry points: argument validation, device checks, the decode
+// workspace pool and the device status words.  Declared in include/attn.h.
+#include "../../include/attn.h"
+#include "internal.h"
+
+#include <math.h>
+#include <mutex>
+
+namespace {
+
+constexpr int kVersion = 100;
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s
+constexpr int kDefaultChunk = 512;
+constexpr int kMaxDevices = 64;
+
+uint64_t g_wait_limit_ns = kDefaultWaitNs;
+int g_fault = 0;
+
+std::mutex g_mu;
+int g_arch_ok[kMaxDevices];              // 0 unknown, 1 sm_103, -1 other
+cudaMemPool_t g_pool[kMaxDevices];
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_device(int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_arch_ok[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_CUDA;
+    }
+    g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  if (dev_out) *dev_out = dev;
+  return g_arch_ok[dev] == 1 ? ATTN_OK : ATTN_ERR_UNSUPPORTED;
+}
+
+// Library-owned stream-ordered pool for the decode partials; it keeps up to
+// 1 GiB cached between calls so repeated decodes do not remap memory.
+int pool_for(int dev, cudaMemPool_t* out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_pool[dev]) {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool;
+    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_CUDA;
+    }
+    uint64_t keep = 1ull << 30;
+    cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    g_pool[dev] = pool;
+  }
+  *out = g_pool[dev];
+  return ATTN_OK;
+}
+
+int chunk_for(int max_S, int num_splits) {
+  if (max_S < 0 || num_splits < 0) return 0;
+  if (num_splits == 0) return kDefaultChunk;
+  int c = (max_S + num_splits - 1) / num_splits;
+  return c < 1 ? 1 : c;
+}
+
+int from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return ATTN_OK;
+  cudaGetLastError();
+  return ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+namespace ea {
+
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+}  // namespace ea
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+             int Hkv, int Sq, int Skv, int D, int causal, float scale, int dtype,
+             cudaStream_t stream) {
+  if (B < 0 || Hq < 0 || Hkv < 0 || Sq < 0 || Skv < 0) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if ((long long)B * Hq * Sq == 0) return ATTN_OK;  // nothing to compute
+  if (Hkv == 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (B > 65535 || Hq > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (!q || !o || (Skv > 0 && (!k || !v))) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(o, 16) || (k && !aligned(k, 16)) || (v && !aligned(v, 16)) ||
+      (lse && !aligned(lse, 4)))
+    return ATTN_ERR_INVALID_ARG;
+  int dev = 0;
+  int st = check_device(&dev);
+  if (st != ATTN_OK) return st;
+
+  ea::FwdArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Sq = Sq;
+  a.Skv = Skv;
+  a.D = D;
+  a.causal = causal != 0;
+  a.scale = scale;
+  a.bf16 = dtype == ATTN_BF16;
+  a.wait_limit_ns = g_wait_limit_ns;
+  a.debug_fault = g_fault;
+  if (Skv == 0) return from_cuda(ea::launch_fwd_empty_keys(a, stream));
+  cudaError_t e = ea::launch_fwd(a, stream);
+  if (e == cudaErrorInvalidValue && !ea::encode_tiled_fn()) return ATTN_ERR_UNSUPPORTED;
+  return from_cuda(e);
+}
+
+int attn_decode_chunk(int max_S, int num_splits) { return chunk_for(max_S, num_splits); }
+
+size_t attn_decode_workspace_bytes(int B, int Hq, int max_S, int D, int num_splits) {
+  if (B < 0 || Hq < 0 || max_S < 0 || D <= 0 || num_splits < 0) return 0;
+  const int chunk = chunk_for(max_S, num_splits);
+  const size_t max_chunks = chunk > 0 ? ((size_t)max_S + chunk - 1) / chunk : 0;
+  return (size_t)B * Hq * max_chunks * (D + 2) * sizeof(float);
+}
+
+int attn_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* seq_lens,
+                void* o, int B, int Hq, int Hkv, int max_S, int D, int num_splits, int dtype,
+                cudaStream_t stream) {
+  if (B < 0 || Hq < 0 || Hkv < 0 || max_S < 0 || num_splits < 0) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if ((long long)B * Hq == 0) return ATTN_OK;
+  if (Hkv == 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (B > 65535 || Hkv > 65535 || Hq > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (!q || !o || !seq_lens || (max_S > 0 && (!k_cache || !v_cache))) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(o, 16) || !aligned(seq_lens, 4) ||
+      (k_cache && !aligned(k_cache, 16)) || (v_cache && !aligned(v_cache, 16)))
+    return ATTN_ERR_INVALID_ARG;
+  int dev = 0;
+  int st = check_device(&dev);
+  if (st != ATTN_OK) return st;
+
+  ea::DecodeArgs a{};
+  a.q = q;
+  a.k = k_cache;
+  a.v = v_cache;
+  a.seq_lens = seq_lens;
+  a.o = o;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.max_S = max_S;
+  a.D = D;
+  a.chunk = chunk_for(max_S, num_splits);
+  a.max_chunks = max_S > 0 ? (max_S + a.chunk - 1) / a.chunk : 0;
+  a.scale = 1.0f / sqrtf((float)D);
+  a.bf16 = dtype == ATTN_BF16;
+  a.wait_limit_ns = g_wait_limit_ns;
+
+  const size_t bytes = attn_decode_workspace_bytes(B, Hq, max_S, D, num_splits);
+  void* ws = nullptr;
+  if (bytes > 0) {
+    cudaMemPool_t pool;
+    if ((st = pool_for(dev, &pool)) != ATTN_OK) return st;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, bytes, pool, stream);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  a.partials = static_cast<float*>(ws);
+  cudaError_t e = ea::launch_decode(a, stream);
+  if (ws) {
+    cudaError_t f = cudaFreeAsync(ws, stream);
+    if (e == cudaSuccess) e = f;
+  }
+  return from_cuda(e);
+}
+
+int attn_check_device_status(cudaStream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return from_cuda(e);
+  unsigned f = 0, d = 0;
+  if ((e = ea::read_fwd_status(&f, stream)) != cudaSuccess) return from_cuda(e);
+  if ((e = ea::read_decode_status(&d, stream)) != cudaSuccess) return from_cuda(e);
+  const unsigned all = f | d;
+  if (all & 1u) return ATTN_ERR_DEVICE_TIMEOUT;
+  if (all & 2u) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+int attn_debug_set(int fault, unsigned wait_limit_us) {
+  if (fault < 0 || fault > 1) return ATTN_ERR_INVALID_ARG;
+  g_fault = fault;
+  g_wait_limit_ns = wait_limit_us ? (uint64_t)wait_limit_us * 1000ull : kDefaultWaitNs;
+  return ATTN_OK;
+}
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration or device";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int attn_version(void) { return kVersion; }
+
+}  // extern "C"

@@ -1,0 +1,56 @@
+// Host-side interface between the C-ABI layer (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ea {
+
+// Arguments of one prefill launch, already validated by the C-ABI layer.
+struct FwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  int B, Hq, Hkv, Sq, Skv, D;
+  int causal;
+  float scale;
+  int bf16;
+  uint64_t wait_limit_ns;
+  int debug_fault;  // 1: the loader withholds the first V tile (bounded-wait test only)
+};
+
+struct DecodeArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const int32_t* seq_lens;
+  void* o;
+  float* partials;  // [B, Hq, max_chunks, D + 2] fp32 workspace
+  int B, Hq, Hkv, max_S, D, chunk, max_chunks;
+  float scale;
+  int bf16;
+  uint64_t wait_limit_ns;
+};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// Returns the driver's cuTensorMapEncodeTiled, or nullptr.
+EncodeTiledFn encode_tiled_fn();
+
+// Each returns a CUDA error (cudaSuccess on a clean launch) or, for a failed
+// tensor-map encoding, cudaErrorInvalidValue.
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_fwd_empty_keys(const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+// Read and clear the device status word of each kernel file.
+cudaError_t read_fwd_status(unsigned* out, cudaStream_t stream);
+cudaError_t read_decode_status(unsigned* out, cudaStream_t stream);
+
+}  // namespace ea

@@ -1,0 +1,132 @@
+/*
+ * exact_attention_43_gb300 -- fused exact attention for one NVIDIA GB300 (sm_103a).
+ *
+ * C ABI: plain pointers and sizes, no C++ or framework types.  Every entry
+ * point returns an attn_status_t code, never aborts and never traps on the
+ * device.  Work is enqueued asynchronously on the caller's CUDA stream; the
+ * library keeps no pointer after a call returns and the caller owns every
+ * buffer.  All tensors are dense, row-major, with the head dimension
+ * innermost.
+ *
+ * Sources of what is computed (page title and the part of the page):
+ *   - abaddon 0.2.0-rc.2, src/cuda_inference/kernels/attention.rs: module doc
+ *     "Algorithm" (tiled exact attention, online softmax, final divide by the
+ *     sum), kernels flash_attention_f16 (layouts [batch, heads, seq, head_dim]
+ *     and [batch, kv_heads, seq, head_dim], GQA kv_head = head * kv_heads /
+ *     heads, causal masking) and flash_attention_cached_f16 /
+ *     FlashAttentionKernel::forward_cached (single-query decode against a
+ *     cache [batch, kv_heads, cache_len, head_dim], scale 1/sqrt(head_dim)),
+ *     and the Shape / Kernel error returns of FlashAttentionKernel::forward;
+ *   - rustytorch flash_attention_forward.cu: kernel flash_attention_forward_kernel
+ *     (arguments q, k, v, o, lse, softmax_scale, causal; LSE laid out
+ *     [batch * heads, seq_len]) and OnlineSoftmaxState::get_log_sum_exp
+ *     (LSE = m + log l, natural log);
+ *   - aprender-gpu 0.32.0, kernels/attention/paged/flash_decoding/reduce_kernel.rs:
+ *     FlashDecodingReduceKernel (per-sequence seq_lens, chunk partials
+ *     [M, num_heads, max_chunks, head_dim + 2], LSE-rescaling merge).
+ */
+#ifndef EXACT_ATTENTION_43_GB300_ATTN_H
+#define EXACT_ATTENTION_43_GB300_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* cudaStream_t;
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,    /* null or misaligned pointer, negative size, Hq % Hkv != 0, ... */
+  ATTN_ERR_UNSUPPORTED = 2,    /* head dim not 64/128, unknown dtype, device is not sm_103 */
+  ATTN_ERR_CUDA = 3,           /* a CUDA call or kernel launch failed */
+  ATTN_ERR_DEVICE_TIMEOUT = 4  /* a kernel's bounded wait ran out (read by attn_check_device_status) */
+} attn_status_t;
+
+typedef enum { ATTN_BF16 = 0, ATTN_FP16 = 1 } attn_dtype_t;
+
+/*
+ * attn_fwd -- prefill attention with per-row log-sum-exp.
+ *
+ *   O[b,h,i,:] = sum_j softmax_j(scale * Q[b,h,i,:] . K[b,g,j,:] + mask) V[b,g,j,:],
+ *   LSE[b,h,i] = ln sum_j exp(scale * Q[b,h,i,:] . K[b,g,j,:] + mask),
+ *   g = h / (Hq / Hkv)  (consecutive query heads share a KV head).
+ *
+ * q, o   device, [B, Hq, Sq, D], dtype `dtype`, 16-byte aligned.
+ * k, v   device, [B, Hkv, Skv, D], dtype `dtype`, 16-byte aligned.
+ * lse    device, [B, Hq, Sq] float32, 4-byte aligned, or NULL to skip it.
+ * causal 0: every key visible.  1: key j visible to query i iff
+ *        j <= i + (Skv - Sq) (aligned bottom-right; j <= i when Sq == Skv).
+ *        A row that sees no key gets O = 0 and LSE = -inf.
+ * scale  any finite float (the softmax temperature, typically 1/sqrt(D)).
+ * D      64 or 128.  dtype: ATTN_BF16 or ATTN_FP16 (O has the dtype of q).
+ * Sizes  B, Hq, Hkv >= 1 unless B*Hq*Sq == 0 (then nothing is done);
+ *        Sq, Skv >= 0; Hq % Hkv == 0; B, Hq <= 65535.
+ * Returns ATTN_OK once the work is enqueued on `stream`; validation errors
+ * are returned before any CUDA call.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+             int Hkv, int Sq, int Skv, int D, int causal, float scale, int dtype,
+             cudaStream_t stream);
+
+/*
+ * attn_decode -- flash-decoding: one query token per sequence against a KV cache.
+ *
+ *   O[b,h,:] = softmax_j(Q[b,h,:] . K[b,g,j,:] / sqrt(D)) V[b,g,j,:],  0 <= j < seq_lens[b].
+ *
+ * The keys of every sequence are split into chunks of
+ * chunk = ceil(max_S / num_splits) positions (512 when num_splits == 0); a
+ * split kernel writes per-chunk partials (o, m, l) to a stream-ordered fp32
+ * workspace of attn_decode_workspace_bytes(...) bytes and a reduce kernel
+ * merges them by LSE rescaling.
+ *
+ * q, o      device, [B, Hq, D], dtype `dtype`, 16-byte aligned.
+ * k_cache,  device, [B, Hkv, max_S, D], dtype `dtype`, 16-byte aligned;
+ * v_cache   only positions [0, seq_lens[b]) are read.
+ * seq_lens  device, [B] int32, 0 <= seq_lens[b] <= max_S.  A value outside
+ *           that range is clamped on the device and reported by
+ *           attn_check_device_status as ATTN_ERR_INVALID_ARG.  A sequence
+ *           of length 0 gets O = 0.
+ * D 64 or 128; Hq % Hkv == 0; num_splits >= 0; B, Hkv <= 65535.
+ * The workspace is taken from a library-owned CUDA memory pool with
+ * cudaMallocFromPoolAsync / cudaFreeAsync on `stream`.
+ */
+int attn_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* seq_lens,
+                void* o, int B, int Hq, int Hkv, int max_S, int D, int num_splits, int dtype,
+                cudaStream_t stream);
+
+/* Bytes of fp32 partials attn_decode allocates for these sizes
+ * (B * Hq * ceil(max_S / chunk) * (D + 2) * 4); 0 on invalid sizes. */
+size_t attn_decode_workspace_bytes(int B, int Hq, int max_S, int D, int num_splits);
+
+/* Chunk length attn_decode uses for (max_S, num_splits); 0 on invalid sizes. */
+int attn_decode_chunk(int max_S, int num_splits);
+
+/*
+ * Synchronise `stream`, then read and clear the library's device status
+ * words.  Returns ATTN_ERR_DEVICE_TIMEOUT if any kernel gave up a bounded
+ * wait, ATTN_ERR_INVALID_ARG if a decode seq_len was clamped, ATTN_ERR_CUDA
+ * if the stream reported an error, else ATTN_OK.
+ */
+int attn_check_device_status(cudaStream_t stream);
+
+/* Test hooks for the bounded waits.  wait_limit_us sets how long any wait
+ * may run before the kernel gives up (0 restores the default of 2 s);
+ * fault = 1 makes the next attn_fwd launches withhold their first V tile so
+ * that their waits run out.  Returns ATTN_OK or ATTN_ERR_INVALID_ARG. */
+int attn_debug_set(int fault, unsigned wait_limit_us);
+
+/* Static description of a status code. */
+const char* attn_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXACT_ATTENTION_43_GB300_ATTN_H */

@@ -1,0 +1,121 @@
+"""The C ABI without a GPU: the library builds and loads, exports every symbol
+include/attn.h declares, and rejects bad arguments before any CUDA call."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_attention_43_gb300 import build, binding
+
+    build.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_north_star_entry_points():
+    names = declared_functions()
+    assert "attn_fwd" in names and "attn_decode" in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in attn.h but not exported"
+    from exact_attention_43_gb300 import binding
+    assert set(binding.EXPORTS) == set(declared_functions())
+
+
+def test_version_and_status_strings(lib):
+    assert lib.attn_version() >= 100
+    for code, text in [(0, "ok"), (1, "invalid argument"), (4, "device wait timed out")]:
+        assert lib.attn_status_string(code).decode() == text
+    assert lib.attn_status_string(99).decode() == "unknown status"
+
+
+FAKE = 0x10000  # never dereferenced: validation returns first
+
+
+def fwd(lib, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, B=1, Hq=4, Hkv=4, Sq=8, Skv=8, D=64,
+        causal=0, scale=0.125, dtype=0):
+    return lib.attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, D, causal, scale, dtype, None)
+
+
+def test_fwd_argument_errors(lib):
+    assert fwd(lib, q=None) == 1
+    assert fwd(lib, o=None) == 1
+    assert fwd(lib, k=None) == 1
+    assert fwd(lib, Hkv=3) == 1            # Hq % Hkv != 0
+    assert fwd(lib, Hkv=0) == 1
+    assert fwd(lib, B=-1) == 1
+    assert fwd(lib, Sq=-5) == 1
+    assert fwd(lib, q=FAKE + 8) == 1       # misaligned
+    assert fwd(lib, lse=FAKE + 2) == 1
+    assert fwd(lib, scale=float("nan")) == 1
+    assert fwd(lib, scale=float("inf")) == 1
+    assert fwd(lib, D=96) == 2
+    assert fwd(lib, D=256) == 2
+    assert fwd(lib, dtype=7) == 2
+    assert fwd(lib, B=70000) == 2
+
+
+def test_fwd_empty_work_is_a_no_op(lib):
+    assert fwd(lib, Sq=0) == 0
+    assert fwd(lib, B=0) == 0
+    assert fwd(lib, Hq=0, q=None, o=None) == 0
+
+
+def dec(lib, q=FAKE, k=FAKE, v=FAKE, lens=FAKE, o=FAKE, B=2, Hq=8, Hkv=2, max_S=64, D=128,
+        splits=0, dtype=0):
+    return lib.attn_decode(q, k, v, lens, o, B, Hq, Hkv, max_S, D, splits, dtype, None)
+
+
+def test_decode_argument_errors(lib):
+    assert dec(lib, lens=None) == 1
+    assert dec(lib, k=None) == 1
+    assert dec(lib, Hkv=3) == 1
+    assert dec(lib, splits=-1) == 1
+    assert dec(lib, max_S=-1) == 1
+    assert dec(lib, o=FAKE + 4) == 1
+    assert dec(lib, lens=FAKE + 2) == 1
+    assert dec(lib, D=32) == 2
+    assert dec(lib, dtype=2) == 2
+    assert dec(lib, B=0) == 0
+
+
+def test_decode_chunking_and_workspace(lib):
+    assert lib.attn_decode_chunk(32768, 64) == 512
+    assert lib.attn_decode_chunk(32768, 0) == 512
+    assert lib.attn_decode_chunk(1000, 3) == 334
+    assert lib.attn_decode_chunk(5, 64) == 1
+    assert lib.attn_decode_chunk(-1, 2) == 0
+    want = 64 * 32 * 64 * (128 + 2) * 4
+    assert lib.attn_decode_workspace_bytes(64, 32, 32768, 128, 64) == want
+    assert lib.attn_decode_workspace_bytes(2, 4, 0, 128, 8) == 0
+    assert lib.attn_decode_workspace_bytes(-2, 4, 10, 128, 8) == 0
+
+
+def test_debug_hook_validation(lib):
+    assert lib.attn_debug_set(5, 0) == 1
+    assert lib.attn_debug_set(0, 0) == 0
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    from exact_attention_43_gb300 import binding
+    with pytest.raises(binding.ExtensionMissing):
+        binding._lib, saved = None, binding._lib
+        try:
+            binding.load(str(tmp_path / "missing.so"))
+        finally:
+            binding._lib = saved
