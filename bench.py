@@ -228,8 +228,10 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=3, help="0 skips the end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clock-soak", type=float, default=1.5,
+                    help="seconds of untimed steps before the warm-up, for clock sampling")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     peaks, peaks_src = load_peaks()
@@ -273,6 +275,13 @@ def main():
     uuid = torch.cuda.get_device_properties(dev).uuid
     sampler = ClockSampler(str(uuid) if uuid else None)
     sampler.start()
+    # untimed load before the warm-up so the 100 ms clock samples see the GPU busy
+    soak_steps, t_end = 0, time.time() + args.clock_soak
+    while time.time() < t_end:
+        for _ in range(20):
+            step()
+        soak_steps += 20
+        torch.cuda.synchronize()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -308,48 +317,53 @@ def main():
         total_s = float(t)
 
     # ------------------------------------------------ end to end from pinned host buffers
-    hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
-    hdq, hdk, hdv = (x.cpu().pin_memory() for x in (dq, dk, dv))
-    hlens = lens.clone().pin_memory()
-    ho = torch.empty_like(hq).pin_memory()
-    hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
-    hdo = torch.empty_like(hdq).pin_memory()
-    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdq, hdk, hdv, hlens))
-    d2h = sum(x.numel() * x.element_size() for x in (ho, hlse, hdo))
+    e2e = None
+    if args.e2e_steps > 0:
+        hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
+        hdq, hdk, hdv = (x.cpu().pin_memory() for x in (dq, dk, dv))
+        hlens = lens.clone().pin_memory()
+        ho = torch.empty_like(hq).pin_memory()
+        hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+        hdo = torch.empty_like(hdq).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdq, hdk, hdv, hlens))
+        d2h = sum(x.numel() * x.element_size() for x in (ho, hlse, hdo))
 
-    def e2e_step():
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        dq.copy_(hdq, non_blocking=True)
-        dk.copy_(hdk, non_blocking=True)
-        dv.copy_(hdv, non_blocking=True)
-        lens_d.copy_(hlens, non_blocking=True)
-        ea.attn_fwd(q, k, v, causal=True, scale=fw.scale, out=o, lse=lse, stream=stream)
-        ea.attn_decode(dq, dk, dv, lens_d, num_splits=dw.num_splits, out=do, stream=stream)
-        ho.copy_(o, non_blocking=True)
-        hlse.copy_(lse, non_blocking=True)
-        hdo.copy_(do, non_blocking=True)
+        def e2e_step():
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            dq.copy_(hdq, non_blocking=True)
+            dk.copy_(hdk, non_blocking=True)
+            dv.copy_(hdv, non_blocking=True)
+            lens_d.copy_(hlens, non_blocking=True)
+            ea.attn_fwd(q, k, v, causal=True, scale=fw.scale, out=o, lse=lse, stream=stream)
+            ea.attn_decode(dq, dk, dv, lens_d, num_splits=dw.num_splits, out=do, stream=stream)
+            ho.copy_(o, non_blocking=True)
+            hlse.copy_(lse, non_blocking=True)
+            hdo.copy_(do, non_blocking=True)
 
-    e2e_step()
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
         e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_s = e0.elapsed_time(e1) / 1e3
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_s = e0.elapsed_time(e1) / 1e3
+        if world > 1:
+            t = torch.tensor([e2e_s], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t)
+        e2e = {"value": 100.0 * (world * roofline_time(fwd_flops, dec_bytes, peaks)
+                            * args.e2e_steps) / e2e_s, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": args.e2e_steps, "ms_per_step": 1e3 * e2e_s / args.e2e_steps}
 
     rt = roofline_time(fwd_flops, dec_bytes, peaks)
     value = 100.0 * (world * rt * args.steps) / total_s
-    e2e_value = 100.0 * (world * rt * args.e2e_steps) / e2e_s
 
     if rank == 0:
         cpu = None
@@ -392,11 +406,10 @@ def main():
                              "algorithmic_flops_per_launch": fwd_flops},
             "peaks": peaks_src,
             "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
-                    "ms_per_step": 1e3 * e2e_s / args.e2e_steps},
+            "e2e": e2e,
             "gpu_launches": 3 * args.steps,
-            "clocks": clocks,
+            "clocks": dict(clocks, window="untimed soak (%d steps) + warm-up + timed region"
+                           % soak_steps),
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -62,10 +62,12 @@ struct SplitLayout {
   static constexpr int RING_OFF = 0;
   static constexpr int SC_OFF = RING_OFF + NST * STAGE;      // scores / probabilities [SUB][G]
   static constexpr int STAT_OFF = SC_OFF + SUB * G * 4;      // m, l, alpha per head
-  static constexpr int BAR_OFF = STAT_OFF + 3 * G * 4 + 16;  // NST barriers
+  static constexpr int BAR_OFF = (STAT_OFF + 3 * G * 4 + 15) / 16 * 16;  // NST barriers
   static constexpr int ABORT_OFF = BAR_OFF + NST * 8;
   static constexpr int BYTES = ABORT_OFF + 16;
   static_assert(WARPS * G * D * 4 <= NST * STAGE, "cross-warp reduction aliases the ring");
+  static_assert(BAR_OFF % 8 == 0, "mbarriers need 8-byte alignment");
+  static_assert(STAGE % 16 == 0 && RING_OFF % 16 == 0, "bulk copies need 16-byte alignment");
 };
 
 template <int D, int G, bool BF16>

@@ -72,6 +72,9 @@ struct Layout {
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;  // [0] TMEM base, [1] abort flag
   static constexpr int BYTES = MISC_OFF + 16;
   static constexpr int ALLOC = BYTES + 1024;  // slack to align the base to 1024 bytes
+  static_assert(BAR_OFF % 8 == 0, "mbarriers need 8-byte alignment");
+  static_assert(REGION % 1024 == 0 && K_OFF % 1024 == 0 && V_OFF % 1024 == 0,
+                "128-byte-swizzled tiles need 1024-byte alignment");
 };
 
 // Wait with no abort short-cut: used only while unwinding, for copies and MMAs in flight.

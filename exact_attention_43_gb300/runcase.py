@@ -1,0 +1,80 @@
+"""Run one synthetic attention case a few times (for profiling and timing).
+
+    python -m exact_attention_43_gb300.runcase fwd --workload mha [--iters 3]
+    python -m exact_attention_43_gb300.runcase fwd --B 1 --H 8 --S 4096 --causal 1
+    python -m exact_attention_43_gb300.runcase decode [--B 8] [--iters 3]
+
+Inputs are drawn on the GPU from the seeded generators in workloads.py.
+Prints one JSON line with the mean CUDA-event time per call.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+
+import torch
+
+from . import binding as ea
+from . import workloads as wl
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("op", choices=["fwd", "decode"])
+    ap.add_argument("--workload", default=None, help="tiny | mha | gqa | long (fwd)")
+    ap.add_argument("--B", type=int, default=None)
+    ap.add_argument("--H", type=int, default=32)
+    ap.add_argument("--Hkv", type=int, default=None)
+    ap.add_argument("--S", type=int, default=2048)
+    ap.add_argument("--D", type=int, default=128)
+    ap.add_argument("--causal", type=int, default=1)
+    ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=1)
+    a = ap.parse_args()
+    dev = torch.device("cuda", 0)
+    ea.load()
+    if a.op == "fwd":
+        if a.workload:
+            w = wl.FWD_WORKLOADS[a.workload]
+        else:
+            w = wl.FwdWorkload("custom", 9, a.B or 1, a.H, a.Hkv or a.H, a.S, a.S, a.D,
+                               torch.bfloat16, bool(a.causal))
+        q, k, v = wl.workload_fwd_inputs(w, device=dev)
+
+        def call():
+            return ea.attn_fwd(q, k, v, causal=w.causal, scale=w.scale)
+
+        units, unit = w.flops(), "TFLOP/s"
+        desc = f"{w.name} B{w.B} Hq{w.Hq} Hkv{w.Hkv} S{w.Sq} D{w.D} causal={w.causal}"
+    else:
+        d = wl.DECODE
+        B = a.B or d.B
+        lens = wl.seq_lens(d.B, d.len_lo, d.len_hi, seed=wl.SEED_BASE + d.index)[:B]
+        q, k, v, lens = wl.decode_inputs(B, d.Hq, d.Hkv, d.max_S, d.D, lens, dtype=d.dtype,
+                                         seed=wl.SEED_BASE + d.index, device=dev)
+        lens_d = lens.to(dev)
+
+        def call():
+            return ea.attn_decode(q, k, v, lens_d, num_splits=d.num_splits)
+
+        units, unit = d.io_bytes(lens), "GB/s"
+        desc = f"decode B{B} Hq{d.Hq} Hkv{d.Hkv} max_S{d.max_S} D{d.D} sumL={int(lens.sum())}"
+    for _ in range(a.warmup):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(a.iters):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    st = ea.check_device_status()
+    ms = e0.elapsed_time(e1) / a.iters
+    rate = units / (ms * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9)
+    print(json.dumps({"case": desc, "ms": ms, unit: rate, "status": st}))
+    return 0 if st == 0 else 1
+
+
+if __name__ == "__main__":
+    raise SystemExit(main())
