@@ -11,7 +11,7 @@ O_MEAN_ABS = 2e-3
 LSE_ABS = 1e-3
 
 GUARD = 64  # elements of canary on each side of an output (128 bytes for 16-bit types)
-CANARY16 = 0x7E5A  # a NaN pattern in both fp16 and bf16
+CANARY16 = 0x7FDA  # a NaN pattern in both fp16 and bf16
 CANARY32 = 0x7FC0DEAD  # a float32 NaN pattern
 
 
@@ -25,13 +25,13 @@ def guarded(shape, dtype, device="cuda"):
         full = torch.full((n + 2 * GUARD,), CANARY16, dtype=torch.int16, device=device)
         view = full[GUARD:GUARD + n].view(dtype).view(shape)
     else:
-        full = torch.full((n + 2 * GUARD,), CANARY32 - (1 << 32), dtype=torch.int32, device=device)
+        full = torch.full((n + 2 * GUARD,), CANARY32, dtype=torch.int32, device=device)
         view = full[GUARD:GUARD + n].view(torch.float32).view(shape)
     return full, view
 
 
 def check_guards(full):
-    pat = CANARY16 if full.dtype == torch.int16 else CANARY32 - (1 << 32)
+    pat = CANARY16 if full.dtype == torch.int16 else CANARY32
     head = full[:GUARD]
     tail = full[-GUARD:]
     assert bool((head == pat).all()), "write before the output buffer"
