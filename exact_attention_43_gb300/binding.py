@@ -25,8 +25,10 @@ ATTN_ERR_DEVICE_TIMEOUT = 4
 ATTN_BF16 = 0
 ATTN_FP16 = 1
 
-EXPORTS = ("attn_fwd", "attn_decode", "attn_decode_workspace_bytes", "attn_decode_chunk",
-           "attn_check_device_status", "attn_debug_set", "attn_status_string", "attn_version")
+EXPORTS = ("attn_fwd", "attn_decode", "attn_decode_noalloc", "attn_decode_workspace_bytes",
+           "attn_decode_chunk", "attn_check_device_status", "attn_debug_set",
+           "attn_status_string", "attn_version")
+NOALLOC_MAX_BYTES = 16 << 20  # ATTN_DECODE_NOALLOC_MAX_BYTES in attn.h
 
 
 class ExtensionMissing(RuntimeError):
@@ -57,6 +59,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_fwd.restype = i
     lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
     lib.attn_decode.restype = i
+    lib.attn_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
+    lib.attn_decode_noalloc.restype = i
     lib.attn_decode_workspace_bytes.argtypes = [i, i, i, i, i]
     lib.attn_decode_workspace_bytes.restype = sz
     lib.attn_decode_chunk.argtypes = [i, i]
@@ -142,6 +146,30 @@ def attn_decode(q, k_cache, v_cache, seq_lens, *, num_splits: int = 0, out=None,
     st = lib.attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), _ptr(out), B, Hq,
                          Hkv, max_S, D, num_splits, _dtype_code(q), _stream(stream))
     _check(st, "attn_decode")
+    return out
+
+
+def attn_decode_noalloc(q, k_cache, v_cache, seq_lens, *, num_splits: int = 0, out=None,
+                        stream=None):
+    """attn_decode for callers that may not allocate GPU memory during the call.
+
+    Same inputs and result as ``attn_decode``; the chunk partials go to a fixed
+    16 MiB scratch array the library reserves per device instead of a
+    per-call allocation.  ``out`` must be given (the wrapper allocates nothing
+    either when it is).  Problems whose partials exceed the scratch raise
+    AttnError (ATTN_ERR_UNSUPPORTED).  Calls that may overlap on the GPU share
+    the scratch and race: order them on one stream.
+    """
+    lib = load()
+    B, Hq, D = q.shape
+    Hkv, max_S = k_cache.shape[1], k_cache.shape[2]
+    if out is None:
+        raise ValueError("attn_decode_noalloc needs a preallocated `out`")
+    if seq_lens.dtype != torch.int32:
+        raise TypeError("seq_lens must be int32")
+    st = lib.attn_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), _ptr(out),
+                                 B, Hq, Hkv, max_S, D, num_splits, _dtype_code(q), _stream(stream))
+    _check(st, "attn_decode_noalloc")
     return out
 
 

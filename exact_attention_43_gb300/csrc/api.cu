@@ -6,6 +6,9 @@
 #include <math.h>
 #include <mutex>
 
+static_assert(ATTN_DECODE_NOALLOC_MAX_BYTES == ea::kNoallocPartialsBytes,
+              "header limit and device scratch size must agree");
+
 namespace {
 
 constexpr int kVersion = 100;
@@ -201,6 +204,49 @@ int attn_decode(const void* q, const void* k_cache, const void* v_cache, const i
     if (e == cudaSuccess) e = f;
   }
   return from_cuda(e);
+}
+
+int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* seq_lens, void* o, int B, int Hq, int Hkv, int max_S, int D,
+                        int num_splits, int dtype, cudaStream_t stream) {
+  if (B < 0 || Hq < 0 || Hkv < 0 || max_S < 0 || num_splits < 0) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if ((long long)B * Hq == 0) return ATTN_OK;
+  if (Hkv == 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (B > 65535 || Hkv > 65535 || Hq > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (!q || !o || !seq_lens || (max_S > 0 && (!k_cache || !v_cache))) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(o, 16) || !aligned(seq_lens, 4) ||
+      (k_cache && !aligned(k_cache, 16)) || (v_cache && !aligned(v_cache, 16)))
+    return ATTN_ERR_INVALID_ARG;
+  // the partials must fit the fixed scratch: larger problems are refused, never allocated
+  const size_t bytes = attn_decode_workspace_bytes(B, Hq, max_S, D, num_splits);
+  if (bytes > ea::kNoallocPartialsBytes) return ATTN_ERR_UNSUPPORTED;
+  int dev = 0;
+  int st = check_device(&dev);
+  if (st != ATTN_OK) return st;
+  float* scratch = nullptr;
+  cudaError_t e = ea::noalloc_partials(dev, &scratch);
+  if (e != cudaSuccess) return from_cuda(e);
+
+  ea::DecodeArgs a{};
+  a.q = q;
+  a.k = k_cache;
+  a.v = v_cache;
+  a.seq_lens = seq_lens;
+  a.o = o;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.max_S = max_S;
+  a.D = D;
+  a.chunk = chunk_for(max_S, num_splits);
+  a.max_chunks = max_S > 0 ? (max_S + a.chunk - 1) / a.chunk : 0;
+  a.scale = 1.0f / sqrtf((float)D);
+  a.bf16 = dtype == ATTN_BF16;
+  a.wait_limit_ns = g_wait_limit_ns;
+  a.partials = scratch;
+  return from_cuda(ea::launch_decode(a, stream));
 }
 
 int attn_check_device_status(cudaStream_t stream) {

@@ -24,6 +24,8 @@
 
 #include <math.h>
 
+#include <mutex>
+
 namespace ea {
 namespace dec {
 
@@ -390,6 +392,37 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.wait_limit_ns = a.wait_limit_ns;
   if (a.D == 64) return a.bf16 ? dec::launch_d<64, true>(a, p, stream) : dec::launch_d<64, false>(a, p, stream);
   return a.bf16 ? dec::launch_d<128, true>(a, p, stream) : dec::launch_d<128, false>(a, p, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Fixed scratch for attn_decode_noalloc: the chunk partials live in this
+// file-scope device array instead of memory allocated per call.  Its size is
+// fixed at build time and every device that loads the library keeps it for the
+// life of the process.  All calls share it: two calls whose kernels overlap on
+// the GPU (different streams, no ordering between them) overwrite each other's
+// partials.  Nothing in it has to start at zero: each call's split kernel
+// writes every partial that the same call's reduce kernel reads.
+static __device__ __align__(256) float g_noalloc_partials[kNoallocPartialsBytes / sizeof(float)];
+
+namespace {
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[64];  // device address of the array, per device ordinal
+}  // namespace
+
+cudaError_t noalloc_partials(int device, float** out) {
+  if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[device]) {
+    // On the host, g_noalloc_partials names a host-side stand-in, not device
+    // memory: the kernels must be given the address the runtime reports for
+    // the current device.
+    void* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_partials);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[device] = static_cast<float*>(ptr);
+  }
+  *out = g_noalloc_ptr[device];
+  return cudaSuccess;
 }
 
 cudaError_t read_decode_status(unsigned* out, cudaStream_t stream) {

@@ -53,4 +53,10 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t read_fwd_status(unsigned* out, cudaStream_t stream);
 cudaError_t read_decode_status(unsigned* out, cudaStream_t stream);
 
+// Size of the fixed device scratch behind attn_decode_noalloc (see attn.h).
+constexpr size_t kNoallocPartialsBytes = 16u << 20;
+// Device address of that scratch on `device`, which must be the current device;
+// resolved with cudaGetSymbolAddress on the first request per device.
+cudaError_t noalloc_partials(int device, float** out);
+
 }  // namespace ea

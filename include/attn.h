@@ -98,6 +98,37 @@ int attn_decode(const void* q, const void* k_cache, const void* v_cache, const i
                 void* o, int B, int Hq, int Hkv, int max_S, int D, int num_splits, int dtype,
                 cudaStream_t stream);
 
+/*
+ * attn_decode_noalloc -- attn_decode for callers that must not allocate GPU memory.
+ *
+ * Some callers cannot allocate device memory while they run: a plugin whose
+ * host application owns the whole device memory budget, a serving loop that
+ * must not risk an allocator call that waits on the device or fails under
+ * memory pressure, or code running where the CUDA allocator is off limits.
+ * This entry point computes exactly what attn_decode computes, with the same
+ * arguments, layouts and status codes, but keeps the per-chunk partials in a
+ * fixed scratch array that the library reserves on every device that loads
+ * it, for the life of the process.  It calls no allocator.  (No counterpart
+ * on the pages: the reduce kernel there simply receives a partials pointer.)
+ *
+ * Limit: attn_decode_workspace_bytes(B, Hq, max_S, D, num_splits) must not
+ * exceed ATTN_DECODE_NOALLOC_MAX_BYTES (16 MiB, e.g. B = 8, Hq = 32,
+ * max_S = 32768, D = 128, 64 splits); larger problems return
+ * ATTN_ERR_UNSUPPORTED before any CUDA call, and nothing is launched.
+ *
+ * The first call on each device looks up the device address of the scratch
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture begins.  All calls share the one scratch array:
+ * calls whose kernels may overlap on the GPU (for instance on two streams
+ * with no ordering between them) race on it, so order them on one stream or
+ * with events.  The array keeps the last call's partials; no call depends on
+ * its earlier contents.
+ */
+#define ATTN_DECODE_NOALLOC_MAX_BYTES ((size_t)16 << 20)
+int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* seq_lens, void* o, int B, int Hq, int Hkv, int max_S, int D,
+                        int num_splits, int dtype, cudaStream_t stream);
+
 /* Bytes of fp32 partials attn_decode allocates for these sizes
  * (B * Hq * ceil(max_S / chunk) * (D + 2) * 4); 0 on invalid sizes. */
 size_t attn_decode_workspace_bytes(int B, int Hq, int max_S, int D, int num_splits);

@@ -94,6 +94,14 @@ def test_decode_argument_errors(lib):
     assert dec(lib, B=0) == 0
 
 
+def test_noalloc_decode_refuses_oversized_partials_before_any_cuda_call(lib):
+    # 64 x 32 x 64 chunks x 130 floats x 4 B = 68 MB > 16 MiB of fixed scratch
+    assert lib.attn_decode_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, 64, 32, 8, 32768, 128, 64, 0,
+                                   None) == 2
+    assert lib.attn_decode_noalloc(FAKE, FAKE, FAKE, None, FAKE, 2, 8, 2, 64, 128, 0, 0, None) == 1
+    assert lib.attn_decode_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 8, 2, 64, 128, 0, 0, None) == 0
+
+
 def test_decode_chunking_and_workspace(lib):
     assert lib.attn_decode_chunk(32768, 64) == 512
     assert lib.attn_decode_chunk(32768, 0) == 512
