@@ -7,22 +7,28 @@
 // the sum at the end; rustytorch flash_attention_forward.cu,
 // OnlineSoftmaxState: LSE = m + log(l)).  How it is computed is GB300-native:
 //
-//  * one CTA owns a 128-row Q tile of one (batch, query head); KV head =
-//    query head / (Hq / Hkv) (abaddon flash_attention_f16, GQA mapping);
-//  * warp 4 streams Q once and K/V 128-key tiles through two-stage rings with
+//  * one CTA owns two 128-row Q tiles (256 consecutive query rows) of one
+//    (batch, query head) and streams the K/V tiles of the matching KV head
+//    once for both; KV head = query head / (Hq / Hkv) (abaddon
+//    flash_attention_f16, GQA mapping);
+//  * warp 8 streams Q once and K, V 128-key tiles through a 4-stage ring with
 //    TMA (3-D tensor maps, 128-byte swizzle, mbarrier transaction counts);
-//  * warp 5 issues tcgen05.mma: S_t = Q K_t^T into one of two TMEM buffers,
-//    then O += P_t V_t with P read from TMEM and V from shared memory;
-//  * warps 0-3 own one query row per thread (TMEM lane = row): load S_t,
-//    mask, row max, exponentiate with exp2 (scale * log2 e folded into one
-//    FMA), accumulate the row sum, write P_t (16-bit) to TMEM, and rescale the
-//    O row in TMEM only when the running max grew by more than 2^8 (exact:
-//    O and l always share the same stale max);
-//  * causal: KV tiles wholly after the tile's last query row are never
-//    loaded (abaddon flash_attention_f16, causal `break`); only tiles that
-//    cross the diagonal or the end of the keys are masked element-wise.
-//    Causal alignment is bottom-right: key j is visible to row i iff
-//    j <= i + (Skv - Sq);
+//  * warp 9 issues tcgen05.mma: S_i = Q_i K_j^T into TMEM, then
+//    O_i += P_i V_j with P read from TMEM and V from shared memory; per KV
+//    tile the order is PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), so while one
+//    warpgroup exponentiates, the tensor core works for the other;
+//  * warpgroup i (warps 4i..4i+3) owns the rows of Q tile i, one row per
+//    thread (TMEM lane = row): load S, mask, row max, exponentiate with exp2
+//    (scale * log2 e folded into one FMA), accumulate the row sum, write P
+//    (16-bit) over the S columns it has consumed, and rescale the O row in
+//    TMEM only when the running max grew by more than 2^8 (exact: O and l
+//    share the same stale max).  Completion of S_i(j) implies completion of
+//    every earlier MMA, so O_i already holds P V up to tile j-1 and P_i(j-1)
+//    has been consumed: the softmax never waits on O inside the loop;
+//  * causal: KV tiles wholly after a Q tile's last row are never loaded or
+//    multiplied (abaddon flash_attention_f16, causal `break`); only tiles
+//    that cross the diagonal or the end of the keys are masked element-wise.
+//    Alignment is bottom-right: key j is visible to row i iff j <= i + (Skv - Sq);
 //  * epilogue: O / l rounded to the input dtype, LSE = ln 2 * (m + log2 l);
 //    a row with no visible key gets O = 0, LSE = -inf.
 #include "internal.h"
@@ -35,22 +41,23 @@ namespace fwd {
 
 __device__ unsigned g_status;
 
-constexpr int BM = 128;            // query rows per CTA (= TMEM lanes)
-constexpr int BN = 128;            // keys per KV tile
-constexpr int NUM_THREADS = 192;   // warps 0-3 softmax/epilogue, 4 loader, 5 MMA
-constexpr int LOADER_WARP = 4;
-constexpr int MMA_WARP = 5;
+constexpr int BM = 128;             // rows per Q tile (= TMEM lanes)
+constexpr int NQ = 2;               // Q tiles per CTA
+constexpr int BN = 128;             // keys per KV tile
+constexpr int NS = 4;               // K/V ring stages
+constexpr int NUM_THREADS = 384;    // warpgroups 0, 1: softmax; warp 8 loader, warp 9 MMA
+constexpr int LOADER_WARP = 8;
+constexpr int MMA_WARP = 9;
 constexpr float RESCALE_LOG2 = 8.0f;  // rescale O when the max grows by more than 2^8
 constexpr uint32_t TMEM_COLS = 512;
-// TMEM column map (fp32 columns): S double buffer, O accumulator, P double buffer
-constexpr uint32_t COL_S = 0;      // S_0 [0,128), S_1 [128,256)
-constexpr uint32_t COL_O = 256;    // O   [256, 256 + D)
-constexpr uint32_t COL_P = 384;    // P_0 [384,448), P_1 [448,512): 128 16-bit values packed in 64 columns
+// TMEM columns: S_i at 128 i (P_i overwrites its first 64 columns), O_i at 256 + 128 i
+constexpr uint32_t COL_S = 0;
+constexpr uint32_t COL_O = 256;
 
 struct Params {
   void* o;
   float* lse;
-  int Hq, Hkv, Sq, Skv, group, num_m_tiles, causal, neg, zero;
+  int Hq, Hkv, Sq, Skv, group, num_m_blocks, causal, neg, zero;
   float c2;  // scale * log2(e); 1 when scale == 0 (then every visible score is set to 0)
   uint64_t wait_limit_ns;
   int debug_fault;
@@ -58,23 +65,23 @@ struct Params {
 
 template <int D>
 struct Layout {
-  static constexpr int REGION = 128 * 128;  // one 128-row x 128-byte swizzle region (64 columns)
+  static constexpr int REGION = 128 * 128;    // 128 rows x 128 bytes (64 columns), swizzled
   static constexpr int NREG = D / 64;
   static constexpr int TILE = NREG * REGION;  // a 128 x D 16-bit tile
-  static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF = Q_OFF + TILE;
-  static constexpr int V_OFF = K_OFF + 2 * TILE;
-  static constexpr int BAR_OFF = V_OFF + 2 * TILE;
+  static constexpr int Q_OFF = 0;             // Q_0, Q_1
+  static constexpr int RING_OFF = Q_OFF + NQ * TILE;
+  static constexpr int BAR_OFF = RING_OFF + NS * TILE;
   enum {
-    Q_FULL, K_FULL, K_EMPTY = K_FULL + 2, V_FULL = K_EMPTY + 2, V_EMPTY = V_FULL + 2,
-    S_FULL = V_EMPTY + 2, P_FULL = S_FULL + 2, O_DONE = P_FULL + 2, DRAIN = O_DONE + 2, NUM_BARS
+    Q_FULL, RING_FULL, RING_EMPTY = RING_FULL + NS, S_FULL = RING_EMPTY + NS,
+    P_FULL = S_FULL + NQ, O_DONE = P_FULL + NQ, DRAIN = O_DONE + NQ, NUM_BARS
   };
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;  // [0] TMEM base, [1] abort flag
   static constexpr int BYTES = MISC_OFF + 16;
   static constexpr int ALLOC = BYTES + 1024;  // slack to align the base to 1024 bytes
   static_assert(BAR_OFF % 8 == 0, "mbarriers need 8-byte alignment");
-  static_assert(REGION % 1024 == 0 && K_OFF % 1024 == 0 && V_OFF % 1024 == 0,
+  static_assert(TILE % 1024 == 0 && RING_OFF % 1024 == 0,
                 "128-byte-swizzled tiles need 1024-byte alignment");
+  static_assert(ALLOC <= 227 * 1024, "shared memory per CTA");
 };
 
 // Wait with no abort short-cut: used only while unwinding, for copies and MMAs in flight.
@@ -92,8 +99,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
 template <int D, bool BF16>
 __device__ __forceinline__ void store_row(const Params& p, int bh, int row, float inv_l,
                                           uint32_t o_taddr) {
-  using T = uint4;
-  T* dst = reinterpret_cast<T*>(static_cast<uint16_t*>(p.o) + ((size_t)bh * p.Sq + row) * D);
+  uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + ((size_t)bh * p.Sq + row) * D);
 #pragma unroll
   for (int c = 0; c < D / 32; ++c) {
     uint32_t r[32];
@@ -110,6 +116,29 @@ __device__ __forceinline__ void store_row(const Params& p, int bh, int row, floa
   }
 }
 
+__device__ __forceinline__ void zero_row(const Params& p, int bh, int row, int D) {
+  uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + ((size_t)bh * p.Sq + row) * D);
+  for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+  if (p.lse) p.lse[(size_t)bh * p.Sq + row] = -INFINITY;
+}
+
+// KV tiles a Q tile starting at row m0 needs, and the first that may need masking.
+__device__ __forceinline__ void tile_range(const Params& p, int m0, int* n_tiles, int* mask_from) {
+  if (m0 >= p.Sq) {
+    *n_tiles = 0;
+    *mask_from = 0;
+    return;
+  }
+  const int last_row = min(m0 + BM, p.Sq) - 1;
+  const int delta = p.Skv - p.Sq;
+  int n_keys = p.Skv;
+  if (p.causal) n_keys = max(0, min(p.Skv, last_row + delta + 1));
+  *n_tiles = (n_keys + BN - 1) / BN;
+  int mf = p.Skv / BN;
+  if (p.causal) mf = min(mf, max(0, m0 + delta + 1) / BN);
+  *mask_from = mf;
+}
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -124,39 +153,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mt = p.num_m_tiles - 1 - (int)blockIdx.x;  // longest causal rows first
+  const int mb = p.num_m_blocks - 1 - (int)blockIdx.x;  // longest causal rows first
   const int hq = blockIdx.y, b = blockIdx.z;
   const int bh = b * p.Hq + hq;
   const int kvh = hq / p.group;
-  const int m0 = mt * BM;
-  const int last_row = min(m0 + BM, p.Sq) - 1;
-  const int delta = p.Skv - p.Sq;
-  int n_keys = p.Skv;
-  if (p.causal) n_keys = max(0, min(p.Skv, last_row + delta + 1));
-  const int n_tiles = (n_keys + BN - 1) / BN;
-  // first KV tile whose keys may be invisible to some row of this tile
-  int mask_from = p.Skv / BN;
-  if (p.causal) mask_from = min(mask_from, max(0, m0 + delta + 1) / BN);
+  const int m_base = mb * (NQ * BM);
+  int n_t[NQ], mask_from[NQ];
+#pragma unroll
+  for (int i = 0; i < NQ; ++i) tile_range(p, m_base + i * BM, &n_t[i], &mask_from[i]);
+  const int n_kv = max(n_t[0], n_t[1]);
 
-  if (n_tiles == 0) {  // no row of this tile sees a key: O = 0, LSE = -inf
-    if (threadIdx.x < BM) {
-      const int row = m0 + threadIdx.x;
-      if (row < p.Sq) {
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + ((size_t)bh * p.Sq + row) * D);
-        for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
-        if (p.lse) p.lse[(size_t)bh * p.Sq + row] = -INFINITY;
-      }
+  if (n_kv == 0) {  // no row of this block sees a key: O = 0, LSE = -inf
+    if (threadIdx.x < NQ * BM) {
+      const int row = m_base + threadIdx.x;
+      if (row < p.Sq) zero_row(p, bh, row, D);
     }
     return;
   }
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::Q_FULL), 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(L::K_FULL + i), 1);
-      mbar_init(bar(L::K_EMPTY + i), 1);
-      mbar_init(bar(L::V_FULL + i), 1);
-      mbar_init(bar(L::V_EMPTY + i), 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(bar(L::RING_FULL + s), 1);
+      mbar_init(bar(L::RING_EMPTY + s), 1);
+    }
+    for (int i = 0; i < NQ; ++i) {
       mbar_init(bar(L::S_FULL + i), 1);
       mbar_init(bar(L::P_FULL + i), BM);
       mbar_init(bar(L::O_DONE + i), 1);
@@ -180,97 +201,121 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem = misc[0];
   const uint64_t lim = p.wait_limit_ns;
 
-  if (warp == LOADER_WARP) {
-    // ------------------------------------------------------------ TMA loader
-    if (lane == 0) {
-      const uint64_t pol_q = policy_evict_first();
-      const uint64_t pol_kv = policy_evict_last();
-      const int kv_z = b * p.Hkv + kvh;
-      mbar_expect_tx(bar(L::Q_FULL), L::TILE);
-      for (int r = 0; r < L::NREG; ++r)
-        tma_load_3d(sb + L::Q_OFF + r * L::REGION, &tmq, bar(L::Q_FULL), r * 64, m0, bh, pol_q);
-      int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};
-      for (int t = 0; t < n_tiles; ++t) {
-        const int s = t & 1;
-        const uint32_t ph = ((t >> 1) & 1) ^ 1;
-        if (!mbar_wait(bar(L::K_EMPTY + s), ph, abort_flag, &g_status, lim)) break;
-        mbar_expect_tx(bar(L::K_FULL + s), L::TILE);
-        for (int r = 0; r < L::NREG; ++r)
-          tma_load_3d(sb + L::K_OFF + s * L::TILE + r * L::REGION, &tmk, bar(L::K_FULL + s), r * 64,
-                      t * BN, kv_z, pol_kv);
-        last_k[s] = t;
-        if (p.debug_fault == 1 && t == 0) continue;  // withhold V_0: consumers must time out
-        if (!mbar_wait(bar(L::V_EMPTY + s), ph, abort_flag, &g_status, lim)) break;
-        mbar_expect_tx(bar(L::V_FULL + s), L::TILE);
-        for (int r = 0; r < L::NREG; ++r)
-          tma_load_3d(sb + L::V_OFF + s * L::TILE + r * L::REGION, &tmv, bar(L::V_FULL + s), r * 64,
-                      t * BN, kv_z, pol_kv);
-        last_v[s] = t;
-      }
-      // every copy issued must have landed before the CTA may exit
-      drain_wait(bar(L::Q_FULL), 0, lim);
-      for (int s = 0; s < 2; ++s) {
-        if (last_k[s] >= 0) drain_wait(bar(L::K_FULL + s), (last_k[s] >> 1) & 1, lim);
-        if (last_v[s] >= 0) drain_wait(bar(L::V_FULL + s), (last_v[s] >> 1) & 1, lim);
-      }
-    }
-    __syncwarp();
-  } else if (warp == MMA_WARP) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = umma_idesc_f16(BF16, BM, BN, false, false);
-      constexpr uint32_t idesc_pv = umma_idesc_f16(BF16, BM, D, false, true);
-      const uint32_t tO = tmem + COL_O;
-      auto issue_pv = [&](int u) -> bool {
-        const int s = u & 1;
-        const uint32_t ph = (u >> 1) & 1;
-        if (!mbar_wait(bar(L::P_FULL + s), ph, abort_flag, &g_status, lim)) return false;
-        if (!mbar_wait(bar(L::V_FULL + s), ph, abort_flag, &g_status, lim)) return false;
-        tc_fence_after();
-        const uint32_t v_base = sb + L::V_OFF + s * L::TILE;
-        const uint32_t tP = tmem + COL_P + 64u * s;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          // V is [key][d] (d contiguous): MN-major B, 16 keys = 2 swizzle atoms of 8 rows;
-          // LBO steps to the next 64-column block of d, SBO to the next 8 keys.
-          const uint64_t bdesc = sdesc_sw128(v_base + kk * 16 * 128, L::REGION, 1024);
-          umma_ts(tO, tP + kk * 8, bdesc, idesc_pv, (u > 0 || kk > 0) ? 1u : 0u);
+  if (warp >= NQ * 4) {
+    // register split: 128 threads x 56 + 256 threads x 224 = 384 threads x 168, the
+    // launch allotment (ptxas allocates each region within its new limit)
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
+    if (warp == LOADER_WARP) {
+      // -------------------------------------------------------------- TMA loader
+      if (lane == 0) {
+        const uint64_t pol_q = policy_evict_first();
+        const uint64_t pol_kv = policy_evict_last();
+        const int kv_z = b * p.Hkv + kvh;
+        mbar_expect_tx(bar(L::Q_FULL), NQ * L::TILE);
+        for (int i = 0; i < NQ; ++i)
+          for (int r = 0; r < L::NREG; ++r)
+            tma_load_3d(sb + L::Q_OFF + i * L::TILE + r * L::REGION, &tmq, bar(L::Q_FULL), r * 64,
+                        m_base + i * BM, bh, pol_q);
+        int issued = 0;
+        for (int ld = 0; ld < 2 * n_kv; ++ld) {  // K_0, V_0, K_1, V_1, ...
+          const int s = ld % NS;
+          const uint32_t ph = ((ld / NS) & 1) ^ 1;
+          if (!mbar_wait(bar(L::RING_EMPTY + s), ph, abort_flag, &g_status, lim)) break;
+          issued = ld + 1;
+          if (p.debug_fault == 1 && ld == 1) continue;  // withhold V_0: consumers must time out
+          mbar_expect_tx(bar(L::RING_FULL + s), L::TILE);
+          const CUtensorMap* tm = (ld & 1) ? &tmv : &tmk;
+          for (int r = 0; r < L::NREG; ++r)
+            tma_load_3d(sb + L::RING_OFF + s * L::TILE + r * L::REGION, tm, bar(L::RING_FULL + s),
+                        r * 64, (ld >> 1) * BN, kv_z, pol_kv);
         }
-        umma_commit(bar(L::O_DONE + s));
-        umma_commit(bar(L::V_EMPTY + s));
-        return true;
-      };
-      bool ok = mbar_wait(bar(L::Q_FULL), 0, abort_flag, &g_status, lim);
-      int t = 0;
-      for (; ok && t < n_tiles; ++t) {
-        const int s = t & 1;
-        const uint32_t ph = (t >> 1) & 1;
-        if (!(ok = mbar_wait(bar(L::K_FULL + s), ph, abort_flag, &g_status, lim))) break;
-        tc_fence_after();
-        const uint32_t k_base = sb + L::K_OFF + s * L::TILE;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          // K-major operands: 16 columns = 32 bytes inside a 128-byte swizzled row
-          const uint32_t off = (kk >> 2) * L::REGION + (kk & 3) * 32;
-          const uint64_t adesc = sdesc_sw128(sb + L::Q_OFF + off, 16, 1024);
-          const uint64_t bdesc = sdesc_sw128(k_base + off, 16, 1024);
-          umma_ss(tmem + COL_S + 128u * s, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+        // every copy issued must have landed before the CTA may exit
+        drain_wait(bar(L::Q_FULL), 0, lim);
+        for (int ld = max(0, issued - NS); ld < issued; ++ld) {
+          if (p.debug_fault == 1 && ld == 1) continue;
+          drain_wait(bar(L::RING_FULL + ld % NS), (ld / NS) & 1, lim);
         }
-        umma_commit(bar(L::S_FULL + s));
-        umma_commit(bar(L::K_EMPTY + s));
-        if (t > 0 && !(ok = issue_pv(t - 1))) break;
       }
-      if (ok) issue_pv(n_tiles - 1);
-      umma_commit(bar(L::DRAIN));  // fires once every MMA issued above has completed
-      drain_wait(bar(L::DRAIN), 0, lim);
+      __syncwarp();
+    } else if (warp == MMA_WARP) {
+      // -------------------------------------------------------------- MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t idesc_qk = umma_idesc_f16(BF16, BM, BN, false, false);
+        constexpr uint32_t idesc_pv = umma_idesc_f16(BF16, BM, D, false, true);
+        auto ring_wait = [&](int ld) -> bool {
+          return mbar_wait(bar(L::RING_FULL + ld % NS), (ld / NS) & 1, abort_flag, &g_status, lim);
+        };
+        auto issue_s = [&](int i, int ld) {  // S_i = Q_i K^T, K in the ring slot of load ld
+          const uint32_t k_base = sb + L::RING_OFF + (ld % NS) * L::TILE;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            // K-major operands: 16 columns = 32 bytes inside a 128-byte swizzled row
+            const uint32_t off = (kk >> 2) * L::REGION + (kk & 3) * 32;
+            const uint64_t adesc = sdesc_sw128(sb + L::Q_OFF + i * L::TILE + off, 16, 1024);
+            const uint64_t bdesc = sdesc_sw128(k_base + off, 16, 1024);
+            umma_ss(tmem + COL_S + 128u * i, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(bar(L::S_FULL + i));
+        };
+        auto issue_pv = [&](int i, int ld, bool acc) {  // O_i += P_i V, V in the ring slot of ld
+          const uint32_t v_base = sb + L::RING_OFF + (ld % NS) * L::TILE;
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            // V is [key][d] (d contiguous): MN-major B, 16 keys = 2 swizzle atoms of 8 rows;
+            // LBO steps to the next 64-column block of d, SBO to the next 8 keys.
+            const uint64_t bdesc = sdesc_sw128(v_base + kk * 16 * 128, L::REGION, 1024);
+            umma_ts(tmem + COL_O + 128u * i, tmem + COL_S + 128u * i + kk * 8, bdesc, idesc_pv,
+                    (acc || kk > 0) ? 1u : 0u);
+          }
+        };
+        bool ok = mbar_wait(bar(L::Q_FULL), 0, abort_flag, &g_status, lim) && ring_wait(0);
+        if (ok) {
+          tc_fence_after();
+          for (int i = 0; i < NQ; ++i)
+            if (n_t[i] > 0) issue_s(i, 0);
+          umma_commit(bar(L::RING_EMPTY + 0));
+        }
+        for (int j = 0; ok && j < n_kv; ++j) {
+          const int ld_v = 2 * j + 1, ld_k = 2 * j + 2;
+          if (!(ok = ring_wait(ld_v))) break;
+          tc_fence_after();
+          bool k_ready = false;
+          for (int i = 0; i < NQ && ok; ++i) {
+            if (j < n_t[i]) {
+              if (!(ok = mbar_wait(bar(L::P_FULL + i), j & 1, abort_flag, &g_status, lim))) break;
+              tc_fence_after();
+              issue_pv(i, ld_v, j > 0);
+              if (j == n_t[i] - 1) umma_commit(bar(L::O_DONE + i));
+            }
+            if (j + 1 < n_t[i]) {
+              if (!k_ready) {
+                if (!(ok = ring_wait(ld_k))) break;
+                tc_fence_after();
+                k_ready = true;
+              }
+              issue_s(i, ld_k);  // after PV_i(j), which read P_i from these columns
+            }
+          }
+          umma_commit(bar(L::RING_EMPTY + ld_v % NS));
+          if (k_ready) umma_commit(bar(L::RING_EMPTY + ld_k % NS));
+        }
+        umma_commit(bar(L::DRAIN));  // fires once every MMA issued above has completed
+        drain_wait(bar(L::DRAIN), 0, lim);
+      }
+      __syncwarp();
     }
-    __syncwarp();
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;" ::: "memory");
     // ------------------------------------------------ softmax + epilogue (rows)
-    const int r = threadIdx.x;  // TMEM lane == tile row
-    const int row = m0 + r;
-    const uint32_t lane_t = tmem + ((uint32_t)(warp * 32) << 16);
-    const int lim_key = p.causal ? row + delta : 0x7fffffff;
+    const int qi = warp >> 2;             // Q tile of this warpgroup
+    const int r = threadIdx.x & 127;      // TMEM lane == tile row
+    const int row = m_base + qi * BM + r;
+    const int n_tiles = n_t[qi];
+    const int mfrom = mask_from[qi];
+    const uint32_t lane_t = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t t_s = lane_t + COL_S + 128u * qi;
+    const uint32_t t_o = lane_t + COL_O + 128u * qi;
+    const int lim_key = p.causal ? row + (p.Skv - p.Sq) : 0x7fffffff;
     const float mval = p.neg ? INFINITY : -INFINITY;
     const float c2 = p.c2;
     float m_used = -INFINITY, l_sum = 0.f;
@@ -281,15 +326,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     };
     bool ok = true;
     for (int t = 0; t < n_tiles; ++t) {
-      const int s = t & 1;
-      const uint32_t ph = (t >> 1) & 1;
-      if (!(ok = wait_warp(bar(L::S_FULL + s), ph))) break;
+      if (!(ok = wait_warp(bar(L::S_FULL + qi), t & 1))) break;
       tc_fence_after();
       float x[BN];
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t rr[32];
-        tmem_ld32(lane_t + COL_S + 128u * s + 32u * c, rr);
+        tmem_ld32(t_s + 32u * c, rr);
 #pragma unroll
         for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(rr[i]);
       }
@@ -297,7 +340,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int j = 0; j < BN; ++j) x[j] = 0.f;
       }
-      if (t >= mask_from) {
+      if (t >= mfrom) {
         const int kbase = t * BN;
 #pragma unroll
         for (int j = 0; j < BN; ++j) {
@@ -340,22 +383,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         m_used = m_new;
       }
       if (__any_sync(0xffffffffu, o_scale)) {
-        // O holds P V up to tile t-1: wait for that MMA, then rescale the rows in place
-        const int u = t - 1;
-        if (!(ok = wait_warp(bar(L::O_DONE + (u & 1)), (u >> 1) & 1))) break;
-        tc_fence_after();
+        // S_i(t) completed, so every earlier MMA did: O_i holds P V up to tile t-1
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t rr[32];
-          tmem_ld32(lane_t + COL_O + 32u * c, rr);
+          tmem_ld32(t_o + 32u * c, rr);
 #pragma unroll
           for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha_o);
-          tmem_st32(lane_t + COL_O + 32u * c, rr);
+          tmem_st32(t_o + 32u * c, rr);
         }
-      }
-      if (t >= 2) {  // P_s was read by the MMA of tile t-2: wait until it completed
-        const int u = t - 2;
-        if (!(ok = wait_warp(bar(L::O_DONE + s), (u >> 1) & 1))) break;
       }
       const float mu = (m_used == -INFINITY) ? 0.f : m_used;
       float ls0 = 0.f, ls1 = 0.f;
@@ -370,24 +406,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ls1 += e1;
           pk[i] = pack2<BF16>(e0, e1);
         }
-        tmem_st32(lane_t + COL_P + 64u * s + 32u * h, pk);
+        tmem_st32(t_s + 32u * h, pk);  // P over the S columns already consumed
       }
       l_sum += ls0 + ls1;
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(L::P_FULL + s));
+      mbar_arrive(bar(L::P_FULL + qi));
     }
+    if (ok && n_tiles > 0) ok = wait_warp(bar(L::O_DONE + qi), 0);
     if (ok) {
-      const int u = n_tiles - 1;
-      ok = wait_warp(bar(L::O_DONE + (u & 1)), (u >> 1) & 1);
-    }
-    if (ok) {
-      tc_fence_after();
-      const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
-      store_row<D, BF16>(p, bh, row, inv_l, lane_t + COL_O);
-      if (p.lse && row < p.Sq)
-        p.lse[(size_t)bh * p.Sq + row] =
-            l_sum > 0.f ? (m_used + log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
+      if (n_tiles > 0) {
+        tc_fence_after();
+        const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
+        store_row<D, BF16>(p, bh, row, inv_l, t_o);
+        if (p.lse && row < p.Sq)
+          p.lse[(size_t)bh * p.Sq + row] =
+              l_sum > 0.f ? (m_used + log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
+      } else if (row < p.Sq) {  // this Q tile sees no key
+        zero_row(p, bh, row, D);
+      }
     }
   }
 
@@ -442,7 +479,7 @@ static cudaError_t launch_t(const FwdArgs& a, cudaStream_t stream) {
   p.Sq = a.Sq;
   p.Skv = a.Skv;
   p.group = a.Hq / a.Hkv;
-  p.num_m_tiles = (a.Sq + BM - 1) / BM;
+  p.num_m_blocks = (a.Sq + NQ * BM - 1) / (NQ * BM);
   p.causal = a.causal ? 1 : 0;
   const float c2 = a.scale * 1.4426950408889634f;
   p.zero = (c2 == 0.f) ? 1 : 0;
@@ -450,7 +487,7 @@ static cudaError_t launch_t(const FwdArgs& a, cudaStream_t stream) {
   p.c2 = p.zero ? 1.f : c2;
   p.wait_limit_ns = a.wait_limit_ns;
   p.debug_fault = a.debug_fault;
-  dim3 grid(p.num_m_tiles, a.Hq, a.B);
+  dim3 grid(p.num_m_blocks, a.Hq, a.B);
   attn_fwd_kernel<D, BF16><<<grid, NUM_THREADS, L::ALLOC, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
