@@ -21,6 +21,7 @@ int g_fault = 0;
 
 std::mutex g_mu;
 int g_arch_ok[kMaxDevices];              // 0 unknown, 1 sm_103, -1 other
+int g_num_sms[kMaxDevices];
 cudaMemPool_t g_pool[kMaxDevices];
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -40,6 +41,12 @@ int check_device(int* dev_out) {
       cudaGetLastError();
       return ATTN_ERR_CUDA;
     }
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_CUDA;
+    }
+    g_num_sms[dev] = sms;
     g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
   }
   if (dev_out) *dev_out = dev;
@@ -114,6 +121,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   if ((long long)B * Hq * Sq == 0) return ATTN_OK;  // nothing to compute
   if (Hkv == 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (B > 65535 || Hq > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (((long long)Sq + 255) / 256 * Hq * B > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
   if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (!q || !o || (Skv > 0 && (!k || !v))) return ATTN_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(o, 16) || (k && !aligned(k, 16)) || (v && !aligned(v, 16)) ||
@@ -140,9 +148,22 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   a.bf16 = dtype == ATTN_BF16;
   a.wait_limit_ns = g_wait_limit_ns;
   a.debug_fault = g_fault;
+  a.num_sms = g_num_sms[dev] > 0 ? g_num_sms[dev] : 1;
   if (Skv == 0) return from_cuda(ea::launch_fwd_empty_keys(a, stream));
-  cudaError_t e = ea::launch_fwd(a, stream);
+  // the persistent kernel's work-item counter: 256 stream-ordered bytes, zeroed
+  cudaMemPool_t pool;
+  if ((st = pool_for(dev, &pool)) != ATTN_OK) return st;
+  void* counter = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(&counter, 256, pool, stream);
+  if (e != cudaSuccess) return from_cuda(e);
+  e = cudaMemsetAsync(counter, 0, sizeof(int), stream);
+  if (e == cudaSuccess) {
+    a.work_counter = static_cast<int*>(counter);
+    e = ea::launch_fwd(a, stream);
+  }
+  cudaError_t f = cudaFreeAsync(counter, stream);
   if (e == cudaErrorInvalidValue && !ea::encode_tiled_fn()) return ATTN_ERR_UNSUPPORTED;
+  if (e == cudaSuccess) e = f;
   return from_cuda(e);
 }
 

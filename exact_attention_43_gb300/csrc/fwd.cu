@@ -7,10 +7,17 @@
 // the sum at the end; rustytorch flash_attention_forward.cu,
 // OnlineSoftmaxState: LSE = m + log(l)).  How it is computed is GB300-native:
 //
-//  * one CTA owns two 128-row Q tiles (256 consecutive query rows) of one
-//    (batch, query head) and streams the K/V tiles of the matching KV head
+//  * a work item is two 128-row Q tiles (256 consecutive query rows) of one
+//    (batch, query head); the K/V tiles of the matching KV head are streamed
 //    once for both; KV head = query head / (Hq / Hkv) (abaddon
 //    flash_attention_f16, GQA mapping);
+//  * the grid is persistent (one CTA per SM): the loader warp claims work
+//    items from a global counter and queues them in shared memory for the
+//    other warps; items are ordered so each group of heads' K and V stays in
+//    L2 and, within a group, the longest causal items come first; the next
+//    item's Q, K, V loads and first S MMAs overlap the current item's last
+//    P V and epilogue (O is handed back through an mbarrier as soon as the
+//    epilogue has read it from TMEM);
 //  * warp 8 streams Q once and K, V 128-key tiles through a 4-stage ring with
 //    TMA (3-D tensor maps, 128-byte swizzle, mbarrier transaction counts);
 //  * warp 9 issues tcgen05.mma: S_i = Q_i K_j^T into TMEM, then
@@ -45,6 +52,7 @@ constexpr int BM = 128;             // rows per Q tile (= TMEM lanes)
 constexpr int NQ = 2;               // Q tiles per CTA
 constexpr int BN = 128;             // keys per KV tile
 constexpr int NS = 4;               // K/V ring stages
+constexpr int NITEM = 4;            // claimed work items queued from the loader to the others
 constexpr int NUM_THREADS = 384;    // warpgroups 0, 1: softmax; warp 8 loader, warp 9 MMA
 constexpr int LOADER_WARP = 8;
 constexpr int MMA_WARP = 9;
@@ -57,7 +65,9 @@ constexpr uint32_t COL_O = 256;
 struct Params {
   void* o;
   float* lse;
-  int Hq, Hkv, Sq, Skv, group, num_m_blocks, causal, neg, zero;
+  int* work_counter;  // zeroed before the launch; CTAs claim work items from it
+  int B, Hq, Hkv, Sq, Skv, group, num_m_blocks, causal, neg, zero;
+  int heads_per_group;  // flattened (batch, head) rows per scheduling group
   float c2;  // scale * log2(e); 1 when scale == 0 (then every visible score is set to 0)
   uint64_t wait_limit_ns;
   int debug_fault;
@@ -72,11 +82,13 @@ struct Layout {
   static constexpr int RING_OFF = Q_OFF + NQ * TILE;
   static constexpr int BAR_OFF = RING_OFF + NS * TILE;
   enum {
-    Q_FULL, RING_FULL, RING_EMPTY = RING_FULL + NS, S_FULL = RING_EMPTY + NS,
-    P_FULL = S_FULL + NQ, O_DONE = P_FULL + NQ, DRAIN = O_DONE + NQ, NUM_BARS
+    Q_FULL, Q_EMPTY, RING_FULL, RING_EMPTY = RING_FULL + NS, S_FULL = RING_EMPTY + NS,
+    P_FULL = S_FULL + NQ, O_DONE = P_FULL + NQ, O_FREE = O_DONE + NQ,
+    ITEM_FULL = O_FREE + NQ, ITEM_EMPTY = ITEM_FULL + NITEM, DRAIN = ITEM_EMPTY + NITEM, NUM_BARS
   };
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;  // [0] TMEM base, [1] abort flag
-  static constexpr int BYTES = MISC_OFF + 16;
+  static constexpr int ITEM_OFF = MISC_OFF + 16;           // NITEM claimed work items
+  static constexpr int BYTES = ITEM_OFF + NITEM * 4;
   static constexpr int ALLOC = BYTES + 1024;  // slack to align the base to 1024 bytes
   static_assert(BAR_OFF % 8 == 0, "mbarriers need 8-byte alignment");
   static_assert(TILE % 1024 == 0 && RING_OFF % 1024 == 0,
@@ -92,26 +104,6 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
     if (global_timer_ns() - t0 > limit_ns) {
       atomicOr(&g_status, kStatusTimeout);
       return;
-    }
-  }
-}
-
-template <int D, bool BF16>
-__device__ __forceinline__ void store_row(const Params& p, int bh, int row, float inv_l,
-                                          uint32_t o_taddr) {
-  uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + ((size_t)bh * p.Sq + row) * D);
-#pragma unroll
-  for (int c = 0; c < D / 32; ++c) {
-    uint32_t r[32];
-    tmem_ld32(o_taddr + c * 32, r);
-    uint32_t w[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      w[i] = pack2<BF16>(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
-    if (row < p.Sq) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        dst[c * 4 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
     }
   }
 }
@@ -139,6 +131,24 @@ __device__ __forceinline__ void tile_range(const Params& p, int m0, int* n_tiles
   *mask_from = mf;
 }
 
+// Work item w -> (256-row block, batch, query head).  Items are grouped by
+// heads_per_group consecutive (batch, head) rows, chosen on the host so that a
+// group's K and V stay resident in L2; inside a group the blocks go from the
+// last (most causal work) to the first, heads innermost, so CTAs working at the
+// same time share KV heads and the longest items start first.
+__device__ __forceinline__ void decode_item(const Params& p, int w, int* mb, int* hq, int* b) {
+  const int BH = p.B * p.Hq;
+  const int full = p.num_m_blocks * p.heads_per_group;
+  const int gi = w / full;
+  const int g0 = gi * p.heads_per_group;
+  const int size = min(p.heads_per_group, BH - g0);
+  const int off = w - gi * full;
+  const int hb = g0 + off % size;
+  *mb = p.num_m_blocks - 1 - off / size;
+  *b = hb / p.Hq;
+  *hq = hb % p.Hq;
+}
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -151,28 +161,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto bar = [&](int i) -> uint32_t { return sb + L::BAR_OFF + 8u * i; };
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mb = p.num_m_blocks - 1 - (int)blockIdx.x;  // longest causal rows first
-  const int hq = blockIdx.y, b = blockIdx.z;
-  const int bh = b * p.Hq + hq;
-  const int kvh = hq / p.group;
-  const int m_base = mb * (NQ * BM);
-  int n_t[NQ], mask_from[NQ];
-#pragma unroll
-  for (int i = 0; i < NQ; ++i) tile_range(p, m_base + i * BM, &n_t[i], &mask_from[i]);
-  const int n_kv = max(n_t[0], n_t[1]);
-
-  if (n_kv == 0) {  // no row of this block sees a key: O = 0, LSE = -inf
-    if (threadIdx.x < NQ * BM) {
-      const int row = m_base + threadIdx.x;
-      if (row < p.Sq) zero_row(p, bh, row, D);
-    }
-    return;
-  }
+  const int n_items = p.num_m_blocks * p.Hq * p.B;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::Q_FULL), 1);
+    mbar_init(bar(L::Q_EMPTY), 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(bar(L::RING_FULL + s), 1);
       mbar_init(bar(L::RING_EMPTY + s), 1);
@@ -181,11 +175,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(bar(L::S_FULL + i), 1);
       mbar_init(bar(L::P_FULL + i), BM);
       mbar_init(bar(L::O_DONE + i), 1);
+      mbar_init(bar(L::O_FREE + i), BM);
+    }
+    for (int q = 0; q < NITEM; ++q) {
+      mbar_init(bar(L::ITEM_FULL + q), 1);
+      mbar_init(bar(L::ITEM_EMPTY + q), 1 + NQ * 4);  // the MMA thread and the 8 softmax warps
     }
     mbar_init(bar(L::DRAIN), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
+  volatile int* item_q = reinterpret_cast<volatile int*>(smem + L::ITEM_OFF);
   if (warp == LOADER_WARP && lane == 0) {
     prefetch_tmap(&tmq);
     prefetch_tmap(&tmk);
@@ -202,38 +202,62 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint64_t lim = p.wait_limit_ns;
 
   if (warp >= NQ * 4) {
-    // register split: 128 threads x 56 + 256 threads x 224 = 384 threads x 168, the
+    // register split: 128 threads x 88 + 256 threads x 208 = 384 threads x 168, the
     // launch allotment (ptxas allocates each region within its new limit)
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 88;" ::: "memory");
     if (warp == LOADER_WARP) {
       // -------------------------------------------------------------- TMA loader
       if (lane == 0) {
         const uint64_t pol_q = policy_evict_first();
         const uint64_t pol_kv = policy_evict_last();
-        const int kv_z = b * p.Hkv + kvh;
-        mbar_expect_tx(bar(L::Q_FULL), NQ * L::TILE);
-        for (int i = 0; i < NQ; ++i)
-          for (int r = 0; r < L::NREG; ++r)
-            tma_load_3d(sb + L::Q_OFF + i * L::TILE + r * L::REGION, &tmq, bar(L::Q_FULL), r * 64,
-                        m_base + i * BM, bh, pol_q);
-        int issued = 0;
-        for (int ld = 0; ld < 2 * n_kv; ++ld) {  // K_0, V_0, K_1, V_1, ...
-          const int s = ld % NS;
-          const uint32_t ph = ((ld / NS) & 1) ^ 1;
-          if (!mbar_wait(bar(L::RING_EMPTY + s), ph, abort_flag, &g_status, lim)) break;
-          issued = ld + 1;
-          if (p.debug_fault == 1 && ld == 1) continue;  // withhold V_0: consumers must time out
-          mbar_expect_tx(bar(L::RING_FULL + s), L::TILE);
-          const CUtensorMap* tm = (ld & 1) ? &tmv : &tmk;
-          for (int r = 0; r < L::NREG; ++r)
-            tma_load_3d(sb + L::RING_OFF + s * L::TILE + r * L::REGION, tm, bar(L::RING_FULL + s),
-                        r * 64, (ld >> 1) * BN, kv_z, pol_kv);
+        int ld = 0, k_item = 0;
+        bool ok = true;
+        for (int r = 0; ok; ++r) {
+          // claim the next work item and queue it for the MMA and softmax warps
+          const int qs = r % NITEM;
+          if (!(ok = mbar_wait(bar(L::ITEM_EMPTY + qs), ((r / NITEM) & 1) ^ 1, abort_flag,
+                               &g_status, lim)))
+            break;
+          int w = atomicAdd(p.work_counter, 1);
+          if (w >= n_items) w = -1;
+          item_q[qs] = w;
+          mbar_arrive(bar(L::ITEM_FULL + qs));
+          if (w < 0) break;
+          int mb, hq, b;
+          decode_item(p, w, &mb, &hq, &b);
+          const int m_base = mb * (NQ * BM);
+          int n_t[NQ], mf[NQ];
+          for (int i = 0; i < NQ; ++i) tile_range(p, m_base + i * BM, &n_t[i], &mf[i]);
+          const int n_kv = max(n_t[0], n_t[1]);
+          if (n_kv == 0) continue;
+          // Q of this item may overwrite Q of the last one once its S MMAs are done
+          if (!(ok = mbar_wait(bar(L::Q_EMPTY), (k_item & 1) ^ 1, abort_flag, &g_status, lim)))
+            break;
+          const int bh = b * p.Hq + hq, kv_z = b * p.Hkv + hq / p.group;
+          mbar_expect_tx(bar(L::Q_FULL), NQ * L::TILE);
+          for (int i = 0; i < NQ; ++i)
+            for (int rr = 0; rr < L::NREG; ++rr)
+              tma_load_3d(sb + L::Q_OFF + i * L::TILE + rr * L::REGION, &tmq, bar(L::Q_FULL),
+                          rr * 64, m_base + i * BM, bh, pol_q);
+          ++k_item;
+          for (int l = 0; l < 2 * n_kv; ++l, ++ld) {  // K_0, V_0, K_1, V_1, ...
+            const int s = ld % NS;
+            if (!(ok = mbar_wait(bar(L::RING_EMPTY + s), ((ld / NS) & 1) ^ 1, abort_flag, &g_status,
+                                 lim)))
+              break;
+            if (p.debug_fault == 1 && ld == 1) continue;  // withhold V_0: consumers must time out
+            mbar_expect_tx(bar(L::RING_FULL + s), L::TILE);
+            const CUtensorMap* tm = (l & 1) ? &tmv : &tmk;
+            for (int rr = 0; rr < L::NREG; ++rr)
+              tma_load_3d(sb + L::RING_OFF + s * L::TILE + rr * L::REGION, tm,
+                          bar(L::RING_FULL + s), rr * 64, (l >> 1) * BN, kv_z, pol_kv);
+          }
         }
         // every copy issued must have landed before the CTA may exit
-        drain_wait(bar(L::Q_FULL), 0, lim);
-        for (int ld = max(0, issued - NS); ld < issued; ++ld) {
-          if (p.debug_fault == 1 && ld == 1) continue;
-          drain_wait(bar(L::RING_FULL + ld % NS), (ld / NS) & 1, lim);
+        if (k_item > 0) drain_wait(bar(L::Q_FULL), (k_item - 1) & 1, lim);
+        for (int l = max(0, ld - NS); l < ld; ++l) {
+          if (p.debug_fault == 1 && l == 1) continue;
+          drain_wait(bar(L::RING_FULL + l % NS), (l / NS) & 1, lim);
         }
       }
       __syncwarp();
@@ -268,36 +292,71 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     (acc || kk > 0) ? 1u : 0u);
           }
         };
-        bool ok = mbar_wait(bar(L::Q_FULL), 0, abort_flag, &g_status, lim) && ring_wait(0);
-        if (ok) {
+        int ld = 0, k_item = 0;
+        int t_cnt[NQ] = {0, 0};  // tiles handed to warpgroup i so far (P_FULL phases)
+        int u_cnt[NQ] = {0, 0};  // items in which warpgroup i used its O accumulator
+        bool ok = true;
+        for (int r = 0; ok; ++r) {
+          const int qs = r % NITEM;
+          if (!(ok = mbar_wait(bar(L::ITEM_FULL + qs), (r / NITEM) & 1, abort_flag, &g_status, lim)))
+            break;
+          const int w = item_q[qs];
+          mbar_arrive(bar(L::ITEM_EMPTY + qs));
+          if (w < 0) break;
+          int mb, hq, b;
+          decode_item(p, w, &mb, &hq, &b);
+          const int m_base = mb * (NQ * BM);
+          int n_t[NQ], mf[NQ];
+          for (int i = 0; i < NQ; ++i) tile_range(p, m_base + i * BM, &n_t[i], &mf[i]);
+          const int n_kv = max(n_t[0], n_t[1]);
+          if (n_kv == 0) continue;
+          if (!(ok = mbar_wait(bar(L::Q_FULL), k_item & 1, abort_flag, &g_status, lim))) break;
+          ++k_item;
+          const int base = ld;
+          if (!(ok = ring_wait(base))) break;
           tc_fence_after();
+          // S_i(0): P_i of the last item lives in these columns, read by an MMA issued earlier
           for (int i = 0; i < NQ; ++i)
-            if (n_t[i] > 0) issue_s(i, 0);
-          umma_commit(bar(L::RING_EMPTY + 0));
-        }
-        for (int j = 0; ok && j < n_kv; ++j) {
-          const int ld_v = 2 * j + 1, ld_k = 2 * j + 2;
-          if (!(ok = ring_wait(ld_v))) break;
-          tc_fence_after();
-          bool k_ready = false;
-          for (int i = 0; i < NQ && ok; ++i) {
-            if (j < n_t[i]) {
-              if (!(ok = mbar_wait(bar(L::P_FULL + i), j & 1, abort_flag, &g_status, lim))) break;
-              tc_fence_after();
-              issue_pv(i, ld_v, j > 0);
-              if (j == n_t[i] - 1) umma_commit(bar(L::O_DONE + i));
-            }
-            if (j + 1 < n_t[i]) {
-              if (!k_ready) {
-                if (!(ok = ring_wait(ld_k))) break;
+            if (n_t[i] > 0) issue_s(i, base);
+          if (n_kv == 1) umma_commit(bar(L::Q_EMPTY));  // every S of the item is issued
+          umma_commit(bar(L::RING_EMPTY + base % NS));
+          for (int j = 0; ok && j < n_kv; ++j) {
+            const int ld_v = base + 2 * j + 1, ld_k = base + 2 * j + 2;
+            if (!(ok = ring_wait(ld_v))) break;
+            tc_fence_after();
+            bool k_ready = false;
+            for (int i = 0; i < NQ && ok; ++i) {
+              if (j < n_t[i]) {
+                if (!(ok = mbar_wait(bar(L::P_FULL + i), t_cnt[i] & 1, abort_flag, &g_status, lim)))
+                  break;
+                // the first P V of an item overwrites O_i: the last epilogue must have read it
+                if (j == 0 && u_cnt[i] > 0 &&
+                    !(ok = mbar_wait(bar(L::O_FREE + i), (u_cnt[i] - 1) & 1, abort_flag, &g_status,
+                                     lim)))
+                  break;
                 tc_fence_after();
-                k_ready = true;
+                issue_pv(i, ld_v, j > 0);
+                ++t_cnt[i];
+                if (j == n_t[i] - 1) {
+                  umma_commit(bar(L::O_DONE + i));
+                  ++u_cnt[i];
+                }
               }
-              issue_s(i, ld_k);  // after PV_i(j), which read P_i from these columns
+              if (j + 1 < n_t[i]) {
+                if (!k_ready) {
+                  if (!(ok = ring_wait(ld_k))) break;
+                  tc_fence_after();
+                  k_ready = true;
+                }
+                issue_s(i, ld_k);  // after PV_i(j), which read P_i from these columns
+              }
             }
+            if (!ok) break;
+            if (j == n_kv - 2) umma_commit(bar(L::Q_EMPTY));  // the item's last S was issued
+            umma_commit(bar(L::RING_EMPTY + ld_v % NS));
+            if (k_ready) umma_commit(bar(L::RING_EMPTY + ld_k % NS));
           }
-          umma_commit(bar(L::RING_EMPTY + ld_v % NS));
-          if (k_ready) umma_commit(bar(L::RING_EMPTY + ld_k % NS));
+          ld = base + 2 * n_kv;
         }
         umma_commit(bar(L::DRAIN));  // fires once every MMA issued above has completed
         drain_wait(bar(L::DRAIN), 0, lim);
@@ -305,125 +364,149 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;" ::: "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 208;" ::: "memory");
     // ------------------------------------------------ softmax + epilogue (rows)
     const int qi = warp >> 2;             // Q tile of this warpgroup
-    const int r = threadIdx.x & 127;      // TMEM lane == tile row
-    const int row = m_base + qi * BM + r;
-    const int n_tiles = n_t[qi];
-    const int mfrom = mask_from[qi];
+    const int r_lane = threadIdx.x & 127; // TMEM lane == tile row
     const uint32_t lane_t = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t t_s = lane_t + COL_S + 128u * qi;
     const uint32_t t_o = lane_t + COL_O + 128u * qi;
-    const int lim_key = p.causal ? row + (p.Skv - p.Sq) : 0x7fffffff;
     const float mval = p.neg ? INFINITY : -INFINITY;
     const float c2 = p.c2;
-    float m_used = -INFINITY, l_sum = 0.f;
     // tcgen05.ld/st are warp-collective: every wait outcome and every rescale
     // decision below is made uniform across the warp before TMEM is touched.
     auto wait_warp = [&](uint32_t b_, uint32_t ph_) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(b_, ph_, abort_flag, &g_status, lim));
     };
+    int t_cnt = 0, u_cnt = 0;
     bool ok = true;
-    for (int t = 0; t < n_tiles; ++t) {
-      if (!(ok = wait_warp(bar(L::S_FULL + qi), t & 1))) break;
-      tc_fence_after();
-      float x[BN];
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t rr[32];
-        tmem_ld32(t_s + 32u * c, rr);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(rr[i]);
+    for (int r = 0; ok; ++r) {
+      const int qs = r % NITEM;
+      if (!(ok = wait_warp(bar(L::ITEM_FULL + qs), (r / NITEM) & 1))) break;
+      const int w = item_q[qs];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::ITEM_EMPTY + qs));
+      if (w < 0) break;
+      int mb, hq, b;
+      decode_item(p, w, &mb, &hq, &b);
+      const int bh = b * p.Hq + hq;
+      const int m0 = mb * (NQ * BM) + qi * BM;
+      const int row = m0 + r_lane;
+      int n_tiles, mfrom;
+      tile_range(p, m0, &n_tiles, &mfrom);
+      if (n_tiles == 0) {  // this Q tile sees no key (or lies past Sq)
+        if (row < p.Sq) zero_row(p, bh, row, D);
+        continue;
       }
-      if (p.zero) {
+      const int lim_key = p.causal ? row + (p.Skv - p.Sq) : 0x7fffffff;
+      float m_used = -INFINITY, l_sum = 0.f;
+      for (int t = 0; t < n_tiles; ++t, ++t_cnt) {
+        if (!(ok = wait_warp(bar(L::S_FULL + qi), t_cnt & 1))) break;
+        tc_fence_after();
+        float x[BN];
+        {
+          uint32_t rr[BN];
+          tmem_ld(t_s, rr);  // the whole S row in one TMEM round trip
 #pragma unroll
-        for (int j = 0; j < BN; ++j) x[j] = 0.f;
-      }
-      if (t >= mfrom) {
-        const int kbase = t * BN;
-#pragma unroll
-        for (int j = 0; j < BN; ++j) {
-          const int key = kbase + j;
-          if (key > lim_key || key >= p.Skv) x[j] = mval;
+          for (int i = 0; i < BN; ++i) x[i] = __uint_as_float(rr[i]);
         }
-      }
-      float red;
-      if (!p.neg) {
-        float a0 = x[0], a1 = x[1], a2 = x[2], a3 = x[3];
+        if (p.zero) {
 #pragma unroll
-        for (int j = 4; j < BN; j += 4) {
-          a0 = fmaxf(a0, x[j]);
-          a1 = fmaxf(a1, x[j + 1]);
-          a2 = fmaxf(a2, x[j + 2]);
-          a3 = fmaxf(a3, x[j + 3]);
+          for (int j = 0; j < BN; ++j) x[j] = 0.f;
         }
-        red = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
-      } else {
-        float a0 = x[0], a1 = x[1], a2 = x[2], a3 = x[3];
+        if (t >= mfrom) {
+          const int kbase = t * BN;
 #pragma unroll
-        for (int j = 4; j < BN; j += 4) {
-          a0 = fminf(a0, x[j]);
-          a1 = fminf(a1, x[j + 1]);
-          a2 = fminf(a2, x[j + 2]);
-          a3 = fminf(a3, x[j + 3]);
+          for (int j = 0; j < BN; ++j) {
+            const int key = kbase + j;
+            if (key > lim_key || key >= p.Skv) x[j] = mval;
+          }
         }
-        red = fminf(fminf(a0, a1), fminf(a2, a3));
-      }
-      const float m_tile = red * c2;  // -inf when every key of the tile is masked
-      const float m_new = fmaxf(m_used, m_tile);
-      const bool grow = m_new > m_used + RESCALE_LOG2;
-      // O needs the factor only once it holds P V of an earlier tile with a finite max
-      const bool o_scale = grow && t > 0 && m_used != -INFINITY;
-      float alpha_o = 1.f;
-      if (grow) {
-        const float alpha = ex2(m_used - m_new);  // 0 while nothing was visible yet
-        l_sum *= alpha;
-        if (o_scale) alpha_o = alpha;
-        m_used = m_new;
-      }
-      if (__any_sync(0xffffffffu, o_scale)) {
-        // S_i(t) completed, so every earlier MMA did: O_i holds P V up to tile t-1
+        float red;
+        if (!p.neg) {
+          float a0 = x[0], a1 = x[1], a2 = x[2], a3 = x[3];
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t rr[32];
-          tmem_ld32(t_o + 32u * c, rr);
+          for (int j = 4; j < BN; j += 4) {
+            a0 = fmaxf(a0, x[j]);
+            a1 = fmaxf(a1, x[j + 1]);
+            a2 = fmaxf(a2, x[j + 2]);
+            a3 = fmaxf(a3, x[j + 3]);
+          }
+          red = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+        } else {
+          float a0 = x[0], a1 = x[1], a2 = x[2], a3 = x[3];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha_o);
-          tmem_st32(t_o + 32u * c, rr);
+          for (int j = 4; j < BN; j += 4) {
+            a0 = fminf(a0, x[j]);
+            a1 = fminf(a1, x[j + 1]);
+            a2 = fminf(a2, x[j + 2]);
+            a3 = fminf(a3, x[j + 3]);
+          }
+          red = fminf(fminf(a0, a1), fminf(a2, a3));
         }
-      }
-      const float mu = (m_used == -INFINITY) ? 0.f : m_used;
-      float ls0 = 0.f, ls1 = 0.f;
+        const float m_tile = red * c2;  // -inf when every key of the tile is masked
+        const float m_new = fmaxf(m_used, m_tile);
+        const bool grow = m_new > m_used + RESCALE_LOG2;
+        // O needs the factor only once it holds P V of an earlier tile with a finite max
+        const bool o_scale = grow && t > 0 && m_used != -INFINITY;
+        float alpha_o = 1.f;
+        if (grow) {
+          const float alpha = ex2(m_used - m_new);  // 0 while nothing was visible yet
+          l_sum *= alpha;
+          if (o_scale) alpha_o = alpha;
+          m_used = m_new;
+        }
+        if (__any_sync(0xffffffffu, o_scale)) {
+          // S_i(t) completed, so every earlier MMA did: O_i holds P V up to tile t-1
+          // (rare; in 32-column pieces because the S row is still live in registers)
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pk[32];
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t rr[32];
+            tmem_ld32(t_o + 32u * c, rr);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float e0 = ex2(fmaf(x[h * 64 + 2 * i], c2, -mu));
-          const float e1 = ex2(fmaf(x[h * 64 + 2 * i + 1], c2, -mu));
+            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha_o);
+            tmem_st32(t_o + 32u * c, rr);
+          }
+        }
+        const float mu = (m_used == -INFINITY) ? 0.f : m_used;
+        float ls0 = 0.f, ls1 = 0.f;
+        uint32_t pk[BN / 2];
+#pragma unroll
+        for (int i = 0; i < BN / 2; ++i) {
+          const float e0 = ex2(fmaf(x[2 * i], c2, -mu));
+          const float e1 = ex2(fmaf(x[2 * i + 1], c2, -mu));
           ls0 += e0;
           ls1 += e1;
           pk[i] = pack2<BF16>(e0, e1);
         }
-        tmem_st32(t_s + 32u * h, pk);  // P over the S columns already consumed
+        tmem_st(t_s, pk);  // P over the S columns already consumed
+        l_sum += ls0 + ls1;
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(L::P_FULL + qi));
       }
-      l_sum += ls0 + ls1;
-      tmem_wait_st();
+      if (!ok) break;
+      if (!(ok = wait_warp(bar(L::O_DONE + qi), u_cnt & 1))) break;
+      ++u_cnt;
+      tc_fence_after();
+      // read the whole O row, hand the accumulator back to the MMA warp, then store
+      uint32_t orow[D];
+      tmem_ld(t_o, orow);
       tc_fence_before();
-      mbar_arrive(bar(L::P_FULL + qi));
-    }
-    if (ok && n_tiles > 0) ok = wait_warp(bar(L::O_DONE + qi), 0);
-    if (ok) {
-      if (n_tiles > 0) {
-        tc_fence_after();
+      mbar_arrive(bar(L::O_FREE + qi));
+      if (row < p.Sq) {
         const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
-        store_row<D, BF16>(p, bh, row, inv_l, t_o);
-        if (p.lse && row < p.Sq)
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + ((size_t)bh * p.Sq + row) * D);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c)
+          dst[c] = make_uint4(
+              pack2<BF16>(__uint_as_float(orow[8 * c + 0]) * inv_l, __uint_as_float(orow[8 * c + 1]) * inv_l),
+              pack2<BF16>(__uint_as_float(orow[8 * c + 2]) * inv_l, __uint_as_float(orow[8 * c + 3]) * inv_l),
+              pack2<BF16>(__uint_as_float(orow[8 * c + 4]) * inv_l, __uint_as_float(orow[8 * c + 5]) * inv_l),
+              pack2<BF16>(__uint_as_float(orow[8 * c + 6]) * inv_l, __uint_as_float(orow[8 * c + 7]) * inv_l));
+        if (p.lse)
           p.lse[(size_t)bh * p.Sq + row] =
               l_sum > 0.f ? (m_used + log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
-      } else if (row < p.Sq) {  // this Q tile sees no key
-        zero_row(p, bh, row, D);
       }
     }
   }
@@ -474,6 +557,8 @@ static cudaError_t launch_t(const FwdArgs& a, cudaStream_t stream) {
   Params p{};
   p.o = a.o;
   p.lse = a.lse;
+  p.work_counter = a.work_counter;
+  p.B = a.B;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
   p.Sq = a.Sq;
@@ -487,7 +572,17 @@ static cudaError_t launch_t(const FwdArgs& a, cudaStream_t stream) {
   p.c2 = p.zero ? 1.f : c2;
   p.wait_limit_ns = a.wait_limit_ns;
   p.debug_fault = a.debug_fault;
-  dim3 grid(p.num_m_blocks, a.Hq, a.B);
+  // scheduling groups: as many (batch, head) rows as keep about 64 MB of K and V
+  // in L2, rounded to whole GQA groups
+  const double kv_head_bytes = 4.0 * (double)a.Skv * D;  // K and V of one KV head
+  const int g = a.Hq / a.Hkv;
+  long long hpg = (long long)(64.0 * (1 << 20) / kv_head_bytes) * g;
+  if (hpg < g) hpg = g;
+  if (hpg > (long long)a.B * a.Hq) hpg = (long long)a.B * a.Hq;
+  p.heads_per_group = (int)hpg;
+  // persistent: one CTA per SM (or one per work item when there are fewer)
+  const long long n_items = (long long)p.num_m_blocks * a.Hq * a.B;
+  const int grid = (int)(n_items < a.num_sms ? n_items : a.num_sms);
   attn_fwd_kernel<D, BF16><<<grid, NUM_THREADS, L::ALLOC, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }

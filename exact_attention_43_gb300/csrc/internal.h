@@ -20,6 +20,8 @@ struct FwdArgs {
   int bf16;
   uint64_t wait_limit_ns;
   int debug_fault;  // 1: the loader withholds the first V tile (bounded-wait test only)
+  int num_sms;      // multiprocessors of the current device (persistent grid size)
+  int* work_counter;  // device int, zero when the kernel starts (work-item claims)
 };
 
 struct DecodeArgs {
