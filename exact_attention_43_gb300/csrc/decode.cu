@@ -13,10 +13,11 @@
 //
 // GB300 design: the split kernel is bandwidth-bound (about 4 flops per cache
 // byte), so it moves K/V with contiguous bulk copies (cp.async.bulk, a chunk's
-// rows of one KV head are contiguous) through a 4-stage shared-memory ring
+// rows of one KV head are contiguous) through a 3-stage shared-memory ring of
+// 128-key sub-tiles (32 KB each; 2 CTAs per SM)
 // and reads every byte once for all query heads of the GQA group: the group's
 // query vectors live in registers, scores are formed with 8 lanes per key
-// (16-byte loads, 3 shuffle levels), the online max/sum run per 64-key
+// (16-byte loads, 3 shuffle levels), the online max/sum run per 128-key
 // sub-tile, and P V uses one lane per 4 output columns.  No tensor cores: the
 // contraction is too thin to pay for them and the bound is HBM.
 #include "internal.h"
@@ -31,11 +32,11 @@ namespace dec {
 
 __device__ unsigned g_status;
 
-constexpr int SUB = 64;        // keys per staged sub-tile
-constexpr int NST = 4;         // ring stages (each holds a K or a V sub-tile)
+constexpr int SUB = 128;       // keys per staged sub-tile (a multiple of 32)
+constexpr int NST = 3;         // ring stages (each holds a K or a V sub-tile)
 constexpr int THREADS = 256;   // 8 warps
 constexpr int WARPS = THREADS / 32;
-constexpr int KEYS_PER_WARP = SUB / WARPS;  // 8
+constexpr int KEYS_PER_WARP = SUB / WARPS;  // 16
 
 struct Params {
   const uint16_t* q;
@@ -199,16 +200,24 @@ __global__ void __launch_bounds__(THREADS) decode_split_kernel(const Params p) {
       if (threadIdx.x == 0 && i + NST < nload) issue(i + NST, pol);
       // online max / sum per head over this sub-tile (log2 units), one warp per head
       for (int g = warp; g < G; g += WARPS) {
-        const float a0 = sc[lane * G + g], a1 = sc[(lane + 32) * G + g];
-        float mx = fmaxf(a0, a1);
+        constexpr int PER_LANE = SUB / 32;
+        float sv[PER_LANE];
+#pragma unroll
+        for (int u = 0; u < PER_LANE; ++u) sv[u] = sc[(lane + 32 * u) * G + g];
+        float mx = sv[0];
+#pragma unroll
+        for (int u = 1; u < PER_LANE; ++u) mx = fmaxf(mx, sv[u]);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         const float m_old = m_run[g];
         const float m_new = fmaxf(m_old, mx);  // finite: key 0 of the sub-tile is valid
-        const float e0 = ex2(a0 - m_new), e1 = ex2(a1 - m_new);
-        sc[lane * G + g] = e0;
-        sc[(lane + 32) * G + g] = e1;
-        float sum = e0 + e1;
+        float sum = 0.f;
+#pragma unroll
+        for (int u = 0; u < PER_LANE; ++u) {
+          const float e = ex2(sv[u] - m_new);
+          sc[(lane + 32 * u) * G + g] = e;
+          sum += e;
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
         __syncwarp();

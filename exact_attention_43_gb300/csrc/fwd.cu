@@ -20,10 +20,11 @@
 //    epilogue has read it from TMEM);
 //  * warp 8 streams Q once and K, V 128-key tiles through a 4-stage ring with
 //    TMA (3-D tensor maps, 128-byte swizzle, mbarrier transaction counts);
-//  * warp 9 issues tcgen05.mma: S_i = Q_i K_j^T into TMEM, then
-//    O_i += P_i V_j with P read from TMEM and V from shared memory; per KV
-//    tile the order is PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), so while one
-//    warpgroup exponentiates, the tensor core works for the other;
+//  * warp 9 + i issues the tcgen05.mma of Q tile i: S_i = Q_i K_j^T into
+//    TMEM, then O_i += P_i V_j with P read from TMEM and V from shared
+//    memory, S_i(j+1) right after P_i V_j.  With one issuer per Q tile, each
+//    reacts to its own warpgroup at once and the tensor core interleaves the
+//    two streams: while one warpgroup exponentiates, it works for the other;
 //  * warpgroup i (warps 4i..4i+3) owns the rows of Q tile i, one row per
 //    thread (TMEM lane = row): load S, mask, row max, exponentiate with exp2
 //    (scale * log2 e folded into one FMA), accumulate the row sum, write P
@@ -53,9 +54,9 @@ constexpr int NQ = 2;               // Q tiles per CTA
 constexpr int BN = 128;             // keys per KV tile
 constexpr int NS = 4;               // K/V ring stages
 constexpr int NITEM = 4;            // claimed work items queued from the loader to the others
-constexpr int NUM_THREADS = 384;    // warpgroups 0, 1: softmax; warp 8 loader, warp 9 MMA
+constexpr int NUM_THREADS = 384;    // warpgroups 0, 1: softmax; warp 8 loader, warps 9, 10 MMA
 constexpr int LOADER_WARP = 8;
-constexpr int MMA_WARP = 9;
+constexpr int MMA_WARP = 9;         // warp 9 + i issues the MMAs of Q tile i
 constexpr float RESCALE_LOG2 = 8.0f;  // rescale O when the max grows by more than 2^8
 constexpr uint32_t TMEM_COLS = 512;
 // TMEM columns: S_i at 128 i (P_i overwrites its first 64 columns), O_i at 256 + 128 i
@@ -84,7 +85,8 @@ struct Layout {
   enum {
     Q_FULL, Q_EMPTY, RING_FULL, RING_EMPTY = RING_FULL + NS, S_FULL = RING_EMPTY + NS,
     P_FULL = S_FULL + NQ, O_DONE = P_FULL + NQ, O_FREE = O_DONE + NQ,
-    ITEM_FULL = O_FREE + NQ, ITEM_EMPTY = ITEM_FULL + NITEM, DRAIN = ITEM_EMPTY + NITEM, NUM_BARS
+    ITEM_FULL = O_FREE + NQ, ITEM_EMPTY = ITEM_FULL + NITEM, DRAIN = ITEM_EMPTY + NITEM,
+    NUM_BARS = DRAIN + NQ
   };
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;  // [0] TMEM base, [1] abort flag
   static constexpr int ITEM_OFF = MISC_OFF + 16;           // NITEM claimed work items
@@ -166,10 +168,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::Q_FULL), 1);
-    mbar_init(bar(L::Q_EMPTY), 1);
+    mbar_init(bar(L::Q_EMPTY), NQ);  // released by both MMA issuers
     for (int s = 0; s < NS; ++s) {
       mbar_init(bar(L::RING_FULL + s), 1);
-      mbar_init(bar(L::RING_EMPTY + s), 1);
+      mbar_init(bar(L::RING_EMPTY + s), NQ);
     }
     for (int i = 0; i < NQ; ++i) {
       mbar_init(bar(L::S_FULL + i), 1);
@@ -179,9 +181,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int q = 0; q < NITEM; ++q) {
       mbar_init(bar(L::ITEM_FULL + q), 1);
-      mbar_init(bar(L::ITEM_EMPTY + q), 1 + NQ * 4);  // the MMA thread and the 8 softmax warps
+      mbar_init(bar(L::ITEM_EMPTY + q), NQ + NQ * 4);  // the MMA issuers and the softmax warps
     }
-    mbar_init(bar(L::DRAIN), 1);
+    for (int i = 0; i < NQ; ++i) mbar_init(bar(L::DRAIN + i), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -261,41 +263,56 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       __syncwarp();
-    } else if (warp == MMA_WARP) {
-      // -------------------------------------------------------------- MMA issuer
+    } else if (warp == MMA_WARP || warp == MMA_WARP + 1) {
+      // ------------------------------------------------ MMA issuers, one per Q tile
+      const int qi = warp - MMA_WARP;
       if (lane == 0) {
         constexpr uint32_t idesc_qk = umma_idesc_f16(BF16, BM, BN, false, false);
         constexpr uint32_t idesc_pv = umma_idesc_f16(BF16, BM, D, false, true);
         auto ring_wait = [&](int ld) -> bool {
           return mbar_wait(bar(L::RING_FULL + ld % NS), (ld / NS) & 1, abort_flag, &g_status, lim);
         };
+        // Shared-memory descriptors are built once; every MMA then only adds a
+        // compile-time offset to the 14-bit start-address field (addresses stay
+        // below 256 KB, so the addition never carries out of the field).
+        const uint64_t q_desc = sdesc_sw128(sb + L::Q_OFF, 16, 1024);
+        const uint64_t k_desc = sdesc_sw128(sb + L::RING_OFF, 16, 1024);
+        const uint64_t v_desc = sdesc_sw128(sb + L::RING_OFF, L::REGION, 1024);
         auto issue_s = [&](int i, int ld) {  // S_i = Q_i K^T, K in the ring slot of load ld
-          const uint32_t k_base = sb + L::RING_OFF + (ld % NS) * L::TILE;
+          const uint64_t a0 = q_desc + (uint64_t)((i * L::TILE) >> 4);
+          const uint64_t b0 = k_desc + (uint64_t)(((ld % NS) * L::TILE) >> 4);
+          const uint32_t d = tmem + COL_S + 128u * i;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             // K-major operands: 16 columns = 32 bytes inside a 128-byte swizzled row
-            const uint32_t off = (kk >> 2) * L::REGION + (kk & 3) * 32;
-            const uint64_t adesc = sdesc_sw128(sb + L::Q_OFF + i * L::TILE + off, 16, 1024);
-            const uint64_t bdesc = sdesc_sw128(k_base + off, 16, 1024);
-            umma_ss(tmem + COL_S + 128u * i, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+            const uint32_t off = ((kk >> 2) * L::REGION + (kk & 3) * 32) >> 4;
+            umma_ss(d, a0 + off, b0 + off, idesc_qk, kk > 0 ? 1u : 0u);
           }
           umma_commit(bar(L::S_FULL + i));
         };
         auto issue_pv = [&](int i, int ld, bool acc) {  // O_i += P_i V, V in the ring slot of ld
-          const uint32_t v_base = sb + L::RING_OFF + (ld % NS) * L::TILE;
+          // V is [key][d] (d contiguous): MN-major B, 16 keys = 2 swizzle atoms of 8 rows;
+          // LBO steps to the next 64-column block of d, SBO to the next 8 keys.
+          const uint64_t b0 = v_desc + (uint64_t)(((ld % NS) * L::TILE) >> 4);
+          const uint32_t d = tmem + COL_O + 128u * i;
+          const uint32_t a = tmem + COL_S + 128u * i;
+          umma_ts(d, a, b0, idesc_pv, acc ? 1u : 0u);
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            // V is [key][d] (d contiguous): MN-major B, 16 keys = 2 swizzle atoms of 8 rows;
-            // LBO steps to the next 64-column block of d, SBO to the next 8 keys.
-            const uint64_t bdesc = sdesc_sw128(v_base + kk * 16 * 128, L::REGION, 1024);
-            umma_ts(tmem + COL_O + 128u * i, tmem + COL_S + 128u * i + kk * 8, bdesc, idesc_pv,
-                    (acc || kk > 0) ? 1u : 0u);
-          }
+          for (int kk = 1; kk < BN / 16; ++kk) umma_ts(d, a + kk * 8, b0 + kk * 128, idesc_pv, 1u);
         };
+        // This warp issues every MMA of Q tile qi: S_qi(j) and O_qi += P_qi V(j).
+        // K and V stages are shared with the other issuer, so each stage is
+        // released once by each of them: with a commit after the MMAs that read
+        // it, or with a plain arrive (after the stage filled, to stay in phase)
+        // when this Q tile does not need it.
         int ld = 0, k_item = 0;
-        int t_cnt[NQ] = {0, 0};  // tiles handed to warpgroup i so far (P_FULL phases)
-        int u_cnt[NQ] = {0, 0};  // items in which warpgroup i used its O accumulator
+        int t_cnt = 0;  // tiles handed to this warpgroup so far (S_FULL / P_FULL phases)
+        int u_cnt = 0;  // items in which this warpgroup used its O accumulator
         bool ok = true;
+        auto release = [&](int l, bool used) {
+          if (used) umma_commit(bar(L::RING_EMPTY + l % NS));
+          else mbar_arrive(bar(L::RING_EMPTY + l % NS));
+        };
         for (int r = 0; ok; ++r) {
           const int qs = r % NITEM;
           if (!(ok = mbar_wait(bar(L::ITEM_FULL + qs), (r / NITEM) & 1, abort_flag, &g_status, lim)))
@@ -310,56 +327,51 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int i = 0; i < NQ; ++i) tile_range(p, m_base + i * BM, &n_t[i], &mf[i]);
           const int n_kv = max(n_t[0], n_t[1]);
           if (n_kv == 0) continue;
+          const int nt = n_t[qi];
           if (!(ok = mbar_wait(bar(L::Q_FULL), k_item & 1, abort_flag, &g_status, lim))) break;
           ++k_item;
           const int base = ld;
+          ld = base + 2 * n_kv;
           if (!(ok = ring_wait(base))) break;
           tc_fence_after();
-          // S_i(0): P_i of the last item lives in these columns, read by an MMA issued earlier
-          for (int i = 0; i < NQ; ++i)
-            if (n_t[i] > 0) issue_s(i, base);
-          if (n_kv == 1) umma_commit(bar(L::Q_EMPTY));  // every S of the item is issued
-          umma_commit(bar(L::RING_EMPTY + base % NS));
-          for (int j = 0; ok && j < n_kv; ++j) {
+          // S(0): P of the last item lives in these columns, read by an MMA issued earlier
+          if (nt > 0) issue_s(qi, base);
+          release(base, nt > 0);
+          if (nt <= 1) {  // every S of this Q tile for the item is issued
+            if (nt == 1) umma_commit(bar(L::Q_EMPTY));
+            else mbar_arrive(bar(L::Q_EMPTY));
+          }
+          for (int j = 0; j < n_kv; ++j) {
             const int ld_v = base + 2 * j + 1, ld_k = base + 2 * j + 2;
             if (!(ok = ring_wait(ld_v))) break;
-            tc_fence_after();
-            bool k_ready = false;
-            for (int i = 0; i < NQ && ok; ++i) {
-              if (j < n_t[i]) {
-                if (!(ok = mbar_wait(bar(L::P_FULL + i), t_cnt[i] & 1, abort_flag, &g_status, lim)))
-                  break;
-                // the first P V of an item overwrites O_i: the last epilogue must have read it
-                if (j == 0 && u_cnt[i] > 0 &&
-                    !(ok = mbar_wait(bar(L::O_FREE + i), (u_cnt[i] - 1) & 1, abort_flag, &g_status,
-                                     lim)))
-                  break;
-                tc_fence_after();
-                issue_pv(i, ld_v, j > 0);
-                ++t_cnt[i];
-                if (j == n_t[i] - 1) {
-                  umma_commit(bar(L::O_DONE + i));
-                  ++u_cnt[i];
-                }
-              }
-              if (j + 1 < n_t[i]) {
-                if (!k_ready) {
-                  if (!(ok = ring_wait(ld_k))) break;
-                  tc_fence_after();
-                  k_ready = true;
-                }
-                issue_s(i, ld_k);  // after PV_i(j), which read P_i from these columns
+            if (j < nt) {
+              if (!(ok = mbar_wait(bar(L::P_FULL + qi), t_cnt & 1, abort_flag, &g_status, lim))) break;
+              // the first P V of an item overwrites O: the last epilogue must have read it
+              if (j == 0 && u_cnt > 0 &&
+                  !(ok = mbar_wait(bar(L::O_FREE + qi), (u_cnt - 1) & 1, abort_flag, &g_status, lim)))
+                break;
+              tc_fence_after();
+              issue_pv(qi, ld_v, j > 0);
+              ++t_cnt;
+              if (j == nt - 1) {
+                umma_commit(bar(L::O_DONE + qi));
+                ++u_cnt;
               }
             }
-            if (!ok) break;
-            if (j == n_kv - 2) umma_commit(bar(L::Q_EMPTY));  // the item's last S was issued
-            umma_commit(bar(L::RING_EMPTY + ld_v % NS));
-            if (k_ready) umma_commit(bar(L::RING_EMPTY + ld_k % NS));
+            release(ld_v, j < nt);
+            if (j + 1 < n_kv) {
+              if (!(ok = ring_wait(ld_k))) break;
+              if (j + 1 < nt) {
+                tc_fence_after();
+                issue_s(qi, ld_k);  // after P V(j), which read P from these columns
+                if (j + 1 == nt - 1) umma_commit(bar(L::Q_EMPTY));  // this tile's last S
+              }
+              release(ld_k, j + 1 < nt);
+            }
           }
-          ld = base + 2 * n_kv;
         }
-        umma_commit(bar(L::DRAIN));  // fires once every MMA issued above has completed
-        drain_wait(bar(L::DRAIN), 0, lim);
+        umma_commit(bar(L::DRAIN + qi));  // fires once every MMA issued above has completed
+        drain_wait(bar(L::DRAIN + qi), 0, lim);
       }
       __syncwarp();
     }
@@ -422,28 +434,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (key > lim_key || key >= p.Skv) x[j] = mval;
           }
         }
-        float red;
+        // row max (min when scale < 0): chain u covers x[u + 8k], k = 0..15, with
+        // three-input max: (k = 0, 1, 2), then (3, 4), ..., (13, 14), then k = 15
+        static_assert(BN == 128, "chains below cover exactly 128 columns");
+        float a[8];
         if (!p.neg) {
-          float a0 = x[0], a1 = x[1], a2 = x[2], a3 = x[3];
 #pragma unroll
-          for (int j = 4; j < BN; j += 4) {
-            a0 = fmaxf(a0, x[j]);
-            a1 = fmaxf(a1, x[j + 1]);
-            a2 = fmaxf(a2, x[j + 2]);
-            a3 = fmaxf(a3, x[j + 3]);
+          for (int u = 0; u < 8; ++u) {
+            a[u] = fmax3(x[u], x[u + 8], x[u + 16]);
+#pragma unroll
+            for (int k = 3; k < 15; k += 2) a[u] = fmax3(a[u], x[u + 8 * k], x[u + 8 * k + 8]);
+            a[u] = fmaxf(a[u], x[u + 120]);
           }
-          red = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+          a[0] = fmax3(a[0], a[1], a[2]);
+          a[3] = fmax3(a[3], a[4], a[5]);
+          a[0] = fmax3(a[0], a[3], fmaxf(a[6], a[7]));
         } else {
-          float a0 = x[0], a1 = x[1], a2 = x[2], a3 = x[3];
 #pragma unroll
-          for (int j = 4; j < BN; j += 4) {
-            a0 = fminf(a0, x[j]);
-            a1 = fminf(a1, x[j + 1]);
-            a2 = fminf(a2, x[j + 2]);
-            a3 = fminf(a3, x[j + 3]);
+          for (int u = 0; u < 8; ++u) {
+            a[u] = fmin3(x[u], x[u + 8], x[u + 16]);
+#pragma unroll
+            for (int k = 3; k < 15; k += 2) a[u] = fmin3(a[u], x[u + 8 * k], x[u + 8 * k + 8]);
+            a[u] = fminf(a[u], x[u + 120]);
           }
-          red = fminf(fminf(a0, a1), fminf(a2, a3));
+          a[0] = fmin3(a[0], a[1], a[2]);
+          a[3] = fmin3(a[3], a[4], a[5]);
+          a[0] = fmin3(a[0], a[3], fminf(a[6], a[7]));
         }
+        const float red = a[0];
         const float m_tile = red * c2;  // -inf when every key of the tile is masked
         const float m_new = fmaxf(m_used, m_tile);
         const bool grow = m_new > m_used + RESCALE_LOG2;

@@ -358,6 +358,19 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Three-input max / min (one instruction on sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Two floats -> one 32-bit word of two 16-bit values, `lo` in the low half (round to nearest even).
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
