@@ -139,6 +139,23 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(seconds, device=None):
+    """The slowest rank's time (every rank gets it); the local value when not distributed."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return seconds
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t)
+
+
+def whole_job_value(roofline_s_per_step, steps, world, max_seconds):
+    """Percent of one GPU's roofline, summed over the replicas (every rank runs the full step)."""
+    return 100.0 * world * roofline_s_per_step * steps / max_seconds
+
+
 def roofline_time(fwd_flops, dec_bytes, peaks):
     return fwd_flops / (peaks["bf16_tflops"] * 1e12) + dec_bytes / (peaks["hbm_gbs"] * 1e9)
 
@@ -311,10 +328,7 @@ def main():
     t_dec = statistics.mean(b.elapsed_time(c) for _, b, c in ev) / 1e3
     if ea.check_device_status() != 0:
         raise RuntimeError("device status error in the timed region")
-    if world > 1:
-        t = torch.tensor([total_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_s = float(t)
+    total_s = max_over_ranks(total_s, dev)
 
     # ------------------------------------------------ end to end from pinned host buffers
     e2e = None
@@ -353,17 +367,14 @@ def main():
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_s = e0.elapsed_time(e1) / 1e3
-        if world > 1:
-            t = torch.tensor([e2e_s], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_s = float(t)
-        e2e = {"value": 100.0 * (world * roofline_time(fwd_flops, dec_bytes, peaks)
-                            * args.e2e_steps) / e2e_s, "unit": UNIT,
+        e2e_s = max_over_ranks(e2e_s, dev)
+        e2e = {"value": whole_job_value(roofline_time(fwd_flops, dec_bytes, peaks),
+                                        args.e2e_steps, world, e2e_s), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": args.e2e_steps, "ms_per_step": 1e3 * e2e_s / args.e2e_steps}
 
     rt = roofline_time(fwd_flops, dec_bytes, peaks)
-    value = 100.0 * (world * rt * args.steps) / total_s
+    value = whole_job_value(rt, args.steps, world, total_s)
 
     if rank == 0:
         cpu = None
