@@ -20,11 +20,17 @@
 //    epilogue has read it from TMEM);
 //  * warp 8 streams Q once and K, V 128-key tiles through a 4-stage ring with
 //    TMA (3-D tensor maps, 128-byte swizzle, mbarrier transaction counts);
-//  * warp 9 + i issues the tcgen05.mma of Q tile i: S_i = Q_i K_j^T into
-//    TMEM, then O_i += P_i V_j with P read from TMEM and V from shared
-//    memory, S_i(j+1) right after P_i V_j.  With one issuer per Q tile, each
-//    reacts to its own warpgroup at once and the tensor core interleaves the
-//    two streams: while one warpgroup exponentiates, it works for the other;
+//  * one thread of warp 9 issues every tcgen05.mma: S_i = Q_i K_j^T into TMEM,
+//    O_i += P_i V_j with P read from TMEM and V from shared memory.  Per KV
+//    tile the order is P_0 V(j), S_0(j+1), P_1 V(j), S_1(j+1): S_0 completes a
+//    whole tile's MMAs before S_1, so softmax 0 runs while the tensor core
+//    works for Q tile 1 and the other way round.  (Two issuers, one per Q
+//    tile, let the tensor core interleave both streams; both S tiles then
+//    finish together and the two softmax warpgroups fall into step, leaving
+//    the tensor core idle while both exponentiate.)  No commit frees a ring
+//    slot: Q tile 1 runs every KV tile of an item and S_1(j+1) is issued after
+//    every MMA that reads K(j+1) or V(j), so softmax warpgroup 1, which waits
+//    for each S_1 anyway, frees both slots with two plain arrives;
 //  * warpgroup i (warps 4i..4i+3) owns the rows of Q tile i, one row per
 //    thread (TMEM lane = row): load S, mask, row max, exponentiate with exp2
 //    (scale * log2 e folded into one FMA), accumulate the row sum, write P
@@ -54,9 +60,10 @@ constexpr int NQ = 2;               // Q tiles per CTA
 constexpr int BN = 128;             // keys per KV tile
 constexpr int NS = 4;               // K/V ring stages
 constexpr int NITEM = 4;            // claimed work items queued from the loader to the others
-constexpr int NUM_THREADS = 384;    // warpgroups 0, 1: softmax; warp 8 loader, warps 9, 10 MMA
+constexpr int NUM_THREADS = 384;    // warpgroups 0, 1: softmax; warp 8 loader, warp 9 MMA
+                                    // (warps 10, 11 only lend their registers to the softmax)
 constexpr int LOADER_WARP = 8;
-constexpr int MMA_WARP = 9;         // warp 9 + i issues the MMAs of Q tile i
+constexpr int MMA_WARP = 9;         // issues the MMAs of both Q tiles
 constexpr float RESCALE_LOG2 = 8.0f;  // rescale O when the max grows by more than 2^8
 constexpr uint32_t TMEM_COLS = 512;
 // TMEM columns: S_i at 128 i (P_i overwrites its first 64 columns), O_i at 256 + 128 i
@@ -86,7 +93,7 @@ struct Layout {
     Q_FULL, Q_EMPTY, RING_FULL, RING_EMPTY = RING_FULL + NS, S_FULL = RING_EMPTY + NS,
     P_FULL = S_FULL + NQ, O_DONE = P_FULL + NQ, O_FREE = O_DONE + NQ,
     ITEM_FULL = O_FREE + NQ, ITEM_EMPTY = ITEM_FULL + NITEM, DRAIN = ITEM_EMPTY + NITEM,
-    NUM_BARS = DRAIN + NQ
+    NUM_BARS = DRAIN + 1
   };
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;  // [0] TMEM base, [1] abort flag
   static constexpr int ITEM_OFF = MISC_OFF + 16;           // NITEM claimed work items
@@ -151,6 +158,7 @@ __device__ __forceinline__ void decode_item(const Params& p, int w, int* mb, int
   *hq = hb % p.Hq;
 }
 
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -168,10 +176,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::Q_FULL), 1);
-    mbar_init(bar(L::Q_EMPTY), NQ);  // released by both MMA issuers
+    mbar_init(bar(L::Q_EMPTY), 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(bar(L::RING_FULL + s), 1);
-      mbar_init(bar(L::RING_EMPTY + s), NQ);
+      mbar_init(bar(L::RING_EMPTY + s), 1);  // freed by softmax warpgroup 1 (see there)
     }
     for (int i = 0; i < NQ; ++i) {
       mbar_init(bar(L::S_FULL + i), 1);
@@ -181,9 +189,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int q = 0; q < NITEM; ++q) {
       mbar_init(bar(L::ITEM_FULL + q), 1);
-      mbar_init(bar(L::ITEM_EMPTY + q), NQ + NQ * 4);  // the MMA issuers and the softmax warps
+      mbar_init(bar(L::ITEM_EMPTY + q), 1 + NQ * 4);  // the MMA issuer and the softmax warps
     }
-    for (int i = 0; i < NQ; ++i) mbar_init(bar(L::DRAIN + i), 1);
+    mbar_init(bar(L::DRAIN), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -263,9 +271,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       __syncwarp();
-    } else if (warp == MMA_WARP || warp == MMA_WARP + 1) {
-      // ------------------------------------------------ MMA issuers, one per Q tile
-      const int qi = warp - MMA_WARP;
+    } else if (warp == MMA_WARP) {
+      // ---------------------------------------------------------- MMA issuer
       if (lane == 0) {
         constexpr uint32_t idesc_qk = umma_idesc_f16(BF16, BM, BN, false, false);
         constexpr uint32_t idesc_pv = umma_idesc_f16(BF16, BM, D, false, true);
@@ -300,19 +307,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int kk = 1; kk < BN / 16; ++kk) umma_ts(d, a + kk * 8, b0 + kk * 128, idesc_pv, 1u);
         };
-        // This warp issues every MMA of Q tile qi: S_qi(j) and O_qi += P_qi V(j).
-        // K and V stages are shared with the other issuer, so each stage is
-        // released once by each of them: with a commit after the MMAs that read
-        // it, or with a plain arrive (after the stage filled, to stay in phase)
-        // when this Q tile does not need it.
+        // One thread issues every MMA of both Q tiles, per KV tile j in the order
+        // P_0 V(j), S_0(j+1), P_1 V(j), S_1(j+1).  S_0(j+1) then completes a full
+        // tile's worth of MMAs before S_1(j+1), so softmax 0 runs while the tensor
+        // pipe works for Q tile 1 and the other way round: the two softmax
+        // warpgroups alternate instead of falling into step with each other.
         int ld = 0, k_item = 0;
-        int t_cnt = 0;  // tiles handed to this warpgroup so far (S_FULL / P_FULL phases)
-        int u_cnt = 0;  // items in which this warpgroup used its O accumulator
+        int t_cnt[NQ] = {}, u_cnt[NQ] = {};  // P_FULL phases, items that used O_i
         bool ok = true;
-        auto release = [&](int l, bool used) {
-          if (used) umma_commit(bar(L::RING_EMPTY + l % NS));
-          else mbar_arrive(bar(L::RING_EMPTY + l % NS));
-        };
         for (int r = 0; ok; ++r) {
           const int qs = r % NITEM;
           if (!(ok = mbar_wait(bar(L::ITEM_FULL + qs), (r / NITEM) & 1, abort_flag, &g_status, lim)))
@@ -327,7 +329,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int i = 0; i < NQ; ++i) tile_range(p, m_base + i * BM, &n_t[i], &mf[i]);
           const int n_kv = max(n_t[0], n_t[1]);
           if (n_kv == 0) continue;
-          const int nt = n_t[qi];
+          n_t[1] = n_kv;  // tile 1 covers every KV tile (its rows are masked or past Sq)
           if (!(ok = mbar_wait(bar(L::Q_FULL), k_item & 1, abort_flag, &g_status, lim))) break;
           ++k_item;
           const int base = ld;
@@ -335,43 +337,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (!(ok = ring_wait(base))) break;
           tc_fence_after();
           // S(0): P of the last item lives in these columns, read by an MMA issued earlier
-          if (nt > 0) issue_s(qi, base);
-          release(base, nt > 0);
-          if (nt <= 1) {  // every S of this Q tile for the item is issued
-            if (nt == 1) umma_commit(bar(L::Q_EMPTY));
-            else mbar_arrive(bar(L::Q_EMPTY));
-          }
-          for (int j = 0; j < n_kv; ++j) {
+          for (int i = 0; i < NQ; ++i)
+            if (n_t[i] > 0) issue_s(i, base);
+          if (n_kv == 1) umma_commit(bar(L::Q_EMPTY));  // every S of the item is issued
+          for (int j = 0; j < n_kv && ok; ++j) {
             const int ld_v = base + 2 * j + 1, ld_k = base + 2 * j + 2;
             if (!(ok = ring_wait(ld_v))) break;
-            if (j < nt) {
-              if (!(ok = mbar_wait(bar(L::P_FULL + qi), t_cnt & 1, abort_flag, &g_status, lim))) break;
+            bool k_ready = false;
+            for (int i = 0; i < NQ; ++i) {
+              if (j >= n_t[i]) continue;
+              if (!(ok = mbar_wait(bar(L::P_FULL + i), t_cnt[i] & 1, abort_flag, &g_status, lim))) break;
               // the first P V of an item overwrites O: the last epilogue must have read it
-              if (j == 0 && u_cnt > 0 &&
-                  !(ok = mbar_wait(bar(L::O_FREE + qi), (u_cnt - 1) & 1, abort_flag, &g_status, lim)))
+              if (j == 0 && u_cnt[i] > 0 &&
+                  !(ok = mbar_wait(bar(L::O_FREE + i), (u_cnt[i] - 1) & 1, abort_flag, &g_status, lim)))
                 break;
               tc_fence_after();
-              issue_pv(qi, ld_v, j > 0);
-              ++t_cnt;
-              if (j == nt - 1) {
-                umma_commit(bar(L::O_DONE + qi));
-                ++u_cnt;
+              issue_pv(i, ld_v, j > 0);
+              ++t_cnt[i];
+              if (j == n_t[i] - 1) {
+                umma_commit(bar(L::O_DONE + i));
+                ++u_cnt[i];
+              }
+              if (j + 1 < n_t[i]) {
+                if (!k_ready) {
+                  if (!(ok = ring_wait(ld_k))) break;
+                  tc_fence_after();
+                  k_ready = true;
+                }
+                issue_s(i, ld_k);  // after P_i V(j), which read P_i from these columns
               }
             }
-            release(ld_v, j < nt);
-            if (j + 1 < n_kv) {
-              if (!(ok = ring_wait(ld_k))) break;
-              if (j + 1 < nt) {
-                tc_fence_after();
-                issue_s(qi, ld_k);  // after P V(j), which read P from these columns
-                if (j + 1 == nt - 1) umma_commit(bar(L::Q_EMPTY));  // this tile's last S
-              }
-              release(ld_k, j + 1 < nt);
-            }
+            if (!ok) break;
+            // ring slots are freed once S_1 completes (see softmax warpgroup 1)
+            if (j + 2 == n_kv) umma_commit(bar(L::Q_EMPTY));  // the item's last S is issued
           }
         }
-        umma_commit(bar(L::DRAIN + qi));  // fires once every MMA issued above has completed
-        drain_wait(bar(L::DRAIN + qi), 0, lim);
+        umma_commit(bar(L::DRAIN));  // fires once every MMA issued above has completed
+        drain_wait(bar(L::DRAIN), 0, lim);
       }
       __syncwarp();
     }
@@ -406,6 +408,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int row = m0 + r_lane;
       int n_tiles, mfrom;
       tile_range(p, m0, &n_tiles, &mfrom);
+      if (qi == 1) {
+        // tile 1 runs every KV tile of the item, also when it lies past Sq: the
+        // completions of its S MMAs free the K/V ring slots
+        int n0, mf0;
+        tile_range(p, m0 - BM, &n0, &mf0);
+        if (n0 > n_tiles) {
+          n_tiles = n0;
+          mfrom = 0;
+        }
+      }
       if (n_tiles == 0) {  // this Q tile sees no key (or lies past Sq)
         if (row < p.Sq) zero_row(p, bh, row, D);
         continue;
@@ -415,6 +427,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int t = 0; t < n_tiles; ++t, ++t_cnt) {
         if (!(ok = wait_warp(bar(L::S_FULL + qi), t_cnt & 1))) break;
         tc_fence_after();
+        if (qi == 1 && r_lane == 0) {
+          // Q tile 1 runs every KV tile, so S_1 number t_cnt read the K of load 2 t_cnt
+          // (loads alternate K, V).  It was issued after every MMA that reads that K
+          // or the V before it (order P_0 V(j), S_0(j+1), P_1 V(j), S_1(j+1), and across
+          // items the last P_1 V before the next S_1(0)), so its completion frees both
+          // ring slots.  This warpgroup consumes every completion of S_1 in order and
+          // the next S_1 needs its P, which keeps the ring protocol exact.
+          if (t_cnt > 0) mbar_arrive(bar(L::RING_EMPTY + (2 * t_cnt - 1) % NS));
+          mbar_arrive(bar(L::RING_EMPTY + (2 * t_cnt) % NS));
+        }
         float x[BN];
         {
           uint32_t rr[BN];
@@ -487,18 +509,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         const float mu = (m_used == -INFINITY) ? 0.f : m_used;
-        float ls0 = 0.f, ls1 = 0.f;
+        const uint64_t c2p = f2_pack(c2, c2), nmu = f2_pack(-mu, -mu);
+        uint64_t ls = f2_pack(0.f, 0.f);
         uint32_t pk[BN / 2];
 #pragma unroll
         for (int i = 0; i < BN / 2; ++i) {
-          const float e0 = ex2(fmaf(x[2 * i], c2, -mu));
-          const float e1 = ex2(fmaf(x[2 * i + 1], c2, -mu));
-          ls0 += e0;
-          ls1 += e1;
+          const uint64_t xy = fma2(f2_pack(x[2 * i], x[2 * i + 1]), c2p, nmu);
+          float a0, a1;
+          f2_unpack(xy, a0, a1);
+          const uint64_t e = f2_pack(ex2(a0), ex2(a1));
+          ls = add2(ls, e);
+          float e0, e1;
+          f2_unpack(e, e0, e1);
           pk[i] = pack2<BF16>(e0, e1);
         }
         tmem_st(t_s, pk);  // P over the S columns already consumed
-        l_sum += ls0 + ls1;
+        {
+          float s0, s1;
+          f2_unpack(ls, s0, s1);
+          l_sum += s0 + s1;
+        }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(L::P_FULL + qi));
