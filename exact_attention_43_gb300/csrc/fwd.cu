@@ -43,8 +43,10 @@
 //    multiplied (abaddon flash_attention_f16, causal `break`); only tiles
 //    that cross the diagonal or the end of the keys are masked element-wise.
 //    Alignment is bottom-right: key j is visible to row i iff j <= i + (Skv - Sq);
-//  * epilogue: O / l rounded to the input dtype, LSE = ln 2 * (m + log2 l);
-//    a row with no visible key gets O = 0, LSE = -inf.
+//  * epilogue: O / l rounded to the input dtype and written through a
+//    128-byte-swizzled shared-memory staging region per warpgroup with TMA
+//    stores (rows past Sq fall outside the tensor map); LSE = ln 2 * (m +
+//    log2 l); a row with no visible key gets O = 0, LSE = -inf.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -88,12 +90,13 @@ struct Layout {
   static constexpr int TILE = NREG * REGION;  // a 128 x D 16-bit tile
   static constexpr int Q_OFF = 0;             // Q_0, Q_1
   static constexpr int RING_OFF = Q_OFF + NQ * TILE;
-  static constexpr int BAR_OFF = RING_OFF + NS * TILE;
+  static constexpr int STAGE_OFF = RING_OFF + NS * TILE;  // O staging: one region per Q tile
+  static constexpr int BAR_OFF = STAGE_OFF + NQ * REGION;
   enum {
     Q_FULL, Q_EMPTY, RING_FULL, RING_EMPTY = RING_FULL + NS, S_FULL = RING_EMPTY + NS,
     P_FULL = S_FULL + NQ, O_DONE = P_FULL + NQ, O_FREE = O_DONE + NQ,
     ITEM_FULL = O_FREE + NQ, ITEM_EMPTY = ITEM_FULL + NITEM, DRAIN = ITEM_EMPTY + NITEM,
-    NUM_BARS = DRAIN + 1
+    STAGE_FREE = DRAIN + 1, STAGE_FULL = STAGE_FREE + NQ, NUM_BARS = STAGE_FULL + NQ
   };
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;  // [0] TMEM base, [1] abort flag
   static constexpr int ITEM_OFF = MISC_OFF + 16;           // NITEM claimed work items
@@ -162,7 +165,8 @@ __device__ __forceinline__ void decode_item(const Params& p, int w, int* mb, int
 template <int D, bool BF16>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                    const __grid_constant__ CUtensorMap tmv, const Params p) {
+                    const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
+                    const Params p) {
   using L = Layout<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
@@ -192,6 +196,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(bar(L::ITEM_EMPTY + q), 1 + NQ * 4);  // the MMA issuer and the softmax warps
     }
     mbar_init(bar(L::DRAIN), 1);
+    for (int i = 0; i < NQ; ++i) {
+      mbar_init(bar(L::STAGE_FREE + i), 1);   // the warpgroup's store thread
+      mbar_init(bar(L::STAGE_FULL + i), BM);  // every thread of the warpgroup
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -200,6 +208,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     prefetch_tmap(&tmq);
     prefetch_tmap(&tmk);
     prefetch_tmap(&tmv);
+    prefetch_tmap(&tmo);
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(misc), TMEM_COLS);
@@ -340,10 +349,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int i = 0; i < NQ; ++i)
             if (n_t[i] > 0) issue_s(i, base);
           if (n_kv == 1) umma_commit(bar(L::Q_EMPTY));  // every S of the item is issued
+#pragma unroll 2
           for (int j = 0; j < n_kv && ok; ++j) {
             const int ld_v = base + 2 * j + 1, ld_k = base + 2 * j + 2;
+            // The tensor core queues only a couple of MMAs, so every wait between two
+            // MMAs idles it: V(j) and K(j+1) are awaited here, once per step, and
+            // each Q tile's P V and S MMAs then go out back to back.
             if (!(ok = ring_wait(ld_v))) break;
-            bool k_ready = false;
+            if (j + 1 < n_kv && !(ok = ring_wait(ld_k))) break;
             for (int i = 0; i < NQ; ++i) {
               if (j >= n_t[i]) continue;
               if (!(ok = mbar_wait(bar(L::P_FULL + i), t_cnt[i] & 1, abort_flag, &g_status, lim))) break;
@@ -358,14 +371,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 umma_commit(bar(L::O_DONE + i));
                 ++u_cnt[i];
               }
-              if (j + 1 < n_t[i]) {
-                if (!k_ready) {
-                  if (!(ok = ring_wait(ld_k))) break;
-                  tc_fence_after();
-                  k_ready = true;
-                }
-                issue_s(i, ld_k);  // after P_i V(j), which read P_i from these columns
-              }
+              if (j + 1 < n_t[i]) issue_s(i, ld_k);  // after P_i V(j), which read P_i from these columns
             }
             if (!ok) break;
             // ring slots are freed once S_1 completes (see softmax warpgroup 1)
@@ -392,7 +398,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto wait_warp = [&](uint32_t b_, uint32_t ph_) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(b_, ph_, abort_flag, &g_status, lim));
     };
-    int t_cnt = 0, u_cnt = 0;
+    int t_cnt = 0, u_cnt = 0, k_stage = 0;
     bool ok = true;
     for (int r = 0; ok; ++r) {
       const int qs = r % NITEM;
@@ -422,7 +428,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (row < p.Sq) zero_row(p, bh, row, D);
         continue;
       }
-      const int lim_key = p.causal ? row + (p.Skv - p.Sq) : 0x7fffffff;
+      // the last key this row may see (negative: none)
+      const int last_key = p.causal ? min(row + (p.Skv - p.Sq), p.Skv - 1) : p.Skv - 1;
       float m_used = -INFINITY, l_sum = 0.f;
       for (int t = 0; t < n_tiles; ++t, ++t_cnt) {
         if (!(ok = wait_warp(bar(L::S_FULL + qi), t_cnt & 1))) break;
@@ -449,12 +456,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int j = 0; j < BN; ++j) x[j] = 0.f;
         }
         if (t >= mfrom) {
-          const int kbase = t * BN;
+          // keys [t BN, t BN + vis) of this tile are visible: one compare and select per key
+          const int vis = last_key + 1 - t * BN;
 #pragma unroll
-          for (int j = 0; j < BN; ++j) {
-            const int key = kbase + j;
-            if (key > lim_key || key >= p.Skv) x[j] = mval;
-          }
+          for (int j = 0; j < BN; ++j) x[j] = (j < vis) ? x[j] : mval;
         }
         // row max (min when scale < 0): chain u covers x[u + 8k], k = 0..15, with
         // three-input max: (k = 0, 1, 2), then (3, 4), ..., (13, 14), then k = 15
@@ -542,21 +547,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tmem_ld(t_o, orow);
       tc_fence_before();
       mbar_arrive(bar(L::O_FREE + qi));
-      if (row < p.Sq) {
-        const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + ((size_t)bh * p.Sq + row) * D);
+      const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
+      // O / l goes out through this warpgroup's staging region (128 rows x 64
+      // columns, the 128-byte swizzle of the tensor map: 16-byte chunk c of row r
+      // at chunk c ^ (r mod 8), so a warp's stores hit every bank once) and one
+      // TMA store per 64 columns; rows past Sq fall outside the tensor map and
+      // are not written.
+      const uint32_t stage = sb + L::STAGE_OFF + qi * L::REGION;
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c)
-          dst[c] = make_uint4(
-              pack2<BF16>(__uint_as_float(orow[8 * c + 0]) * inv_l, __uint_as_float(orow[8 * c + 1]) * inv_l),
-              pack2<BF16>(__uint_as_float(orow[8 * c + 2]) * inv_l, __uint_as_float(orow[8 * c + 3]) * inv_l),
-              pack2<BF16>(__uint_as_float(orow[8 * c + 4]) * inv_l, __uint_as_float(orow[8 * c + 5]) * inv_l),
-              pack2<BF16>(__uint_as_float(orow[8 * c + 6]) * inv_l, __uint_as_float(orow[8 * c + 7]) * inv_l));
-        if (p.lse)
-          p.lse[(size_t)bh * p.Sq + row] =
-              l_sum > 0.f ? (m_used + log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
+      for (int h = 0; h < D / 64; ++h, ++k_stage) {
+        if (r_lane == 0) {
+          bulk_wait_read_all();  // the last store has read the region
+          mbar_arrive(bar(L::STAGE_FREE + qi));
+        }
+        if (!(ok = wait_warp(bar(L::STAGE_FREE + qi), k_stage & 1))) break;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const int col = 64 * h + 8 * c;
+          const uint4 v = make_uint4(
+              pack2<BF16>(__uint_as_float(orow[col + 0]) * inv_l, __uint_as_float(orow[col + 1]) * inv_l),
+              pack2<BF16>(__uint_as_float(orow[col + 2]) * inv_l, __uint_as_float(orow[col + 3]) * inv_l),
+              pack2<BF16>(__uint_as_float(orow[col + 4]) * inv_l, __uint_as_float(orow[col + 5]) * inv_l),
+              pack2<BF16>(__uint_as_float(orow[col + 6]) * inv_l, __uint_as_float(orow[col + 7]) * inv_l));
+          st_shared_v4(stage + r_lane * 128 + ((c ^ (r_lane & 7)) << 4), v);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(L::STAGE_FULL + qi));
+        if (r_lane == 0) {
+          if (!(ok = mbar_wait(bar(L::STAGE_FULL + qi), k_stage & 1, abort_flag, &g_status, lim))) break;
+          tma_store_3d(&tmo, stage, 64 * h, m0, bh);
+          bulk_commit();
+        }
       }
+      if (!ok) break;
+      if (p.lse && row < p.Sq)
+        p.lse[(size_t)bh * p.Sq + row] =
+            l_sum > 0.f ? (m_used + log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
     }
+    if (r_lane == 0) bulk_wait_all();  // this warpgroup's O stores are complete
   }
 
   tc_fence_before();
@@ -597,8 +625,8 @@ static cudaError_t launch_t(const FwdArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, BF16>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
-  CUtensorMap tq, tk, tv;
-  if (!make_map(&tq, a.q, D, a.Sq, a.B * a.Hq, BF16) ||
+  CUtensorMap tq, tk, tv, to;
+  if (!make_map(&tq, a.q, D, a.Sq, a.B * a.Hq, BF16) || !make_map(&to, a.o, D, a.Sq, a.B * a.Hq, BF16) ||
       !make_map(&tk, a.k, D, a.Skv, a.B * a.Hkv, BF16) ||
       !make_map(&tv, a.v, D, a.Skv, a.B * a.Hkv, BF16))
     return cudaErrorInvalidValue;
@@ -631,7 +659,7 @@ static cudaError_t launch_t(const FwdArgs& a, cudaStream_t stream) {
   // persistent: one CTA per SM (or one per work item when there are fewer)
   const long long n_items = (long long)p.num_m_blocks * a.Hq * a.B;
   const int grid = (int)(n_items < a.num_sms ? n_items : a.num_sms);
-  attn_fwd_kernel<D, BF16><<<grid, NUM_THREADS, L::ALLOC, stream>>>(tq, tk, tv, p);
+  attn_fwd_kernel<D, BF16><<<grid, NUM_THREADS, L::ALLOC, stream>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 
