@@ -206,9 +206,12 @@ int attn_decode(const void* q, const void* k_cache, const void* v_cache, const i
   a.D = D;
   a.chunk = chunk_for(max_S, num_splits);
   a.max_chunks = max_S > 0 ? (max_S + a.chunk - 1) / a.chunk : 0;
+  // the split kernel numbers its (chunk, head group, sequence) items with an int
+  if ((long long)B * Hq * a.max_chunks > INT_MAX) return ATTN_ERR_UNSUPPORTED;
   a.scale = 1.0f / sqrtf((float)D);
   a.bf16 = dtype == ATTN_BF16;
   a.wait_limit_ns = g_wait_limit_ns;
+  a.num_sms = g_num_sms[dev] > 0 ? g_num_sms[dev] : 1;
 
   const size_t bytes = attn_decode_workspace_bytes(B, Hq, max_S, D, num_splits);
   void* ws = nullptr;
@@ -263,9 +266,12 @@ int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
   a.D = D;
   a.chunk = chunk_for(max_S, num_splits);
   a.max_chunks = max_S > 0 ? (max_S + a.chunk - 1) / a.chunk : 0;
+  // the split kernel numbers its (chunk, head group, sequence) items with an int
+  if ((long long)B * Hq * a.max_chunks > INT_MAX) return ATTN_ERR_UNSUPPORTED;
   a.scale = 1.0f / sqrtf((float)D);
   a.bf16 = dtype == ATTN_BF16;
   a.wait_limit_ns = g_wait_limit_ns;
+  a.num_sms = g_num_sms[dev] > 0 ? g_num_sms[dev] : 1;
   a.partials = scratch;
   return from_cuda(ea::launch_decode(a, stream));
 }

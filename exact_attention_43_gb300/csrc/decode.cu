@@ -14,12 +14,14 @@
 // GB300 design: the split kernel is bandwidth-bound (about 4 flops per cache
 // byte), so it moves K/V with contiguous bulk copies (cp.async.bulk, a chunk's
 // rows of one KV head are contiguous) through a 3-stage shared-memory ring of
-// 128-key sub-tiles (32 KB each; 2 CTAs per SM)
-// and reads every byte once for all query heads of the GQA group: the group's
-// query vectors live in registers, scores are formed with 8 lanes per key
-// (16-byte loads, 3 shuffle levels), the online max/sum run per 128-key
-// sub-tile, and P V uses one lane per 4 output columns.  No tensor cores: the
-// contraction is too thin to pay for them and the bound is HBM.
+// 128-key sub-tiles (32 KB each; 2 CTAs per SM) and reads every byte once for
+// all query heads of the GQA group.  A CTA takes up to four consecutive chunks
+// of one (sequence, KV head) and keeps its ring streaming across them, writing
+// one partial per chunk; the group's query vectors live in registers, scores
+// are formed with 8 lanes per key (16-byte loads, packed f32x2 FMAs, 3 shuffle
+// levels), the online max/sum run per 128-key sub-tile, and P V uses one lane
+// per 4 output columns with packed FMAs.  No tensor cores: the contraction is
+// too thin to pay for them and the bound is HBM.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -45,7 +47,8 @@ struct Params {
   const int32_t* seq_lens;
   float* part;
   uint16_t* o;
-  int Hq, Hkv, max_S, chunk, max_chunks, group, heads_per_cta;
+  int B, Hq, Hkv, max_S, chunk, max_chunks, group, heads_per_cta;
+  int cpb;  // consecutive chunks per split-kernel CTA
   float c2;  // scale * log2(e)
   uint64_t wait_limit_ns;
 };
@@ -62,17 +65,38 @@ __device__ __forceinline__ int clamp_len(const Params& p, int b) {
 template <int D, int G>
 struct SplitLayout {
   static constexpr int STAGE = SUB * D * 2;
+  static constexpr int GH = (G + 1) / 2;                      // heads per cross-warp reduction pass
   static constexpr int RING_OFF = 0;
   static constexpr int SC_OFF = RING_OFF + NST * STAGE;      // scores / probabilities [SUB][G]
-  static constexpr int STAT_OFF = SC_OFF + SUB * G * 4;      // m, l, alpha per head
-  static constexpr int BAR_OFF = (STAT_OFF + 3 * G * 4 + 15) / 16 * 16;  // NST barriers
+  static constexpr int RED_OFF = SC_OFF + SUB * G * 4;       // [WARPS][GH][D] P V partial sums
+  static constexpr int STAT_OFF = RED_OFF + WARPS * GH * D * 4;  // m, l, alpha per head
+  static constexpr int BAR_OFF = (STAT_OFF + 3 * G * 4 + 15) / 16 * 16;  // NST ring barriers
   static constexpr int ABORT_OFF = BAR_OFF + NST * 8;
   static constexpr int BYTES = ABORT_OFF + 16;
-  static_assert(WARPS * G * D * 4 <= NST * STAGE, "cross-warp reduction aliases the ring");
   static_assert(BAR_OFF % 8 == 0, "mbarriers need 8-byte alignment");
   static_assert(STAGE % 16 == 0 && RING_OFF % 16 == 0, "bulk copies need 16-byte alignment");
+  static_assert(SC_OFF % 16 == 0, "probabilities are read as float4");
 };
 
+// Two 16-bit values of one 32-bit word as an f32 pair (low half first), for the
+// packed f32x2 arithmetic.
+template <bool BF16>
+__device__ __forceinline__ uint64_t pair_of(uint32_t w) {
+  if constexpr (BF16) {
+    return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+  } else {
+    const float2 f = unpack2<false>(w);
+    return f2_pack(f.x, f.y);
+  }
+}
+
+// A CTA takes up to p.cpb consecutive chunks of one (sequence, KV head, head
+// group) and streams their K and V rows through one ring that does not drain
+// between its chunks (thread 0 issues load j + NST as soon as load j has been
+// consumed, whichever chunk it belongs to), writing one partial per chunk.  A
+// 512-key chunk is only 256 KB of K and V: with one CTA per chunk, each CTA's
+// first load and epilogue went unhidden (85 % of HBM bandwidth at chunk 512
+// against 94 % at chunk 2048).
 template <int D, int G, bool BF16>
 __global__ void __launch_bounds__(THREADS) decode_split_kernel(const Params p) {
   using L = SplitLayout<D, G>;
@@ -81,56 +105,57 @@ __global__ void __launch_bounds__(THREADS) decode_split_kernel(const Params p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t sb = smem_u32(smem);
   float* sc = reinterpret_cast<float*>(smem + L::SC_OFF);
+  float* red = reinterpret_cast<float*>(smem + L::RED_OFF);
   float* m_run = reinterpret_cast<float*>(smem + L::STAT_OFF);
   float* l_run = m_run + G;
   float* alpha_s = l_run + G;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::ABORT_OFF);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int c = blockIdx.x;
   const int kvh = blockIdx.y / (p.group / G);
   const int h0 = kvh * p.group + (blockIdx.y % (p.group / G)) * G;  // first query head of this CTA
   const int b = blockIdx.z;
   const int len = clamp_len(p, b);
-  const int n_chunks = (len + p.chunk - 1) / p.chunk;
-  if (c >= n_chunks) return;
-  const int k0 = c * p.chunk;
-  const int n = min(p.chunk, len - k0);
-  const int nsub = (n + SUB - 1) / SUB;
-  const int nload = 2 * nsub;  // K_0, V_0, K_1, V_1, ...
-  const size_t row0 = ((size_t)b * p.Hkv + kvh) * p.max_S + k0;
-  const uint16_t* kg = p.k + row0 * D;
-  const uint16_t* vg = p.v + row0 * D;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c0 = blockIdx.x * p.cpb;                                // first chunk of this CTA
+  const int c1 = min(c0 + p.cpb, (len + p.chunk - 1) / p.chunk);   // end of its chunks
+  if (c0 >= c1) return;
+  const size_t row0 = ((size_t)b * p.Hkv + kvh) * p.max_S;
+  auto chunk_rows = [&](int c) -> int { return min(p.chunk, len - c * p.chunk); };
+  auto ring_bar = [&](int j) -> uint32_t { return sb + L::BAR_OFF + 8 * (j % NST); };
 
-  int issued = 0;  // loads issued so far (thread 0 only)
-  auto issue = [&](int i, uint64_t pol) {  // called by thread 0 only, in increasing i
-    const int st = i % NST;
-    issued = i + 1;
-    const int sub = i >> 1;
-    const int rows = min(SUB, n - sub * SUB);
-    const uint16_t* src = ((i & 1) ? vg : kg) + (size_t)sub * SUB * D;
-    const uint32_t bar = sb + L::BAR_OFF + 8 * st;
-    mbar_expect_tx(bar, rows * D * 2);
-    bulk_load(sb + L::RING_OFF + st * L::STAGE, src, rows * D * 2, bar, pol);
-  };
-
+  // ------------------------------------------------ load stream (thread 0 only)
+  int l_c = c0, l_off = 0, l_nload = 2 * ((chunk_rows(c0) + SUB - 1) / SUB), issued = 0;
   uint64_t pol = 0;
+  auto issue_next = [&]() {  // the next K or V sub-tile of this CTA's chunks
+    if (l_c >= c1) return;
+    const int sub = l_off >> 1;
+    const int rows = min(SUB, chunk_rows(l_c) - sub * SUB);
+    const size_t r = row0 + (size_t)l_c * p.chunk + (size_t)sub * SUB;
+    const uint16_t* src = ((l_off & 1) ? p.v : p.k) + r * D;
+    const uint32_t bar = ring_bar(issued);
+    mbar_expect_tx(bar, rows * D * 2);
+    bulk_load(sb + L::RING_OFF + (issued % NST) * L::STAGE, src, rows * D * 2, bar, pol);
+    ++issued;
+    if (++l_off == l_nload && ++l_c < c1) {
+      l_off = 0;
+      l_nload = 2 * ((chunk_rows(l_c) + SUB - 1) / SUB);
+    }
+  };
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NST; ++i) mbar_init(sb + L::BAR_OFF + 8 * i, 1);
+    for (int i = 0; i < NST; ++i) mbar_init(ring_bar(i), 1);
     *abort_flag = 0;
     fence_barrier_init();
     pol = policy_evict_first();
-    for (int i = 0; i < min(NST, nload); ++i) issue(i, pol);
-  }
-  if (threadIdx.x < G) {
-    m_run[threadIdx.x] = -INFINITY;
-    l_run[threadIdx.x] = 0.f;
+    for (int i = 0; i < NST; ++i) issue_next();
   }
 
   // query vectors of the group, pre-multiplied by scale * log2 e, for this lane's key slice
-  // (8 lanes share a key; lane slice s owns elements [8 (8 v + s), 8 (8 v + s) + 8) for v < D / 64)
+  // (8 lanes share a key; lane slice s owns elements [8 (8 v + s), 8 (8 v + s) + 8) for v < D / 64),
+  // as pairs of consecutive elements for the packed f32x2 FMA
   const int slice = lane & 7;
-  float qr[G][EPL];
+  const uint64_t zero2 = f2_pack(0.f, 0.f);
+  const uint64_t c2p = f2_pack(p.c2, p.c2);
+  uint64_t qr[G][EPL / 2];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     const uint4* qs = reinterpret_cast<const uint4*>(p.q + ((size_t)b * p.Hq + h0 + g) * D);
@@ -139,171 +164,204 @@ __global__ void __launch_bounds__(THREADS) decode_split_kernel(const Params p) {
       const uint4 w = qs[v4 * 8 + slice];
       const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = unpack2<BF16>(ws[i]);
-        qr[g][v4 * 8 + 2 * i] = f.x * p.c2;
-        qr[g][v4 * 8 + 2 * i + 1] = f.y * p.c2;
-      }
+      for (int i = 0; i < 4; ++i) qr[g][v4 * 4 + i] = fma2(pair_of<BF16>(ws[i]), c2p, zero2);
     }
   }
-  float acc[G][DPL];
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) acc[g][e] = 0.f;
-  __syncthreads();
 
+  int gl = 0;  // loads consumed
   bool ok = true;
-  for (int sub = 0; sub < nsub && ok; ++sub) {
-    const int rows = min(SUB, n - sub * SUB);
-    // ---------------------------------------------------------------- scores
-    {
-      const int i = 2 * sub, st = i % NST;
-      ok = mbar_wait(sb + L::BAR_OFF + 8 * st, (i / NST) & 1, abort_flag, &g_status, p.wait_limit_ns);
-      if (__syncthreads_or(!ok)) { ok = false; break; }
-      const uint8_t* tile = smem + L::RING_OFF + st * L::STAGE;
+  for (int c = c0; c < c1; ++c) {
+    const int n = chunk_rows(c);
+    const int nsub = (n + SUB - 1) / SUB;
+    if (threadIdx.x < G) {
+      m_run[threadIdx.x] = -INFINITY;
+      l_run[threadIdx.x] = 0.f;
+    }
+    __syncthreads();
+    uint64_t acc[G][DPL / 2];  // P V accumulators, pairs of adjacent output columns
 #pragma unroll
-      for (int step = 0; step < KEYS_PER_WARP / 4; ++step) {
-        const int key = warp * KEYS_PER_WARP + step * 4 + (lane >> 3);
-        float dot[G];
+    for (int g = 0; g < G; ++g)
 #pragma unroll
-        for (int g = 0; g < G; ++g) dot[g] = 0.f;
-        if (key < rows) {
-          // lane slice s reads 16-byte chunks s, s + 8, ...: a quarter-warp covers 128
-          // contiguous bytes of one row, so the loads are free of bank conflicts
-          const uint4* kr = reinterpret_cast<const uint4*>(tile + key * D * 2);
+      for (int e = 0; e < DPL / 2; ++e) acc[g][e] = zero2;
+
+    for (int sub = 0; sub < nsub && ok; ++sub) {
+      const int rows = min(SUB, n - sub * SUB);
+      // -------------------------------------------------------------- scores
+      {
+        ok = mbar_wait(ring_bar(gl), (gl / NST) & 1, abort_flag, &g_status, p.wait_limit_ns);
+        if (__syncthreads_or(!ok)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* tile = smem + L::RING_OFF + (gl % NST) * L::STAGE;
 #pragma unroll
-          for (int v4 = 0; v4 < EPL / 8; ++v4) {
-            const uint4 w = kr[v4 * 8 + slice];
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        for (int step = 0; step < KEYS_PER_WARP / 4; ++step) {
+          const int key = warp * KEYS_PER_WARP + step * 4 + (lane >> 3);
+          uint64_t d2[G];
 #pragma unroll
-            for (int i2 = 0; i2 < 4; ++i2) {
-              const float2 f = unpack2<BF16>(ws[i2]);
+          for (int g = 0; g < G; ++g) d2[g] = zero2;
+          if (key < rows) {
+            // lane slice s reads 16-byte chunks s, s + 8, ...: a quarter-warp covers 128
+            // contiguous bytes of one row, so the loads are free of bank conflicts
+            const uint4* kr = reinterpret_cast<const uint4*>(tile + key * D * 2);
 #pragma unroll
-              for (int g = 0; g < G; ++g)
-                dot[g] = fmaf(qr[g][v4 * 8 + 2 * i2], f.x, fmaf(qr[g][v4 * 8 + 2 * i2 + 1], f.y, dot[g]));
+            for (int v4 = 0; v4 < EPL / 8; ++v4) {
+              const uint4 w = kr[v4 * 8 + slice];
+              const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+              for (int i2 = 0; i2 < 4; ++i2) {
+                const uint64_t kp = pair_of<BF16>(ws[i2]);
+#pragma unroll
+                for (int g = 0; g < G; ++g) d2[g] = fma2(qr[g][v4 * 4 + i2], kp, d2[g]);
+              }
+            }
+          }
+          float dot[G];
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            float lo, hi;
+            f2_unpack(d2[g], lo, hi);
+            dot[g] = lo + hi;
+            dot[g] += __shfl_xor_sync(0xffffffffu, dot[g], 1);
+            dot[g] += __shfl_xor_sync(0xffffffffu, dot[g], 2);
+            dot[g] += __shfl_xor_sync(0xffffffffu, dot[g], 4);
+          }
+          if (slice == 0) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) sc[key * G + g] = key < rows ? dot[g] : -INFINITY;
+          }
+        }
+        __syncthreads();  // scores visible; every read of this stage done
+        if (threadIdx.x == 0) issue_next();
+        ++gl;
+        // online max / sum per head over this sub-tile (log2 units), one warp per head
+        for (int g = warp; g < G; g += WARPS) {
+          constexpr int PER_LANE = SUB / 32;
+          float sv[PER_LANE];
+#pragma unroll
+          for (int u = 0; u < PER_LANE; ++u) sv[u] = sc[(lane + 32 * u) * G + g];
+          float mx = sv[0];
+#pragma unroll
+          for (int u = 1; u < PER_LANE; ++u) mx = fmaxf(mx, sv[u]);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          const float m_old = m_run[g];
+          const float m_new = fmaxf(m_old, mx);  // finite: key 0 of the sub-tile is valid
+          float sum = 0.f;
+#pragma unroll
+          for (int u = 0; u < PER_LANE; ++u) {
+            const float e = ex2(sv[u] - m_new);
+            sc[(lane + 32 * u) * G + g] = e;
+            sum += e;
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+          __syncwarp();
+          if (lane == 0) {
+            const float alpha = ex2(m_old - m_new);  // 0 on the first sub-tile
+            alpha_s[g] = alpha;
+            l_run[g] = l_run[g] * alpha + sum;
+            m_run[g] = m_new;
+          }
+        }
+        __syncthreads();
+      }
+      // ------------------------------------------------------------------ P V
+      {
+        ok = mbar_wait(ring_bar(gl), (gl / NST) & 1, abort_flag, &g_status, p.wait_limit_ns);
+        if (__syncthreads_or(!ok)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* tile = smem + L::RING_OFF + (gl % NST) * L::STAGE;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const uint64_t a2 = f2_pack(alpha_s[g], alpha_s[g]);
+#pragma unroll
+          for (int e = 0; e < DPL / 2; ++e) acc[g][e] = fma2(acc[g][e], a2, zero2);
+        }
+#pragma unroll
+        for (int kk = 0; kk < KEYS_PER_WARP; ++kk) {
+          const int key = warp * KEYS_PER_WARP + kk;
+          if (key < rows) {
+            uint64_t vv[DPL / 2];
+            if constexpr (DPL == 4) {
+              const uint2 w = *reinterpret_cast<const uint2*>(tile + key * D * 2 + lane * 8);
+              vv[0] = pair_of<BF16>(w.x);
+              vv[1] = pair_of<BF16>(w.y);
+            } else {
+              vv[0] = pair_of<BF16>(*reinterpret_cast<const uint32_t*>(tile + key * D * 2 + lane * 4));
+            }
+            // the group's probabilities of this key in one shared-memory load
+            float pr[G];
+            if constexpr (G % 4 == 0) {
+#pragma unroll
+              for (int q4 = 0; q4 < G / 4; ++q4) {
+                const float4 t = reinterpret_cast<const float4*>(sc + key * G)[q4];
+                pr[4 * q4] = t.x;
+                pr[4 * q4 + 1] = t.y;
+                pr[4 * q4 + 2] = t.z;
+                pr[4 * q4 + 3] = t.w;
+              }
+            } else if constexpr (G == 2) {
+              const float2 t = reinterpret_cast<const float2*>(sc)[key];
+              pr[0] = t.x;
+              pr[1] = t.y;
+            } else {
+              pr[0] = sc[key];
+            }
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              const uint64_t p2 = f2_pack(pr[g], pr[g]);
+#pragma unroll
+              for (int e = 0; e < DPL / 2; ++e) acc[g][e] = fma2(p2, vv[e], acc[g][e]);
             }
           }
         }
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          dot[g] += __shfl_xor_sync(0xffffffffu, dot[g], 1);
-          dot[g] += __shfl_xor_sync(0xffffffffu, dot[g], 2);
-          dot[g] += __shfl_xor_sync(0xffffffffu, dot[g], 4);
-        }
-        if (slice == 0) {
-#pragma unroll
-          for (int g = 0; g < G; ++g) sc[key * G + g] = key < rows ? dot[g] : -INFINITY;
-        }
+        __syncthreads();  // every read of this stage done
+        if (threadIdx.x == 0) issue_next();
+        ++gl;
       }
-      __syncthreads();  // scores visible; every read of this stage done
-      if (threadIdx.x == 0 && i + NST < nload) issue(i + NST, pol);
-      // online max / sum per head over this sub-tile (log2 units), one warp per head
-      for (int g = warp; g < G; g += WARPS) {
-        constexpr int PER_LANE = SUB / 32;
-        float sv[PER_LANE];
+    }
+    if (!ok) break;
+
+    // ---------------------------------------- partials: cross-warp sum of P V
+    const size_t pbase = (((size_t)b * p.Hq + h0) * p.max_chunks + c) * (D + 2);
+    const size_t hstride = (size_t)p.max_chunks * (D + 2);
 #pragma unroll
-        for (int u = 0; u < PER_LANE; ++u) sv[u] = sc[(lane + 32 * u) * G + g];
-        float mx = sv[0];
+    for (int pass = 0; pass < G / L::GH; ++pass) {
 #pragma unroll
-        for (int u = 1; u < PER_LANE; ++u) mx = fmaxf(mx, sv[u]);
+      for (int gg = 0; gg < L::GH; ++gg)
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        const float m_old = m_run[g];
-        const float m_new = fmaxf(m_old, mx);  // finite: key 0 of the sub-tile is valid
-        float sum = 0.f;
-#pragma unroll
-        for (int u = 0; u < PER_LANE; ++u) {
-          const float e = ex2(sv[u] - m_new);
-          sc[(lane + 32 * u) * G + g] = e;
-          sum += e;
+        for (int e = 0; e < DPL / 2; ++e) {
+          float lo, hi;
+          f2_unpack(acc[pass * L::GH + gg][e], lo, hi);
+          red[(warp * L::GH + gg) * D + lane * DPL + 2 * e] = lo;
+          red[(warp * L::GH + gg) * D + lane * DPL + 2 * e + 1] = hi;
         }
+      __syncthreads();
+      for (int idx = threadIdx.x; idx < L::GH * D; idx += THREADS) {
+        const int gg = idx / D, d = idx % D;
+        float s = 0.f;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        __syncwarp();
-        if (lane == 0) {
-          const float alpha = ex2(m_old - m_new);  // 0 on the first sub-tile
-          alpha_s[g] = alpha;
-          l_run[g] = l_run[g] * alpha + sum;
-          m_run[g] = m_new;
-        }
+        for (int w = 0; w < WARPS; ++w) s += red[(w * L::GH + gg) * D + d];
+        p.part[pbase + (pass * L::GH + gg) * hstride + d] = s;
       }
       __syncthreads();
     }
-    // ---------------------------------------------------------------- P V
-    {
-      const int i = 2 * sub + 1, st = i % NST;
-      ok = mbar_wait(sb + L::BAR_OFF + 8 * st, (i / NST) & 1, abort_flag, &g_status, p.wait_limit_ns);
-      if (__syncthreads_or(!ok)) { ok = false; break; }
-      const uint8_t* tile = smem + L::RING_OFF + st * L::STAGE;
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float a = alpha_s[g];
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) acc[g][e] *= a;
-      }
-#pragma unroll
-      for (int kk = 0; kk < KEYS_PER_WARP; ++kk) {
-        const int key = warp * KEYS_PER_WARP + kk;
-        if (key < rows) {
-          float vv[DPL];
-          if constexpr (DPL == 4) {
-            const uint2 w = *reinterpret_cast<const uint2*>(tile + key * D * 2 + lane * 8);
-            const float2 f0 = unpack2<BF16>(w.x), f1 = unpack2<BF16>(w.y);
-            vv[0] = f0.x; vv[1] = f0.y; vv[2] = f1.x; vv[3] = f1.y;
-          } else {
-            const uint32_t w = *reinterpret_cast<const uint32_t*>(tile + key * D * 2 + lane * 4);
-            const float2 f0 = unpack2<BF16>(w);
-            vv[0] = f0.x; vv[1] = f0.y;
-          }
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const float pr = sc[key * G + g];
-#pragma unroll
-            for (int e = 0; e < DPL; ++e) acc[g][e] = fmaf(pr, vv[e], acc[g][e]);
-          }
-        }
-      }
-      __syncthreads();  // every read of this stage done
-      if (threadIdx.x == 0 && i + NST < nload) issue(i + NST, pol);
+    if (threadIdx.x < G) {
+      const int g = threadIdx.x;
+      p.part[pbase + g * hstride + D] = m_run[g] * 0.69314718055994531f;  // natural-log units
+      p.part[pbase + g * hstride + D + 1] = l_run[g];
     }
   }
 
-  if (!ok) {
+  if (!ok && threadIdx.x == 0) {
     // unwind: wait (bounded) for the copies still in flight, then leave
-    if (threadIdx.x == 0) {
-      const uint64_t t0 = global_timer_ns();
-      for (int i = max(0, issued - NST); i < issued; ++i) {
-        const uint32_t bar = sb + L::BAR_OFF + 8 * (i % NST);
-        while (!mbar_try_wait(bar, (i / NST) & 1)) {
-          if (global_timer_ns() - t0 > p.wait_limit_ns) break;
-        }
-      }
-    }
-    __syncthreads();
-    return;
-  }
-
-  // cross-warp sum of the P V partials (aliases the ring: every copy has been consumed)
-  float* red = reinterpret_cast<float*>(smem + L::RING_OFF);
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) red[(warp * G + g) * D + lane * DPL + e] = acc[g][e];
-  __syncthreads();
-  const size_t pbase = (((size_t)b * p.Hq + h0) * p.max_chunks + c) * (D + 2);
-  const size_t hstride = (size_t)p.max_chunks * (D + 2);
-  for (int idx = threadIdx.x; idx < G * D; idx += THREADS) {
-    const int g = idx / D, d = idx % D;
-    float s = 0.f;
-#pragma unroll
-    for (int w = 0; w < WARPS; ++w) s += red[(w * G + g) * D + d];
-    p.part[pbase + g * hstride + d] = s;
-  }
-  if (threadIdx.x < G) {
-    const int g = threadIdx.x;
-    p.part[pbase + g * hstride + D] = m_run[g] * 0.69314718055994531f;  // natural-log units
-    p.part[pbase + g * hstride + D + 1] = l_run[g];
+    const uint64_t t0 = global_timer_ns();
+    for (int i = max(gl, issued - NST); i < issued; ++i)
+      while (!mbar_try_wait(ring_bar(i), (i / NST) & 1))
+        if (global_timer_ns() - t0 > p.wait_limit_ns) break;
   }
 }
 
@@ -323,23 +381,41 @@ __global__ void __launch_bounds__(32) decode_reduce_kernel(const Params p) {
 #pragma unroll
   for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
   float total = 0.f;
-  for (int c = 0; c < n; ++c) {
-    const float* pc = base + (size_t)c * (D + 2);
-    const float m_c = pc[D];
-    if (!(m_c > -1e30f)) continue;  // empty chunk
-    const float w = ex2((m_c - M) * 1.4426950408889634f);
-    total = fmaf(pc[D + 1], w, total);
-    if constexpr (DPL == 4) {
-      const float2 a = *reinterpret_cast<const float2*>(pc + lane * 4);
-      const float2 bb = *reinterpret_cast<const float2*>(pc + lane * 4 + 2);
-      acc[0] = fmaf(a.x, w, acc[0]);
-      acc[1] = fmaf(a.y, w, acc[1]);
-      acc[2] = fmaf(bb.x, w, acc[2]);
-      acc[3] = fmaf(bb.y, w, acc[3]);
-    } else {
-      const float2 a = *reinterpret_cast<const float2*>(pc + lane * 2);
-      acc[0] = fmaf(a.x, w, acc[0]);
-      acc[1] = fmaf(a.y, w, acc[1]);
+  // four chunks per pass, their loads issued together
+  constexpr int U = 4;
+  for (int cb = 0; cb < n; cb += U) {
+    float m_c[U], l_c[U], oc[U][DPL];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      m_c[u] = -INFINITY;
+      l_c[u] = 0.f;
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) oc[u][e] = 0.f;
+      if (cb + u < n) {
+        const float* pc = base + (size_t)(cb + u) * (D + 2);
+        m_c[u] = pc[D];
+        l_c[u] = pc[D + 1];
+        if constexpr (DPL == 4) {
+          const float2 a = *reinterpret_cast<const float2*>(pc + lane * 4);
+          const float2 bb = *reinterpret_cast<const float2*>(pc + lane * 4 + 2);
+          oc[u][0] = a.x;
+          oc[u][1] = a.y;
+          oc[u][2] = bb.x;
+          oc[u][3] = bb.y;
+        } else {
+          const float2 a = *reinterpret_cast<const float2*>(pc + lane * 2);
+          oc[u][0] = a.x;
+          oc[u][1] = a.y;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (!(m_c[u] > -1e30f)) continue;  // empty chunk, or past the last one
+      const float w = ex2((m_c[u] - M) * 1.4426950408889634f);
+      total = fmaf(l_c[u], w, total);
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) acc[e] = fmaf(oc[u][e], w, acc[e]);
     }
   }
   const float inv = total > 0.f ? 1.f / total : 0.f;  // no chunk (len 0): O = 0
@@ -359,7 +435,7 @@ static cudaError_t launch_t(const DecodeArgs& a, const Params& p, cudaStream_t s
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
   if (e != cudaSuccess) return e;
   if (a.max_chunks > 0) {
-    dim3 grid(a.max_chunks, a.Hkv * (p.group / G), a.B);
+    dim3 grid((a.max_chunks + p.cpb - 1) / p.cpb, a.Hkv * (p.group / G), a.B);
     decode_split_kernel<D, G, BF16><<<grid, THREADS, L::BYTES, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -373,6 +449,16 @@ static cudaError_t launch_d(const DecodeArgs& a, Params& p, cudaStream_t stream)
   const int G = p.group;
   // heads per CTA: the largest of 8, 4, 2, 1 dividing the group
   p.heads_per_cta = (G % 8 == 0) ? 8 : (G % 4 == 0) ? 4 : (G % 2 == 0) ? 2 : 1;
+  // chunks per CTA: the most of 4, 2, 1 that keeps a CTA at no more than 2048
+  // keys (longer ranges balance worse over ragged sequence lengths) and still
+  // leaves at least 8 CTAs per multiprocessor (counting empty chunks)
+  const long long per_x = (long long)a.B * a.Hkv * (G / p.heads_per_cta);
+  p.cpb = 1;
+  for (int cpb = 4; cpb > 1; cpb >>= 1)
+    if ((long long)cpb * a.chunk <= 2048 && per_x * ((a.max_chunks + cpb - 1) / cpb) >= 8LL * a.num_sms) {
+      p.cpb = cpb;
+      break;
+    }
   switch (p.heads_per_cta) {
     case 8: return launch_t<D, 8, BF16>(a, p, stream);
     case 4: return launch_t<D, 4, BF16>(a, p, stream);
@@ -391,6 +477,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.seq_lens = a.seq_lens;
   p.part = a.partials;
   p.o = static_cast<uint16_t*>(a.o);
+  p.B = a.B;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
   p.max_S = a.max_S;

@@ -32,6 +32,7 @@ struct DecodeArgs {
   void* o;
   float* partials;  // [B, Hq, max_chunks, D + 2] fp32 workspace
   int B, Hq, Hkv, max_S, D, chunk, max_chunks;
+  int num_sms;      // multiprocessors of the device (persistent split-kernel grid)
   float scale;
   int bf16;
   uint64_t wait_limit_ns;
