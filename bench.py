@@ -18,7 +18,9 @@ barrier and a device synchronize on both sides; inputs are larger than L2
 (the decode leg streams ~4.4 GB between prefill calls, so no step starts with
 a warm L2).  Inputs are resident in HBM when the timed region starts; the
 e2e figure repeats the step from pinned host buffers with the copies inside
-its timed region.
+its timed region: the prefill's Q, K, V, the decode queries, the valid prefix
+(seq_lens rows) of every (sequence, KV head) of the K and V caches, and
+seq_lens in; O, LSE and the decode output back.
 """
 
 from __future__ import annotations
@@ -339,7 +341,14 @@ def main():
         ho = torch.empty_like(hq).pin_memory()
         hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
         hdo = torch.empty_like(hdq).pin_memory()
-        h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdq, hdk, hdv, hlens))
+        # The decode step reads only the first seq_lens[b] rows of each (sequence, KV
+        # head) of the cache, so those prefixes are what goes over each step (one
+        # contiguous copy per (sequence, head) and tensor); rows past seq_lens are
+        # never read.
+        lens_l = [int(x) for x in lens]
+        kv_prefix = [(b, h, n) for b, n in enumerate(lens_l) for h in range(hdk.shape[1]) if n > 0]
+        h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdq, hlens))
+        h2d += 2 * sum(n for _, _, n in kv_prefix) * hdk.shape[3] * hdk.element_size()
         d2h = sum(x.numel() * x.element_size() for x in (ho, hlse, hdo))
 
         def e2e_step():
@@ -347,8 +356,9 @@ def main():
             k.copy_(hk, non_blocking=True)
             v.copy_(hv, non_blocking=True)
             dq.copy_(hdq, non_blocking=True)
-            dk.copy_(hdk, non_blocking=True)
-            dv.copy_(hdv, non_blocking=True)
+            for b, h, n in kv_prefix:
+                dk[b, h, :n].copy_(hdk[b, h, :n], non_blocking=True)
+                dv[b, h, :n].copy_(hdv[b, h, :n], non_blocking=True)
             lens_d.copy_(hlens, non_blocking=True)
             ea.attn_fwd(q, k, v, causal=True, scale=fw.scale, out=o, lse=lse, stream=stream)
             ea.attn_decode(dq, dk, dv, lens_d, num_splits=dw.num_splits, out=do, stream=stream)

@@ -381,8 +381,8 @@ __global__ void __launch_bounds__(32) decode_reduce_kernel(const Params p) {
 #pragma unroll
   for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
   float total = 0.f;
-  // four chunks per pass, their loads issued together
-  constexpr int U = 4;
+  // eight chunks per pass, their loads issued together
+  constexpr int U = 8;
   for (int cb = 0; cb < n; cb += U) {
     float m_c[U], l_c[U], oc[U][DPL];
 #pragma unroll

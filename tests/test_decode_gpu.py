@@ -49,6 +49,20 @@ def test_decode_cases(case):
     assert np.max(np.abs(ref - ref_c)) < 1e-12
 
 
+def test_multi_chunk_ctas():
+    """Enough (sequence, KV head) pairs that a CTA takes four consecutive chunks
+    (on a 152-SM part: 16 x 8 pairs, 64 chunks of 125 keys), with lengths that end
+    inside a CTA's range, on a chunk boundary, at zero and at one key; 125 is not
+    a multiple of the 128-key sub-tile."""
+    lens = [8000, 7999, 125, 126, 250, 499, 500, 501, 0, 1, 3000, 4321, 6000, 7500, 375, 626]
+    B, Hq, Hkv, max_S, D = len(lens), 32, 8, 8000, 128
+    lens_t = torch.tensor(lens, dtype=torch.int32)
+    q, k, v, lens_t = wl.decode_inputs(B, Hq, Hkv, max_S, D, lens_t, seed=2500)
+    o = run_decode(q, k, v, lens_t, 64)
+    ref = oracle.decode(q, k, v, lens_t, scale=1 / np.sqrt(D))
+    compare_o(o, ref, "decode multi-chunk CTAs")
+
+
 def test_zero_length_sequences():
     lens = torch.tensor([0, 10, 0], dtype=torch.int32)
     q, k, v, lens = wl.decode_inputs(3, 4, 2, 64, 128, lens, seed=11)
