@@ -20,17 +20,22 @@
 //    epilogue has read it from TMEM);
 //  * warp 8 streams Q once and K, V 128-key tiles through a 4-stage ring with
 //    TMA (3-D tensor maps, 128-byte swizzle, mbarrier transaction counts);
-//  * one thread of warp 9 issues every tcgen05.mma: S_i = Q_i K_j^T into TMEM,
-//    O_i += P_i V_j with P read from TMEM and V from shared memory.  Per KV
-//    tile the order is P_0 V(j), S_0(j+1), P_1 V(j), S_1(j+1): S_0 completes a
-//    whole tile's MMAs before S_1, so softmax 0 runs while the tensor core
-//    works for Q tile 1 and the other way round.  (Two issuers, one per Q
-//    tile, let the tensor core interleave both streams; both S tiles then
-//    finish together and the two softmax warpgroups fall into step, leaving
-//    the tensor core idle while both exponentiate.)  No commit frees a ring
-//    slot: Q tile 1 runs every KV tile of an item and S_1(j+1) is issued after
-//    every MMA that reads K(j+1) or V(j), so softmax warpgroup 1, which waits
-//    for each S_1 anyway, frees both slots with two plain arrives;
+//  * one thread of warp 9 + i issues the tcgen05.mma of Q tile i: S_i = Q_i K_j^T
+//    into TMEM, O_i += P_i V_j with P read from TMEM and V from shared memory.
+//    The two issuers hand a token back and forth, so per KV tile their batches
+//    reach the tensor core in the order P_0 V(j), S_0(j+1), P_1 V(j), S_1(j+1):
+//    S_0 completes a whole tile's MMAs before S_1, and softmax 0 runs while the
+//    tensor core works for Q tile 1 and the other way round.  (Issuers that do
+//    not take turns let the tensor core interleave both streams; both S tiles
+//    then finish together and the softmax warpgroups fall into step.)  Each
+//    issuer makes its other waits (its P, the K/V ring, O free) while the other
+//    one's batch executes, so only the hand-off lies between two batches: the
+//    tensor core queues just two or three MMAs, and a single issuer's barrier
+//    checks between batches idled it.  Both Q tiles step through every KV tile
+//    of an item; the shorter one's extra steps are empty batches.  No commit
+//    frees a ring slot: after S_i(c) completes (issued after every MMA of its
+//    issuer that reads K(c) or V(c-1)), softmax warpgroup i, which waits for
+//    it anyway, releases its use of both slots with plain arrives;
 //  * warpgroup i (warps 4i..4i+3) owns the rows of Q tile i, one row per
 //    thread (TMEM lane = row): load S, mask, row max, exponentiate with exp2
 //    (scale * log2 e folded into one FMA), accumulate the row sum, write P
@@ -62,10 +67,10 @@ constexpr int NQ = 2;               // Q tiles per CTA
 constexpr int BN = 128;             // keys per KV tile
 constexpr int NS = 4;               // K/V ring stages
 constexpr int NITEM = 4;            // claimed work items queued from the loader to the others
-constexpr int NUM_THREADS = 384;    // warpgroups 0, 1: softmax; warp 8 loader, warp 9 MMA
-                                    // (warps 10, 11 only lend their registers to the softmax)
+constexpr int NUM_THREADS = 384;    // warpgroups 0, 1: softmax; warp 8 loader, warps 9, 10 MMA
+                                    // (warp 11 only lends its registers to the softmax)
 constexpr int LOADER_WARP = 8;
-constexpr int MMA_WARP = 9;         // issues the MMAs of both Q tiles
+constexpr int MMA_WARP = 9;         // warp 9 + i issues the MMAs of Q tile i
 constexpr float RESCALE_LOG2 = 8.0f;  // rescale O when the max grows by more than 2^8
 constexpr uint32_t TMEM_COLS = 512;
 // TMEM columns: S_i at 128 i (P_i overwrites its first 64 columns), O_i at 256 + 128 i
@@ -95,8 +100,9 @@ struct Layout {
   enum {
     Q_FULL, Q_EMPTY, RING_FULL, RING_EMPTY = RING_FULL + NS, S_FULL = RING_EMPTY + NS,
     P_FULL = S_FULL + NQ, O_DONE = P_FULL + NQ, O_FREE = O_DONE + NQ,
-    ITEM_FULL = O_FREE + NQ, ITEM_EMPTY = ITEM_FULL + NITEM, DRAIN = ITEM_EMPTY + NITEM,
-    STAGE_FREE = DRAIN + 1, STAGE_FULL = STAGE_FREE + NQ, NUM_BARS = STAGE_FULL + NQ
+    ITEM_FULL = O_FREE + NQ, ITEM_EMPTY = ITEM_FULL + NITEM, TOK = ITEM_EMPTY + NITEM,
+    DRAIN = TOK + NQ,
+    STAGE_FREE = DRAIN + NQ, STAGE_FULL = STAGE_FREE + NQ, NUM_BARS = STAGE_FULL + NQ
   };
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;  // [0] TMEM base, [1] abort flag
   static constexpr int ITEM_OFF = MISC_OFF + 16;           // NITEM claimed work items
@@ -180,10 +186,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::Q_FULL), 1);
-    mbar_init(bar(L::Q_EMPTY), 1);
+    mbar_init(bar(L::Q_EMPTY), NQ);  // one arrival per issuer
     for (int s = 0; s < NS; ++s) {
       mbar_init(bar(L::RING_FULL + s), 1);
-      mbar_init(bar(L::RING_EMPTY + s), 1);  // freed by softmax warpgroup 1 (see there)
+      mbar_init(bar(L::RING_EMPTY + s), NQ);  // freed by both softmax warpgroups (see there)
     }
     for (int i = 0; i < NQ; ++i) {
       mbar_init(bar(L::S_FULL + i), 1);
@@ -193,9 +199,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int q = 0; q < NITEM; ++q) {
       mbar_init(bar(L::ITEM_FULL + q), 1);
-      mbar_init(bar(L::ITEM_EMPTY + q), 1 + NQ * 4);  // the MMA issuer and the softmax warps
+      mbar_init(bar(L::ITEM_EMPTY + q), NQ + NQ * 4);  // the MMA issuers and the softmax warps
     }
-    mbar_init(bar(L::DRAIN), 1);
+    for (int i = 0; i < NQ; ++i) {
+      mbar_init(bar(L::TOK + i), 1);  // issuer i finished issuing a batch
+      mbar_init(bar(L::DRAIN + i), 1);
+    }
     for (int i = 0; i < NQ; ++i) {
       mbar_init(bar(L::STAGE_FREE + i), 1);   // the warpgroup's store thread
       mbar_init(bar(L::STAGE_FULL + i), BM);  // every thread of the warpgroup
@@ -280,8 +289,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       __syncwarp();
-    } else if (warp == MMA_WARP) {
-      // ---------------------------------------------------------- MMA issuer
+    } else if (warp == MMA_WARP || warp == MMA_WARP + 1) {
+      // ------------------------------------------------ MMA issuers, one per Q tile
+      const int qi = warp - MMA_WARP;
       if (lane == 0) {
         constexpr uint32_t idesc_qk = umma_idesc_f16(BF16, BM, BN, false, false);
         constexpr uint32_t idesc_pv = umma_idesc_f16(BF16, BM, D, false, true);
@@ -291,38 +301,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // Shared-memory descriptors are built once; every MMA then only adds a
         // compile-time offset to the 14-bit start-address field (addresses stay
         // below 256 KB, so the addition never carries out of the field).
-        const uint64_t q_desc = sdesc_sw128(sb + L::Q_OFF, 16, 1024);
+        const uint64_t q_desc = sdesc_sw128(sb + L::Q_OFF + qi * L::TILE, 16, 1024);
         const uint64_t k_desc = sdesc_sw128(sb + L::RING_OFF, 16, 1024);
         const uint64_t v_desc = sdesc_sw128(sb + L::RING_OFF, L::REGION, 1024);
-        auto issue_s = [&](int i, int ld) {  // S_i = Q_i K^T, K in the ring slot of load ld
-          const uint64_t a0 = q_desc + (uint64_t)((i * L::TILE) >> 4);
+        const uint32_t t_s = tmem + COL_S + 128u * qi, t_o = tmem + COL_O + 128u * qi;
+        auto issue_s = [&](int ld) {  // S = Q K^T, K in the ring slot of load ld
           const uint64_t b0 = k_desc + (uint64_t)(((ld % NS) * L::TILE) >> 4);
-          const uint32_t d = tmem + COL_S + 128u * i;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             // K-major operands: 16 columns = 32 bytes inside a 128-byte swizzled row
             const uint32_t off = ((kk >> 2) * L::REGION + (kk & 3) * 32) >> 4;
-            umma_ss(d, a0 + off, b0 + off, idesc_qk, kk > 0 ? 1u : 0u);
+            umma_ss(t_s, q_desc + off, b0 + off, idesc_qk, kk > 0 ? 1u : 0u);
           }
-          umma_commit(bar(L::S_FULL + i));
+          umma_commit(bar(L::S_FULL + qi));
         };
-        auto issue_pv = [&](int i, int ld, bool acc) {  // O_i += P_i V, V in the ring slot of ld
+        auto issue_pv = [&](int ld, bool acc) {  // O += P V, V in the ring slot of ld
           // V is [key][d] (d contiguous): MN-major B, 16 keys = 2 swizzle atoms of 8 rows;
           // LBO steps to the next 64-column block of d, SBO to the next 8 keys.
           const uint64_t b0 = v_desc + (uint64_t)(((ld % NS) * L::TILE) >> 4);
-          const uint32_t d = tmem + COL_O + 128u * i;
-          const uint32_t a = tmem + COL_S + 128u * i;
-          umma_ts(d, a, b0, idesc_pv, acc ? 1u : 0u);
+          umma_ts(t_o, t_s, b0, idesc_pv, acc ? 1u : 0u);
 #pragma unroll
-          for (int kk = 1; kk < BN / 16; ++kk) umma_ts(d, a + kk * 8, b0 + kk * 128, idesc_pv, 1u);
+          for (int kk = 1; kk < BN / 16; ++kk) umma_ts(t_o, t_s + kk * 8, b0 + kk * 128, idesc_pv, 1u);
         };
-        // One thread issues every MMA of both Q tiles, per KV tile j in the order
-        // P_0 V(j), S_0(j+1), P_1 V(j), S_1(j+1).  S_0(j+1) then completes a full
-        // tile's worth of MMAs before S_1(j+1), so softmax 0 runs while the tensor
-        // pipe works for Q tile 1 and the other way round: the two softmax
-        // warpgroups alternate instead of falling into step with each other.
-        int ld = 0, k_item = 0;
-        int t_cnt[NQ] = {}, u_cnt[NQ] = {};  // P_FULL phases, items that used O_i
+        // The two issuers hand a token back and forth, so their batches reach the
+        // tensor core in the order P_0 V(j), S_0(j+1), P_1 V(j), S_1(j+1): S_0 then
+        // completes a tile's worth of MMAs before S_1 and the softmax warpgroups
+        // alternate.  Each issuer makes its other waits (its P, the K/V ring, O
+        // free) while the other one's batch executes; only the hand-off lies
+        // between two batches, and the tensor core queues just a couple of MMAs.
+        // Both Q tiles step through every KV tile of an item: the shorter one's
+        // extra steps are empty batches (a commit, no MMA) that keep the two in
+        // step and release ring slots in order.
+        int g = 0;  // batches issued
+        auto token_wait = [&]() -> bool {
+          if (qi == 0) return g == 0 || mbar_wait(bar(L::TOK + 1), (g - 1) & 1, abort_flag, &g_status, lim);
+          return mbar_wait(bar(L::TOK + 0), g & 1, abort_flag, &g_status, lim);
+        };
+        auto token_pass = [&]() {
+          tc_fence_before();
+          mbar_arrive(bar(L::TOK + qi));
+          ++g;
+        };
+        int ld = 0, k_item = 0, t_cnt = 0, n_items = 0;
         bool ok = true;
         for (int r = 0; ok; ++r) {
           const int qs = r % NITEM;
@@ -338,48 +358,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int i = 0; i < NQ; ++i) tile_range(p, m_base + i * BM, &n_t[i], &mf[i]);
           const int n_kv = max(n_t[0], n_t[1]);
           if (n_kv == 0) continue;
-          n_t[1] = n_kv;  // tile 1 covers every KV tile (its rows are masked or past Sq)
-          if (!(ok = mbar_wait(bar(L::Q_FULL), k_item & 1, abort_flag, &g_status, lim))) break;
-          ++k_item;
+          const int nt = n_t[qi];
           const int base = ld;
           ld = base + 2 * n_kv;
+          // ---- first batch of the item: S(0)
+          if (!(ok = mbar_wait(bar(L::Q_FULL), k_item & 1, abort_flag, &g_status, lim))) break;
+          ++k_item;
           if (!(ok = ring_wait(base))) break;
+          if (!(ok = token_wait())) break;
           tc_fence_after();
-          // S(0): P of the last item lives in these columns, read by an MMA issued earlier
-          for (int i = 0; i < NQ; ++i)
-            if (n_t[i] > 0) issue_s(i, base);
-          if (n_kv == 1) umma_commit(bar(L::Q_EMPTY));  // every S of the item is issued
-#pragma unroll 2
+          // P of the last item lives in these columns, read by an MMA issued earlier
+          if (nt > 0) issue_s(base);
+          else umma_commit(bar(L::S_FULL + qi));  // nothing to multiply for this tile
+          if (nt == 1) umma_commit(bar(L::Q_EMPTY));  // this tile's last S
+          else if (nt == 0) mbar_arrive(bar(L::Q_EMPTY));
+          token_pass();
+          // ---- one batch per KV tile j: P V(j), then S(j+1)
           for (int j = 0; j < n_kv && ok; ++j) {
             const int ld_v = base + 2 * j + 1, ld_k = base + 2 * j + 2;
-            // The tensor core queues only a couple of MMAs, so every wait between two
-            // MMAs idles it: V(j) and K(j+1) are awaited here, once per step, and
-            // each Q tile's P V and S MMAs then go out back to back.
             if (!(ok = ring_wait(ld_v))) break;
             if (j + 1 < n_kv && !(ok = ring_wait(ld_k))) break;
-            for (int i = 0; i < NQ; ++i) {
-              if (j >= n_t[i]) continue;
-              if (!(ok = mbar_wait(bar(L::P_FULL + i), t_cnt[i] & 1, abort_flag, &g_status, lim))) break;
-              // the first P V of an item overwrites O: the last epilogue must have read it
-              if (j == 0 && u_cnt[i] > 0 &&
-                  !(ok = mbar_wait(bar(L::O_FREE + i), (u_cnt[i] - 1) & 1, abort_flag, &g_status, lim)))
-                break;
-              tc_fence_after();
-              issue_pv(i, ld_v, j > 0);
-              ++t_cnt[i];
-              if (j == n_t[i] - 1) {
-                umma_commit(bar(L::O_DONE + i));
-                ++u_cnt[i];
-              }
-              if (j + 1 < n_t[i]) issue_s(i, ld_k);  // after P_i V(j), which read P_i from these columns
+            if (!(ok = mbar_wait(bar(L::P_FULL + qi), t_cnt & 1, abort_flag, &g_status, lim))) break;
+            ++t_cnt;
+            // the first P V of an item overwrites O: the last epilogue must have read it
+            if (j == 0 && nt > 0 && n_items > 0 &&
+                !(ok = mbar_wait(bar(L::O_FREE + qi), (n_items - 1) & 1, abort_flag, &g_status, lim)))
+              break;
+            if (!(ok = token_wait())) break;
+            tc_fence_after();
+            if (j < nt) issue_pv(ld_v, j > 0);
+            if (j == n_kv - 1) {
+              umma_commit(bar(L::O_DONE + qi));
+              ++n_items;
             }
-            if (!ok) break;
-            // ring slots are freed once S_1 completes (see softmax warpgroup 1)
-            if (j + 2 == n_kv) umma_commit(bar(L::Q_EMPTY));  // the item's last S is issued
+            if (j + 1 < n_kv) {
+              if (j + 1 < nt) {
+                issue_s(ld_k);  // after P V(j), which read P from these columns
+                if (j + 1 == nt - 1) umma_commit(bar(L::Q_EMPTY));  // this tile's last S
+              } else {
+                umma_commit(bar(L::S_FULL + qi));  // an empty step for this tile
+              }
+            }
+            token_pass();
           }
         }
-        umma_commit(bar(L::DRAIN));  // fires once every MMA issued above has completed
-        drain_wait(bar(L::DRAIN), 0, lim);
+        umma_commit(bar(L::DRAIN + qi));  // fires once every MMA issued above has completed
+        drain_wait(bar(L::DRAIN + qi), 0, lim);
       }
       __syncwarp();
     }
@@ -412,19 +436,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int bh = b * p.Hq + hq;
       const int m0 = mb * (NQ * BM) + qi * BM;
       const int row = m0 + r_lane;
-      int n_tiles, mfrom;
-      tile_range(p, m0, &n_tiles, &mfrom);
-      if (qi == 1) {
-        // tile 1 runs every KV tile of the item, also when it lies past Sq: the
-        // completions of its S MMAs free the K/V ring slots
-        int n0, mf0;
-        tile_range(p, m0 - BM, &n0, &mf0);
-        if (n0 > n_tiles) {
-          n_tiles = n0;
-          mfrom = 0;
-        }
-      }
-      if (n_tiles == 0) {  // this Q tile sees no key (or lies past Sq)
+      int n_own, mfrom;
+      tile_range(p, m0, &n_own, &mfrom);
+      int n_oth, mf_oth;
+      tile_range(p, m0 + (qi == 0 ? BM : -BM), &n_oth, &mf_oth);
+      // both Q tiles step through every KV tile of the item; past its own range a
+      // step only passes the barriers (its issuer multiplies nothing there)
+      const int n_tiles = max(n_own, n_oth);
+      if (n_tiles == 0) {  // no key for the whole item
         if (row < p.Sq) zero_row(p, bh, row, D);
         continue;
       }
@@ -434,15 +453,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int t = 0; t < n_tiles; ++t, ++t_cnt) {
         if (!(ok = wait_warp(bar(L::S_FULL + qi), t_cnt & 1))) break;
         tc_fence_after();
-        if (qi == 1 && r_lane == 0) {
-          // Q tile 1 runs every KV tile, so S_1 number t_cnt read the K of load 2 t_cnt
-          // (loads alternate K, V).  It was issued after every MMA that reads that K
-          // or the V before it (order P_0 V(j), S_0(j+1), P_1 V(j), S_1(j+1), and across
-          // items the last P_1 V before the next S_1(0)), so its completion frees both
-          // ring slots.  This warpgroup consumes every completion of S_1 in order and
-          // the next S_1 needs its P, which keeps the ring protocol exact.
+        if (r_lane == 0) {
+          // Both Q tiles step through every KV tile, so S_i number t_cnt belongs to the
+          // K of load 2 t_cnt (loads alternate K, V).  Its issuer issued it (or the
+          // empty step's commit) after every MMA of its own that reads that K or the V
+          // before it, so its completion frees this tile's use of both ring slots;
+          // each slot takes one arrival per Q tile.  This warpgroup consumes every
+          // completion of S_i in order and the next S_i needs its P, which keeps the
+          // ring protocol exact.
           if (t_cnt > 0) mbar_arrive(bar(L::RING_EMPTY + (2 * t_cnt - 1) % NS));
           mbar_arrive(bar(L::RING_EMPTY + (2 * t_cnt) % NS));
+        }
+        if (t >= n_own) {  // an empty step: no S was computed for this tile
+          tc_fence_before();
+          mbar_arrive(bar(L::P_FULL + qi));
+          continue;
         }
         float x[BN];
         {
@@ -548,6 +573,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_before();
       mbar_arrive(bar(L::O_FREE + qi));
       const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
+      if (!(l_sum > 0.f)) {
+        // no visible key (or no P V at all for this tile): O = 0, not stale TMEM times 0
+#pragma unroll
+        for (int i = 0; i < D; ++i) orow[i] = 0u;
+      }
       // O / l goes out through this warpgroup's staging region (128 rows x 64
       // columns, the 128-byte swizzle of the tensor map: 16-byte chunk c of row r
       // at chunk c ^ (r mod 8), so a warp's stores hit every bank once) and one
