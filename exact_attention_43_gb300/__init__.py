@@ -11,6 +11,7 @@ from .binding import (  # noqa: F401
     ExtensionMissing,
     attn_decode,
     attn_decode_noalloc,
+    attn_decode_paged,
     attn_fwd,
     check_device_status,
     debug_set,

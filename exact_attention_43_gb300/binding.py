@@ -25,7 +25,8 @@ ATTN_ERR_DEVICE_TIMEOUT = 4
 ATTN_BF16 = 0
 ATTN_FP16 = 1
 
-EXPORTS = ("attn_fwd", "attn_decode", "attn_decode_noalloc", "attn_decode_workspace_bytes",
+EXPORTS = ("attn_fwd", "attn_decode", "attn_decode_paged", "attn_decode_noalloc",
+           "attn_decode_workspace_bytes",
            "attn_decode_chunk", "attn_check_device_status", "attn_debug_set",
            "attn_status_string", "attn_version")
 NOALLOC_MAX_BYTES = 16 << 20  # ATTN_DECODE_NOALLOC_MAX_BYTES in attn.h
@@ -59,6 +60,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_fwd.restype = i
     lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
     lib.attn_decode.restype = i
+    lib.attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, vp]
+    lib.attn_decode_paged.restype = i
     lib.attn_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
     lib.attn_decode_noalloc.restype = i
     lib.attn_decode_workspace_bytes.argtypes = [i, i, i, i, i]
@@ -146,6 +149,28 @@ def attn_decode(q, k_cache, v_cache, seq_lens, *, num_splits: int = 0, out=None,
     st = lib.attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), _ptr(out), B, Hq,
                          Hkv, max_S, D, num_splits, _dtype_code(q), _stream(stream))
     _check(st, "attn_decode")
+    return out
+
+
+def attn_decode_paged(q, k_pages, v_pages, block_table, seq_lens, *, num_splits: int = 0, out=None,
+                      stream=None):
+    """Flash-decoding over a paged cache: q [B,Hq,D], pages [num_pages,Hkv,page_size,D],
+    block_table [B,max_pages] int32, seq_lens [B] int32 (all CUDA)."""
+    lib = load()
+    B, Hq, D = q.shape
+    num_pages, Hkv, page_size = k_pages.shape[0], k_pages.shape[1], k_pages.shape[2]
+    max_pages = block_table.shape[1]
+    for t in (q, k_pages, v_pages, block_table, seq_lens):
+        if not t.is_contiguous():
+            raise ValueError("decode inputs must be contiguous")
+    if seq_lens.dtype != torch.int32 or block_table.dtype != torch.int32:
+        raise TypeError("seq_lens and block_table must be int32")
+    if out is None:
+        out = torch.empty_like(q)
+    st = lib.attn_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
+                               _ptr(seq_lens), _ptr(out), B, Hq, Hkv, num_pages, page_size,
+                               max_pages, D, num_splits, _dtype_code(q), _stream(stream))
+    _check(st, "attn_decode_paged")
     return out
 
 

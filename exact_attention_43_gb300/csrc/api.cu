@@ -176,6 +176,25 @@ size_t attn_decode_workspace_bytes(int B, int Hq, int max_S, int D, int num_spli
   return (size_t)B * Hq * max_chunks * (D + 2) * sizeof(float);
 }
 
+// Partials workspace from the library pool, stream-ordered around the two kernels.
+static int decode_with_pool(ea::DecodeArgs& a, int dev, size_t bytes, cudaStream_t stream) {
+  void* ws = nullptr;
+  if (bytes > 0) {
+    cudaMemPool_t pool;
+    const int st = pool_for(dev, &pool);
+    if (st != ATTN_OK) return st;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, bytes, pool, stream);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  a.partials = static_cast<float*>(ws);
+  cudaError_t e = ea::launch_decode(a, stream);
+  if (ws) {
+    cudaError_t f = cudaFreeAsync(ws, stream);
+    if (e == cudaSuccess) e = f;
+  }
+  return from_cuda(e);
+}
+
 int attn_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* seq_lens,
                 void* o, int B, int Hq, int Hkv, int max_S, int D, int num_splits, int dtype,
                 cudaStream_t stream) {
@@ -213,21 +232,55 @@ int attn_decode(const void* q, const void* k_cache, const void* v_cache, const i
   a.wait_limit_ns = g_wait_limit_ns;
   a.num_sms = g_num_sms[dev] > 0 ? g_num_sms[dev] : 1;
 
-  const size_t bytes = attn_decode_workspace_bytes(B, Hq, max_S, D, num_splits);
-  void* ws = nullptr;
-  if (bytes > 0) {
-    cudaMemPool_t pool;
-    if ((st = pool_for(dev, &pool)) != ATTN_OK) return st;
-    cudaError_t e = cudaMallocFromPoolAsync(&ws, bytes, pool, stream);
-    if (e != cudaSuccess) return from_cuda(e);
-  }
-  a.partials = static_cast<float*>(ws);
-  cudaError_t e = ea::launch_decode(a, stream);
-  if (ws) {
-    cudaError_t f = cudaFreeAsync(ws, stream);
-    if (e == cudaSuccess) e = f;
-  }
-  return from_cuda(e);
+  return decode_with_pool(a, dev, attn_decode_workspace_bytes(B, Hq, max_S, D, num_splits), stream);
+}
+
+int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                      const int32_t* block_table, const int32_t* seq_lens, void* o, int B, int Hq,
+                      int Hkv, int num_pages, int page_size, int max_pages, int D, int num_splits,
+                      int dtype, cudaStream_t stream) {
+  if (B < 0 || Hq < 0 || Hkv < 0 || num_pages < 0 || page_size < 1 || max_pages < 0 || num_splits < 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if ((long long)max_pages * page_size > INT_MAX) return ATTN_ERR_UNSUPPORTED;
+  const int max_S = max_pages * page_size;  // logical positions per sequence
+  if ((long long)B * Hq == 0) return ATTN_OK;
+  if (Hkv == 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (B > 65535 || Hkv > 65535 || Hq > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (!q || !o || !seq_lens) return ATTN_ERR_INVALID_ARG;
+  if (max_S > 0 && (!k_pages || !v_pages || !block_table || num_pages == 0)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(o, 16) || !aligned(seq_lens, 4) ||
+      (k_pages && !aligned(k_pages, 16)) || (v_pages && !aligned(v_pages, 16)) ||
+      (block_table && !aligned(block_table, 4)))
+    return ATTN_ERR_INVALID_ARG;
+  int dev = 0;
+  int st = check_device(&dev);
+  if (st != ATTN_OK) return st;
+
+  ea::DecodeArgs a{};
+  a.q = q;
+  a.k = k_pages;
+  a.v = v_pages;
+  a.seq_lens = seq_lens;
+  a.o = o;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.max_S = max_S;
+  a.D = D;
+  a.chunk = chunk_for(max_S, num_splits);
+  a.max_chunks = max_S > 0 ? (max_S + a.chunk - 1) / a.chunk : 0;
+  if ((long long)B * Hq * a.max_chunks > INT_MAX) return ATTN_ERR_UNSUPPORTED;
+  a.scale = 1.0f / sqrtf((float)D);
+  a.bf16 = dtype == ATTN_BF16;
+  a.wait_limit_ns = g_wait_limit_ns;
+  a.num_sms = g_num_sms[dev] > 0 ? g_num_sms[dev] : 1;
+  a.block_table = max_S > 0 ? block_table : nullptr;
+  a.page_size = page_size;
+  a.max_pages = max_pages;
+  a.num_pages = num_pages;
+  return decode_with_pool(a, dev, attn_decode_workspace_bytes(B, Hq, max_S, D, num_splits), stream);
 }
 
 int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
@@ -284,7 +337,7 @@ int attn_check_device_status(cudaStream_t stream) {
   if ((e = ea::read_decode_status(&d, stream)) != cudaSuccess) return from_cuda(e);
   const unsigned all = f | d;
   if (all & 1u) return ATTN_ERR_DEVICE_TIMEOUT;
-  if (all & 2u) return ATTN_ERR_INVALID_ARG;
+  if (all & 6u) return ATTN_ERR_INVALID_ARG;  // a seq_len clamped, a page index replaced
   return ATTN_OK;
 }
 

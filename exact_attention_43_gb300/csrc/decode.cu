@@ -51,6 +51,10 @@ struct Params {
   int cpb;  // consecutive chunks per split-kernel CTA
   float c2;  // scale * log2(e)
   uint64_t wait_limit_ns;
+  // paged cache (block_table != nullptr): k, v are [num_pages, Hkv, page_size, D] and
+  // position j of sequence b is row j % page_size of page block_table[b, j / page_size]
+  const int32_t* block_table;
+  int page_size, max_pages, num_pages;
 };
 
 __device__ __forceinline__ int clamp_len(const Params& p, int b) {
@@ -62,14 +66,16 @@ __device__ __forceinline__ int clamp_len(const Params& p, int b) {
   return L;
 }
 
-template <int D, int G>
+template <int D, int G, bool PAGED>
 struct SplitLayout {
   static constexpr int STAGE = SUB * D * 2;
   static constexpr int GH = (G + 1) / 2;                      // heads per cross-warp reduction pass
   static constexpr int RING_OFF = 0;
   static constexpr int SC_OFF = RING_OFF + NST * STAGE;      // scores / probabilities [SUB][G]
   static constexpr int RED_OFF = SC_OFF + SUB * G * 4;       // [WARPS][GH][D] P V partial sums
-  static constexpr int STAT_OFF = RED_OFF + WARPS * GH * D * 4;  // m, l, alpha per head
+  static constexpr int PT_OFF = RED_OFF + WARPS * GH * D * 4;    // block-table slice (paged cache)
+  static constexpr int PT_MAX = PAGED ? 520 : 0;                  // entries it holds
+  static constexpr int STAT_OFF = PT_OFF + PT_MAX * 4;            // m, l, alpha per head
   static constexpr int BAR_OFF = (STAT_OFF + 3 * G * 4 + 15) / 16 * 16;  // NST ring barriers
   static constexpr int ABORT_OFF = BAR_OFF + NST * 8;
   static constexpr int BYTES = ABORT_OFF + 16;
@@ -97,9 +103,9 @@ __device__ __forceinline__ uint64_t pair_of(uint32_t w) {
 // 512-key chunk is only 256 KB of K and V: with one CTA per chunk, each CTA's
 // first load and epilogue went unhidden (85 % of HBM bandwidth at chunk 512
 // against 94 % at chunk 2048).
-template <int D, int G, bool BF16>
+template <int D, int G, bool BF16, bool PAGED>
 __global__ void __launch_bounds__(THREADS) decode_split_kernel(const Params p) {
-  using L = SplitLayout<D, G>;
+  using L = SplitLayout<D, G, PAGED>;
   constexpr int EPL = D / 8;   // key elements per lane when 8 lanes share a key
   constexpr int DPL = D / 32;  // output columns per lane in P V
   extern __shared__ __align__(128) uint8_t smem[];
@@ -123,6 +129,31 @@ __global__ void __launch_bounds__(THREADS) decode_split_kernel(const Params p) {
   auto chunk_rows = [&](int c) -> int { return min(p.chunk, len - c * p.chunk); };
   auto ring_bar = [&](int j) -> uint32_t { return sb + L::BAR_OFF + 8 * (j % NST); };
 
+  // Paged cache: the block-table entries of this CTA's positions, checked once and
+  // kept in shared memory, so the loader thread does not wait on a global load per
+  // page.  (Ranges of more pages than the buffer holds read the table directly.)
+  int* pt = reinterpret_cast<int*>(smem + L::PT_OFF);
+  int pg_lo = 0, pg_n = 0;
+  if constexpr (PAGED) {
+    pg_lo = (c0 * p.chunk) / p.page_size;
+    pg_n = (min(len, c1 * p.chunk) - 1) / p.page_size + 1 - pg_lo;
+  }
+  const bool pt_smem = pg_n <= L::PT_MAX;
+  auto page_of = [&](int pg) -> int {  // physical page of logical page pg, within the pool
+    int phys = __ldg(p.block_table + (size_t)b * p.max_pages + pg);
+    if (phys < 0 || phys >= p.num_pages) {  // never read outside the page pool
+      atomicOr(&g_status, kStatusBadPage);
+      phys = 0;
+    }
+    return phys;
+  };
+  if constexpr (PAGED) {
+    if (pt_smem) {
+      for (int i = threadIdx.x; i < pg_n; i += THREADS) pt[i] = page_of(pg_lo + i);
+      __syncthreads();
+    }
+  }
+
   // ------------------------------------------------ load stream (thread 0 only)
   int l_c = c0, l_off = 0, l_nload = 2 * ((chunk_rows(c0) + SUB - 1) / SUB), issued = 0;
   uint64_t pol = 0;
@@ -130,11 +161,28 @@ __global__ void __launch_bounds__(THREADS) decode_split_kernel(const Params p) {
     if (l_c >= c1) return;
     const int sub = l_off >> 1;
     const int rows = min(SUB, chunk_rows(l_c) - sub * SUB);
-    const size_t r = row0 + (size_t)l_c * p.chunk + (size_t)sub * SUB;
-    const uint16_t* src = ((l_off & 1) ? p.v : p.k) + r * D;
-    const uint32_t bar = ring_bar(issued);
-    mbar_expect_tx(bar, rows * D * 2);
-    bulk_load(sb + L::RING_OFF + (issued % NST) * L::STAGE, src, rows * D * 2, bar, pol);
+    if constexpr (!PAGED) {
+      const size_t r = row0 + (size_t)l_c * p.chunk + (size_t)sub * SUB;
+      const uint16_t* src = ((l_off & 1) ? p.v : p.k) + r * D;
+      const uint32_t bar = ring_bar(issued);
+      mbar_expect_tx(bar, rows * D * 2);
+      bulk_load(sb + L::RING_OFF + (issued % NST) * L::STAGE, src, rows * D * 2, bar, pol);
+    } else {
+      const uint16_t* base = (l_off & 1) ? p.v : p.k;
+      const uint32_t bar = ring_bar(issued);
+      const uint32_t dst = sb + L::RING_OFF + (issued % NST) * L::STAGE;
+      mbar_expect_tx(bar, rows * D * 2);
+      // one copy per page the sub-tile's positions fall in, into one stage and one barrier
+      const int pos0 = l_c * p.chunk + sub * SUB;
+      int pg = pos0 / p.page_size, off = pos0 - pg * p.page_size;
+      for (int done = 0; done < rows; ++pg, off = 0) {
+        const int phys = pt_smem ? pt[pg - pg_lo] : page_of(pg);
+        const int seg = min(rows - done, p.page_size - off);
+        bulk_load(dst + done * D * 2, base + (((size_t)phys * p.Hkv + kvh) * p.page_size + off) * D,
+                  seg * D * 2, bar, pol);
+        done += seg;
+      }
+    }
     ++issued;
     if (++l_off == l_nload && ++l_c < c1) {
       l_off = 0;
@@ -428,16 +476,23 @@ __global__ void __launch_bounds__(32) decode_reduce_kernel(const Params p) {
   }
 }
 
-template <int D, int G, bool BF16>
-static cudaError_t launch_t(const DecodeArgs& a, const Params& p, cudaStream_t stream) {
-  using L = SplitLayout<D, G>;
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G, BF16>,
+template <int D, int G, bool BF16, bool PAGED>
+static cudaError_t launch_split(const DecodeArgs& a, const Params& p, cudaStream_t stream) {
+  using L = SplitLayout<D, G, PAGED>;
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G, BF16, PAGED>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
   if (e != cudaSuccess) return e;
+  dim3 grid((a.max_chunks + p.cpb - 1) / p.cpb, a.Hkv * (p.group / G), a.B);
+  decode_split_kernel<D, G, BF16, PAGED><<<grid, THREADS, L::BYTES, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int D, int G, bool BF16>
+static cudaError_t launch_t(const DecodeArgs& a, const Params& p, cudaStream_t stream) {
   if (a.max_chunks > 0) {
-    dim3 grid((a.max_chunks + p.cpb - 1) / p.cpb, a.Hkv * (p.group / G), a.B);
-    decode_split_kernel<D, G, BF16><<<grid, THREADS, L::BYTES, stream>>>(p);
-    e = cudaGetLastError();
+    // the contiguous-cache kernel is a separate instantiation, free of the page logic
+    const cudaError_t e = p.block_table ? launch_split<D, G, BF16, true>(a, p, stream)
+                                        : launch_split<D, G, BF16, false>(a, p, stream);
     if (e != cudaSuccess) return e;
   }
   decode_reduce_kernel<D, BF16><<<dim3(a.Hq, a.B), 32, 0, stream>>>(p);
@@ -486,6 +541,10 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.group = a.Hq / a.Hkv;
   p.c2 = a.scale * 1.4426950408889634f;
   p.wait_limit_ns = a.wait_limit_ns;
+  p.block_table = a.block_table;
+  p.page_size = a.page_size;
+  p.max_pages = a.max_pages;
+  p.num_pages = a.num_pages;
   if (a.D == 64) return a.bf16 ? dec::launch_d<64, true>(a, p, stream) : dec::launch_d<64, false>(a, p, stream);
   return a.bf16 ? dec::launch_d<128, true>(a, p, stream) : dec::launch_d<128, false>(a, p, stream);
 }

@@ -32,7 +32,10 @@ struct DecodeArgs {
   void* o;
   float* partials;  // [B, Hq, max_chunks, D + 2] fp32 workspace
   int B, Hq, Hkv, max_S, D, chunk, max_chunks;
-  int num_sms;      // multiprocessors of the device (persistent split-kernel grid)
+  int num_sms;      // multiprocessors of the device
+  // paged cache: block_table != nullptr, see attn_decode_paged
+  const int32_t* block_table;
+  int page_size, max_pages, num_pages;
   float scale;
   int bf16;
   uint64_t wait_limit_ns;

@@ -16,6 +16,7 @@ namespace ea {
 
 constexpr unsigned kStatusTimeout = 1u;        // a bounded wait ran out
 constexpr unsigned kStatusSeqLenClamped = 2u;  // a decode seq_len was outside [0, max_S]
+constexpr unsigned kStatusBadPage = 4u;        // a paged-decode block-table entry was outside the pool
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

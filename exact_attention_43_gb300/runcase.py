@@ -2,7 +2,7 @@
 
     python -m exact_attention_43_gb300.runcase fwd --workload mha [--iters 3]
     python -m exact_attention_43_gb300.runcase fwd --B 1 --H 8 --S 4096 --causal 1
-    python -m exact_attention_43_gb300.runcase decode [--B 8] [--iters 3]
+    python -m exact_attention_43_gb300.runcase decode [--B 8] [--iters 3] [--page-size 64]
 
 Inputs are drawn on the GPU from the seeded generators in workloads.py.
 Prints one JSON line with the mean CUDA-event time per call.
@@ -31,6 +31,7 @@ def main():
     ap.add_argument("--causal", type=int, default=1)
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--warmup", type=int, default=1)
+    ap.add_argument("--page-size", type=int, default=0, help="decode over a paged cache")
     a = ap.parse_args()
     dev = torch.device("cuda", 0)
     ea.load()
@@ -54,12 +55,21 @@ def main():
         q, k, v, lens = wl.decode_inputs(B, d.Hq, d.Hkv, d.max_S, d.D, lens, dtype=d.dtype,
                                          seed=wl.SEED_BASE + d.index, device=dev)
         lens_d = lens.to(dev)
+        desc = f"decode B{B} Hq{d.Hq} Hkv{d.Hkv} max_S{d.max_S} D{d.D} sumL={int(lens.sum())}"
+        if a.page_size > 0:
+            kp, vp, table = wl.paged_cache(k, v, [int(x) for x in lens], a.page_size,
+                                           seed=wl.SEED_BASE + d.index + 100)
+            del k, v
+            kp, vp, table = kp.to(dev), vp.to(dev), table.to(dev)
+            desc += f" paged {a.page_size}"
 
-        def call():
-            return ea.attn_decode(q, k, v, lens_d, num_splits=d.num_splits)
+            def call():
+                return ea.attn_decode_paged(q, kp, vp, table, lens_d, num_splits=d.num_splits)
+        else:
+            def call():
+                return ea.attn_decode(q, k, v, lens_d, num_splits=d.num_splits)
 
         units, unit = d.io_bytes(lens), "GB/s"
-        desc = f"decode B{B} Hq{d.Hq} Hkv{d.Hkv} max_S{d.max_S} D{d.D} sumL={int(lens.sum())}"
     for _ in range(a.warmup):
         call()
     torch.cuda.synchronize()

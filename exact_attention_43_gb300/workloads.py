@@ -164,6 +164,37 @@ def workload_decode_inputs(w: DecodeWorkload, device="cpu"):
                          seed=SEED_BASE + w.index, device=device)
 
 
+def paged_cache(k, v, lens, page_size: int, *, seed: int, spare_pages: int = 3):
+    """Scatter contiguous caches [B, Hkv, max_S, D] into a page pool.
+
+    Returns k_pages, v_pages [num_pages, Hkv, page_size, D] and block_table
+    [B, ceil(max_S / page_size)] int32.  Each sequence gets ceil(len / page_size)
+    pages at seeded random places in the pool; `spare_pages` pages belong to no
+    sequence, and block-table entries past a sequence's pages are -1 (never
+    read).  Positions past max_S inside a last page are zero.
+    """
+    k, v = k.cpu(), v.cpu()
+    B, Hkv, max_S, D = k.shape
+    max_pages = -(-max_S // page_size)
+    need = [-(-int(n) // page_size) for n in lens]
+    num_pages = sum(need) + spare_pages
+    g = _gen(seed, "cpu")
+    phys = torch.randperm(num_pages, generator=g)
+    k_pages = torch.zeros((num_pages, Hkv, page_size, D), dtype=k.dtype)
+    v_pages = torch.zeros_like(k_pages)
+    table = torch.full((B, max_pages), -1, dtype=torch.int32)
+    nxt = 0
+    for b in range(B):
+        for pg in range(need[b]):
+            pid = int(phys[nxt])
+            nxt += 1
+            table[b, pg] = pid
+            lo, hi = pg * page_size, min((pg + 1) * page_size, max_S)
+            k_pages[pid, :, : hi - lo] = k[b, :, lo:hi]
+            v_pages[pid, :, : hi - lo] = v[b, :, lo:hi]
+    return k_pages, v_pages, table
+
+
 def sample_rows(S: int, n: int, *, seed: int):
     """n distinct query rows drawn uniformly from [0, S) without replacement, sorted."""
     g = _gen(seed, "cpu")

@@ -99,6 +99,35 @@ int attn_decode(const void* q, const void* k_cache, const void* v_cache, const i
                 cudaStream_t stream);
 
 /*
+ * attn_decode_paged -- attn_decode over a paged KV cache.
+ *
+ * Same computation, chunking, partials and merge as attn_decode; only where
+ * the keys and values live differs.  The pages place the flash-decoding code
+ * under a paged-cache directory but give no page layout; the layout here keeps
+ * one page of one KV head contiguous, so a page is read with one bulk copy:
+ *
+ * k_pages,    device, [num_pages, Hkv, page_size, D], dtype `dtype`, 16-byte
+ * v_pages     aligned; a page holds page_size consecutive positions of one
+ *             sequence, for every KV head.
+ * block_table device, [B, max_pages] int32, 4-byte aligned: position j of
+ *             sequence b is row j % page_size of page block_table[b, j / page_size].
+ *             Only the first ceil(seq_lens[b] / page_size) entries of a row are
+ *             read.  An entry outside [0, num_pages) is replaced by page 0 (no
+ *             read leaves the pool) and reported by attn_check_device_status as
+ *             ATTN_ERR_INVALID_ARG.
+ * seq_lens    device, [B] int32, 0 <= seq_lens[b] <= max_pages * page_size
+ *             (clamped and reported as in attn_decode).
+ * page_size >= 1; num_pages, max_pages >= 0 (num_pages >= 1 when max_pages > 0);
+ * max_pages * page_size plays the role of max_S for the chunking and for
+ * attn_decode_workspace_bytes.  Other arguments, the workspace and the status
+ * codes are those of attn_decode.
+ */
+int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                      const int32_t* block_table, const int32_t* seq_lens, void* o, int B, int Hq,
+                      int Hkv, int num_pages, int page_size, int max_pages, int D, int num_splits,
+                      int dtype, cudaStream_t stream);
+
+/*
  * attn_decode_noalloc -- attn_decode for callers that must not allocate GPU memory.
  *
  * Some callers cannot allocate device memory while they run: a plugin whose

@@ -94,6 +94,25 @@ def test_decode_argument_errors(lib):
     assert dec(lib, B=0) == 0
 
 
+def paged(lib, q=FAKE, kp=FAKE, vp=FAKE, bt=FAKE, lens=FAKE, o=FAKE, B=2, Hq=8, Hkv=2, num_pages=4,
+          page_size=16, max_pages=4, D=128, splits=0, dtype=0):
+    return lib.attn_decode_paged(q, kp, vp, bt, lens, o, B, Hq, Hkv, num_pages, page_size, max_pages,
+                                 D, splits, dtype, None)
+
+
+def test_paged_decode_argument_errors(lib):
+    assert paged(lib, bt=None) == 1             # pages but no block table
+    assert paged(lib, num_pages=0) == 1         # block table into an empty pool
+    assert paged(lib, page_size=0) == 1
+    assert paged(lib, max_pages=-1) == 1
+    assert paged(lib, bt=FAKE + 2) == 1         # int32 table not 4-byte aligned
+    assert paged(lib, kp=FAKE + 8) == 1         # pages not 16-byte aligned
+    assert paged(lib, Hkv=3) == 1
+    assert paged(lib, D=96) == 2
+    assert paged(lib, page_size=1 << 16, max_pages=1 << 16) == 2  # positions overflow an int
+    assert paged(lib, B=0) == 0
+
+
 def test_noalloc_decode_refuses_oversized_partials_before_any_cuda_call(lib):
     # 64 x 32 x 64 chunks x 130 floats x 4 B = 68 MB > 16 MiB of fixed scratch
     assert lib.attn_decode_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, 64, 32, 8, 32768, 128, 64, 0,
