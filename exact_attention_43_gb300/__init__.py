@@ -10,6 +10,7 @@ from .binding import (  # noqa: F401
     AttnError,
     ExtensionMissing,
     attn_decode,
+    attn_decode_fused,
     attn_decode_noalloc,
     attn_decode_paged,
     attn_fwd,

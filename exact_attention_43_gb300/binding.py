@@ -25,7 +25,8 @@ ATTN_ERR_DEVICE_TIMEOUT = 4
 ATTN_BF16 = 0
 ATTN_FP16 = 1
 
-EXPORTS = ("attn_fwd", "attn_decode", "attn_decode_paged", "attn_decode_noalloc",
+EXPORTS = ("attn_fwd", "attn_decode", "attn_decode_fused", "attn_decode_paged",
+           "attn_decode_noalloc",
            "attn_decode_workspace_bytes",
            "attn_decode_chunk", "attn_check_device_status", "attn_debug_set",
            "attn_status_string", "attn_version")
@@ -60,6 +61,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_fwd.restype = i
     lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
     lib.attn_decode.restype = i
+    lib.attn_decode_fused.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
+    lib.attn_decode_fused.restype = i
     lib.attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, vp]
     lib.attn_decode_paged.restype = i
     lib.attn_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
@@ -149,6 +152,27 @@ def attn_decode(q, k_cache, v_cache, seq_lens, *, num_splits: int = 0, out=None,
     st = lib.attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), _ptr(out), B, Hq,
                          Hkv, max_S, D, num_splits, _dtype_code(q), _stream(stream))
     _check(st, "attn_decode")
+    return out
+
+
+def attn_decode_fused(q, k_cache, v_cache, seq_lens, *, num_splits: int = 0, out=None,
+                      stream=None):
+    """``attn_decode`` in one kernel launch: the last split CTA of each (sequence,
+    head group) merges the group's chunk partials.  Calls that may overlap on the
+    GPU share the library's merge counters: order them on one stream."""
+    lib = load()
+    B, Hq, D = q.shape
+    Hkv, max_S = k_cache.shape[1], k_cache.shape[2]
+    for t in (q, k_cache, v_cache, seq_lens):
+        if not t.is_contiguous():
+            raise ValueError("decode inputs must be contiguous")
+    if seq_lens.dtype != torch.int32:
+        raise TypeError("seq_lens must be int32")
+    if out is None:
+        out = torch.empty_like(q)
+    st = lib.attn_decode_fused(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), _ptr(out),
+                               B, Hq, Hkv, max_S, D, num_splits, _dtype_code(q), _stream(stream))
+    _check(st, "attn_decode_fused")
     return out
 
 

@@ -195,43 +195,75 @@ static int decode_with_pool(ea::DecodeArgs& a, int dev, size_t bytes, cudaStream
   return from_cuda(e);
 }
 
-int attn_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* seq_lens,
-                void* o, int B, int Hq, int Hkv, int max_S, int D, int num_splits, int dtype,
-                cudaStream_t stream) {
+// Checks of the contiguous-cache decode entry points that need no CUDA call,
+// and their arguments.  Returns ATTN_OK with *empty set when B * Hq == 0.
+static int decode_contiguous_args(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* seq_lens, void* o, int B, int Hq, int Hkv,
+                                  int max_S, int D, int num_splits, int dtype, ea::DecodeArgs* a,
+                                  bool* empty) {
+  *empty = false;
   if (B < 0 || Hq < 0 || Hkv < 0 || max_S < 0 || num_splits < 0) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_UNSUPPORTED;
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
-  if ((long long)B * Hq == 0) return ATTN_OK;
+  if ((long long)B * Hq == 0) {
+    *empty = true;
+    return ATTN_OK;
+  }
   if (Hkv == 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (B > 65535 || Hkv > 65535 || Hq > 65535) return ATTN_ERR_UNSUPPORTED;
   if (!q || !o || !seq_lens || (max_S > 0 && (!k_cache || !v_cache))) return ATTN_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(o, 16) || !aligned(seq_lens, 4) ||
       (k_cache && !aligned(k_cache, 16)) || (v_cache && !aligned(v_cache, 16)))
     return ATTN_ERR_INVALID_ARG;
-  int dev = 0;
-  int st = check_device(&dev);
-  if (st != ATTN_OK) return st;
-
-  ea::DecodeArgs a{};
-  a.q = q;
-  a.k = k_cache;
-  a.v = v_cache;
-  a.seq_lens = seq_lens;
-  a.o = o;
-  a.B = B;
-  a.Hq = Hq;
-  a.Hkv = Hkv;
-  a.max_S = max_S;
-  a.D = D;
-  a.chunk = chunk_for(max_S, num_splits);
-  a.max_chunks = max_S > 0 ? (max_S + a.chunk - 1) / a.chunk : 0;
+  *a = ea::DecodeArgs{};
+  a->q = q;
+  a->k = k_cache;
+  a->v = v_cache;
+  a->seq_lens = seq_lens;
+  a->o = o;
+  a->B = B;
+  a->Hq = Hq;
+  a->Hkv = Hkv;
+  a->max_S = max_S;
+  a->D = D;
+  a->chunk = chunk_for(max_S, num_splits);
+  a->max_chunks = max_S > 0 ? (max_S + a->chunk - 1) / a->chunk : 0;
   // the split kernel numbers its (chunk, head group, sequence) items with an int
-  if ((long long)B * Hq * a.max_chunks > INT_MAX) return ATTN_ERR_UNSUPPORTED;
-  a.scale = 1.0f / sqrtf((float)D);
-  a.bf16 = dtype == ATTN_BF16;
-  a.wait_limit_ns = g_wait_limit_ns;
-  a.num_sms = g_num_sms[dev] > 0 ? g_num_sms[dev] : 1;
+  if ((long long)B * Hq * a->max_chunks > INT_MAX) return ATTN_ERR_UNSUPPORTED;
+  a->scale = 1.0f / sqrtf((float)D);
+  a->bf16 = dtype == ATTN_BF16;
+  a->wait_limit_ns = g_wait_limit_ns;
+  return ATTN_OK;
+}
 
+int attn_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* seq_lens,
+                void* o, int B, int Hq, int Hkv, int max_S, int D, int num_splits, int dtype,
+                cudaStream_t stream) {
+  ea::DecodeArgs a;
+  bool empty;
+  int st = decode_contiguous_args(q, k_cache, v_cache, seq_lens, o, B, Hq, Hkv, max_S, D,
+                                  num_splits, dtype, &a, &empty);
+  if (st != ATTN_OK || empty) return st;
+  int dev = 0;
+  if ((st = check_device(&dev)) != ATTN_OK) return st;
+  a.num_sms = g_num_sms[dev] > 0 ? g_num_sms[dev] : 1;
+  return decode_with_pool(a, dev, attn_decode_workspace_bytes(B, Hq, max_S, D, num_splits), stream);
+}
+
+int attn_decode_fused(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* seq_lens, void* o, int B, int Hq, int Hkv, int max_S, int D,
+                      int num_splits, int dtype, cudaStream_t stream) {
+  ea::DecodeArgs a;
+  bool empty;
+  int st = decode_contiguous_args(q, k_cache, v_cache, seq_lens, o, B, Hq, Hkv, max_S, D,
+                                  num_splits, dtype, &a, &empty);
+  if (st != ATTN_OK || empty) return st;
+  if ((size_t)B * Hq > ea::kDecodeTickets) return ATTN_ERR_UNSUPPORTED;
+  int dev = 0;
+  if ((st = check_device(&dev)) != ATTN_OK) return st;
+  a.num_sms = g_num_sms[dev] > 0 ? g_num_sms[dev] : 1;
+  cudaError_t e = ea::decode_tickets(dev, &a.tickets, stream);
+  if (e != cudaSuccess) return from_cuda(e);
   return decode_with_pool(a, dev, attn_decode_workspace_bytes(B, Hq, max_S, D, num_splits), stream);
 }
 
@@ -286,46 +318,19 @@ int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
 int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
                         const int32_t* seq_lens, void* o, int B, int Hq, int Hkv, int max_S, int D,
                         int num_splits, int dtype, cudaStream_t stream) {
-  if (B < 0 || Hq < 0 || Hkv < 0 || max_S < 0 || num_splits < 0) return ATTN_ERR_INVALID_ARG;
-  if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_UNSUPPORTED;
-  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
-  if ((long long)B * Hq == 0) return ATTN_OK;
-  if (Hkv == 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
-  if (B > 65535 || Hkv > 65535 || Hq > 65535) return ATTN_ERR_UNSUPPORTED;
-  if (!q || !o || !seq_lens || (max_S > 0 && (!k_cache || !v_cache))) return ATTN_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(o, 16) || !aligned(seq_lens, 4) ||
-      (k_cache && !aligned(k_cache, 16)) || (v_cache && !aligned(v_cache, 16)))
-    return ATTN_ERR_INVALID_ARG;
+  ea::DecodeArgs a;
+  bool empty;
+  int st = decode_contiguous_args(q, k_cache, v_cache, seq_lens, o, B, Hq, Hkv, max_S, D,
+                                  num_splits, dtype, &a, &empty);
+  if (st != ATTN_OK || empty) return st;
   // the partials must fit the fixed scratch: larger problems are refused, never allocated
   const size_t bytes = attn_decode_workspace_bytes(B, Hq, max_S, D, num_splits);
   if (bytes > ea::kNoallocPartialsBytes) return ATTN_ERR_UNSUPPORTED;
   int dev = 0;
-  int st = check_device(&dev);
-  if (st != ATTN_OK) return st;
-  float* scratch = nullptr;
-  cudaError_t e = ea::noalloc_partials(dev, &scratch);
+  if ((st = check_device(&dev)) != ATTN_OK) return st;
+  cudaError_t e = ea::noalloc_partials(dev, &a.partials);
   if (e != cudaSuccess) return from_cuda(e);
-
-  ea::DecodeArgs a{};
-  a.q = q;
-  a.k = k_cache;
-  a.v = v_cache;
-  a.seq_lens = seq_lens;
-  a.o = o;
-  a.B = B;
-  a.Hq = Hq;
-  a.Hkv = Hkv;
-  a.max_S = max_S;
-  a.D = D;
-  a.chunk = chunk_for(max_S, num_splits);
-  a.max_chunks = max_S > 0 ? (max_S + a.chunk - 1) / a.chunk : 0;
-  // the split kernel numbers its (chunk, head group, sequence) items with an int
-  if ((long long)B * Hq * a.max_chunks > INT_MAX) return ATTN_ERR_UNSUPPORTED;
-  a.scale = 1.0f / sqrtf((float)D);
-  a.bf16 = dtype == ATTN_BF16;
-  a.wait_limit_ns = g_wait_limit_ns;
   a.num_sms = g_num_sms[dev] > 0 ? g_num_sms[dev] : 1;
-  a.partials = scratch;
   return from_cuda(ea::launch_decode(a, stream));
 }
 

@@ -55,6 +55,8 @@ struct Params {
   // position j of sequence b is row j % page_size of page block_table[b, j / page_size]
   const int32_t* block_table;
   int page_size, max_pages, num_pages;
+  // single-launch decode: one zeroed counter per (sequence, head group) CTA row
+  unsigned* tickets;
 };
 
 __device__ __forceinline__ int clamp_len(const Params& p, int b) {
@@ -103,7 +105,10 @@ __device__ __forceinline__ uint64_t pair_of(uint32_t w) {
 // 512-key chunk is only 256 KB of K and V: with one CTA per chunk, each CTA's
 // first load and epilogue went unhidden (85 % of HBM bandwidth at chunk 512
 // against 94 % at chunk 2048).
-template <int D, int G, bool BF16, bool PAGED>
+template <int D, int G, bool BF16>
+__device__ __forceinline__ void merge_group(const Params& p, int b, int h0, int n, float* red, float* tot);
+
+template <int D, int G, bool BF16, bool PAGED, bool MERGE = false>
 __global__ void __launch_bounds__(THREADS) decode_split_kernel(const Params p) {
   using L = SplitLayout<D, G, PAGED>;
   constexpr int EPL = D / 8;   // key elements per lane when 8 lanes share a key
@@ -122,9 +127,18 @@ __global__ void __launch_bounds__(THREADS) decode_split_kernel(const Params p) {
   const int h0 = kvh * p.group + (blockIdx.y % (p.group / G)) * G;  // first query head of this CTA
   const int b = blockIdx.z;
   const int len = clamp_len(p, b);
+  const int nch = (len + p.chunk - 1) / p.chunk;                   // chunks of this sequence
   const int c0 = blockIdx.x * p.cpb;                                // first chunk of this CTA
-  const int c1 = min(c0 + p.cpb, (len + p.chunk - 1) / p.chunk);   // end of its chunks
-  if (c0 >= c1) return;
+  const int c1 = min(c0 + p.cpb, nch);                              // end of its chunks
+  if (c0 >= c1) {
+    if constexpr (MERGE) {
+      // an empty sequence has nothing to merge: its first CTA writes O = 0
+      if (len == 0 && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < G * D / 2; i += THREADS)
+          reinterpret_cast<uint32_t*>(p.o + ((size_t)b * p.Hq + h0) * D)[i] = 0u;
+    }
+    return;
+  }
   const size_t row0 = ((size_t)b * p.Hkv + kvh) * p.max_S;
   auto chunk_rows = [&](int c) -> int { return min(p.chunk, len - c * p.chunk); };
   auto ring_bar = [&](int j) -> uint32_t { return sb + L::BAR_OFF + 8 * (j % NST); };
@@ -218,19 +232,24 @@ __global__ void __launch_bounds__(THREADS) decode_split_kernel(const Params p) {
 
   int gl = 0;  // loads consumed
   bool ok = true;
+  uint64_t acc[G][DPL / 2];  // P V accumulators, pairs of adjacent output columns
   for (int c = c0; c < c1; ++c) {
     const int n = chunk_rows(c);
     const int nsub = (n + SUB - 1) / SUB;
-    if (threadIdx.x < G) {
+    // one partial per chunk; the single-launch decode runs the online softmax on
+    // across the CTA's chunks and writes one partial for all of them
+    const bool fresh = !MERGE || c == c0;
+    if (fresh && threadIdx.x < G) {
       m_run[threadIdx.x] = -INFINITY;
       l_run[threadIdx.x] = 0.f;
     }
     __syncthreads();
-    uint64_t acc[G][DPL / 2];  // P V accumulators, pairs of adjacent output columns
+    if (fresh) {
 #pragma unroll
-    for (int g = 0; g < G; ++g)
+      for (int g = 0; g < G; ++g)
 #pragma unroll
-      for (int e = 0; e < DPL / 2; ++e) acc[g][e] = zero2;
+        for (int e = 0; e < DPL / 2; ++e) acc[g][e] = zero2;
+    }
 
     for (int sub = 0; sub < nsub && ok; ++sub) {
       const int rows = min(SUB, n - sub * SUB);
@@ -372,9 +391,10 @@ __global__ void __launch_bounds__(THREADS) decode_split_kernel(const Params p) {
       }
     }
     if (!ok) break;
+    if (MERGE && c + 1 < c1) continue;  // the CTA's partial is written after its last chunk
 
     // ---------------------------------------- partials: cross-warp sum of P V
-    const size_t pbase = (((size_t)b * p.Hq + h0) * p.max_chunks + c) * (D + 2);
+    const size_t pbase = (((size_t)b * p.Hq + h0) * p.max_chunks + (MERGE ? c0 : c)) * (D + 2);
     const size_t hstride = (size_t)p.max_chunks * (D + 2);
 #pragma unroll
     for (int pass = 0; pass < G / L::GH; ++pass) {
@@ -410,6 +430,99 @@ __global__ void __launch_bounds__(THREADS) decode_split_kernel(const Params p) {
     for (int i = max(gl, issued - NST); i < issued; ++i)
       while (!mbar_try_wait(ring_bar(i), (i / NST) & 1))
         if (global_timer_ns() - t0 > p.wait_limit_ns) break;
+  }
+
+  if constexpr (MERGE) {
+    // Single launch: a ticket counts the finished CTAs of this (sequence, head
+    // group); the last one merges the group's partials and puts the ticket back
+    // to zero for the next call.  A CTA that gave up a wait still takes its
+    // ticket, so the count stays exact (its chunks' partials are not written and
+    // the status word reports it).
+    __threadfence();  // this thread's partial stores, ordered before the ticket
+    __syncthreads();
+    int* last = reinterpret_cast<int*>(smem + L::ABORT_OFF + 4);
+    if (threadIdx.x == 0) {
+      unsigned* t = p.tickets + (size_t)b * gridDim.y + blockIdx.y;
+      const int is_last = atomicAdd(t, 1u) == (unsigned)((nch + p.cpb - 1) / p.cpb - 1);
+      if (is_last) {
+        atomicExch(t, 0u);
+        __threadfence();  // the other CTAs' partials, ordered before this CTA's reads
+      }
+      *last = is_last;
+    }
+    __syncthreads();
+    if (*last) merge_group<D, G, BF16>(p, b, h0, (nch + p.cpb - 1) / p.cpb, red, sc);
+  }
+}
+
+// The reduce kernel's merge, run by the last CTA of a (sequence, head group) in
+// the single-launch decode over the n partials of the group's CTAs (partial x at
+// chunk slot x * cpb): WARPS / G warps per query head share the partials, each
+// warp weights its partials by e^(m_x - M) with the head's overall max M, and
+// the warps' sums are added in shared memory.  Partials are read from L2
+// (written by other CTAs of this launch).
+template <int D, int G, bool BF16>
+__device__ __forceinline__ void merge_group(const Params& p, int b, int h0, int n, float* red, float* tot) {
+  constexpr int DPL = D / 32;
+  constexpr int WPH = WARPS / G;  // warps per query head
+  constexpr int U = 4;            // chunks whose loads are issued together
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = warp / WPH, s = warp % WPH;
+  const float* base = p.part + ((size_t)b * p.Hq + h0 + g) * p.max_chunks * (D + 2);
+  float M = -INFINITY;
+  const size_t step = (size_t)p.cpb * (D + 2);
+  for (int c = lane; c < n; c += 32) M = fmaxf(M, __ldcg(base + c * step + D));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float acc[DPL];
+#pragma unroll
+  for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
+  float total = 0.f;
+  for (int cb = s * U; cb < n; cb += WPH * U) {
+    float m_c[U], l_c[U], oc[U][DPL];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      m_c[u] = -INFINITY;
+      l_c[u] = 0.f;
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) oc[u][e] = 0.f;
+      if (cb + u < n) {
+        const float* pc = base + (cb + u) * step;
+        m_c[u] = __ldcg(pc + D);
+        l_c[u] = __ldcg(pc + D + 1);
+#pragma unroll
+        for (int e2 = 0; e2 < DPL / 2; ++e2) {
+          const float2 t = __ldcg(reinterpret_cast<const float2*>(pc + lane * DPL) + e2);
+          oc[u][2 * e2] = t.x;
+          oc[u][2 * e2 + 1] = t.y;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (!(m_c[u] > -1e30f)) continue;  // past the last partial
+      const float w = ex2((m_c[u] - M) * 1.4426950408889634f);
+      total = fmaf(l_c[u], w, total);
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) acc[e] = fmaf(oc[u][e], w, acc[e]);
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < DPL; ++e) red[warp * D + lane * DPL + e] = acc[e];
+  if (lane == 0) tot[warp] = total;
+  __syncthreads();
+  for (int i = threadIdx.x; i < G * D / 2; i += THREADS) {
+    const int gg = (2 * i) / D, d = (2 * i) % D;
+    float a0 = 0.f, a1 = 0.f, t = 0.f;
+#pragma unroll
+    for (int w = 0; w < WPH; ++w) {
+      a0 += red[(gg * WPH + w) * D + d];
+      a1 += red[(gg * WPH + w) * D + d + 1];
+      t += tot[gg * WPH + w];
+    }
+    const float inv = t > 0.f ? 1.f / t : 0.f;
+    reinterpret_cast<uint32_t*>(p.o + ((size_t)b * p.Hq + h0 + gg) * D)[d / 2] =
+        pack2<BF16>(a0 * inv, a1 * inv);
   }
 }
 
@@ -476,19 +589,20 @@ __global__ void __launch_bounds__(32) decode_reduce_kernel(const Params p) {
   }
 }
 
-template <int D, int G, bool BF16, bool PAGED>
+template <int D, int G, bool BF16, bool PAGED, bool MERGE = false>
 static cudaError_t launch_split(const DecodeArgs& a, const Params& p, cudaStream_t stream) {
   using L = SplitLayout<D, G, PAGED>;
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G, BF16, PAGED>,
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G, BF16, PAGED, MERGE>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
   if (e != cudaSuccess) return e;
   dim3 grid((a.max_chunks + p.cpb - 1) / p.cpb, a.Hkv * (p.group / G), a.B);
-  decode_split_kernel<D, G, BF16, PAGED><<<grid, THREADS, L::BYTES, stream>>>(p);
+  decode_split_kernel<D, G, BF16, PAGED, MERGE><<<grid, THREADS, L::BYTES, stream>>>(p);
   return cudaGetLastError();
 }
 
 template <int D, int G, bool BF16>
 static cudaError_t launch_t(const DecodeArgs& a, const Params& p, cudaStream_t stream) {
+  if (a.max_chunks > 0 && p.tickets) return launch_split<D, G, BF16, false, true>(a, p, stream);
   if (a.max_chunks > 0) {
     // the contiguous-cache kernel is a separate instantiation, free of the page logic
     const cudaError_t e = p.block_table ? launch_split<D, G, BF16, true>(a, p, stream)
@@ -545,6 +659,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.page_size = a.page_size;
   p.max_pages = a.max_pages;
   p.num_pages = a.num_pages;
+  p.tickets = a.tickets;
   if (a.D == 64) return a.bf16 ? dec::launch_d<64, true>(a, p, stream) : dec::launch_d<64, false>(a, p, stream);
   return a.bf16 ? dec::launch_d<128, true>(a, p, stream) : dec::launch_d<128, false>(a, p, stream);
 }
@@ -577,6 +692,32 @@ cudaError_t noalloc_partials(int device, float** out) {
     g_noalloc_ptr[device] = static_cast<float*>(ptr);
   }
   *out = g_noalloc_ptr[device];
+  return cudaSuccess;
+}
+
+// Tickets of the single-launch decode (attn_decode_fused): one counter per
+// (sequence, head group) row of split-kernel CTAs.  Every counter is zero
+// between calls: the CTA that finds itself last in its row puts it back.  The
+// array is zeroed once per device on first use, on the calling stream.  Calls
+// whose kernels overlap on the GPU share the counters and must not run at once.
+static __device__ unsigned g_decode_tickets[kDecodeTickets];
+
+namespace {
+unsigned* g_ticket_ptr[64];
+}  // namespace
+
+cudaError_t decode_tickets(int device, unsigned** out, cudaStream_t stream) {
+  if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_ticket_ptr[device]) {
+    void* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_decode_tickets);
+    if (e != cudaSuccess) return e;
+    e = cudaMemsetAsync(ptr, 0, sizeof(unsigned) * kDecodeTickets, stream);
+    if (e != cudaSuccess) return e;
+    g_ticket_ptr[device] = static_cast<unsigned*>(ptr);
+  }
+  *out = g_ticket_ptr[device];
   return cudaSuccess;
 }
 

@@ -36,6 +36,9 @@ struct DecodeArgs {
   // paged cache: block_table != nullptr, see attn_decode_paged
   const int32_t* block_table;
   int page_size, max_pages, num_pages;
+  // single launch (attn_decode_fused): zeroed counters, one per (sequence, head
+  // group); nullptr selects the split kernel + reduce kernel pair
+  unsigned* tickets;
   float scale;
   int bf16;
   uint64_t wait_limit_ns;
@@ -64,5 +67,11 @@ constexpr size_t kNoallocPartialsBytes = 16u << 20;
 // Device address of that scratch on `device`, which must be the current device;
 // resolved with cudaGetSymbolAddress on the first request per device.
 cudaError_t noalloc_partials(int device, float** out);
+
+// Counters of the single-launch decode: at least B * Hq of them are needed.
+constexpr size_t kDecodeTickets = 1u << 20;
+// Device address of those counters on `device` (the current device); the first
+// request per device zeroes them with a memset enqueued on `stream`.
+cudaError_t decode_tickets(int device, unsigned** out, cudaStream_t stream);
 
 }  // namespace ea

@@ -2,7 +2,7 @@
 
     python -m exact_attention_43_gb300.runcase fwd --workload mha [--iters 3]
     python -m exact_attention_43_gb300.runcase fwd --B 1 --H 8 --S 4096 --causal 1
-    python -m exact_attention_43_gb300.runcase decode [--B 8] [--iters 3] [--page-size 64]
+    python -m exact_attention_43_gb300.runcase decode [--B 8] [--iters 3] [--page-size 64 | --fused]
 
 Inputs are drawn on the GPU from the seeded generators in workloads.py.
 Prints one JSON line with the mean CUDA-event time per call.
@@ -32,6 +32,7 @@ def main():
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--warmup", type=int, default=1)
     ap.add_argument("--page-size", type=int, default=0, help="decode over a paged cache")
+    ap.add_argument("--fused", action="store_true", help="single-launch decode (attn_decode_fused)")
     a = ap.parse_args()
     dev = torch.device("cuda", 0)
     ea.load()
@@ -65,6 +66,11 @@ def main():
 
             def call():
                 return ea.attn_decode_paged(q, kp, vp, table, lens_d, num_splits=d.num_splits)
+        elif a.fused:
+            desc += " fused"
+
+            def call():
+                return ea.attn_decode_fused(q, k, v, lens_d, num_splits=d.num_splits)
         else:
             def call():
                 return ea.attn_decode(q, k, v, lens_d, num_splits=d.num_splits)

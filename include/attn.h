@@ -99,6 +99,26 @@ int attn_decode(const void* q, const void* k_cache, const void* v_cache, const i
                 cudaStream_t stream);
 
 /*
+ * attn_decode_fused -- attn_decode in one kernel launch.
+ *
+ * Same arguments, layouts, chunking, partials workspace and status codes as
+ * attn_decode; the result agrees with it to fp32 rounding (the merge adds the
+ * chunk terms in another order).  Instead of a second (reduce) kernel, each
+ * split-kernel CTA takes a ticket from a counter of its (sequence, head group)
+ * when its partials are written, and the CTA that takes the last ticket merges
+ * that group's partials by the same LSE rescaling and writes O.  The counters
+ * are a library-owned device array, zeroed once per device by a memset that
+ * the first call enqueues on its stream (make that first call before any
+ * stream capture begins) and left at zero by every call.  Calls whose kernels
+ * may overlap on the GPU (two streams with no ordering between them) share
+ * the counters: order them on one stream or with events.
+ * B * Hq <= 1048576, else ATTN_ERR_UNSUPPORTED before any CUDA call.
+ */
+int attn_decode_fused(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* seq_lens, void* o, int B, int Hq, int Hkv, int max_S, int D,
+                      int num_splits, int dtype, cudaStream_t stream);
+
+/*
  * attn_decode_paged -- attn_decode over a paged KV cache.
  *
  * Same computation, chunking, partials and merge as attn_decode; only where

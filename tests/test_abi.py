@@ -94,6 +94,23 @@ def test_decode_argument_errors(lib):
     assert dec(lib, B=0) == 0
 
 
+def test_fused_decode_argument_errors(lib):
+    def fused(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, lens=FAKE, o=FAKE, B=2, Hq=8, Hkv=2, max_S=64, D=128,
+                 splits=0, dtype=0)
+        a.update(kw)
+        return lib.attn_decode_fused(a["q"], a["k"], a["v"], a["lens"], a["o"], a["B"], a["Hq"],
+                                     a["Hkv"], a["max_S"], a["D"], a["splits"], a["dtype"], None)
+
+    assert fused(lens=None) == 1
+    assert fused(Hkv=3) == 1
+    assert fused(o=FAKE + 4) == 1
+    assert fused(D=32) == 2
+    assert fused(B=0) == 0
+    # more (sequence, query head) pairs than merge counters: refused before any CUDA call
+    assert fused(B=32769, Hq=32, Hkv=8) == 2
+
+
 def paged(lib, q=FAKE, kp=FAKE, vp=FAKE, bt=FAKE, lens=FAKE, o=FAKE, B=2, Hq=8, Hkv=2, num_pages=4,
           page_size=16, max_pages=4, D=128, splits=0, dtype=0):
     return lib.attn_decode_paged(q, kp, vp, bt, lens, o, B, Hq, Hkv, num_pages, page_size, max_pages,
