@@ -15,12 +15,17 @@ one, single-key and constant-V closed forms, causal row 0, scale = 0 gives the
 mean of V and ln|A|, permutation invariance, GQA == MHA with repeated KV heads,
 decode == prefill with one query over the prefix, chunked merge == unchunked,
 hand-worked examples in ``tests/golden/``, PyTorch's float64 math-path
-``scaled_dot_product_attention`` and a pure-Python brute force on tiny shapes.
+``scaled_dot_product_attention`` and a pure-Python brute force on tiny shapes;
+sliding windows against a brute force with explicit key sets, the diagonal
+window's closed form and PyTorch SDPA on the explicit key slice; packed
+variable-length batches against the batched definition (equal lengths) and
+PyTorch SDPA per sequence.
 No function here is "parity unpinned".
 """
 
 from .attention import (  # noqa: F401
     sdpa,
+    sdpa_varlen,
     softmax_probs,
     decode,
     decode_partials,

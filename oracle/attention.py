@@ -33,7 +33,16 @@ Readings where the pages are silent (each also listed in the design doc):
   length 0 has O = 0;
 * the per-chunk partial o_c is unnormalised (sum of e^(s - m_c) v), the only
   reading under which the reduce's arithmetic gives the softmax;
-* the chunk max m_c is in the natural-log units of the scaled scores.
+* the chunk max m_c is in the natural-log units of the scaled scores;
+* local (sliding-window) attention, which the flash-attention backward page
+  names only as an ``Is_local`` switch, keeps key j for query i iff
+  i + d - window_left <= j <= i + d + window_right with d = Skv - Sq (the
+  same bottom-right alignment as the causal mask); a bound of -1 is absent,
+  and causal is the right bound 0;
+* variable-length batches (the same page's ``Varlen`` switch) are packed:
+  sequence b owns query rows [cu_q[b], cu_q[b+1]) of a [total_q, H, D] array
+  and key rows [cu_k[b], cu_k[b+1]) of [total_k, Hkv, D]; each sequence is
+  attended on its own, and its LSE goes to an [H, total_q] array.
 
 Every array is converted to float64 first; no blocking, fusion or reordering
 is applied beyond restricting the score matrix to the requested query rows.
@@ -53,20 +62,30 @@ def _f64(x) -> np.ndarray:
     return np.asarray(x, dtype=np.float64)
 
 
-def _visible(rows: np.ndarray, Sq: int, Skv: int, causal: bool) -> np.ndarray:
+def _visible(rows: np.ndarray, Sq: int, Skv: int, causal: bool, window_left: int = -1,
+             window_right: int = -1) -> np.ndarray:
     """Boolean [R, Skv] mask of the keys each query row may attend to.
 
     Causal mask as in rustytorch ``flash_attention_forward_small_kernel``
     (score set to -inf when the key position is after the query position),
-    aligned bottom-right so that the last query sees every key.
+    aligned bottom-right so that the last query sees every key.  A window
+    bound w >= 0 keeps only keys within w positions of the row's diagonal
+    key on that side.
     """
     j = np.arange(Skv)[None, :]
-    if not causal:
-        return np.ones((rows.shape[0], Skv), dtype=bool)
-    return j <= (rows[:, None] + (Skv - Sq))
+    diag = rows[:, None] + (Skv - Sq)               # the row's diagonal key
+    keep = np.ones((rows.shape[0], Skv), dtype=bool)
+    if causal:
+        keep &= j <= diag
+    if window_right >= 0:
+        keep &= j <= diag + window_right
+    if window_left >= 0:
+        keep &= j >= diag - window_left
+    return keep
 
 
-def softmax_probs(q, k, *, causal: bool, scale: float, rows=None):
+def softmax_probs(q, k, *, causal: bool, scale: float, rows=None, window_left: int = -1,
+                  window_right: int = -1):
     """Materialised attention probabilities P for one head.
 
     q: [Sq, D], k: [Skv, D].  Returns (P [R, Skv], m [R], l [R]) in float64,
@@ -79,7 +98,10 @@ def softmax_probs(q, k, *, causal: bool, scale: float, rows=None):
     Sq, Skv = q.shape[0], k.shape[0]
     rows = np.arange(Sq) if rows is None else np.asarray(rows, dtype=np.int64)
     s = scale * (q[rows] @ k.T)                      # score rows, materialised
-    vis = _visible(rows, Sq, Skv, causal)
+    if window_left == -1 and window_right == -1:
+        vis = _visible(rows, Sq, Skv, causal)
+    else:
+        vis = _visible(rows, Sq, Skv, causal, window_left, window_right)
     s = np.where(vis, s, -np.inf)
     m = s.max(axis=1) if Skv > 0 else np.full(rows.shape[0], -np.inf)
     empty = ~np.isfinite(m)
@@ -91,7 +113,8 @@ def softmax_probs(q, k, *, causal: bool, scale: float, rows=None):
     return p, np.where(empty, -np.inf, m), np.where(empty, 0.0, l)
 
 
-def sdpa(q, k, v, *, causal: bool, scale: float, rows=None):
+def sdpa(q, k, v, *, causal: bool, scale: float, rows=None, window_left: int = -1,
+         window_right: int = -1):
     """Exact attention O = softmax(scale Q K^T [+ causal mask]) V and its LSE.
 
     q: [B, Hq, Sq, D]; k, v: [B, Hkv, Skv, D] with Hq a multiple of Hkv.
@@ -99,7 +122,8 @@ def sdpa(q, k, v, *, causal: bool, scale: float, rows=None):
     mapping in abaddon ``flash_attention_f16``).
 
     rows: None (every query row), a 1-D index array used for every head, or a
-    2-D [Hq, R] array of per-head row indices.  Returns
+    2-D [Hq, R] array of per-head row indices.  window_left / window_right:
+    sliding-window bounds (-1: none), see ``_visible``.  Returns
     (O [B, Hq, R, D], LSE [B, Hq, R]) in float64; LSE = m + ln(l) in natural
     log of the scaled scores, -inf for a row with no visible key.
     """
@@ -125,10 +149,46 @@ def sdpa(q, k, v, *, causal: bool, scale: float, rows=None):
         for h in range(Hq):
             kv = h // group
             p, m, l = softmax_probs(q[b, h], k[b, kv], causal=causal, scale=scale,
-                                    rows=rows_h[h])
+                                    rows=rows_h[h], window_left=window_left,
+                                    window_right=window_right)
             out[b, h] = p @ v[b, kv]
             with np.errstate(divide="ignore"):
                 lse[b, h] = np.where(l > 0, m + np.log(np.where(l > 0, l, 1.0)), -np.inf)
+    return out, lse
+
+
+def sdpa_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, *, causal: bool, scale: float,
+                window_left: int = -1, window_right: int = -1):
+    """Attention over a packed batch of sequences of different lengths.
+
+    q: [total_q, Hq, D]; k, v: [total_k, Hkv, D]; cu_seqlens_q, cu_seqlens_k:
+    [B + 1] non-decreasing offsets.  Sequence b is the plain ``sdpa`` of its
+    own rows (query rows cu_q[b]..cu_q[b+1]-1, key rows cu_k[b]..cu_k[b+1]-1),
+    with its own bottom-right causal / window alignment.  Returns
+    (O [total_q, Hq, D], LSE [Hq, total_q]) float64; rows outside every
+    sequence are 0 in O and -inf in LSE.
+    """
+    q = _f64(q)
+    k = _f64(k)
+    v = _f64(v)
+    cq = [int(x) for x in np.asarray(_f64(cu_seqlens_q)).reshape(-1)]
+    ck = [int(x) for x in np.asarray(_f64(cu_seqlens_k)).reshape(-1)]
+    if len(cq) != len(ck):
+        raise ValueError("cu_seqlens_q and cu_seqlens_k need the same length")
+    total_q, Hq, D = q.shape
+    out = np.zeros((total_q, Hq, D))
+    lse = np.full((Hq, total_q), -np.inf)
+    for b in range(len(cq) - 1):
+        q0, q1, k0, k1 = cq[b], cq[b + 1], ck[b], ck[b + 1]
+        if q1 <= q0:
+            continue
+        qb = q[q0:q1].transpose(1, 0, 2)[None]       # [1, Hq, Sq_b, D]
+        kb = k[k0:k1].transpose(1, 0, 2)[None]
+        vb = v[k0:k1].transpose(1, 0, 2)[None]
+        ob, lb = sdpa(qb, kb, vb, causal=causal, scale=scale, window_left=window_left,
+                      window_right=window_right)
+        out[q0:q1] = ob[0].transpose(1, 0, 2)
+        lse[:, q0:q1] = lb[0]
     return out, lse
 
 

@@ -1,8 +1,9 @@
 """Pins that tie the float64 oracle to what the definition of attention fixes.
 
 Each pin is a function ``pin_*(impl)`` that raises AssertionError when the
-implementation ``impl`` (a namespace with ``sdpa``, ``softmax_probs``,
-``decode``, ``decode_partials`` and ``merge_partials``) disagrees with a fact
+implementation ``impl`` (a namespace with ``sdpa``, ``sdpa_varlen``,
+``softmax_probs``, ``decode``, ``decode_partials`` and ``merge_partials``)
+disagrees with a fact
 that does not depend on the oracle: a closed form, an invariant, a hand-worked
 example, an independent library routine or a brute-force loop.  The same pins
 run against the real oracle (must all pass) and against mutants of it with a
@@ -202,6 +203,130 @@ def pin_empty_rows(impl):
     _close(o[0, 0, 3], v[0, 0, 0], 1e-12, "first non-empty row")
 
 
+# ------------------------------------------------ sliding window and varlen pins
+
+def _window_keys(i, Sq, Skv, causal, wl, wr):
+    """Keys query i keeps, enumerated one by one from the window's wording."""
+    diag = i + Skv - Sq
+    keys = []
+    for j in range(Skv):
+        if causal and j > diag:
+            continue
+        if wr >= 0 and j > diag + wr:
+            continue
+        if wl >= 0 and j < diag - wl:
+            continue
+        keys.append(j)
+    return keys
+
+
+WINDOW_CASES = [  # (Sq, Skv, causal, window_left, window_right)
+    (6, 6, True, 2, -1), (6, 6, False, 1, 2), (5, 9, True, 3, -1), (9, 5, True, 0, -1),
+    (7, 7, False, -1, 0), (7, 7, False, 0, -1), (4, 10, False, 2, 2), (8, 3, False, 1, 1),
+    (6, 6, True, 0, 5),
+]
+
+
+def pin_window_brute_force(impl):
+    """Pure-Python loops over the explicitly enumerated key set of each row."""
+    for n, (Sq, Skv, causal, wl, wr) in enumerate(WINDOW_CASES):
+        q, k, v = _rand((1, 2, Sq, 3), 300 + n), _rand((1, 1, Skv, 3), 320 + n), _rand((1, 1, Skv, 3), 340 + n)
+        o, lse = impl.sdpa(q, k, v, causal=causal, scale=0.9, window_left=wl, window_right=wr)
+        for h in range(2):
+            for i in range(Sq):
+                keys = _window_keys(i, Sq, Skv, causal, wl, wr)
+                if not keys:
+                    assert np.all(o[0, h, i] == 0) and np.isneginf(lse[0, h, i]), f"window {n} empty row"
+                    continue
+                sc = [0.9 * sum(q[0, h, i, d] * k[0, 0, j, d] for d in range(3)) for j in keys]
+                mx = max(sc)
+                w = [math.exp(x - mx) for x in sc]
+                tot = sum(w)
+                want = [sum(w[t] * v[0, 0, j, d] for t, j in enumerate(keys)) / tot for d in range(3)]
+                _close(o[0, h, i], want, 1e-12, f"window case {n} row {i} O")
+                _close(lse[0, h, i], mx + math.log(tot), 1e-12, f"window case {n} row {i} LSE")
+
+
+def pin_window_diagonal(impl):
+    """A window of width zero keeps only the diagonal key: O = V[i + d], LSE = its score."""
+    for Sq, Skv in ((5, 5), (3, 8)):
+        q, k, v = _rand((1, 1, Sq, 4), 360), _rand((1, 1, Skv, 4), 361), _rand((1, 1, Skv, 4), 362)
+        d = Skv - Sq
+        for causal, wr in ((True, -1), (False, 0)):
+            o, lse = impl.sdpa(q, k, v, causal=causal, scale=0.6, window_left=0, window_right=wr)
+            _close(o[0, 0], v[0, 0, d:d + Sq], 1e-12, "diagonal window O")
+            _close(lse[0, 0], 0.6 * np.einsum("id,id->i", q[0, 0], k[0, 0, d:d + Sq]), 1e-12,
+                   "diagonal window LSE")
+
+
+def pin_window_torch_slice(impl):
+    """Each row equals PyTorch SDPA (no mask) over that row's contiguous key slice."""
+    Sq, Skv = 9, 13
+    q, k, v = _rand((1, 1, Sq, 5), 370), _rand((1, 1, Skv, 5), 371), _rand((1, 1, Skv, 5), 372)
+    tq, tk, tv = (torch.from_numpy(x) for x in (q, k, v))
+    for causal, wl, wr in ((True, 3, -1), (False, 2, 4), (False, 5, 0)):
+        o, lse = impl.sdpa(q, k, v, causal=causal, scale=0.4, window_left=wl, window_right=wr)
+        for i in range(Sq):
+            diag = i + Skv - Sq
+            lo = max(0, diag - wl)
+            hi = min(Skv - 1, diag if causal else diag + wr)
+            want = torch.nn.functional.scaled_dot_product_attention(
+                tq[:, :, i:i + 1], tk[:, :, lo:hi + 1], tv[:, :, lo:hi + 1], scale=0.4)
+            want_l = torch.logsumexp(0.4 * (tk[0, 0, lo:hi + 1] @ tq[0, 0, i]), dim=0)
+            _close(o[0, 0, i], want[0, 0, 0].numpy(), 1e-10, f"slice row {i} O")
+            _close(lse[0, 0, i], float(want_l), 1e-10, f"slice row {i} LSE")
+
+
+def pin_window_wide_is_plain(impl):
+    """Windows at least as wide as the keys change nothing."""
+    q, k, v = _rand((2, 2, 7, 4), 380), _rand((2, 1, 11, 4), 381), _rand((2, 1, 11, 4), 382)
+    for causal in (False, True):
+        o0, l0 = impl.sdpa(q, k, v, causal=causal, scale=0.7)
+        o1, l1 = impl.sdpa(q, k, v, causal=causal, scale=0.7, window_left=11, window_right=11)
+        _close(o1, o0, 1e-12, "wide window O")
+        _close(l1, l0, 1e-12, "wide window LSE")
+
+
+def _cu(lens):
+    return np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+
+
+def pin_varlen_equal_lengths(impl):
+    """Packed sequences of one length equal the batched [B, H, S, D] definition."""
+    B, S, Hq, Hkv, D = 3, 6, 4, 2, 5
+    q, k, v = _rand((B, S, Hq, D), 390), _rand((B, S, Hkv, D), 391), _rand((B, S, Hkv, D), 392)
+    cu = _cu([S] * B)
+    for causal, wl in ((True, -1), (False, -1), (True, 2)):
+        o, lse = impl.sdpa_varlen(q.reshape(B * S, Hq, D), k.reshape(B * S, Hkv, D),
+                                  v.reshape(B * S, Hkv, D), cu, cu, causal=causal, scale=0.5,
+                                  window_left=wl)
+        want_o, want_l = impl.sdpa(q.transpose(0, 2, 1, 3), k.transpose(0, 2, 1, 3),
+                                   v.transpose(0, 2, 1, 3), causal=causal, scale=0.5, window_left=wl)
+        _close(o, want_o.transpose(0, 2, 1, 3).reshape(B * S, Hq, D), 1e-12, "varlen equal O")
+        _close(lse, want_l.transpose(1, 0, 2).reshape(Hq, B * S), 1e-12, "varlen equal LSE")
+
+
+def pin_varlen_torch_per_sequence(impl):
+    """Ragged packed batches: every sequence equals PyTorch SDPA on its own rows."""
+    lq, lk = [5, 0, 3, 7], [4, 6, 3, 9]          # query and key lengths differ per sequence
+    cq, ck = _cu(lq), _cu(lk)
+    Hq, D = 2, 4
+    q, k, v = _rand((int(cq[-1]) + 2, Hq, D), 400), _rand((int(ck[-1]), 1, D), 401), _rand((int(ck[-1]), 1, D), 402)
+    o, lse = impl.sdpa_varlen(q, k, v, cq, ck, causal=False, scale=0.8)
+    for b in range(4):
+        if lq[b] == 0:
+            continue
+        tq = torch.from_numpy(q[cq[b]:cq[b + 1]]).permute(1, 0, 2)[None]
+        tk = torch.from_numpy(k[ck[b]:ck[b + 1]]).permute(1, 0, 2)[None].expand(1, Hq, -1, -1)
+        tv = torch.from_numpy(v[ck[b]:ck[b + 1]]).permute(1, 0, 2)[None].expand(1, Hq, -1, -1)
+        want = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, scale=0.8)
+        want_l = torch.logsumexp(0.8 * tq @ tk.transpose(-1, -2), dim=-1)
+        _close(o[cq[b]:cq[b + 1]], want[0].permute(1, 0, 2).numpy(), 1e-10, f"varlen seq {b} O")
+        _close(lse[:, cq[b]:cq[b + 1]], want_l[0].numpy(), 1e-10, f"varlen seq {b} LSE")
+    assert np.all(o[int(cq[-1]):] == 0) and np.all(np.isneginf(lse[:, int(cq[-1]):])), \
+        "rows outside every sequence"
+
+
 # ----------------------------------------------------------------- decode pins
 
 def _decode_case(seed, B=3, Hq=4, Hkv=2, max_S=40, D=8):
@@ -264,6 +389,8 @@ ALL_PINS = [
     pin_permutation, pin_gqa_equals_repeated_mha, pin_rows_subset, pin_torch_math_sdpa,
     pin_brute_force, pin_hand_worked, pin_empty_rows, pin_decode_equals_prefill,
     pin_decode_zero_len, pin_chunked_equals_unchunked, pin_partials_definition,
+    pin_window_brute_force, pin_window_diagonal, pin_window_torch_slice, pin_window_wide_is_plain,
+    pin_varlen_equal_lengths, pin_varlen_torch_per_sequence,
 ]
 
 

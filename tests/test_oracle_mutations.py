@@ -12,8 +12,9 @@ import oracle
 from oracle import attention as A
 from tests import pins
 
-BASE = dict(sdpa=oracle.sdpa, softmax_probs=oracle.softmax_probs, decode=oracle.decode,
-            decode_partials=oracle.decode_partials, merge_partials=oracle.merge_partials)
+BASE = dict(sdpa=oracle.sdpa, sdpa_varlen=oracle.sdpa_varlen, softmax_probs=oracle.softmax_probs,
+            decode=oracle.decode, decode_partials=oracle.decode_partials,
+            merge_partials=oracle.merge_partials)
 
 
 def _impl(**over):
@@ -24,35 +25,92 @@ def _impl(**over):
 
 def _with_visible(fn):
     """Run the oracle with a mutated causal visibility rule."""
-    def sdpa(q, k, v, *, causal, scale, rows=None):
+    def sdpa(q, k, v, *, causal, scale, rows=None, **kw):
         saved = A._visible
         A._visible = fn
         try:
-            return oracle.sdpa(q, k, v, causal=causal, scale=scale, rows=rows)
+            return oracle.sdpa(q, k, v, causal=causal, scale=scale, rows=rows, **kw)
         finally:
             A._visible = saved
 
-    def probs(q, k, *, causal, scale, rows=None):
+    def probs(q, k, *, causal, scale, rows=None, **kw):
         saved = A._visible
         A._visible = fn
         try:
-            return oracle.softmax_probs(q, k, causal=causal, scale=scale, rows=rows)
+            return oracle.softmax_probs(q, k, causal=causal, scale=scale, rows=rows, **kw)
         finally:
             A._visible = saved
-    return dict(sdpa=sdpa, softmax_probs=probs)
+
+    def varlen(*a, **kw):
+        saved = A._visible
+        A._visible = fn
+        try:
+            return oracle.sdpa_varlen(*a, **kw)
+        finally:
+            A._visible = saved
+    return dict(sdpa=sdpa, softmax_probs=probs, sdpa_varlen=varlen)
 
 
-def _strict(rows, Sq, Skv, causal):
+def _windowed(causal_rule):
+    """A visibility rule with the given causal test and the real window bounds."""
+    def rule(rows, Sq, Skv, causal, window_left=-1, window_right=-1):
+        j = np.arange(Skv)[None, :]
+        diag = rows[:, None] + (Skv - Sq)
+        keep = causal_rule(j, rows[:, None], diag) if causal else np.ones((rows.shape[0], Skv), bool)
+        if window_right >= 0:
+            keep = keep & (j <= diag + window_right)
+        if window_left >= 0:
+            keep = keep & (j >= diag - window_left)
+        return keep
+    return rule
+
+
+_strict = _windowed(lambda j, i, diag: j < diag)
+_top_left = _windowed(lambda j, i, diag: j <= i)
+
+
+def _window_left_strict(rows, Sq, Skv, causal, window_left=-1, window_right=-1):
     j = np.arange(Skv)[None, :]
-    return np.ones((rows.shape[0], Skv), bool) if not causal else j < rows[:, None] + (Skv - Sq)
+    diag = rows[:, None] + (Skv - Sq)
+    keep = (j <= diag) if causal else np.ones((rows.shape[0], Skv), bool)
+    if window_right >= 0:
+        keep = keep & (j <= diag + window_right)
+    if window_left >= 0:
+        keep = keep & (j > diag - window_left)     # mistake: drops the key at the bound
+    return keep
 
 
-def _top_left(rows, Sq, Skv, causal):
+def _window_top_left(rows, Sq, Skv, causal, window_left=-1, window_right=-1):
     j = np.arange(Skv)[None, :]
-    return np.ones((rows.shape[0], Skv), bool) if not causal else j <= rows[:, None]
+    diag = rows[:, None] + (Skv - Sq)
+    keep = (j <= diag) if causal else np.ones((rows.shape[0], Skv), bool)
+    if window_right >= 0:
+        keep = keep & (j <= diag + window_right)
+    if window_left >= 0:
+        keep = keep & (j >= rows[:, None] - window_left)   # mistake: left bound not aligned
+    return keep
 
 
-def _sdpa_gqa_modulo(q, k, v, *, causal, scale, rows=None):
+def _window_right_ignored(rows, Sq, Skv, causal, window_left=-1, window_right=-1):
+    j = np.arange(Skv)[None, :]
+    diag = rows[:, None] + (Skv - Sq)
+    keep = (j <= diag) if causal else np.ones((rows.shape[0], Skv), bool)
+    if window_left >= 0:
+        keep = keep & (j >= diag - window_left)
+    return keep
+
+
+def _varlen_shared_offsets(q, k, v, cq, ck, **kw):
+    # mistake: the key rows of each sequence taken at the query offsets
+    return oracle.sdpa_varlen(q, k, v, cq, cq, **kw)
+
+
+def _varlen_lse_row_major(q, k, v, cq, ck, **kw):
+    o, lse = oracle.sdpa_varlen(q, k, v, cq, ck, **kw)
+    return o, lse.reshape(-1).reshape(lse.shape[1], lse.shape[0]).T
+
+
+def _sdpa_gqa_modulo(q, k, v, *, causal, scale, rows=None, **kw):
     q, k, v = (A._f64(x) for x in (q, k, v))
     Hq, Hkv = q.shape[1], k.shape[1]
     outs, lses = [], []
@@ -66,16 +124,16 @@ def _sdpa_gqa_modulo(q, k, v, *, causal, scale, rows=None):
     return np.concatenate(outs, axis=1), np.concatenate(lses, axis=1)
 
 
-def _sdpa_no_scale(q, k, v, *, causal, scale, rows=None):
-    return oracle.sdpa(q, k, v, causal=causal, scale=1.0, rows=rows)
+def _sdpa_no_scale(q, k, v, *, causal, scale, rows=None, **kw):
+    return oracle.sdpa(q, k, v, causal=causal, scale=1.0, rows=rows, **kw)
 
 
-def _sdpa_lse_log2(q, k, v, *, causal, scale, rows=None):
-    o, lse = oracle.sdpa(q, k, v, causal=causal, scale=scale, rows=rows)
+def _sdpa_lse_log2(q, k, v, *, causal, scale, rows=None, **kw):
+    o, lse = oracle.sdpa(q, k, v, causal=causal, scale=scale, rows=rows, **kw)
     return o, lse / math.log(2.0)
 
 
-def _sdpa_lse_no_max(q, k, v, *, causal, scale, rows=None):
+def _sdpa_lse_no_max(q, k, v, *, causal, scale, rows=None, **kw):
     o, lse = oracle.sdpa(q, k, v, causal=causal, scale=scale, rows=rows)
     _, m, l = (None, None, None)
     out_l = np.empty_like(lse)
@@ -90,7 +148,7 @@ def _sdpa_lse_no_max(q, k, v, *, causal, scale, rows=None):
     return o, out_l
 
 
-def _sdpa_transposed_scores(q, k, v, *, causal, scale, rows=None):
+def _sdpa_transposed_scores(q, k, v, *, causal, scale, rows=None, **kw):
     q, k, v = (A._f64(x) for x in (q, k, v))
     if q.shape[2] != k.shape[2] or q.shape[1] != k.shape[1]:
         raise ValueError("mutant only defined for square MHA")
@@ -151,6 +209,11 @@ MUTANTS = {
     "partials_normalised": _impl(decode_partials=_partials_normalised),
     "merge_without_rescale": _impl(merge_partials=_merge_without_rescale),
     "merge_unweighted_l": _impl(merge_partials=_merge_drops_l_weight),
+    "window_left_bound_exclusive": _impl(**_with_visible(_window_left_strict)),
+    "window_left_not_bottom_right": _impl(**_with_visible(_window_top_left)),
+    "window_right_bound_ignored": _impl(**_with_visible(_window_right_ignored)),
+    "varlen_key_offsets_from_queries": _impl(sdpa_varlen=_varlen_shared_offsets),
+    "varlen_lse_row_major": _impl(sdpa_varlen=_varlen_lse_row_major),
 }
 
 
