@@ -14,6 +14,8 @@ from .binding import (  # noqa: F401
     attn_decode_noalloc,
     attn_decode_paged,
     attn_fwd,
+    attn_fwd_qkvpacked,
+    attn_fwd_varlen,
     check_device_status,
     debug_set,
     decode_chunk,

@@ -25,7 +25,7 @@ ATTN_ERR_DEVICE_TIMEOUT = 4
 ATTN_BF16 = 0
 ATTN_FP16 = 1
 
-EXPORTS = ("attn_fwd", "attn_decode", "attn_decode_fused", "attn_decode_paged",
+EXPORTS = ("attn_fwd", "attn_fwd_varlen", "attn_fwd_qkvpacked", "attn_decode", "attn_decode_fused", "attn_decode_paged",
            "attn_decode_noalloc",
            "attn_decode_workspace_bytes",
            "attn_decode_chunk", "attn_check_device_status", "attn_debug_set",
@@ -59,6 +59,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
     lib.attn_fwd.restype = i
+    lib.attn_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, i, i, f,
+                                    i, vp]
+    lib.attn_fwd_varlen.restype = i
+    lib.attn_fwd_qkvpacked.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
+    lib.attn_fwd_qkvpacked.restype = i
     lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
     lib.attn_decode.restype = i
     lib.attn_decode_fused.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
@@ -134,6 +139,60 @@ def attn_fwd(q, k, v, *, causal: bool, scale: float | None = None, out=None, lse
     st = lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Skv, D,
                       1 if causal else 0, float(scale), _dtype_code(q), _stream(stream))
     _check(st, "attn_fwd")
+    return out, lse
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int, *,
+                    causal: bool = True, window=(-1, -1), scale=None, out=None, lse=None,
+                    return_lse: bool = True, stream=None):
+    """Packed variable-length prefill: q [total_q,Hq,D], k/v [total_k,Hkv,D], cu_seqlens_* [B+1]
+    int32 (all CUDA); window = (left, right), -1 for no bound.  Returns (O, LSE [Hq,total_q])."""
+    lib = load()
+    total_q, Hq, D = q.shape
+    total_k, Hkv = k.shape[0], k.shape[1]
+    for t in (q, k, v, cu_seqlens_q, cu_seqlens_k):
+        if not t.is_contiguous():
+            raise ValueError("varlen inputs must be contiguous")
+    if cu_seqlens_q.dtype != torch.int32 or cu_seqlens_k.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    if cu_seqlens_q.numel() != cu_seqlens_k.numel() or cu_seqlens_q.numel() < 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k need the same B + 1 entries")
+    B = cu_seqlens_q.numel() - 1
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
+    wl, wr = window
+    st = lib.attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q),
+                             _ptr(cu_seqlens_k), B, Hq, Hkv, total_q, total_k, int(max_seqlen_q),
+                             int(max_seqlen_k), D, 1 if causal else 0, int(wl), int(wr),
+                             float(scale), _dtype_code(q), _stream(stream))
+    _check(st, "attn_fwd_varlen")
+    return out, lse
+
+
+def attn_fwd_qkvpacked(qkv, *, causal: bool = True, window=(-1, -1), scale=None, out=None,
+                       lse=None, return_lse: bool = True, stream=None):
+    """Prefill reading Q, K, V in place from qkv [B,S,3,H,D] (CUDA).  Returns (O [B,S,H,D],
+    LSE [H,B,S])."""
+    lib = load()
+    if qkv.dim() != 5 or qkv.shape[2] != 3:
+        raise ValueError("qkv must be [B, S, 3, H, D]")
+    if not qkv.is_contiguous():
+        raise ValueError("qkv must be contiguous")
+    B, S, _, H, D = qkv.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, S, H, D), dtype=qkv.dtype, device=qkv.device)
+    if lse is None and return_lse:
+        lse = torch.empty((H, B, S), dtype=torch.float32, device=qkv.device)
+    wl, wr = window
+    st = lib.attn_fwd_qkvpacked(_ptr(qkv), _ptr(out), _ptr(lse), B, S, H, D, 1 if causal else 0,
+                                int(wl), int(wr), float(scale), _dtype_code(qkv), _stream(stream))
+    _check(st, "attn_fwd_qkvpacked")
     return out, lse
 
 

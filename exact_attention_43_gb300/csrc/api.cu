@@ -110,6 +110,50 @@ EncodeTiledFn encode_tiled_fn() {
 
 }  // namespace ea
 
+// The persistent prefill kernel with its zeroed work-item counter.
+static int run_fwd(ea::FwdArgs& a, int dev, cudaStream_t stream) {
+  int st;
+  // the persistent kernel's work-item counter: 256 stream-ordered bytes, zeroed
+  cudaMemPool_t pool;
+  if ((st = pool_for(dev, &pool)) != ATTN_OK) return st;
+  void* counter = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(&counter, 256, pool, stream);
+  if (e != cudaSuccess) return from_cuda(e);
+  e = cudaMemsetAsync(counter, 0, sizeof(int), stream);
+  if (e == cudaSuccess) {
+    a.work_counter = static_cast<int*>(counter);
+    e = ea::launch_fwd(a, stream);
+  }
+  cudaError_t f = cudaFreeAsync(counter, stream);
+  if (e == cudaErrorInvalidValue && !ea::encode_tiled_fn()) return ATTN_ERR_UNSUPPORTED;
+  if (e == cudaSuccess) e = f;
+  return from_cuda(e);
+}
+
+// Token-major prefill (attn_fwd_varlen, attn_fwd_qkvpacked): the checks of the
+// window and the longest lengths, then the launch.
+static int run_fwd_tm(ea::FwdArgs& a, int max_q, int max_k, int window_left, int window_right,
+                      cudaStream_t stream) {
+  if (window_left < -1 || window_right < -1) return ATTN_ERR_INVALID_ARG;
+  if (!isfinite(a.scale)) return ATTN_ERR_INVALID_ARG;
+  // keeps every key index of the masks inside an int
+  if ((long long)max_q + max_k > 0x3fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  if (((long long)max_q + 255) / 256 * a.Hq * a.B > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  int dev = 0;
+  int st = check_device(&dev);
+  if (st != ATTN_OK) return st;
+  a.vl = 1;
+  a.Sq = max_q;
+  a.Skv = max_k;
+  // a bound at least max_q + max_k away from every diagonal excludes no key
+  a.win_left = window_left > max_q + max_k ? -1 : window_left;
+  a.win_right = window_right > max_q + max_k ? -1 : window_right;
+  a.wait_limit_ns = g_wait_limit_ns;
+  a.debug_fault = 0;
+  a.num_sms = g_num_sms[dev] > 0 ? g_num_sms[dev] : 1;
+  return run_fwd(a, dev, stream);
+}
+
 extern "C" {
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
@@ -150,21 +194,82 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   a.debug_fault = g_fault;
   a.num_sms = g_num_sms[dev] > 0 ? g_num_sms[dev] : 1;
   if (Skv == 0) return from_cuda(ea::launch_fwd_empty_keys(a, stream));
-  // the persistent kernel's work-item counter: 256 stream-ordered bytes, zeroed
-  cudaMemPool_t pool;
-  if ((st = pool_for(dev, &pool)) != ATTN_OK) return st;
-  void* counter = nullptr;
-  cudaError_t e = cudaMallocFromPoolAsync(&counter, 256, pool, stream);
-  if (e != cudaSuccess) return from_cuda(e);
-  e = cudaMemsetAsync(counter, 0, sizeof(int), stream);
-  if (e == cudaSuccess) {
-    a.work_counter = static_cast<int*>(counter);
-    e = ea::launch_fwd(a, stream);
-  }
-  cudaError_t f = cudaFreeAsync(counter, stream);
-  if (e == cudaErrorInvalidValue && !ea::encode_tiled_fn()) return ATTN_ERR_UNSUPPORTED;
-  if (e == cudaSuccess) e = f;
-  return from_cuda(e);
+  return run_fwd(a, dev, stream);
+}
+
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int B, int Hq, int Hkv,
+                    int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int D, int causal,
+                    int window_left, int window_right, float scale, int dtype, cudaStream_t stream) {
+  if (B < 0 || Hq < 0 || Hkv < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 ||
+      max_seqlen_k < 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || Hq == 0 || total_q == 0 || max_seqlen_q == 0) return ATTN_OK;  // no query row
+  if (Hkv == 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (B > 65535 || Hq > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (!q || !o || !cu_seqlens_q || !cu_seqlens_k || (total_k > 0 && (!k || !v)))
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(o, 16) || (k && !aligned(k, 16)) || (v && !aligned(v, 16)) ||
+      (lse && !aligned(lse, 4)) || !aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4))
+    return ATTN_ERR_INVALID_ARG;
+  ea::FwdArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.causal = causal != 0;
+  a.scale = scale;
+  a.bf16 = dtype == ATTN_BF16;
+  a.cu_q = cu_seqlens_q;
+  a.cu_k = cu_seqlens_k;
+  a.total_q = total_q;
+  a.total_k = total_k;
+  a.q_rstride = (long long)Hq * D;
+  a.k_rstride = (long long)Hkv * D;
+  a.o_rstride = (long long)Hq * D;
+  return run_fwd_tm(a, max_seqlen_q, max_seqlen_k, window_left, window_right, stream);
+}
+
+int attn_fwd_qkvpacked(const void* qkv, void* o, float* lse, int B, int S, int H, int D, int causal,
+                       int window_left, int window_right, float scale, int dtype,
+                       cudaStream_t stream) {
+  if (B < 0 || S < 0 || H < 0) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if ((long long)B * S * H == 0) return ATTN_OK;
+  if (B > 65535 || H > 65535) return ATTN_ERR_UNSUPPORTED;
+  if ((long long)B * S > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  if (!qkv || !o || !aligned(qkv, 16) || !aligned(o, 16) || (lse && !aligned(lse, 4)))
+    return ATTN_ERR_INVALID_ARG;
+  const size_t plane = (size_t)H * D;  // elements of one of Q, K, V of one token
+  ea::FwdArgs a{};
+  a.q = qkv;
+  a.k = static_cast<const uint16_t*>(qkv) + plane;
+  a.v = static_cast<const uint16_t*>(qkv) + 2 * plane;
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.Hq = H;
+  a.Hkv = H;
+  a.D = D;
+  a.causal = causal != 0;
+  a.scale = scale;
+  a.bf16 = dtype == ATTN_BF16;
+  a.cu_q = nullptr;  // sequence b starts at token b * S
+  a.cu_k = nullptr;
+  a.total_q = B * S;
+  a.total_k = B * S;
+  a.q_rstride = 3 * (long long)plane;
+  a.k_rstride = 3 * (long long)plane;
+  a.o_rstride = (long long)plane;
+  return run_fwd_tm(a, S, S, window_left, window_right, stream);
 }
 
 int attn_decode_chunk(int max_S, int num_splits) { return chunk_for(max_S, num_splits); }

@@ -86,7 +86,43 @@ struct Params {
   float c2;  // scale * log2(e); 1 when scale == 0 (then every visible score is set to 0)
   uint64_t wait_limit_ns;
   int debug_fault;
+  // token-major layouts (attn_fwd_varlen, attn_fwd_qkvpacked; the VL kernels): Q, K, V
+  // and O are [tokens, heads, D] (row strides in the tensor maps); sequence b's
+  // queries are tokens [cu_q[b], cu_q[b+1]) and its keys [cu_k[b], cu_k[b+1]), or
+  // b * Sq and b * Skv onwards when cu_q is null; Sq and Skv are then the longest
+  // lengths.  LSE of head h, token t is at h * total_q + t.
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int total_q, total_k;
+  int win_left, win_right;  // sliding-window bounds (-1: none); causal is win_right = 0
+  int o_rstride;            // elements between consecutive tokens of O
 };
+
+// Query and key rows of one sequence in the token-major layouts.
+struct Seq {
+  int q0, nq;  // first query token, query count
+  int k0, nk;  // first key token, key count
+};
+
+// Offsets outside the arrays, decreasing offsets and lengths above the longest
+// length are clamped (no access leaves the arrays) and reported in the status word.
+__device__ __forceinline__ Seq seq_of(const Params& p, int b) {
+  Seq s;
+  if (!p.cu_q) {
+    s.q0 = b * p.Sq;
+    s.nq = p.Sq;
+    s.k0 = b * p.Skv;
+    s.nk = p.Skv;
+    return s;
+  }
+  const int a = p.cu_q[b], e = p.cu_q[b + 1], c = p.cu_k[b], f = p.cu_k[b + 1];
+  s.q0 = min(max(a, 0), p.total_q);
+  s.nq = min(min(max(e, s.q0), p.total_q) - s.q0, p.Sq);
+  s.k0 = min(max(c, 0), p.total_k);
+  s.nk = min(min(max(f, s.k0), p.total_k) - s.k0, p.Skv);
+  if (s.q0 != a || s.nq != e - a || s.k0 != c || s.nk != f - c) atomicOr(&g_status, kStatusSeqLenClamped);
+  return s;
+}
 
 template <int D>
 struct Layout {
@@ -132,6 +168,14 @@ __device__ __forceinline__ void zero_row(const Params& p, int bh, int row, int D
   if (p.lse) p.lse[(size_t)bh * p.Sq + row] = -INFINITY;
 }
 
+// The same for a row of the token-major layouts (O row stride o_rstride, LSE [Hq, total_q]).
+__device__ __forceinline__ void zero_row_tm(const Params& p, const Seq& s, int hq, int row, int D) {
+  uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
+                                        (size_t)(s.q0 + row) * p.o_rstride + (size_t)hq * D);
+  for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+  if (p.lse) p.lse[(size_t)hq * p.total_q + s.q0 + row] = -INFINITY;
+}
+
 // KV tiles a Q tile starting at row m0 needs, and the first that may need masking.
 __device__ __forceinline__ void tile_range(const Params& p, int m0, int* n_tiles, int* mask_from) {
   if (m0 >= p.Sq) {
@@ -147,6 +191,59 @@ __device__ __forceinline__ void tile_range(const Params& p, int m0, int* n_tiles
   int mf = p.Skv / BN;
   if (p.causal) mf = min(mf, max(0, m0 + delta + 1) / BN);
   *mask_from = mf;
+}
+
+// Token-major kernels: the KV tiles [*lo, *hi) that a Q tile at row m0 of sequence s
+// needs (*lo == *hi: none), the first tile *mr holding a key past some row's right
+// bound or past the keys, and the tile *ml below which tiles hold a key before some
+// row's left bound.  Row i of the sequence keeps keys
+// [i + d - win_left, i + d + win_right] of [0, nk), d = nk - nq (-1: no bound).
+__device__ __forceinline__ void tile_span(const Params& p, const Seq& s, int m0, int* lo, int* hi,
+                                          int* mr, int* ml) {
+  *lo = *hi = *mr = *ml = 0;
+  if (m0 >= s.nq || s.nk <= 0) return;
+  const int last_row = min(m0 + BM, s.nq) - 1;
+  const int delta = s.nk - s.nq;
+  int k_hi = s.nk - 1, r0 = s.nk;  // last key of any row; first key past row m0's right bound
+  if (p.win_right >= 0) {
+    k_hi = min(k_hi, last_row + delta + p.win_right);
+    r0 = min(r0, max(0, m0 + delta + p.win_right + 1));
+  }
+  int k_lo = 0, l1 = 0;  // first key of any row; first key of the last row
+  if (p.win_left >= 0) {
+    k_lo = max(0, m0 + delta - p.win_left);
+    l1 = max(0, last_row + delta - p.win_left);
+  }
+  if (k_hi < k_lo) return;
+  *lo = k_lo / BN;
+  *hi = k_hi / BN + 1;
+  *mr = r0 / BN;
+  *ml = (l1 + BN - 1) / BN;
+}
+
+// The KV tiles of a token-major work item (two Q tiles from row m_base): both Q
+// tiles step through tiles t0 .. t0 + n_kv - 1; Q tile qi multiplies steps
+// [a, e) of them and masks tiles at or after mr and before ml per key.
+struct ItemTiles {
+  int t0, n_kv, a, e, mr, ml;
+};
+
+__device__ __forceinline__ ItemTiles item_tiles(const Params& p, const Seq& s, int m_base, int qi) {
+  static_assert(NQ == 2, "two Q tiles per item");
+  int lo0, hi0, mr0, ml0, lo1, hi1, mr1, ml1;
+  tile_span(p, s, m_base, &lo0, &hi0, &mr0, &ml0);
+  tile_span(p, s, m_base + BM, &lo1, &hi1, &mr1, &ml1);
+  // rows grow with the tile, so tile 1's keys never start before tile 0's
+  const bool ne0 = hi0 > lo0, ne1 = hi1 > lo1;
+  ItemTiles it;
+  it.t0 = ne0 ? lo0 : (ne1 ? lo1 : 0);
+  it.n_kv = (ne1 ? hi1 : (ne0 ? hi0 : 0)) - it.t0;
+  const bool ne = qi == 0 ? ne0 : ne1;
+  it.a = ne ? (qi == 0 ? lo0 : lo1) - it.t0 : 0;
+  it.e = ne ? (qi == 0 ? hi0 : hi1) - it.t0 : 0;
+  it.mr = qi == 0 ? mr0 : mr1;
+  it.ml = qi == 0 ? ml0 : ml1;
+  return it;
 }
 
 // Work item w -> (256-row block, batch, query head).  Items are grouped by
@@ -168,7 +265,7 @@ __device__ __forceinline__ void decode_item(const Params& p, int w, int* mb, int
 }
 
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool VL>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
@@ -254,19 +351,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           int mb, hq, b;
           decode_item(p, w, &mb, &hq, &b);
           const int m_base = mb * (NQ * BM);
-          int n_t[NQ], mf[NQ];
-          for (int i = 0; i < NQ; ++i) tile_range(p, m_base + i * BM, &n_t[i], &mf[i]);
-          const int n_kv = max(n_t[0], n_t[1]);
+          int n_kv, q_y, q_z, k_y0, kv_z;  // tensor-map coordinates of Q and of K/V tile 0
+          if constexpr (VL) {
+            const Seq sq = seq_of(p, b);
+            const ItemTiles it = item_tiles(p, sq, m_base, 0);
+            n_kv = it.n_kv;
+            q_y = sq.q0 + m_base;
+            q_z = hq;
+            k_y0 = sq.k0 + it.t0 * BN;
+            kv_z = hq / p.group;
+          } else {
+            int n_t[NQ], mf[NQ];
+            for (int i = 0; i < NQ; ++i) tile_range(p, m_base + i * BM, &n_t[i], &mf[i]);
+            n_kv = max(n_t[0], n_t[1]);
+            q_y = m_base;
+            q_z = b * p.Hq + hq;
+            k_y0 = 0;
+            kv_z = b * p.Hkv + hq / p.group;
+          }
           if (n_kv == 0) continue;
           // Q of this item may overwrite Q of the last one once its S MMAs are done
           if (!(ok = mbar_wait(bar(L::Q_EMPTY), (k_item & 1) ^ 1, abort_flag, &g_status, lim)))
             break;
-          const int bh = b * p.Hq + hq, kv_z = b * p.Hkv + hq / p.group;
           mbar_expect_tx(bar(L::Q_FULL), NQ * L::TILE);
           for (int i = 0; i < NQ; ++i)
             for (int rr = 0; rr < L::NREG; ++rr)
               tma_load_3d(sb + L::Q_OFF + i * L::TILE + rr * L::REGION, &tmq, bar(L::Q_FULL),
-                          rr * 64, m_base + i * BM, bh, pol_q);
+                          rr * 64, q_y + i * BM, q_z, pol_q);
           ++k_item;
           for (int l = 0; l < 2 * n_kv; ++l, ++ld) {  // K_0, V_0, K_1, V_1, ...
             const int s = ld % NS;
@@ -278,7 +389,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const CUtensorMap* tm = (l & 1) ? &tmv : &tmk;
             for (int rr = 0; rr < L::NREG; ++rr)
               tma_load_3d(sb + L::RING_OFF + s * L::TILE + rr * L::REGION, tm,
-                          bar(L::RING_FULL + s), rr * 64, (l >> 1) * BN, kv_z, pol_kv);
+                          bar(L::RING_FULL + s), rr * 64, k_y0 + (l >> 1) * BN, kv_z, pol_kv);
           }
         }
         // every copy issued must have landed before the CTA may exit
@@ -354,11 +465,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           int mb, hq, b;
           decode_item(p, w, &mb, &hq, &b);
           const int m_base = mb * (NQ * BM);
-          int n_t[NQ], mf[NQ];
-          for (int i = 0; i < NQ; ++i) tile_range(p, m_base + i * BM, &n_t[i], &mf[i]);
-          const int n_kv = max(n_t[0], n_t[1]);
+          // this Q tile multiplies KV steps [a_own, e_own) of the item's n_kv
+          int n_kv, a_own, e_own;
+          if constexpr (VL) {
+            const ItemTiles it = item_tiles(p, seq_of(p, b), m_base, qi);
+            n_kv = it.n_kv;
+            a_own = it.a;
+            e_own = it.e;
+          } else {
+            int n_t[NQ], mf[NQ];
+            for (int i = 0; i < NQ; ++i) tile_range(p, m_base + i * BM, &n_t[i], &mf[i]);
+            n_kv = max(n_t[0], n_t[1]);
+            a_own = 0;
+            e_own = n_t[qi];
+          }
           if (n_kv == 0) continue;
-          const int nt = n_t[qi];
           const int base = ld;
           ld = base + 2 * n_kv;
           // ---- first batch of the item: S(0)
@@ -368,10 +489,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (!(ok = token_wait())) break;
           tc_fence_after();
           // P of the last item lives in these columns, read by an MMA issued earlier
-          if (nt > 0) issue_s(base);
+          if (a_own <= 0 && 0 < e_own) issue_s(base);
           else umma_commit(bar(L::S_FULL + qi));  // nothing to multiply for this tile
-          if (nt == 1) umma_commit(bar(L::Q_EMPTY));  // this tile's last S
-          else if (nt == 0) mbar_arrive(bar(L::Q_EMPTY));
+          if (e_own == a_own) mbar_arrive(bar(L::Q_EMPTY));
+          else if (e_own == 1) umma_commit(bar(L::Q_EMPTY));  // this tile's last S
           token_pass();
           // ---- one batch per KV tile j: P V(j), then S(j+1)
           for (int j = 0; j < n_kv && ok; ++j) {
@@ -381,20 +502,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (!(ok = mbar_wait(bar(L::P_FULL + qi), t_cnt & 1, abort_flag, &g_status, lim))) break;
             ++t_cnt;
             // the first P V of an item overwrites O: the last epilogue must have read it
-            if (j == 0 && nt > 0 && n_items > 0 &&
+            if (j == a_own && e_own > a_own && n_items > 0 &&
                 !(ok = mbar_wait(bar(L::O_FREE + qi), (n_items - 1) & 1, abort_flag, &g_status, lim)))
               break;
             if (!(ok = token_wait())) break;
             tc_fence_after();
-            if (j < nt) issue_pv(ld_v, j > 0);
+            if (a_own <= j && j < e_own) issue_pv(ld_v, j > a_own);
             if (j == n_kv - 1) {
               umma_commit(bar(L::O_DONE + qi));
               ++n_items;
             }
             if (j + 1 < n_kv) {
-              if (j + 1 < nt) {
+              if (a_own <= j + 1 && j + 1 < e_own) {
                 issue_s(ld_k);  // after P V(j), which read P from these columns
-                if (j + 1 == nt - 1) umma_commit(bar(L::Q_EMPTY));  // this tile's last S
+                if (j + 1 == e_own - 1) umma_commit(bar(L::Q_EMPTY));  // this tile's last S
               } else {
                 umma_commit(bar(L::S_FULL + qi));  // an empty step for this tile
               }
@@ -436,19 +557,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int bh = b * p.Hq + hq;
       const int m0 = mb * (NQ * BM) + qi * BM;
       const int row = m0 + r_lane;
-      int n_own, mfrom;
-      tile_range(p, m0, &n_own, &mfrom);
-      int n_oth, mf_oth;
-      tile_range(p, m0 + (qi == 0 ? BM : -BM), &n_oth, &mf_oth);
-      // both Q tiles step through every KV tile of the item; past its own range a
-      // step only passes the barriers (its issuer multiplies nothing there)
-      const int n_tiles = max(n_own, n_oth);
-      if (n_tiles == 0) {  // no key for the whole item
-        if (row < p.Sq) zero_row(p, bh, row, D);
-        continue;
+      // Both Q tiles step through every KV tile of the item; outside its own steps
+      // [a_own, e_own) a step only passes the barriers (its issuer multiplies nothing
+      // there).  Tile t0 + t at or after mfrom (or before mleft) is masked per key.
+      int n_tiles, a_own, e_own, mfrom, mleft = 0, t0 = 0;
+      int first_key = 0, last_key;  // the keys this row may see (last_key < first_key: none)
+      Seq sq{};
+      if constexpr (VL) {
+        sq = seq_of(p, b);
+        const ItemTiles it = item_tiles(p, sq, mb * (NQ * BM), qi);
+        n_tiles = it.n_kv;
+        a_own = it.a;
+        e_own = it.e;
+        mfrom = it.mr;
+        mleft = it.ml;
+        t0 = it.t0;
+        if (n_tiles == 0) {  // no key for the whole item
+          if (row < sq.nq) zero_row_tm(p, sq, hq, row, D);
+          continue;
+        }
+        const int d = sq.nk - sq.nq;
+        last_key = sq.nk - 1;
+        if (p.win_right >= 0) last_key = min(last_key, row + d + p.win_right);
+        if (p.win_left >= 0) first_key = row + d - p.win_left;
+      } else {
+        int n_own, n_oth, mf_oth;
+        tile_range(p, m0, &n_own, &mfrom);
+        tile_range(p, m0 + (qi == 0 ? BM : -BM), &n_oth, &mf_oth);
+        n_tiles = max(n_own, n_oth);
+        a_own = 0;
+        e_own = n_own;
+        if (n_tiles == 0) {  // no key for the whole item
+          if (row < p.Sq) zero_row(p, bh, row, D);
+          continue;
+        }
+        last_key = p.causal ? min(row + (p.Skv - p.Sq), p.Skv - 1) : p.Skv - 1;
       }
-      // the last key this row may see (negative: none)
-      const int last_key = p.causal ? min(row + (p.Skv - p.Sq), p.Skv - 1) : p.Skv - 1;
       float m_used = -INFINITY, l_sum = 0.f;
       for (int t = 0; t < n_tiles; ++t, ++t_cnt) {
         if (!(ok = wait_warp(bar(L::S_FULL + qi), t_cnt & 1))) break;
@@ -464,7 +608,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (t_cnt > 0) mbar_arrive(bar(L::RING_EMPTY + (2 * t_cnt - 1) % NS));
           mbar_arrive(bar(L::RING_EMPTY + (2 * t_cnt) % NS));
         }
-        if (t >= n_own) {  // an empty step: no S was computed for this tile
+        if (t < a_own || t >= e_own) {  // an empty step: no S was computed for this tile
           tc_fence_before();
           mbar_arrive(bar(L::P_FULL + qi));
           continue;
@@ -480,7 +624,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int j = 0; j < BN; ++j) x[j] = 0.f;
         }
-        if (t >= mfrom) {
+        if constexpr (VL) {
+          const int tk = t0 + t;
+          if (tk >= mfrom || tk < mleft) {
+            // keys [first_key, last_key] of the row, relative to this tile
+            const int lo_v = first_key - tk * BN, hi_v = last_key + 1 - tk * BN;
+#pragma unroll
+            for (int j = 0; j < BN; ++j) x[j] = (j >= lo_v && j < hi_v) ? x[j] : mval;
+          }
+        } else if (t >= mfrom) {
           // keys [t BN, t BN + vis) of this tile are visible: one compare and select per key
           const int vis = last_key + 1 - t * BN;
 #pragma unroll
@@ -584,35 +736,60 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // TMA store per 64 columns; rows past Sq fall outside the tensor map and
       // are not written.
       const uint32_t stage = sb + L::STAGE_OFF + qi * L::REGION;
+      bool direct = false;
+      if constexpr (VL) direct = m0 + BM > sq.nq;  // rows past the sequence belong to the next one
+      if (direct) {
+        // a sequence's last, partial Q tile: each thread stores its own row
+        if (row < sq.nq) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
+                                                (size_t)(sq.q0 + row) * p.o_rstride + (size_t)hq * D);
 #pragma unroll
-      for (int h = 0; h < D / 64; ++h, ++k_stage) {
-        if (r_lane == 0) {
-          bulk_wait_read_all();  // the last store has read the region
-          mbar_arrive(bar(L::STAGE_FREE + qi));
+          for (int c = 0; c < D / 8; ++c) {
+            const int col = 8 * c;
+            dst[c] = make_uint4(
+                pack2<BF16>(__uint_as_float(orow[col + 0]) * inv_l, __uint_as_float(orow[col + 1]) * inv_l),
+                pack2<BF16>(__uint_as_float(orow[col + 2]) * inv_l, __uint_as_float(orow[col + 3]) * inv_l),
+                pack2<BF16>(__uint_as_float(orow[col + 4]) * inv_l, __uint_as_float(orow[col + 5]) * inv_l),
+                pack2<BF16>(__uint_as_float(orow[col + 6]) * inv_l, __uint_as_float(orow[col + 7]) * inv_l));
+          }
         }
-        if (!(ok = wait_warp(bar(L::STAGE_FREE + qi), k_stage & 1))) break;
+      } else {
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const int col = 64 * h + 8 * c;
-          const uint4 v = make_uint4(
-              pack2<BF16>(__uint_as_float(orow[col + 0]) * inv_l, __uint_as_float(orow[col + 1]) * inv_l),
-              pack2<BF16>(__uint_as_float(orow[col + 2]) * inv_l, __uint_as_float(orow[col + 3]) * inv_l),
-              pack2<BF16>(__uint_as_float(orow[col + 4]) * inv_l, __uint_as_float(orow[col + 5]) * inv_l),
-              pack2<BF16>(__uint_as_float(orow[col + 6]) * inv_l, __uint_as_float(orow[col + 7]) * inv_l));
-          st_shared_v4(stage + r_lane * 128 + ((c ^ (r_lane & 7)) << 4), v);
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(bar(L::STAGE_FULL + qi));
-        if (r_lane == 0) {
-          if (!(ok = mbar_wait(bar(L::STAGE_FULL + qi), k_stage & 1, abort_flag, &g_status, lim))) break;
-          tma_store_3d(&tmo, stage, 64 * h, m0, bh);
-          bulk_commit();
+        for (int h = 0; h < D / 64; ++h, ++k_stage) {
+          if (r_lane == 0) {
+            bulk_wait_read_all();  // the last store has read the region
+            mbar_arrive(bar(L::STAGE_FREE + qi));
+          }
+          if (!(ok = wait_warp(bar(L::STAGE_FREE + qi), k_stage & 1))) break;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const int col = 64 * h + 8 * c;
+            const uint4 v = make_uint4(
+                pack2<BF16>(__uint_as_float(orow[col + 0]) * inv_l, __uint_as_float(orow[col + 1]) * inv_l),
+                pack2<BF16>(__uint_as_float(orow[col + 2]) * inv_l, __uint_as_float(orow[col + 3]) * inv_l),
+                pack2<BF16>(__uint_as_float(orow[col + 4]) * inv_l, __uint_as_float(orow[col + 5]) * inv_l),
+                pack2<BF16>(__uint_as_float(orow[col + 6]) * inv_l, __uint_as_float(orow[col + 7]) * inv_l));
+            st_shared_v4(stage + r_lane * 128 + ((c ^ (r_lane & 7)) << 4), v);
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(bar(L::STAGE_FULL + qi));
+          if (r_lane == 0) {
+            if (!(ok = mbar_wait(bar(L::STAGE_FULL + qi), k_stage & 1, abort_flag, &g_status, lim))) break;
+            if constexpr (VL) tma_store_3d(&tmo, stage, 64 * h, sq.q0 + m0, hq);
+            else tma_store_3d(&tmo, stage, 64 * h, m0, bh);
+            bulk_commit();
+          }
         }
       }
       if (!ok) break;
-      if (p.lse && row < p.Sq)
+      if constexpr (VL) {
+        if (p.lse && row < sq.nq)
+          p.lse[(size_t)hq * p.total_q + sq.q0 + row] =
+              l_sum > 0.f ? (m_used + log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
+      } else if (p.lse && row < p.Sq) {
         p.lse[(size_t)bh * p.Sq + row] =
             l_sum > 0.f ? (m_used + log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
+      }
     }
     if (r_lane == 0) bulk_wait_all();  // this warpgroup's O stores are complete
   }
@@ -635,11 +812,14 @@ __global__ void fill_empty_kernel(uint16_t* o, float* lse, size_t rows, int D) {
   }
 }
 
-static bool make_map(CUtensorMap* map, const void* base, int D, int S, int BH, bool bf16) {
+// 3-D tensor map over 16-bit elements: D contiguous, then n1 rows s1 elements
+// apart, then n2 planes s2 elements apart; 64 x 128 x 1 boxes, 128-byte swizzle.
+static bool make_map(CUtensorMap* map, const void* base, int D, long long n1, long long n2,
+                     long long s1, long long s2, bool bf16) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return false;
-  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)BH};
-  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)S * D * 2};
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)n1, (cuuint64_t)n2};
+  const cuuint64_t strides[2] = {(cuuint64_t)s1 * 2, (cuuint64_t)s2 * 2};
   const cuuint32_t box[3] = {64, 128, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
@@ -649,17 +829,31 @@ static bool make_map(CUtensorMap* map, const void* base, int D, int S, int BH, b
   return r == CUDA_SUCCESS;
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool VL>
 static cudaError_t launch_t(const FwdArgs& a, cudaStream_t stream) {
   using L = Layout<D>;
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, BF16>,
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, BF16, VL>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
   CUtensorMap tq, tk, tv, to;
-  if (!make_map(&tq, a.q, D, a.Sq, a.B * a.Hq, BF16) || !make_map(&to, a.o, D, a.Sq, a.B * a.Hq, BF16) ||
-      !make_map(&tk, a.k, D, a.Skv, a.B * a.Hkv, BF16) ||
-      !make_map(&tv, a.v, D, a.Skv, a.B * a.Hkv, BF16))
+  if (VL) {
+    // [tokens, heads, D] with the given token strides; with no keys at all the K/V
+    // maps cover one (never read) row of q, since a map cannot be empty
+    const long long tk_rows = a.total_k > 0 ? a.total_k : 1;
+    const void* kb = a.total_k > 0 ? a.k : a.q;
+    const void* vb = a.total_k > 0 ? a.v : a.q;
+    const long long kst = a.total_k > 0 ? a.k_rstride : a.q_rstride;
+    if (!make_map(&tq, a.q, D, a.total_q, a.Hq, a.q_rstride, D, BF16) ||
+        !make_map(&to, a.o, D, a.total_q, a.Hq, a.o_rstride, D, BF16) ||
+        !make_map(&tk, kb, D, tk_rows, a.total_k > 0 ? a.Hkv : 1, kst, D, BF16) ||
+        !make_map(&tv, vb, D, tk_rows, a.total_k > 0 ? a.Hkv : 1, kst, D, BF16))
+      return cudaErrorInvalidValue;
+  } else if (!make_map(&tq, a.q, D, a.Sq, (long long)a.B * a.Hq, D, (long long)a.Sq * D, BF16) ||
+             !make_map(&to, a.o, D, a.Sq, (long long)a.B * a.Hq, D, (long long)a.Sq * D, BF16) ||
+             !make_map(&tk, a.k, D, a.Skv, (long long)a.B * a.Hkv, D, (long long)a.Skv * D, BF16) ||
+             !make_map(&tv, a.v, D, a.Skv, (long long)a.B * a.Hkv, D, (long long)a.Skv * D, BF16)) {
     return cudaErrorInvalidValue;
+  }
   Params p{};
   p.o = a.o;
   p.lse = a.lse;
@@ -678,9 +872,16 @@ static cudaError_t launch_t(const FwdArgs& a, cudaStream_t stream) {
   p.c2 = p.zero ? 1.f : c2;
   p.wait_limit_ns = a.wait_limit_ns;
   p.debug_fault = a.debug_fault;
+  p.cu_q = a.cu_q;
+  p.cu_k = a.cu_k;
+  p.total_q = a.total_q;
+  p.total_k = a.total_k;
+  p.win_left = a.win_left;
+  p.win_right = a.causal ? 0 : a.win_right;
+  p.o_rstride = (int)a.o_rstride;
   // scheduling groups: as many (batch, head) rows as keep about 64 MB of K and V
   // in L2, rounded to whole GQA groups
-  const double kv_head_bytes = 4.0 * (double)a.Skv * D;  // K and V of one KV head
+  const double kv_head_bytes = 4.0 * (double)(a.Skv > 0 ? a.Skv : 1) * D;  // K and V of one KV head
   const int g = a.Hq / a.Hkv;
   long long hpg = (long long)(64.0 * (1 << 20) / kv_head_bytes) * g;
   if (hpg < g) hpg = g;
@@ -689,15 +890,21 @@ static cudaError_t launch_t(const FwdArgs& a, cudaStream_t stream) {
   // persistent: one CTA per SM (or one per work item when there are fewer)
   const long long n_items = (long long)p.num_m_blocks * a.Hq * a.B;
   const int grid = (int)(n_items < a.num_sms ? n_items : a.num_sms);
-  attn_fwd_kernel<D, BF16><<<grid, NUM_THREADS, L::ALLOC, stream>>>(tq, tk, tv, to, p);
+  attn_fwd_kernel<D, BF16, VL><<<grid, NUM_THREADS, L::ALLOC, stream>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 
 }  // namespace fwd
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
-  if (a.D == 64) return a.bf16 ? fwd::launch_t<64, true>(a, stream) : fwd::launch_t<64, false>(a, stream);
-  return a.bf16 ? fwd::launch_t<128, true>(a, stream) : fwd::launch_t<128, false>(a, stream);
+  if (a.vl) {
+    if (a.D == 64)
+      return a.bf16 ? fwd::launch_t<64, true, true>(a, stream) : fwd::launch_t<64, false, true>(a, stream);
+    return a.bf16 ? fwd::launch_t<128, true, true>(a, stream) : fwd::launch_t<128, false, true>(a, stream);
+  }
+  if (a.D == 64)
+    return a.bf16 ? fwd::launch_t<64, true, false>(a, stream) : fwd::launch_t<64, false, false>(a, stream);
+  return a.bf16 ? fwd::launch_t<128, true, false>(a, stream) : fwd::launch_t<128, false, false>(a, stream);
 }
 
 cudaError_t launch_fwd_empty_keys(const FwdArgs& a, cudaStream_t stream) {

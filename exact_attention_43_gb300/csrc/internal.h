@@ -22,6 +22,16 @@ struct FwdArgs {
   int debug_fault;  // 1: the loader withholds the first V tile (bounded-wait test only)
   int num_sms;      // multiprocessors of the current device (persistent grid size)
   int* work_counter;  // device int, zero when the kernel starts (work-item claims)
+  // token-major layouts (attn_fwd_varlen, attn_fwd_qkvpacked): vl = 1; q, k, v, o
+  // are [tokens, heads, D] with the token strides below (elements); sequence b's
+  // offsets come from cu_q / cu_k ([B + 1]), or are b * Sq / b * Skv when cu_q is
+  // null; Sq and Skv are the longest lengths; LSE is [Hq, total_q]
+  int vl;
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int total_q, total_k;
+  long long q_rstride, k_rstride, o_rstride;
+  int win_left, win_right;  // sliding-window bounds, -1: none
 };
 
 struct DecodeArgs {

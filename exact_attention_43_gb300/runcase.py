@@ -2,6 +2,7 @@
 
     python -m exact_attention_43_gb300.runcase fwd --workload mha [--iters 3]
     python -m exact_attention_43_gb300.runcase fwd --B 1 --H 8 --S 4096 --causal 1
+    python -m exact_attention_43_gb300.runcase fwd --workload mha --layout qkvpacked [--window 256]
     python -m exact_attention_43_gb300.runcase decode [--B 8] [--iters 3] [--page-size 64 | --fused]
 
 Inputs are drawn on the GPU from the seeded generators in workloads.py.
@@ -33,6 +34,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=1)
     ap.add_argument("--page-size", type=int, default=0, help="decode over a paged cache")
     ap.add_argument("--fused", action="store_true", help="single-launch decode (attn_decode_fused)")
+    ap.add_argument("--layout", default="dense", choices=["dense", "varlen", "qkvpacked"],
+                    help="fwd: [B,H,S,D] arrays, packed sequences, or one [B,S,3,H,D] projection")
+    ap.add_argument("--window", type=int, default=-1, help="fwd token-major layouts: left window")
     a = ap.parse_args()
     dev = torch.device("cuda", 0)
     ea.load()
@@ -43,12 +47,37 @@ def main():
             w = wl.FwdWorkload("custom", 9, a.B or 1, a.H, a.Hkv or a.H, a.S, a.S, a.D,
                                torch.bfloat16, bool(a.causal))
         q, k, v = wl.workload_fwd_inputs(w, device=dev)
-
-        def call():
-            return ea.attn_fwd(q, k, v, causal=w.causal, scale=w.scale)
-
         units, unit = w.flops(), "TFLOP/s"
         desc = f"{w.name} B{w.B} Hq{w.Hq} Hkv{w.Hkv} S{w.Sq} D{w.D} causal={w.causal}"
+        if a.layout == "dense":
+            def call():
+                return ea.attn_fwd(q, k, v, causal=w.causal, scale=w.scale)
+        else:
+            win = (a.window, -1)
+            if a.window >= 0:  # flops of the keys the window keeps, counted row by row
+                diag = torch.arange(w.Sq, dtype=torch.int64) + (w.Skv - w.Sq)
+                hi = torch.clamp(diag if w.causal else torch.full_like(diag, w.Skv - 1), max=w.Skv - 1)
+                lo = torch.clamp(diag - a.window, min=0)
+                units = 4.0 * w.B * w.Hq * w.D * float(torch.clamp(hi - lo + 1, min=0).sum())
+                desc += f" window={a.window}"
+            desc += f" {a.layout}"
+            if a.layout == "qkvpacked":
+                assert w.Hq == w.Hkv and w.Sq == w.Skv
+                qkv = torch.stack([x.transpose(1, 2) for x in (q, k, v)], dim=2).contiguous()
+                del q, k, v
+
+                def call():
+                    return ea.attn_fwd_qkvpacked(qkv, causal=w.causal, window=win, scale=w.scale)
+            else:
+                tq, tk, tv = (x.transpose(1, 2).reshape(-1, x.shape[1], x.shape[3]).contiguous()
+                              for x in (q, k, v))
+                del q, k, v
+                cq = torch.arange(0, (w.B + 1) * w.Sq, w.Sq, dtype=torch.int32, device=dev)
+                ck = torch.arange(0, (w.B + 1) * w.Skv, w.Skv, dtype=torch.int32, device=dev)
+
+                def call():
+                    return ea.attn_fwd_varlen(tq, tk, tv, cq, ck, w.Sq, w.Skv, causal=w.causal,
+                                              window=win, scale=w.scale)
     else:
         d = wl.DECODE
         B = a.B or d.B

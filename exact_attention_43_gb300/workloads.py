@@ -195,6 +195,23 @@ def paged_cache(k, v, lens, page_size: int, *, seed: int, spare_pages: int = 3):
     return k_pages, v_pages, table
 
 
+def varlen_inputs(lens_q, lens_k, Hq, Hkv, D, *, dtype=torch.bfloat16, seed=SEED_BASE,
+                  pad_q: int = 0, device="cpu"):
+    """Packed variable-length batch: q [total_q, Hq, D], k and v [total_k, Hkv, D] and the
+    offsets cu_q, cu_k ([B + 1] int32, on the CPU).  Sequence b owns query rows
+    cu_q[b]..cu_q[b+1]-1 and key rows cu_k[b]..cu_k[b+1]-1; `pad_q` extra query rows
+    at the end belong to no sequence."""
+    cu_q = torch.zeros(len(lens_q) + 1, dtype=torch.int32)
+    cu_k = torch.zeros(len(lens_k) + 1, dtype=torch.int32)
+    cu_q[1:] = torch.cumsum(torch.as_tensor(lens_q, dtype=torch.int64), 0).to(torch.int32)
+    cu_k[1:] = torch.cumsum(torch.as_tensor(lens_k, dtype=torch.int64), 0).to(torch.int32)
+    total_q, total_k = int(cu_q[-1]) + pad_q, int(cu_k[-1])
+    q = normal((total_q, Hq, D), seed=seed + 20, dtype=dtype, device=device)
+    k = normal((total_k, Hkv, D), seed=seed + 21, dtype=dtype, device=device)
+    v = normal((total_k, Hkv, D), seed=seed + 22, dtype=dtype, device=device)
+    return q, k, v, cu_q, cu_k
+
+
 def sample_rows(S: int, n: int, *, seed: int):
     """n distinct query rows drawn uniformly from [0, S) without replacement, sorted."""
     g = _gen(seed, "cpu")

@@ -73,6 +73,53 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
              cudaStream_t stream);
 
 /*
+ * attn_fwd_varlen -- attn_fwd over a packed batch of sequences of different
+ * lengths, with an optional sliding window.
+ *
+ * The flash-attention backward page names `Varlen` and `Is_local` switches
+ * without defining them; the readings here:
+ *   sequence b has query tokens [cu_seqlens_q[b], cu_seqlens_q[b+1]) and key
+ *   tokens [cu_seqlens_k[b], cu_seqlens_k[b+1]), attended on their own; with
+ *   d = (its keys) - (its queries), its query i keeps key j iff
+ *   j <= i + d (causal) and i + d - window_left <= j <= i + d + window_right,
+ *   a bound of -1 being absent (causal makes the right bound 0).
+ *
+ * q, o        device, [total_q, Hq, D], dtype `dtype`, 16-byte aligned.
+ * k, v        device, [total_k, Hkv, D], 16-byte aligned (unused if total_k == 0).
+ * lse         device, [Hq, total_q] float32, 4-byte aligned, or NULL.
+ * cu_seqlens_q, cu_seqlens_k  device, [B + 1] int32, non-decreasing offsets
+ *             within [0, total_q] / [0, total_k]; a sequence's lengths must not
+ *             exceed max_seqlen_q / max_seqlen_k.  Offsets or lengths outside
+ *             those ranges are clamped on the device (no access leaves the
+ *             arrays) and reported by attn_check_device_status as
+ *             ATTN_ERR_INVALID_ARG.  Rows outside every sequence are not written.
+ * A row that keeps no key gets O = 0 and LSE = -inf.  Every element of k and v
+ * must be finite: a tile that ends inside a sequence also reads the next
+ * sequence's keys, whose probabilities are exactly 0.
+ * window_left, window_right >= -1; max_seqlen_q + max_seqlen_k < 2^30;
+ * B, Hq <= 65535; D 64 or 128; scale finite; Hq % Hkv == 0.
+ */
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int B, int Hq, int Hkv,
+                    int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int D, int causal,
+                    int window_left, int window_right, float scale, int dtype, cudaStream_t stream);
+
+/*
+ * attn_fwd_qkvpacked -- attn_fwd reading Q, K and V in place from one packed
+ * projection (the llm.c attention page's (B, N, 3, NH, d) QKV tensor, which it
+ * permutes into three (B, NH, N, d) arrays first; here no copy is made).
+ *
+ * qkv   device, [B, S, 3, H, D], dtype `dtype`, 16-byte aligned.
+ * o     device, [B, S, H, D] (the llm.c page's unpermuted output layout).
+ * lse   device, [H, B, S] float32 or NULL.
+ * causal, window_left, window_right, scale as in attn_fwd_varlen (every
+ * sequence has S queries and S keys).  B * S < 2^31, 2 S < 2^30.
+ */
+int attn_fwd_qkvpacked(const void* qkv, void* o, float* lse, int B, int S, int H, int D, int causal,
+                       int window_left, int window_right, float scale, int dtype,
+                       cudaStream_t stream);
+
+/*
  * attn_decode -- flash-decoding: one query token per sequence against a KV cache.
  *
  *   O[b,h,:] = softmax_j(Q[b,h,:] . K[b,g,j,:] / sqrt(D)) V[b,g,j,:],  0 <= j < seq_lens[b].

@@ -94,6 +94,39 @@ def test_decode_argument_errors(lib):
     assert dec(lib, B=0) == 0
 
 
+def test_varlen_and_packed_argument_errors(lib):
+    def vl(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, cq=FAKE, ck=FAKE, B=2, Hq=8, Hkv=2,
+                 tq=100, tk=100, mq=64, mk=64, D=128, causal=1, wl=-1, wr=-1, scale=0.1, dtype=0)
+        a.update(kw)
+        return lib.attn_fwd_varlen(a["q"], a["k"], a["v"], a["o"], a["lse"], a["cq"], a["ck"], a["B"],
+                                   a["Hq"], a["Hkv"], a["tq"], a["tk"], a["mq"], a["mk"], a["D"],
+                                   a["causal"], a["wl"], a["wr"], a["scale"], a["dtype"], None)
+
+    assert vl(cq=None) == 1
+    assert vl(k=None) == 1
+    assert vl(k=None, v=None, tk=0, wl=-2) == 1        # a window bound below -1
+    assert vl(Hkv=3) == 1
+    assert vl(lse=FAKE + 2) == 1
+    assert vl(scale=float("inf")) == 1
+    assert vl(D=96) == 2
+    assert vl(mq=1 << 29, mk=1 << 29) == 2              # key indices would leave an int
+    assert vl(B=0) == 0 and vl(tq=0) == 0 and vl(mq=0) == 0
+
+    def pk(**kw):
+        a = dict(qkv=FAKE, o=FAKE, lse=FAKE, B=2, S=100, H=4, D=64, causal=1, wl=-1, wr=-1,
+                 scale=0.1, dtype=1)
+        a.update(kw)
+        return lib.attn_fwd_qkvpacked(a["qkv"], a["o"], a["lse"], a["B"], a["S"], a["H"], a["D"],
+                                      a["causal"], a["wl"], a["wr"], a["scale"], a["dtype"], None)
+
+    assert pk(qkv=None) == 1
+    assert pk(o=FAKE + 8) == 1
+    assert pk(wr=-3) == 1
+    assert pk(dtype=5) == 2
+    assert pk(S=0) == 0
+
+
 def test_fused_decode_argument_errors(lib):
     def fused(**kw):
         a = dict(q=FAKE, k=FAKE, v=FAKE, lens=FAKE, o=FAKE, B=2, Hq=8, Hkv=2, max_S=64, D=128,
