@@ -625,10 +625,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int j = 0; j < BN; ++j) x[j] = 0.f;
         }
         if constexpr (VL) {
+          // keys [first_key, last_key] of the row, relative to this tile; a tile at or
+          // after mleft holds no key before any row's left bound and a tile before mfrom
+          // none past any row's right bound, so it tests only the side it can cross
           const int tk = t0 + t;
-          if (tk >= mfrom || tk < mleft) {
-            // keys [first_key, last_key] of the row, relative to this tile
-            const int lo_v = first_key - tk * BN, hi_v = last_key + 1 - tk * BN;
+          const int lo_v = first_key - tk * BN, hi_v = last_key + 1 - tk * BN;
+          if (tk >= mfrom && tk >= mleft) {
+#pragma unroll
+            for (int j = 0; j < BN; ++j) x[j] = (j < hi_v) ? x[j] : mval;
+          } else if (tk < mleft && tk < mfrom) {
+#pragma unroll
+            for (int j = 0; j < BN; ++j) x[j] = (j >= lo_v) ? x[j] : mval;
+          } else if (tk < mleft) {
 #pragma unroll
             for (int j = 0; j < BN; ++j) x[j] = (j >= lo_v && j < hi_v) ? x[j] : mval;
           }
