@@ -108,8 +108,13 @@ __device__ __forceinline__ uint64_t pair_of(uint32_t w) {
 template <int D, int G, bool BF16>
 __device__ __forceinline__ void merge_group(const Params& p, int b, int h0, int n, float* red, float* tot);
 
-template <int D, int G, bool BF16, bool PAGED, bool MERGE = false>
+// PG: 0 contiguous cache; 1 paged cache, thread 0 issues the copies; 2 paged cache
+// with small pages, the lanes of warp 0 issue them (a 128-key sub-tile spans at
+// least four pages).  Each is its own instantiation: sharing code with the
+// others cost the larger-page and contiguous kernels several percent.
+template <int D, int G, bool BF16, int PG, bool MERGE = false>
 __global__ void __launch_bounds__(THREADS) decode_split_kernel(const Params p) {
+  constexpr bool PAGED = PG != 0, WIDE = PG == 2;
   using L = SplitLayout<D, G, PAGED>;
   constexpr int EPL = D / 8;   // key elements per lane when 8 lanes share a key
   constexpr int DPL = D / 32;  // output columns per lane in P V
@@ -168,7 +173,7 @@ __global__ void __launch_bounds__(THREADS) decode_split_kernel(const Params p) {
     }
   }
 
-  // ------------------------------------------------ load stream (thread 0 only)
+  // ---------------------- load stream (thread 0; all of warp 0 for the paged cache)
   int l_c = c0, l_off = 0, l_nload = 2 * ((chunk_rows(c0) + SUB - 1) / SUB), issued = 0;
   uint64_t pol = 0;
   auto issue_next = [&]() {  // the next K or V sub-tile of this CTA's chunks
@@ -181,7 +186,7 @@ __global__ void __launch_bounds__(THREADS) decode_split_kernel(const Params p) {
       const uint32_t bar = ring_bar(issued);
       mbar_expect_tx(bar, rows * D * 2);
       bulk_load(sb + L::RING_OFF + (issued % NST) * L::STAGE, src, rows * D * 2, bar, pol);
-    } else {
+    } else if constexpr (!WIDE) {
       const uint16_t* base = (l_off & 1) ? p.v : p.k;
       const uint32_t bar = ring_bar(issued);
       const uint32_t dst = sb + L::RING_OFF + (issued % NST) * L::STAGE;
@@ -196,6 +201,26 @@ __global__ void __launch_bounds__(THREADS) decode_split_kernel(const Params p) {
                   seg * D * 2, bar, pol);
         done += seg;
       }
+    } else {
+      // the same copies, issued by the 32 lanes of warp 0 after lane 0 has set the
+      // byte count
+      const uint16_t* base = (l_off & 1) ? p.v : p.k;
+      const uint32_t bar = ring_bar(issued);
+      const uint32_t dst = sb + L::RING_OFF + (issued % NST) * L::STAGE;
+      if (lane == 0) mbar_expect_tx(bar, rows * D * 2);
+      __syncwarp();
+      const int pos0 = l_c * p.chunk + sub * SUB;
+      const int pg0 = pos0 / p.page_size, off0 = pos0 - pg0 * p.page_size;
+      const int first = min(rows, p.page_size - off0);  // positions in the first page
+      const int n_seg = 1 + (rows - first + p.page_size - 1) / p.page_size;
+      for (int sg = lane; sg < n_seg; sg += 32) {
+        const int done = sg == 0 ? 0 : first + (sg - 1) * p.page_size;
+        const int off = sg == 0 ? off0 : 0;
+        const int seg = min(rows - done, p.page_size - off);
+        const int phys = pt_smem ? pt[pg0 + sg - pg_lo] : page_of(pg0 + sg);
+        bulk_load(dst + done * D * 2, base + (((size_t)phys * p.Hkv + kvh) * p.page_size + off) * D,
+                  seg * D * 2, bar, pol);
+      }
     }
     ++issued;
     if (++l_off == l_nload && ++l_c < c1) {
@@ -207,8 +232,17 @@ __global__ void __launch_bounds__(THREADS) decode_split_kernel(const Params p) {
     for (int i = 0; i < NST; ++i) mbar_init(ring_bar(i), 1);
     *abort_flag = 0;
     fence_barrier_init();
-    pol = policy_evict_first();
-    for (int i = 0; i < NST; ++i) issue_next();
+    if constexpr (!WIDE) {
+      pol = policy_evict_first();
+      for (int i = 0; i < NST; ++i) issue_next();
+    }
+  }
+  if constexpr (WIDE) {
+    if (warp == 0) {
+      __syncwarp();  // the barriers are initialised
+      pol = policy_evict_first();
+      for (int i = 0; i < NST; ++i) issue_next();
+    }
   }
 
   // query vectors of the group, pre-multiplied by scale * log2 e, for this lane's key slice
@@ -299,7 +333,7 @@ __global__ void __launch_bounds__(THREADS) decode_split_kernel(const Params p) {
           }
         }
         __syncthreads();  // scores visible; every read of this stage done
-        if (threadIdx.x == 0) issue_next();
+        if (WIDE ? warp == 0 : threadIdx.x == 0) issue_next();
         ++gl;
         // online max / sum per head over this sub-tile (log2 units), one warp per head
         for (int g = warp; g < G; g += WARPS) {
@@ -386,7 +420,7 @@ __global__ void __launch_bounds__(THREADS) decode_split_kernel(const Params p) {
           }
         }
         __syncthreads();  // every read of this stage done
-        if (threadIdx.x == 0) issue_next();
+        if (WIDE ? warp == 0 : threadIdx.x == 0) issue_next();
         ++gl;
       }
     }
@@ -589,24 +623,25 @@ __global__ void __launch_bounds__(32) decode_reduce_kernel(const Params p) {
   }
 }
 
-template <int D, int G, bool BF16, bool PAGED, bool MERGE = false>
+template <int D, int G, bool BF16, int PG, bool MERGE = false>
 static cudaError_t launch_split(const DecodeArgs& a, const Params& p, cudaStream_t stream) {
-  using L = SplitLayout<D, G, PAGED>;
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G, BF16, PAGED, MERGE>,
+  using L = SplitLayout<D, G, PG != 0>;
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G, BF16, PG, MERGE>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
   if (e != cudaSuccess) return e;
   dim3 grid((a.max_chunks + p.cpb - 1) / p.cpb, a.Hkv * (p.group / G), a.B);
-  decode_split_kernel<D, G, BF16, PAGED, MERGE><<<grid, THREADS, L::BYTES, stream>>>(p);
+  decode_split_kernel<D, G, BF16, PG, MERGE><<<grid, THREADS, L::BYTES, stream>>>(p);
   return cudaGetLastError();
 }
 
 template <int D, int G, bool BF16>
 static cudaError_t launch_t(const DecodeArgs& a, const Params& p, cudaStream_t stream) {
-  if (a.max_chunks > 0 && p.tickets) return launch_split<D, G, BF16, false, true>(a, p, stream);
+  if (a.max_chunks > 0 && p.tickets) return launch_split<D, G, BF16, 0, true>(a, p, stream);
   if (a.max_chunks > 0) {
     // the contiguous-cache kernel is a separate instantiation, free of the page logic
-    const cudaError_t e = p.block_table ? launch_split<D, G, BF16, true>(a, p, stream)
-                                        : launch_split<D, G, BF16, false>(a, p, stream);
+    const cudaError_t e = !p.block_table     ? launch_split<D, G, BF16, 0>(a, p, stream)
+                          : p.page_size <= 32 ? launch_split<D, G, BF16, 2>(a, p, stream)
+                                              : launch_split<D, G, BF16, 1>(a, p, stream);
     if (e != cudaSuccess) return e;
   }
   decode_reduce_kernel<D, BF16><<<dim3(a.Hq, a.B), 32, 0, stream>>>(p);

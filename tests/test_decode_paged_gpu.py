@@ -48,15 +48,17 @@ def test_paged_decode_cases(case):
     compare_o(o, ref, f"paged decode {case}")
 
 
-def test_paged_equals_contiguous_at_full_size():
+@pytest.mark.parametrize("page", [16, 64])
+def test_paged_equals_contiguous_at_full_size(page):
     """The decode workload (B64 Hq32 Hkv8 D128, lens U[512, 32768], 64 splits) with
-    64-position pages gives exactly the contiguous kernel's output: the same keys
-    in the same sub-tiles, only fetched from other addresses."""
+    16- and 64-position pages (copies issued by warp 0's lanes, or by one thread)
+    gives exactly the contiguous kernel's output: the same keys in the same
+    sub-tiles, only fetched from other addresses."""
     import exact_attention_43_gb300 as ea
 
     w = wl.DECODE
     q, k, v, lens = wl.workload_decode_inputs(w, device="cuda")
-    kp, vp, table = wl.paged_cache(k, v, [int(x) for x in lens], 64, seed=3200)
+    kp, vp, table = wl.paged_cache(k, v, [int(x) for x in lens], page, seed=3200)
     ref = ea.attn_decode(q, k, v, lens.cuda(), num_splits=w.num_splits)
     del k, v
     got = ea.attn_decode_paged(q, kp.cuda(), vp.cuda(), table.cuda(), lens.cuda(),
@@ -66,13 +68,14 @@ def test_paged_equals_contiguous_at_full_size():
     assert torch.equal(got, ref)
 
 
-def test_block_table_entry_outside_the_pool_is_reported():
+@pytest.mark.parametrize("page", [16, 64])
+def test_block_table_entry_outside_the_pool_is_reported(page):
     import exact_attention_43_gb300 as ea
 
     lens = [200, 100]
     q, k, v, lens_t = wl.decode_inputs(2, 8, 2, 256, 128, torch.tensor(lens, dtype=torch.int32),
                                        seed=3300)
-    kp, vp, table = wl.paged_cache(k, v, lens, 64, seed=3301)
+    kp, vp, table = wl.paged_cache(k, v, lens, page, seed=3301)
     table[1, 0] = kp.shape[0] + 5  # past the pool: the kernel reads page 0 instead
     o = ea.attn_decode_paged(q.cuda(), kp.cuda(), vp.cuda(), table.cuda(), lens_t.cuda())
     torch.cuda.synchronize()
