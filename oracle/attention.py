@@ -25,7 +25,7 @@ Sources (page title, then the part of the page followed):
   global max over chunks, second pass = sum of o_c * e^(m_c - M) and
   l_c * e^(m_c - M) skipping empty chunks, final normalisation by the sum.
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
 
 * causal alignment for Sq != Skv is bottom-right: key j is visible to query i
   iff j <= i + (Skv - Sq); it equals the pages' j <= i when Sq == Skv;

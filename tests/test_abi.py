@@ -25,7 +25,7 @@ def declared_functions():
     return sorted(set(re.findall(r"\b(attn_[a-z_]+)\s*\(", text)))
 
 
-def test_header_declares_the_north_star_entry_points():
+def test_header_declares_the_prefill_and_decode_entry_points():
     names = declared_functions()
     assert "attn_fwd" in names and "attn_decode" in names
 
