@@ -19,12 +19,14 @@ hand-worked examples in ``tests/golden/``, PyTorch's float64 math-path
 sliding windows against a brute force with explicit key sets, the diagonal
 window's closed form and PyTorch SDPA on the explicit key slice; packed
 variable-length batches against the batched definition (equal lengths) and
-PyTorch SDPA per sequence.
+PyTorch SDPA per sequence; the backward against PyTorch float64 autograd,
+central finite differences of the forward and a single-key closed form.
 No function here is "parity unpinned".
 """
 
 from .attention import (  # noqa: F401
     sdpa,
+    sdpa_backward,
     sdpa_varlen,
     softmax_probs,
     decode,

@@ -18,6 +18,10 @@ Sources (page title, then the part of the page followed):
   normalise, multiply by V).
 * llm.c ``llmc/attention.cuh`` -- ``softmax_forward_kernel5`` (causal row
   softmax: only positions <= own_pos take part).
+* llm.c ``llmc/attention.cuh`` -- ``attention_backward`` and
+  ``softmax_autoregressive_backward_inplace_kernel``: datt = dout V^T,
+  dv = att^T dout, dpreatt = scale * att * (datt - sum_j att * datt) per row,
+  dq = dpreatt K, dk = dpreatt^T Q.
 * aprender-gpu 0.32.0, ``kernels/attention/paged/flash_decoding/
   reduce_kernel.rs`` -- ``FlashDecodingReduceKernel``: partials laid out
   [M, num_heads, max_chunks, head_dim + 2] (o at [0, D), chunk max at D, chunk
@@ -39,6 +43,8 @@ Readings where the pages are silent:
   i + d - window_left <= j <= i + d + window_right with d = Skv - Sq (the
   same bottom-right alignment as the causal mask); a bound of -1 is absent,
   and causal is the right bound 0;
+* with grouped-query heads, the gradient of a shared K or V head is the sum
+  over the query heads that read it (llm.c has one KV head per query head);
 * variable-length batches (the same page's ``Varlen`` switch) are packed:
   sequence b owns query rows [cu_q[b], cu_q[b+1]) of a [total_q, H, D] array
   and key rows [cu_k[b], cu_k[b+1]) of [total_k, Hkv, D]; each sequence is
@@ -190,6 +196,40 @@ def sdpa_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, *, causal: bool, scale: flo
         out[q0:q1] = ob[0].transpose(1, 0, 2)
         lse[:, q0:q1] = lb[0]
     return out, lse
+
+
+def sdpa_backward(q, k, v, dout, *, causal: bool, scale: float):
+    """Gradients of O = sdpa(q, k, v) for an incoming dO, as the llm.c page's
+    ``attention_backward`` computes them for each (batch, query head):
+
+    datt = dO V^T; dV += att^T dO; local = sum_j att * datt (per row);
+    dpreatt = scale * att * (datt - local); dQ = dpreatt K; dK += dpreatt^T Q,
+
+    att being the materialised probabilities (bottom-right causal mask as in
+    ``sdpa``).  Shapes as ``sdpa``; dout [B, Hq, Sq, D].  Returns (dQ, dK, dV)
+    in float64, dK and dV summed over the query heads of each KV head.
+    """
+    q = _f64(q)
+    k = _f64(k)
+    v = _f64(v)
+    do = _f64(dout)
+    B, Hq, Sq, D = q.shape
+    Hkv = k.shape[1]
+    group = Hq // Hkv
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for b in range(B):
+        for h in range(Hq):
+            kv = h // group
+            att, _, _ = softmax_probs(q[b, h], k[b, kv], causal=causal, scale=scale)
+            datt = do[b, h] @ v[b, kv].T                    # [Sq, Skv]
+            dv[b, kv] += att.T @ do[b, h]
+            local = (att * datt).sum(axis=1, keepdims=True)
+            dpre = scale * att * (datt - local)
+            dq[b, h] = dpre @ k[b, kv]
+            dk[b, kv] += dpre.T @ q[b, h]
+    return dq, dk, dv
 
 
 def decode(q, k_cache, v_cache, seq_lens, *, scale: float):

@@ -1,7 +1,7 @@
 """Pins that tie the float64 oracle to what the definition of attention fixes.
 
 Each pin is a function ``pin_*(impl)`` that raises AssertionError when the
-implementation ``impl`` (a namespace with ``sdpa``, ``sdpa_varlen``,
+implementation ``impl`` (a namespace with ``sdpa``, ``sdpa_varlen``, ``sdpa_backward``,
 ``softmax_probs``, ``decode``, ``decode_partials`` and ``merge_partials``)
 disagrees with a fact
 that does not depend on the oracle: a closed form, an invariant, a hand-worked
@@ -327,6 +327,58 @@ def pin_varlen_torch_per_sequence(impl):
         "rows outside every sequence"
 
 
+# ---------------------------------------------------------------- backward pins
+
+def pin_backward_torch_autograd(impl):
+    """PyTorch float64 autograd through its own SDPA (GQA by repeating K and V heads)."""
+    for causal, (Hq, Hkv) in ((True, (4, 2)), (False, (2, 2)), (True, (3, 1))):
+        q, k, v = _rand((2, Hq, 9, 6), 500), _rand((2, Hkv, 9, 6), 501), _rand((2, Hkv, 9, 6), 502)
+        do = _rand((2, Hq, 9, 6), 503)
+        tq, tk, tv = (torch.from_numpy(x).requires_grad_() for x in (q, k, v))
+        G = Hq // Hkv
+        o = torch.nn.functional.scaled_dot_product_attention(
+            tq, tk.repeat_interleave(G, dim=1), tv.repeat_interleave(G, dim=1), is_causal=causal,
+            scale=0.45)
+        o.backward(torch.from_numpy(do))
+        dq, dk, dv = impl.sdpa_backward(q, k, v, do, causal=causal, scale=0.45)
+        _close(dq, tq.grad.numpy(), 1e-10, f"autograd dQ causal={causal}")
+        _close(dk, tk.grad.numpy(), 1e-10, f"autograd dK causal={causal}")
+        _close(dv, tv.grad.numpy(), 1e-10, f"autograd dV causal={causal}")
+
+
+def pin_backward_finite_differences(impl):
+    """Central differences of sum(dO * O) through the forward, Sq != Skv bottom-right causal."""
+    q, k, v = _rand((1, 2, 4, 3), 510), _rand((1, 1, 6, 3), 511), _rand((1, 1, 6, 3), 512)
+    do = _rand((1, 2, 4, 3), 513)
+    dq, dk, dv = impl.sdpa_backward(q, k, v, do, causal=True, scale=0.7)
+    eps = 1e-6
+
+    def loss(q_, k_, v_):
+        o, _ = impl.sdpa(q_, k_, v_, causal=True, scale=0.7)
+        return float((o * do).sum())
+
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(*x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args_p = {"q": (xp, k, v), "k": (q, xp, v), "v": (q, k, xp)}[name]
+            args_m = {"q": (xm, k, v), "k": (q, xm, v), "v": (q, k, xm)}[name]
+            num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+        _close(g, num, 1e-7, f"finite differences d{name}")
+
+
+def pin_backward_single_key(impl):
+    """One key: P = 1 whatever Q and K are, so dQ = dK = 0 and dV = sum of dO."""
+    q, k, v = _rand((1, 2, 5, 4), 520), _rand((1, 2, 1, 4), 521), _rand((1, 2, 1, 4), 522)
+    do = _rand((1, 2, 5, 4), 523)
+    dq, dk, dv = impl.sdpa_backward(q, k, v, do, causal=False, scale=0.9)
+    _close(dq, np.zeros_like(dq), 1e-12, "single key dQ")
+    _close(dk, np.zeros_like(dk), 1e-12, "single key dK")
+    _close(dv[0, :, 0], do[0].sum(axis=1), 1e-12, "single key dV")
+
+
 # ----------------------------------------------------------------- decode pins
 
 def _decode_case(seed, B=3, Hq=4, Hkv=2, max_S=40, D=8):
@@ -391,6 +443,7 @@ ALL_PINS = [
     pin_decode_zero_len, pin_chunked_equals_unchunked, pin_partials_definition,
     pin_window_brute_force, pin_window_diagonal, pin_window_torch_slice, pin_window_wide_is_plain,
     pin_varlen_equal_lengths, pin_varlen_torch_per_sequence,
+    pin_backward_torch_autograd, pin_backward_finite_differences, pin_backward_single_key,
 ]
 
 

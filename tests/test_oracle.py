@@ -8,7 +8,8 @@ import oracle
 from tests import pins
 
 IMPL = types.SimpleNamespace(
-    sdpa=oracle.sdpa, sdpa_varlen=oracle.sdpa_varlen, softmax_probs=oracle.softmax_probs,
+    sdpa=oracle.sdpa, sdpa_varlen=oracle.sdpa_varlen, sdpa_backward=oracle.sdpa_backward,
+    softmax_probs=oracle.softmax_probs,
     decode=oracle.decode,
     decode_partials=oracle.decode_partials, merge_partials=oracle.merge_partials)
 

@@ -12,7 +12,8 @@ import oracle
 from oracle import attention as A
 from tests import pins
 
-BASE = dict(sdpa=oracle.sdpa, sdpa_varlen=oracle.sdpa_varlen, softmax_probs=oracle.softmax_probs,
+BASE = dict(sdpa=oracle.sdpa, sdpa_varlen=oracle.sdpa_varlen, sdpa_backward=oracle.sdpa_backward,
+            softmax_probs=oracle.softmax_probs,
             decode=oracle.decode, decode_partials=oracle.decode_partials,
             merge_partials=oracle.merge_partials)
 
@@ -197,6 +198,33 @@ def _merge_drops_l_weight(partials, seq_lens, *, chunk):
     return out
 
 
+def _bwd_without_local_sum(q, k, v, dout, *, causal, scale):
+    # mistake: dpreatt = scale * att * datt, the row term sum_j att * datt dropped
+    q, k, v, do = (A._f64(x) for x in (q, k, v, dout))
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    G = q.shape[1] // k.shape[1]
+    for b in range(q.shape[0]):
+        for h in range(q.shape[1]):
+            att, _, _ = oracle.softmax_probs(q[b, h], k[b, h // G], causal=causal, scale=scale)
+            datt = do[b, h] @ v[b, h // G].T
+            dv[b, h // G] += att.T @ do[b, h]
+            dpre = scale * att * datt
+            dq[b, h] = dpre @ k[b, h // G]
+            dk[b, h // G] += dpre.T @ q[b, h]
+    return dq, dk, dv
+
+
+def _bwd_dk_not_summed_over_group(q, k, v, dout, *, causal, scale):
+    dq, dk, dv = oracle.sdpa_backward(q, k, v, dout, causal=causal, scale=scale)
+    G = A._f64(q).shape[1] // A._f64(k).shape[1]
+    return dq, dk / G, dv                           # mistake: an average, not the sum
+
+
+def _bwd_unscaled(q, k, v, dout, *, causal, scale):
+    dq, dk, dv = oracle.sdpa_backward(q, k, v, dout, causal=causal, scale=scale)
+    return dq / scale, dk / scale, dv               # mistake: the chain rule's scale dropped
+
+
 MUTANTS = {
     "causal_strict_diagonal": _impl(**_with_visible(_strict)),
     "causal_top_left_alignment": _impl(**_with_visible(_top_left)),
@@ -214,6 +242,9 @@ MUTANTS = {
     "window_right_bound_ignored": _impl(**_with_visible(_window_right_ignored)),
     "varlen_key_offsets_from_queries": _impl(sdpa_varlen=_varlen_shared_offsets),
     "varlen_lse_row_major": _impl(sdpa_varlen=_varlen_lse_row_major),
+    "backward_row_term_dropped": _impl(sdpa_backward=_bwd_without_local_sum),
+    "backward_group_average": _impl(sdpa_backward=_bwd_dk_not_summed_over_group),
+    "backward_unscaled": _impl(sdpa_backward=_bwd_unscaled),
 }
 
 
