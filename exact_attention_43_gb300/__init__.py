@@ -9,6 +9,7 @@ LSE-rescaling reduce) run in hand-written CUDA kernels behind the C ABI of
 from .binding import (  # noqa: F401
     AttnError,
     ExtensionMissing,
+    attn_bwd,
     attn_decode,
     attn_decode_fused,
     attn_decode_noalloc,

@@ -25,7 +25,8 @@ ATTN_ERR_DEVICE_TIMEOUT = 4
 ATTN_BF16 = 0
 ATTN_FP16 = 1
 
-EXPORTS = ("attn_fwd", "attn_fwd_varlen", "attn_fwd_qkvpacked", "attn_decode", "attn_decode_fused", "attn_decode_paged",
+EXPORTS = ("attn_fwd", "attn_fwd_varlen", "attn_fwd_qkvpacked", "attn_bwd",
+           "attn_bwd_workspace_bytes", "attn_decode", "attn_decode_fused", "attn_decode_paged",
            "attn_decode_noalloc",
            "attn_decode_workspace_bytes",
            "attn_decode_chunk", "attn_check_device_status", "attn_debug_set",
@@ -64,6 +65,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_fwd_varlen.restype = i
     lib.attn_fwd_qkvpacked.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
     lib.attn_fwd_qkvpacked.restype = i
+    lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
+    lib.attn_bwd.restype = i
+    lib.attn_bwd_workspace_bytes.argtypes = [i, i, i, i]
+    lib.attn_bwd_workspace_bytes.restype = sz
     lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
     lib.attn_decode.restype = i
     lib.attn_decode_fused.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
@@ -194,6 +199,30 @@ def attn_fwd_qkvpacked(qkv, *, causal: bool = True, window=(-1, -1), scale=None,
                                 int(wl), int(wr), float(scale), _dtype_code(qkv), _stream(stream))
     _check(st, "attn_fwd_qkvpacked")
     return out, lse
+
+
+def attn_bwd(q, k, v, o, lse, dout, *, causal: bool = True, scale=None, dq=None, dk=None, dv=None,
+             stream=None):
+    """Gradients of attn_fwd: q, o, dout [B,Hq,Sq,D], k, v [B,Hkv,Skv,D], lse [B,Hq,Sq] float32
+    (the forward's outputs o and lse).  Returns (dQ, dK, dV)."""
+    lib = load()
+    B, Hq, Sq, D = q.shape
+    Hkv, Skv = k.shape[1], k.shape[2]
+    for t in (q, k, v, o, lse, dout):
+        if not t.is_contiguous():
+            raise ValueError("backward inputs must be contiguous")
+    if lse.dtype != torch.float32:
+        raise TypeError("lse must be float32")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    st = lib.attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                      _ptr(dv), B, Hq, Hkv, Sq, Skv, D, 1 if causal else 0, float(scale),
+                      _dtype_code(q), _stream(stream))
+    _check(st, "attn_bwd")
+    return dq, dk, dv
 
 
 def attn_decode(q, k_cache, v_cache, seq_lens, *, num_splits: int = 0, out=None, stream=None):

@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libexact_attention.so")
-SOURCES = ["api.cu", "fwd.cu", "decode.cu"]
+SOURCES = ["api.cu", "fwd.cu", "decode.cu", "bwd.cu"]
 HEADERS = ["ptx.cuh", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

@@ -272,6 +272,81 @@ int attn_fwd_qkvpacked(const void* qkv, void* o, float* lse, int B, int S, int H
   return run_fwd_tm(a, S, S, window_left, window_right, stream);
 }
 
+size_t attn_bwd_workspace_bytes(int B, int Hq, int Sq, int D) {
+  if (B < 0 || Hq < 0 || Sq < 0 || D <= 0) return 0;
+  const size_t rows = (size_t)B * Hq * Sq;
+  return rows * sizeof(float) * (D + 1) + 256;  // dQ accumulator, row terms, alignment
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq, int Skv,
+             int D, int causal, float scale, int dtype, cudaStream_t stream) {
+  if (B < 0 || Hq < 0 || Hkv < 0 || Sq < 0 || Skv < 0) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || Hq == 0 || (Sq == 0 && Skv == 0)) return ATTN_OK;  // nothing to compute
+  if (Hkv == 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (B > 65535 || Hkv > 65535 || Hq > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (Sq > 0 && (!q || !o || !lse || !dout || !dq)) return ATTN_ERR_INVALID_ARG;
+  if (Skv > 0 && (!k || !v || !dk || !dv)) return ATTN_ERR_INVALID_ARG;
+  const void* a16[] = {q, k, v, o, dout, dq, dk, dv};
+  for (const void* ptr : a16)
+    if (ptr && !aligned(ptr, 16)) return ATTN_ERR_INVALID_ARG;
+  if (lse && !aligned(lse, 4)) return ATTN_ERR_INVALID_ARG;
+  int dev = 0;
+  int st = check_device(&dev);
+  if (st != ATTN_OK) return st;
+
+  ea::BwdArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.dout = dout;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Sq = Sq;
+  a.Skv = Skv;
+  a.D = D;
+  a.causal = causal != 0;
+  a.scale = scale;
+  a.bf16 = dtype == ATTN_BF16;
+  a.wait_limit_ns = g_wait_limit_ns;
+  const size_t rows = (size_t)B * Hq * Sq;
+  if (Skv == 0) {
+    // no key: O was 0 whatever Q, K, V were, so every gradient is 0 (dK, dV are empty)
+    cudaError_t e = cudaMemsetAsync(dq, 0, rows * D * 2, stream);
+    return from_cuda(e);
+  }
+  void* ws = nullptr;
+  if (rows > 0) {
+    cudaMemPool_t pool;
+    if ((st = pool_for(dev, &pool)) != ATTN_OK) return st;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, attn_bwd_workspace_bytes(B, Hq, Sq, D), pool, stream);
+    if (e != cudaSuccess) return from_cuda(e);
+    a.dq_acc = static_cast<float*>(ws);
+    a.delta = a.dq_acc + rows * D;
+    e = cudaMemsetAsync(a.dq_acc, 0, rows * D * sizeof(float), stream);
+    if (e != cudaSuccess) {
+      cudaFreeAsync(ws, stream);
+      return from_cuda(e);
+    }
+  }
+  cudaError_t e = ea::launch_bwd(a, stream);
+  if (ws) {
+    cudaError_t f = cudaFreeAsync(ws, stream);
+    if (e == cudaSuccess) e = f;
+  }
+  if (e == cudaErrorInvalidValue && !ea::encode_tiled_fn()) return ATTN_ERR_UNSUPPORTED;
+  return from_cuda(e);
+}
+
 int attn_decode_chunk(int max_S, int num_splits) { return chunk_for(max_S, num_splits); }
 
 size_t attn_decode_workspace_bytes(int B, int Hq, int max_S, int D, int num_splits) {
@@ -442,10 +517,11 @@ int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
 int attn_check_device_status(cudaStream_t stream) {
   cudaError_t e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return from_cuda(e);
-  unsigned f = 0, d = 0;
+  unsigned f = 0, d = 0, g = 0;
   if ((e = ea::read_fwd_status(&f, stream)) != cudaSuccess) return from_cuda(e);
   if ((e = ea::read_decode_status(&d, stream)) != cudaSuccess) return from_cuda(e);
-  const unsigned all = f | d;
+  if ((e = ea::read_bwd_status(&g, stream)) != cudaSuccess) return from_cuda(e);
+  const unsigned all = f | d | g;
   if (all & 1u) return ATTN_ERR_DEVICE_TIMEOUT;
   if (all & 6u) return ATTN_ERR_INVALID_ARG;  // a seq_len clamped, a page index replaced
   return ATTN_OK;

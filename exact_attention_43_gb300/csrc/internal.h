@@ -54,6 +54,26 @@ struct DecodeArgs {
   uint64_t wait_limit_ns;
 };
 
+// Arguments of one backward call (attn_bwd), already validated.
+struct BwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const float* lse;  // [B, Hq, Sq] natural log, from the forward pass
+  const void* dout;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* delta;   // [B, Hq, Sq] fp32 workspace
+  float* dq_acc;  // [B, Hq, Sq, D] fp32 workspace, zeroed before the launch
+  int B, Hq, Hkv, Sq, Skv, D;
+  int causal;
+  float scale;
+  int bf16;
+  uint64_t wait_limit_ns;
+};
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -67,10 +87,12 @@ EncodeTiledFn encode_tiled_fn();
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_fwd_empty_keys(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
 
 // Read and clear the device status word of each kernel file.
 cudaError_t read_fwd_status(unsigned* out, cudaStream_t stream);
 cudaError_t read_decode_status(unsigned* out, cudaStream_t stream);
+cudaError_t read_bwd_status(unsigned* out, cudaStream_t stream);
 
 // Size of the fixed device scratch behind attn_decode_noalloc (see attn.h).
 constexpr size_t kNoallocPartialsBytes = 16u << 20;

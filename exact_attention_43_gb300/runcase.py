@@ -3,6 +3,7 @@
     python -m exact_attention_43_gb300.runcase fwd --workload mha [--iters 3]
     python -m exact_attention_43_gb300.runcase fwd --B 1 --H 8 --S 4096 --causal 1
     python -m exact_attention_43_gb300.runcase fwd --workload mha --layout qkvpacked [--window 256]
+    python -m exact_attention_43_gb300.runcase bwd --workload mha
     python -m exact_attention_43_gb300.runcase decode [--B 8] [--iters 3] [--page-size 64 | --fused]
 
 Inputs are drawn on the GPU from the seeded generators in workloads.py.
@@ -22,7 +23,7 @@ from . import workloads as wl
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("op", choices=["fwd", "decode"])
+    ap.add_argument("op", choices=["fwd", "bwd", "decode"])
     ap.add_argument("--workload", default=None, help="tiny | mha | gqa | long (fwd)")
     ap.add_argument("--B", type=int, default=None)
     ap.add_argument("--H", type=int, default=32)
@@ -40,7 +41,7 @@ def main():
     a = ap.parse_args()
     dev = torch.device("cuda", 0)
     ea.load()
-    if a.op == "fwd":
+    if a.op in ("fwd", "bwd"):
         if a.workload:
             w = wl.FWD_WORKLOADS[a.workload]
         else:
@@ -49,7 +50,16 @@ def main():
         q, k, v = wl.workload_fwd_inputs(w, device=dev)
         units, unit = w.flops(), "TFLOP/s"
         desc = f"{w.name} B{w.B} Hq{w.Hq} Hkv{w.Hkv} S{w.Sq} D{w.D} causal={w.causal}"
-        if a.layout == "dense":
+        if a.op == "bwd":
+            # five products per (query, key) pair against the forward's two
+            units = 2.5 * w.flops()
+            desc += " backward"
+            do = wl.normal(tuple(q.shape), seed=wl.SEED_BASE + 50, dtype=q.dtype, device=dev)
+            o, lse = ea.attn_fwd(q, k, v, causal=w.causal, scale=w.scale)
+
+            def call():
+                return ea.attn_bwd(q, k, v, o, lse, do, causal=w.causal, scale=w.scale)
+        elif a.layout == "dense":
             def call():
                 return ea.attn_fwd(q, k, v, causal=w.causal, scale=w.scale)
         else:

@@ -120,6 +120,32 @@ int attn_fwd_qkvpacked(const void* qkv, void* o, float* lse, int B, int S, int H
                        cudaStream_t stream);
 
 /*
+ * attn_bwd -- gradients of attn_fwd: dQ, dK, dV for an incoming dO.
+ *
+ * As the llm.c attention page's attention_backward computes them:
+ *   dP = dO V^T, dV = P^T dO, dS = scale * P * (dP - rowsum(P * dP)),
+ *   dQ = dS K, dK = dS^T Q,
+ * P being the forward's probabilities, re-formed here from its LSE
+ * (P = e^(scale Q K^T - LSE) on the visible keys), and rowsum(P * dP) taken as
+ * rowsum(dO * O).  A KV head's dK and dV are summed over the query heads that
+ * share it.  Same layouts, causal rule and head mapping as attn_fwd.
+ *
+ * q, o, dout, dq   device, [B, Hq, Sq, D], dtype `dtype`, 16-byte aligned.
+ * k, v, dk, dv     device, [B, Hkv, Skv, D], 16-byte aligned.
+ * lse              device, [B, Hq, Sq] float32, the forward's (natural log).
+ * o, lse must be attn_fwd's outputs for these q, k, v, causal and scale.
+ * A workspace of attn_bwd_workspace_bytes(B, Hq, Sq, D) bytes (fp32 dQ
+ * accumulator and row terms) is taken from the library's stream-ordered pool.
+ * D 64 or 128; B, Hq, Hkv <= 65535; scale finite.  With Skv == 0, dq = 0.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq, int Skv,
+             int D, int causal, float scale, int dtype, cudaStream_t stream);
+
+/* Bytes of workspace attn_bwd allocates for these sizes; 0 on invalid sizes. */
+size_t attn_bwd_workspace_bytes(int B, int Hq, int Sq, int D);
+
+/*
  * attn_decode -- flash-decoding: one query token per sequence against a KV cache.
  *
  *   O[b,h,:] = softmax_j(Q[b,h,:] . K[b,g,j,:] / sqrt(D)) V[b,g,j,:],  0 <= j < seq_lens[b].

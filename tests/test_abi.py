@@ -127,6 +127,27 @@ def test_varlen_and_packed_argument_errors(lib):
     assert pk(S=0) == 0
 
 
+def test_backward_argument_errors(lib):
+    def bw(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, do=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, B=2,
+                 Hq=8, Hkv=2, Sq=64, Skv=64, D=128, causal=1, scale=0.1, dtype=0)
+        a.update(kw)
+        return lib.attn_bwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["do"], a["dq"], a["dk"],
+                            a["dv"], a["B"], a["Hq"], a["Hkv"], a["Sq"], a["Skv"], a["D"],
+                            a["causal"], a["scale"], a["dtype"], None)
+
+    assert bw(lse=None) == 1
+    assert bw(dk=None) == 1
+    assert bw(dq=FAKE + 8) == 1
+    assert bw(Hkv=3) == 1
+    assert bw(scale=float("nan")) == 1
+    assert bw(D=32) == 2 and bw(dtype=7) == 2
+    assert bw(B=0) == 0 and bw(Sq=0, Skv=0) == 0
+    # fp32 dQ accumulator and row terms, plus alignment slack
+    assert lib.attn_bwd_workspace_bytes(2, 8, 64, 128) == 2 * 8 * 64 * 4 * 129 + 256
+    assert lib.attn_bwd_workspace_bytes(-1, 8, 64, 128) == 0
+
+
 def test_fused_decode_argument_errors(lib):
     def fused(**kw):
         a = dict(q=FAKE, k=FAKE, v=FAKE, lens=FAKE, o=FAKE, B=2, Hq=8, Hkv=2, max_S=64, D=128,
