@@ -16,13 +16,16 @@
 //    GQA group and every Q tile that sees the keys (causal tiles that see none are
 //    skipped), so K/V gradients need no atomics;
 //  * per Q tile one thread issues the tcgen05 MMAs: S^T = K Q^T and
-//    dP^T = V dO^T into TMEM; four compute warps (one key row per thread, TMEM
-//    lane = key) form P^T = 2^(S^T c - LSE_2) and dS^T = P^T (dP^T - delta), write
+//    dP^T = V dO^T into TMEM; eight compute warps (two threads per key row, each
+//    with 64 of the tile's 128 queries; TMEM lane = key) form P^T = 2^(S^T c - LSE_2) and dS^T = P^T (dP^T - delta), write
 //    both to TMEM as 16-bit (over the columns they came from) and dS^T also to a
 //    128-byte-swizzled shared-memory tile; then dV += P^T dO and dK += dS^T Q (A
-//    from TMEM) and dQ_part = dS K (A: the dS^T tile read M-major) over S^T's
+//    from TMEM) and dQ_part = dS K (A: the dS^T tile read M-major) over dP^T's
 //    columns; the compute warps add scale * dQ_part (TMEM lane = query row) into
 //    an fp32 accumulator with 16-byte vector atomics;
+//  * Q and dO are double-buffered (the next Q tile's loads run during this one's
+//    MMAs) and the next S^T is issued before the compute warps have read this
+//    dQ_part, so the tensor core has work queued while they add it;
 //  * a last kernel rounds the dQ accumulator to the input type.
 #include "internal.h"
 #include "ptx.cuh"
@@ -36,11 +39,12 @@ __device__ unsigned g_status;
 
 constexpr int BM = 128;  // queries per Q tile
 constexpr int BN = 128;  // keys per K/V tile (= TMEM lanes)
-constexpr int THREADS = 160;  // warps 0-3 compute, warp 4 loads and issues
-constexpr int ISSUER_WARP = 4;
+constexpr int THREADS = 288;  // warps 0-7 compute, warp 8 loads and issues
+constexpr int ISSUER_WARP = 8;
+constexpr int NCOMP = 256;    // compute threads: warps w and w + 4 share TMEM lanes 32 (w mod 4) ...
 constexpr uint32_t TMEM_COLS = 512;
-// TMEM columns: S^T at 0 (P^T over its first 64; dQ_part over its first D once
-// dV has read P^T), dP^T at 128 (dS^T over its first 64), dV at 256, dK at 256 + D
+// TMEM columns: S^T at 0 (P^T over its first 64), dP^T at 128 (dS^T over its first
+// 64; dQ_part over its first D once dK has read dS^T), dV at 256, dK at 256 + D
 
 struct Params {
   const float* lse;    // [B, Hq, Sq], natural log
@@ -61,12 +65,12 @@ struct Layout {
   static constexpr int TILE = NREG * REGION;  // 128 x D
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = TILE;
-  static constexpr int Q_OFF = 2 * TILE;
-  static constexpr int DO_OFF = 3 * TILE;
-  static constexpr int DS_OFF = 4 * TILE;               // dS^T: 128 keys x 128 queries
+  static constexpr int Q_OFF = 2 * TILE;                // two buffers
+  static constexpr int DO_OFF = 4 * TILE;               // two buffers
+  static constexpr int DS_OFF = 6 * TILE;               // dS^T: 128 keys x 128 queries
   static constexpr int VEC_OFF = DS_OFF + 2 * REGION;   // LSE (log2 units), delta of the Q tile
   static constexpr int BAR_OFF = VEC_OFF + 2 * BM * 4;
-  enum { KV_FULL, QD_FULL, S_FULL, P_FULL, DQ_FULL, DQ_FREE, VEC_READY, NUM_BARS };
+  enum { KV_FULL, QD_FULL, S_FULL = QD_FULL + 2, P_FULL, DQ_FULL, DQ_FREE, VEC_READY, DRAIN, NUM_BARS };
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;  // [0] TMEM base, [1] abort flag
   static constexpr int BYTES = MISC_OFF + 16;
   static constexpr int ALLOC = BYTES + 1024;  // slack to align the base to 1024 bytes
@@ -146,7 +150,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t lim = p.wait_limit_ns;
 
-  const int n0 = blockIdx.x * BN, hk = blockIdx.y, b = blockIdx.z;
+  // key tiles vary slowest, so the causal tiles that most Q tiles see start first
+  const int n0 = blockIdx.z * BN, hk = blockIdx.x, b = blockIdx.y;
   const int dlen = p.Skv - p.Sq;  // key j is visible to query i iff j <= i + dlen (causal)
   const int n_mt = (p.Sq + BM - 1) / BM;
   int m_lo = 0;  // first Q tile with a row that sees a key of this tile
@@ -160,11 +165,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar(L::KV_FULL), 1);
     mbar_init(bar(L::QD_FULL), 1);
+    mbar_init(bar(L::QD_FULL + 1), 1);
     mbar_init(bar(L::S_FULL), 1);
-    mbar_init(bar(L::P_FULL), BM);
+    mbar_init(bar(L::P_FULL), NCOMP);
     mbar_init(bar(L::DQ_FULL), 1);
-    mbar_init(bar(L::DQ_FREE), BM);
-    mbar_init(bar(L::VEC_READY), BM);
+    mbar_init(bar(L::DQ_FREE), NCOMP);
+    mbar_init(bar(L::VEC_READY), NCOMP);
+    mbar_init(bar(L::DRAIN), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -197,49 +204,64 @@ __global__ void __launch_bounds__(THREADS, 1)
       // rows are the K dimension, LBO steps to the next 64 columns, SBO to the next 8 rows
       const uint64_t k_km = sdesc_sw128(sb + L::K_OFF, 16, 1024);
       const uint64_t v_km = sdesc_sw128(sb + L::V_OFF, 16, 1024);
-      const uint64_t q_km = sdesc_sw128(sb + L::Q_OFF, 16, 1024);
-      const uint64_t do_km = sdesc_sw128(sb + L::DO_OFF, 16, 1024);
       const uint64_t k_mn = sdesc_sw128(sb + L::K_OFF, L::REGION, 1024);
-      const uint64_t q_mn = sdesc_sw128(sb + L::Q_OFF, L::REGION, 1024);
-      const uint64_t do_mn = sdesc_sw128(sb + L::DO_OFF, L::REGION, 1024);
       const uint64_t ds_mn = sdesc_sw128(sb + L::DS_OFF, L::REGION, 1024);
       constexpr uint32_t idesc_s = umma_idesc_f16(BF16, BN, BM, false, false);
       constexpr uint32_t idesc_kv = umma_idesc_f16(BF16, BN, D, false, true);
       constexpr uint32_t idesc_dq = umma_idesc_f16(BF16, BM, D, true, true);
       const uint32_t t_s = tmem, t_dp = tmem + 128, t_dv = tmem + 256, t_dk = tmem + 256 + D;
-      int n_qd = 0, n_s = 0, n_dq = 0;  // phases of QD_FULL, S_FULL, DQ_FULL started
-      bool ok = true;
-      for (int it = 0; it < n_iter && ok; ++it) {
-        const int h = hk * p.group + it / per_head, m = m_lo + it % per_head;
-        // Q, dO of this tile may overwrite the last ones once its MMAs are done
-        if (it > 0 && !(ok = mbar_wait(bar(L::DQ_FULL), (it - 1) & 1, abort_flag, &g_status, lim)))
-          break;
-        mbar_expect_tx(bar(L::QD_FULL), 2 * L::TILE);
+      // Q, dO of iteration i go to buffer i & 1
+      auto load_qd = [&](int i) {
+        const int h = hk * p.group + i / per_head, m = m_lo + i % per_head;
+        const uint32_t fb = bar(L::QD_FULL + (i & 1));
+        mbar_expect_tx(fb, 2 * L::TILE);
         for (int rr = 0; rr < L::NREG; ++rr) {
-          tma_load_3d(sb + L::Q_OFF + rr * L::REGION, &tmq, bar(L::QD_FULL), rr * 64, m * BM,
+          tma_load_3d(sb + L::Q_OFF + (i & 1) * L::TILE + rr * L::REGION, &tmq, fb, rr * 64, m * BM,
                       b * p.Hq + h, pol_q);
-          tma_load_3d(sb + L::DO_OFF + rr * L::REGION, &tmdo, bar(L::QD_FULL), rr * 64, m * BM,
+          tma_load_3d(sb + L::DO_OFF + (i & 1) * L::TILE + rr * L::REGION, &tmdo, fb, rr * 64, m * BM,
                       b * p.Hq + h, pol_q);
         }
+      };
+      int n_qd = 0;  // Q/dO loads issued
+      load_qd(0);
+      ++n_qd;
+      if (n_iter > 1) {
+        load_qd(1);
         ++n_qd;
-        if (!(ok = mbar_wait(bar(L::QD_FULL), it & 1, abort_flag, &g_status, lim))) break;
+      }
+      bool ok = true;
+      for (int it = 0; it < n_iter && ok; ++it) {
+        const uint32_t qo = (it & 1) * L::TILE;
+        const uint64_t q_km = sdesc_sw128(sb + L::Q_OFF + qo, 16, 1024);
+        const uint64_t do_km = sdesc_sw128(sb + L::DO_OFF + qo, 16, 1024);
+        const uint64_t q_mn = sdesc_sw128(sb + L::Q_OFF + qo, L::REGION, 1024);
+        const uint64_t do_mn = sdesc_sw128(sb + L::DO_OFF + qo, L::REGION, 1024);
+        if (!(ok = mbar_wait(bar(L::QD_FULL + (it & 1)), (it >> 1) & 1, abort_flag, &g_status, lim)))
+          break;
         if (it == 0 && !(ok = mbar_wait(bar(L::KV_FULL), 0, abort_flag, &g_status, lim))) break;
-        // S^T's columns held the last dQ_part: the compute warps must have read it
+        tc_fence_after();
+        // S^T = K Q^T: its columns' last P^T was read by the last dV, issued before
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * L::REGION + (kk & 3) * 32) >> 4;
+          umma_ss(t_s, k_km + off, q_km + off, idesc_s, kk > 0 ? 1u : 0u);
+        }
+        // dP^T's columns held the last dQ_part: the compute warps must have read it
         if (it > 0 && !(ok = mbar_wait(bar(L::DQ_FREE), (it - 1) & 1, abort_flag, &g_status, lim)))
           break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * L::REGION + (kk & 3) * 32) >> 4;
-          umma_ss(t_s, k_km + off, q_km + off, idesc_s, kk > 0 ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * L::REGION + (kk & 3) * 32) >> 4;
           umma_ss(t_dp, v_km + off, do_km + off, idesc_s, kk > 0 ? 1u : 0u);
         }
         umma_commit(bar(L::S_FULL));
-        ++n_s;
+        // the other buffer's last reader, iteration it - 1, has completed (its DQ_FULL
+        // preceded DQ_FREE): load iteration it + 1 into it
+        if (it > 0 && it + 1 < n_iter) {
+          load_qd(it + 1);
+          ++n_qd;
+        }
         if (!(ok = mbar_wait(bar(L::P_FULL), it & 1, abort_flag, &g_status, lim))) break;
         tc_fence_after();
         // dV += P^T dO and dK += dS^T Q over the tile's 128 queries, 16 per MMA
@@ -249,28 +271,33 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
           umma_ts(t_dk, t_dp + kk * 8, q_mn + kk * 128, idesc_kv, (it > 0 || kk > 0) ? 1u : 0u);
-        // dQ_part = dS K over the tile's 128 keys, into S^T's columns (after dV read P^T)
+        // dQ_part = dS K over the tile's 128 keys, into dP^T's columns (after dK read dS^T)
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          umma_ss(t_s, ds_mn + kk * 128, k_mn + kk * 128, idesc_dq, kk > 0 ? 1u : 0u);
+          umma_ss(t_dp, ds_mn + kk * 128, k_mn + kk * 128, idesc_dq, kk > 0 ? 1u : 0u);
         umma_commit(bar(L::DQ_FULL));
-        ++n_dq;
       }
-      // nothing may be in flight when the CTA exits: wait for the last phase of each
-      // barrier this thread started (no later phase follows, so none is missed)
+      // nothing may be in flight when the CTA exits: the last load into each buffer
+      // (no later phase follows, so none is missed) and every MMA issued above (one
+      // more commit, on a barrier of its own, tracks them all, also after an abort)
       drain_wait(bar(L::KV_FULL), 0, lim);
-      if (n_qd > 0) drain_wait(bar(L::QD_FULL), (n_qd - 1) & 1, lim);
-      if (n_s > 0) drain_wait(bar(L::S_FULL), (n_s - 1) & 1, lim);
-      if (n_dq > 0) drain_wait(bar(L::DQ_FULL), (n_dq - 1) & 1, lim);
+      for (int i = max(0, n_qd - 2); i < n_qd; ++i)
+        drain_wait(bar(L::QD_FULL + (i & 1)), (i >> 1) & 1, lim);
+      umma_commit(bar(L::DRAIN));
+      drain_wait(bar(L::DRAIN), 0, lim);
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------ compute warps: one key row per thread
-    const int r = threadIdx.x;  // TMEM lane: key n0 + r (S^T, dP^T, dK, dV), query m0 + r (dQ_part)
-    const uint32_t lane_t = tmem + ((uint32_t)(warp * 32) << 16);
+    // ------------------------------------------------ compute warps: two threads per key row
+    // TMEM lane r: key n0 + r (S^T, dP^T, dK, dV), query m0 + r (dQ_part); warps w and
+    // w + 4 share the lanes of quarter w and split the columns between them
+    const int quarter = warp & 3, half = warp >> 2;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_t = tmem + ((uint32_t)(quarter * 32) << 16);
     float* v_lse = reinterpret_cast<float*>(smem + L::VEC_OFF);
     float* v_dl = v_lse + BM;
     const int key = n0 + r;
+    const int c0 = half * 64;  // this thread's 64 of the tile's 128 queries
     auto wait_warp = [&](uint32_t b_, uint32_t ph_) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(b_, ph_, abort_flag, &g_status, lim));
     };
@@ -279,41 +306,44 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int h = hk * p.group + it / per_head, m = m_lo + it % per_head;
       const int m0 = m * BM;
       const size_t bh = (size_t)b * p.Hq + h;
-      // the row vectors of this Q tile: every thread read the last ones before P_FULL
-      // completed, which the last DQ_FULL implies
+      // the row vectors of this Q tile (half 0: LSE, half 1: delta): every thread read
+      // the last ones before P_FULL completed, which the last DQ_FULL implies
       {
         const int qi = m0 + r;
-        v_lse[r] = qi < p.Sq ? p.lse[bh * p.Sq + qi] * 1.4426950408889634f : INFINITY;
-        v_dl[r] = qi < p.Sq ? p.delta[bh * p.Sq + qi] : 0.f;
+        if (half == 0) v_lse[r] = qi < p.Sq ? p.lse[bh * p.Sq + qi] * 1.4426950408889634f : INFINITY;
+        else v_dl[r] = qi < p.Sq ? p.delta[bh * p.Sq + qi] : 0.f;
         mbar_arrive(bar(L::VEC_READY));
       }
       if (!(ok = wait_warp(bar(L::VEC_READY), it & 1))) break;
       if (!(ok = wait_warp(bar(L::S_FULL), it & 1))) break;
       tc_fence_after();
+      {
+        uint32_t pp[32], dd[32];  // this thread's 64 queries of P^T, dS^T as 16-bit pairs
 #pragma unroll
-      for (int c0 = 0; c0 < BM; c0 += 64) {
-        uint32_t sr[64], dr[64];
-        tmem_ld(lane_t + c0, sr);
-        tmem_ld(lane_t + 128 + c0, dr);
-        uint32_t pp[32], dd[32];
+        for (int g = 0; g < 2; ++g) {  // 32 queries at a time
+          uint32_t sr[32], dr[32];
+          tmem_ld32(lane_t + c0 + 32 * g, sr);
+          tmem_ld32(lane_t + 128 + c0 + 32 * g, dr);
 #pragma unroll
-        for (int j = 0; j < 64; j += 2) {
-          float pv[2], dsv[2];
+          for (int j = 0; j < 32; j += 2) {
+            float pv[2], dsv[2];
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int q = m0 + c0 + j + u;
-            const bool vis = q < p.Sq && key < p.Skv && (!p.causal || key <= q + dlen);
-            const float x = fmaf(__uint_as_float(sr[j + u]), p.c2, -v_lse[c0 + j + u]);
-            pv[u] = vis ? ex2(x) : 0.f;
-            dsv[u] = pv[u] * (__uint_as_float(dr[j + u]) - v_dl[c0 + j + u]);
+            for (int u = 0; u < 2; ++u) {
+              const int cq = c0 + 32 * g + j + u;  // query column in the tile
+              const int q = m0 + cq;
+              const bool vis = q < p.Sq && key < p.Skv && (!p.causal || key <= q + dlen);
+              const float x = fmaf(__uint_as_float(sr[j + u]), p.c2, -v_lse[cq]);
+              pv[u] = vis ? ex2(x) : 0.f;
+              dsv[u] = pv[u] * (__uint_as_float(dr[j + u]) - v_dl[cq]);
+            }
+            pp[16 * g + (j >> 1)] = pack2<BF16>(pv[0], pv[1]);
+            dd[16 * g + (j >> 1)] = pack2<BF16>(dsv[0], dsv[1]);
           }
-          pp[j >> 1] = pack2<BF16>(pv[0], pv[1]);
-          dd[j >> 1] = pack2<BF16>(dsv[0], dsv[1]);
         }
         tmem_st32(lane_t + (c0 >> 1), pp);        // P^T over S^T's columns
         tmem_st32(lane_t + 128 + (c0 >> 1), dd);  // dS^T over dP^T's columns
         // dS^T row r, queries c0 .. c0 + 63: 16-byte chunk c at chunk c ^ (r mod 8)
-        const uint32_t reg = sb + L::DS_OFF + (c0 / 64) * L::REGION + r * 128;
+        const uint32_t reg = sb + L::DS_OFF + half * L::REGION + r * 128;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           st_shared_v4(reg + ((c ^ (r & 7)) << 4),
@@ -325,13 +355,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_arrive(bar(L::P_FULL));
       if (!(ok = wait_warp(bar(L::DQ_FULL), it & 1))) break;
       tc_fence_after();
-      // dQ_part row r (query m0 + r) into the fp32 accumulator
+      // dQ_part row r (query m0 + r), this half's D / 2 columns, into the fp32 accumulator
       const bool live = m0 + r < p.Sq;
-      float* dst = p.dq_acc + (bh * p.Sq + (live ? m0 + r : 0)) * D;
+      float* dst = p.dq_acc + (bh * p.Sq + (live ? m0 + r : 0)) * D + half * (D / 2);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
         uint32_t v[32];
-        tmem_ld32(lane_t + 32 * c, v);
+        tmem_ld32(lane_t + 128 + half * (D / 2) + 32 * c, v);
         if (live) {
 #pragma unroll
           for (int i = 0; i < 8; ++i)
@@ -345,27 +375,22 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_before();
       mbar_arrive(bar(L::DQ_FREE));
     }
-    // dV and dK rows of this tile's keys (zero when no query sees them)
-    if (ok && key < p.Skv) {
-      uint4* dvr = reinterpret_cast<uint4*>(p.dv + (((size_t)b * p.Hkv + hk) * p.Skv + key) * D);
-      uint4* dkr = reinterpret_cast<uint4*>(p.dk + (((size_t)b * p.Hkv + hk) * p.Skv + key) * D);
+    // this tile's dV rows (half 0) and dK rows (half 1); zero when no query sees the key
+    if (ok) {
+      const float f = half == 0 ? 1.f : p.scale;
+      uint16_t* grad = half == 0 ? p.dv : p.dk;
+      uint4* row = reinterpret_cast<uint4*>(grad + (((size_t)b * p.Hkv + hk) * p.Skv + key) * D);
       if (n_iter == 0) {
-        for (int i = 0; i < D / 8; ++i) dvr[i] = dkr[i] = make_uint4(0, 0, 0, 0);
-      }
-    }
-    if (ok && n_iter > 0) {
+        if (key < p.Skv)
+          for (int i = 0; i < D / 8; ++i) row[i] = make_uint4(0, 0, 0, 0);
+      } else {
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32], w[32];
-        tmem_ld32(lane_t + 256 + 32 * c, v);
-        tmem_ld32(lane_t + 256 + D + 32 * c, w);
-        if (key < p.Skv) {
-          uint4* dvr = reinterpret_cast<uint4*>(p.dv + (((size_t)b * p.Hkv + hk) * p.Skv + key) * D);
-          uint4* dkr = reinterpret_cast<uint4*>(p.dk + (((size_t)b * p.Hkv + hk) * p.Skv + key) * D);
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(lane_t + 256 + half * D + 32 * c, v);
+          if (key < p.Skv) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            dvr[4 * c + i] = pack8<BF16>(v + 8 * i, 1.f);
-            dkr[4 * c + i] = pack8<BF16>(w + 8 * i, p.scale);
+            for (int i = 0; i < 4; ++i) row[4 * c + i] = pack8<BF16>(v + 8 * i, f);
           }
         }
       }
@@ -433,7 +458,7 @@ static cudaError_t launch_t(const BwdArgs& a, cudaStream_t stream) {
     p.scale = a.scale;
     p.c2 = a.scale * 1.4426950408889634f;
     p.wait_limit_ns = a.wait_limit_ns;
-    dim3 grid((a.Skv + BN - 1) / BN, a.Hkv, a.B);
+    dim3 grid(a.Hkv, a.B, (a.Skv + BN - 1) / BN);
     attn_bwd_kernel<D, BF16><<<grid, THREADS, L::ALLOC, stream>>>(tq, tk, tv, tg, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
