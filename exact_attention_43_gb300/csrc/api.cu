@@ -318,6 +318,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   a.scale = scale;
   a.bf16 = dtype == ATTN_BF16;
   a.wait_limit_ns = g_wait_limit_ns;
+  a.num_sms = g_num_sms[dev] > 0 ? g_num_sms[dev] : 1;
   const size_t rows = (size_t)B * Hq * Sq;
   if (Skv == 0) {
     // no key: O was 0 whatever Q, K, V were, so every gradient is 0 (dK, dV are empty)

@@ -53,6 +53,7 @@ struct Params {
   uint16_t* dk;        // [B, Hkv, Skv, D]
   uint16_t* dv;
   int B, Hq, Hkv, Sq, Skv, group, causal;
+  int kv_slowest;  // 1: grid (KV head, batch, key tile), 0: (key tile, KV head, batch)
   float c2;     // scale * log2(e)
   float scale;
   uint64_t wait_limit_ns;
@@ -150,8 +151,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t lim = p.wait_limit_ns;
 
-  // key tiles vary slowest, so the causal tiles that most Q tiles see start first
-  const int n0 = blockIdx.z * BN, hk = blockIdx.x, b = blockIdx.y;
+  // Key tiles vary fastest: CTAs that run at the same time share a few heads, whose
+  // fp32 dQ rows then stay in L2 for their atomics, and within a head the causal
+  // tiles that most Q tiles see start first.  When one CTA's work is a large share
+  // of an SM's, key tiles vary slowest instead, so those long CTAs start first.
+  const int n0 = (p.kv_slowest ? blockIdx.z : blockIdx.x) * BN;
+  const int hk = p.kv_slowest ? blockIdx.x : blockIdx.y, b = p.kv_slowest ? blockIdx.y : blockIdx.z;
   const int dlen = p.Skv - p.Sq;  // key j is visible to query i iff j <= i + dlen (causal)
   const int n_mt = (p.Sq + BM - 1) / BM;
   int m_lo = 0;  // first Q tile with a row that sees a key of this tile
@@ -301,19 +306,25 @@ __global__ void __launch_bounds__(THREADS, 1)
     auto wait_warp = [&](uint32_t b_, uint32_t ph_) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(b_, ph_, abort_flag, &g_status, lim));
     };
+    // row r's LSE (half 0, log2 units) or delta (half 1) for iteration i, loaded one
+    // iteration ahead so its latency hides behind the current one
+    auto row_value = [&](int i) -> float {
+      const int hi = hk * p.group + i / per_head, qi = (m_lo + i % per_head) * BM + r;
+      if (qi >= p.Sq) return half == 0 ? INFINITY : 0.f;
+      const size_t idx = ((size_t)b * p.Hq + hi) * p.Sq + qi;
+      return half == 0 ? p.lse[idx] * 1.4426950408889634f : p.delta[idx];
+    };
+    float next_v = n_iter > 0 ? row_value(0) : 0.f;
     bool ok = true;
     for (int it = 0; it < n_iter && ok; ++it) {
       const int h = hk * p.group + it / per_head, m = m_lo + it % per_head;
       const int m0 = m * BM;
       const size_t bh = (size_t)b * p.Hq + h;
-      // the row vectors of this Q tile (half 0: LSE, half 1: delta): every thread read
-      // the last ones before P_FULL completed, which the last DQ_FULL implies
-      {
-        const int qi = m0 + r;
-        if (half == 0) v_lse[r] = qi < p.Sq ? p.lse[bh * p.Sq + qi] * 1.4426950408889634f : INFINITY;
-        else v_dl[r] = qi < p.Sq ? p.delta[bh * p.Sq + qi] : 0.f;
-        mbar_arrive(bar(L::VEC_READY));
-      }
+      // the row vectors of this Q tile: every thread read the last ones before P_FULL
+      // completed, which the last DQ_FULL implies
+      (half == 0 ? v_lse : v_dl)[r] = next_v;
+      mbar_arrive(bar(L::VEC_READY));
+      if (it + 1 < n_iter) next_v = row_value(it + 1);
       if (!(ok = wait_warp(bar(L::VEC_READY), it & 1))) break;
       if (!(ok = wait_warp(bar(L::S_FULL), it & 1))) break;
       tc_fence_after();
@@ -458,7 +469,22 @@ static cudaError_t launch_t(const BwdArgs& a, cudaStream_t stream) {
     p.scale = a.scale;
     p.c2 = a.scale * 1.4426950408889634f;
     p.wait_limit_ns = a.wait_limit_ns;
-    dim3 grid(a.Hkv, a.B, (a.Skv + BN - 1) / BN);
+    // the longest CTA (key tile 0) against an SM's share of all (query head, Q tile)
+    // iterations: above a fifth, start the long CTAs first
+    const long long n_kt = (a.Skv + BN - 1) / BN, n_mt = (a.Sq + BM - 1) / BM;
+    long long total = 0;
+    for (long long t = 0; t < n_kt; ++t) {
+      long long m_lo = 0;
+      if (a.causal) {
+        const long long lo = t * BN - (a.Skv - a.Sq) - (BM - 1);
+        m_lo = lo <= 0 ? 0 : ((lo + BM - 1) / BM < n_mt ? (lo + BM - 1) / BM : n_mt);
+      }
+      total += n_mt - m_lo;
+    }
+    total *= (long long)a.B * a.Hq;
+    const long long longest = n_mt * (a.Hq / a.Hkv);
+    p.kv_slowest = longest * 5 * (a.num_sms > 0 ? a.num_sms : 1) > total ? 1 : 0;
+    const dim3 grid = p.kv_slowest ? dim3(a.Hkv, a.B, (unsigned)n_kt) : dim3((unsigned)n_kt, a.Hkv, a.B);
     attn_bwd_kernel<D, BF16><<<grid, THREADS, L::ALLOC, stream>>>(tq, tk, tv, tg, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -72,6 +72,7 @@ struct BwdArgs {
   float scale;
   int bf16;
   uint64_t wait_limit_ns;
+  int num_sms;  // multiprocessors of the device (CTA ordering)
 };
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
