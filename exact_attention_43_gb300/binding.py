@@ -120,6 +120,29 @@ def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
+def _cuda16(t, name):
+    """The device of `t`, which must be a 16-bit (bf16 / fp16) CUDA tensor."""
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    _dtype_code(t)
+    return t.device
+
+
+def _expect(t, name, shape, dtype, device):
+    """Raise unless `t` is a contiguous tensor of this shape and dtype on `device`:
+    the library trusts the sizes it is given, so nothing may be smaller than they say."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
 def attn_fwd(q, k, v, *, causal: bool, scale: float | None = None, out=None, lse=None,
              return_lse: bool = True, stream=None):
     """Prefill attention: q [B,Hq,Sq,D], k/v [B,Hkv,Skv,D] (contiguous CUDA tensors).
@@ -128,19 +151,21 @@ def attn_fwd(q, k, v, *, causal: bool, scale: float | None = None, out=None, lse
     return_lse is False and no lse buffer was given).
     """
     lib = load()
+    dev = _cuda16(q, "q")
     B, Hq, Sq, D = q.shape
     Hkv, Skv = k.shape[1], k.shape[2]
-    for t in (q, k, v):
-        if not t.is_contiguous():
-            raise ValueError("q, k and v must be contiguous")
-    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != D:
-        raise ValueError("k and v must be [B, Hkv, Skv, D] matching q")
+    _expect(q, "q", (B, Hq, Sq, D), q.dtype, dev)
+    _expect(k, "k", (B, Hkv, Skv, D), q.dtype, dev)
+    _expect(v, "v", (B, Hkv, Skv, D), q.dtype, dev)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
         out = torch.empty_like(q)
+    _expect(out, "out", q.shape, q.dtype, dev)
     if lse is None and return_lse:
         lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _expect(lse, "lse", (B, Hq, Sq), torch.float32, dev)
     st = lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Skv, D,
                       1 if causal else 0, float(scale), _dtype_code(q), _stream(stream))
     _check(st, "attn_fwd")
@@ -153,22 +178,26 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_
     """Packed variable-length prefill: q [total_q,Hq,D], k/v [total_k,Hkv,D], cu_seqlens_* [B+1]
     int32 (all CUDA); window = (left, right), -1 for no bound.  Returns (O, LSE [Hq,total_q])."""
     lib = load()
+    dev = _cuda16(q, "q")
     total_q, Hq, D = q.shape
     total_k, Hkv = k.shape[0], k.shape[1]
-    for t in (q, k, v, cu_seqlens_q, cu_seqlens_k):
-        if not t.is_contiguous():
-            raise ValueError("varlen inputs must be contiguous")
-    if cu_seqlens_q.dtype != torch.int32 or cu_seqlens_k.dtype != torch.int32:
-        raise TypeError("cu_seqlens must be int32")
-    if cu_seqlens_q.numel() != cu_seqlens_k.numel() or cu_seqlens_q.numel() < 1:
-        raise ValueError("cu_seqlens_q and cu_seqlens_k need the same B + 1 entries")
+    _expect(q, "q", (total_q, Hq, D), q.dtype, dev)
+    _expect(k, "k", (total_k, Hkv, D), q.dtype, dev)
+    _expect(v, "v", (total_k, Hkv, D), q.dtype, dev)
+    if cu_seqlens_q.dim() != 1 or cu_seqlens_q.numel() < 1:
+        raise ValueError("cu_seqlens_q must hold B + 1 offsets")
     B = cu_seqlens_q.numel() - 1
+    _expect(cu_seqlens_q, "cu_seqlens_q", (B + 1,), torch.int32, dev)
+    _expect(cu_seqlens_k, "cu_seqlens_k", (B + 1,), torch.int32, dev)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
         out = torch.empty_like(q)
+    _expect(out, "out", q.shape, q.dtype, dev)
     if lse is None and return_lse:
         lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _expect(lse, "lse", (Hq, total_q), torch.float32, dev)
     wl, wr = window
     st = lib.attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q),
                              _ptr(cu_seqlens_k), B, Hq, Hkv, total_q, total_k, int(max_seqlen_q),
@@ -183,17 +212,20 @@ def attn_fwd_qkvpacked(qkv, *, causal: bool = True, window=(-1, -1), scale=None,
     """Prefill reading Q, K, V in place from qkv [B,S,3,H,D] (CUDA).  Returns (O [B,S,H,D],
     LSE [H,B,S])."""
     lib = load()
+    dev = _cuda16(qkv, "qkv")
     if qkv.dim() != 5 or qkv.shape[2] != 3:
         raise ValueError("qkv must be [B, S, 3, H, D]")
-    if not qkv.is_contiguous():
-        raise ValueError("qkv must be contiguous")
     B, S, _, H, D = qkv.shape
+    _expect(qkv, "qkv", (B, S, 3, H, D), qkv.dtype, dev)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
         out = torch.empty((B, S, H, D), dtype=qkv.dtype, device=qkv.device)
+    _expect(out, "out", (B, S, H, D), qkv.dtype, dev)
     if lse is None and return_lse:
         lse = torch.empty((H, B, S), dtype=torch.float32, device=qkv.device)
+    if lse is not None:
+        _expect(lse, "lse", (H, B, S), torch.float32, dev)
     wl, wr = window
     st = lib.attn_fwd_qkvpacked(_ptr(qkv), _ptr(out), _ptr(lse), B, S, H, D, 1 if causal else 0,
                                 int(wl), int(wr), float(scale), _dtype_code(qkv), _stream(stream))
@@ -206,18 +238,22 @@ def attn_bwd(q, k, v, o, lse, dout, *, causal: bool = True, scale=None, dq=None,
     """Gradients of attn_fwd: q, o, dout [B,Hq,Sq,D], k, v [B,Hkv,Skv,D], lse [B,Hq,Sq] float32
     (the forward's outputs o and lse).  Returns (dQ, dK, dV)."""
     lib = load()
+    dev = _cuda16(q, "q")
     B, Hq, Sq, D = q.shape
     Hkv, Skv = k.shape[1], k.shape[2]
-    for t in (q, k, v, o, lse, dout):
-        if not t.is_contiguous():
-            raise ValueError("backward inputs must be contiguous")
-    if lse.dtype != torch.float32:
-        raise TypeError("lse must be float32")
+    for t, name in ((q, "q"), (o, "o"), (dout, "dout")):
+        _expect(t, name, (B, Hq, Sq, D), q.dtype, dev)
+    for t, name in ((k, "k"), (v, "v")):
+        _expect(t, name, (B, Hkv, Skv, D), q.dtype, dev)
+    _expect(lse, "lse", (B, Hq, Sq), torch.float32, dev)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    _expect(dq, "dq", q.shape, q.dtype, dev)
+    _expect(dk, "dk", k.shape, q.dtype, dev)
+    _expect(dv, "dv", v.shape, q.dtype, dev)
     st = lib.attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
                       _ptr(dv), B, Hq, Hkv, Sq, Skv, D, 1 if causal else 0, float(scale),
                       _dtype_code(q), _stream(stream))
@@ -225,16 +261,24 @@ def attn_bwd(q, k, v, o, lse, dout, *, causal: bool = True, scale=None, dq=None,
     return dq, dk, dv
 
 
+def _decode_shapes(q, k_cache, v_cache, seq_lens, out):
+    """Check the contiguous-cache decode arguments; returns (B, Hq, Hkv, max_S, D)."""
+    dev = _cuda16(q, "q")
+    B, Hq, D = q.shape
+    Hkv, max_S = k_cache.shape[1], k_cache.shape[2]
+    _expect(q, "q", (B, Hq, D), q.dtype, dev)
+    _expect(k_cache, "k_cache", (B, Hkv, max_S, D), q.dtype, dev)
+    _expect(v_cache, "v_cache", (B, Hkv, max_S, D), q.dtype, dev)
+    _expect(seq_lens, "seq_lens", (B,), torch.int32, dev)
+    if out is not None:
+        _expect(out, "out", (B, Hq, D), q.dtype, dev)
+    return B, Hq, Hkv, max_S, D
+
+
 def attn_decode(q, k_cache, v_cache, seq_lens, *, num_splits: int = 0, out=None, stream=None):
     """Flash-decoding: q [B,Hq,D], caches [B,Hkv,max_S,D], seq_lens [B] int32 (all CUDA)."""
     lib = load()
-    B, Hq, D = q.shape
-    Hkv, max_S = k_cache.shape[1], k_cache.shape[2]
-    for t in (q, k_cache, v_cache, seq_lens):
-        if not t.is_contiguous():
-            raise ValueError("decode inputs must be contiguous")
-    if seq_lens.dtype != torch.int32:
-        raise TypeError("seq_lens must be int32")
+    B, Hq, Hkv, max_S, D = _decode_shapes(q, k_cache, v_cache, seq_lens, out)
     if out is None:
         out = torch.empty_like(q)
     st = lib.attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), _ptr(out), B, Hq,
@@ -249,13 +293,7 @@ def attn_decode_fused(q, k_cache, v_cache, seq_lens, *, num_splits: int = 0, out
     head group) merges the group's chunk partials.  Calls that may overlap on the
     GPU share the library's merge counters: order them on one stream."""
     lib = load()
-    B, Hq, D = q.shape
-    Hkv, max_S = k_cache.shape[1], k_cache.shape[2]
-    for t in (q, k_cache, v_cache, seq_lens):
-        if not t.is_contiguous():
-            raise ValueError("decode inputs must be contiguous")
-    if seq_lens.dtype != torch.int32:
-        raise TypeError("seq_lens must be int32")
+    B, Hq, Hkv, max_S, D = _decode_shapes(q, k_cache, v_cache, seq_lens, out)
     if out is None:
         out = torch.empty_like(q)
     st = lib.attn_decode_fused(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), _ptr(out),
@@ -269,16 +307,20 @@ def attn_decode_paged(q, k_pages, v_pages, block_table, seq_lens, *, num_splits:
     """Flash-decoding over a paged cache: q [B,Hq,D], pages [num_pages,Hkv,page_size,D],
     block_table [B,max_pages] int32, seq_lens [B] int32 (all CUDA)."""
     lib = load()
+    dev = _cuda16(q, "q")
     B, Hq, D = q.shape
     num_pages, Hkv, page_size = k_pages.shape[0], k_pages.shape[1], k_pages.shape[2]
+    if block_table.dim() != 2:
+        raise ValueError("block_table must be [B, max_pages]")
     max_pages = block_table.shape[1]
-    for t in (q, k_pages, v_pages, block_table, seq_lens):
-        if not t.is_contiguous():
-            raise ValueError("decode inputs must be contiguous")
-    if seq_lens.dtype != torch.int32 or block_table.dtype != torch.int32:
-        raise TypeError("seq_lens and block_table must be int32")
+    _expect(q, "q", (B, Hq, D), q.dtype, dev)
+    _expect(k_pages, "k_pages", (num_pages, Hkv, page_size, D), q.dtype, dev)
+    _expect(v_pages, "v_pages", (num_pages, Hkv, page_size, D), q.dtype, dev)
+    _expect(block_table, "block_table", (B, max_pages), torch.int32, dev)
+    _expect(seq_lens, "seq_lens", (B,), torch.int32, dev)
     if out is None:
         out = torch.empty_like(q)
+    _expect(out, "out", (B, Hq, D), q.dtype, dev)
     st = lib.attn_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
                                _ptr(seq_lens), _ptr(out), B, Hq, Hkv, num_pages, page_size,
                                max_pages, D, num_splits, _dtype_code(q), _stream(stream))
@@ -298,12 +340,9 @@ def attn_decode_noalloc(q, k_cache, v_cache, seq_lens, *, num_splits: int = 0, o
     the scratch and race: order them on one stream.
     """
     lib = load()
-    B, Hq, D = q.shape
-    Hkv, max_S = k_cache.shape[1], k_cache.shape[2]
     if out is None:
         raise ValueError("attn_decode_noalloc needs a preallocated `out`")
-    if seq_lens.dtype != torch.int32:
-        raise TypeError("seq_lens must be int32")
+    B, Hq, Hkv, max_S, D = _decode_shapes(q, k_cache, v_cache, seq_lens, out)
     st = lib.attn_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), _ptr(out),
                                  B, Hq, Hkv, max_S, D, num_splits, _dtype_code(q), _stream(stream))
     _check(st, "attn_decode_noalloc")
