@@ -3,7 +3,12 @@
 ``attn_fwd`` (prefill, causal or not, grouped-query heads, per-row LSE) and
 ``attn_decode`` (flash-decoding: split-KV chunk partials merged by an
 LSE-rescaling reduce) run in hand-written CUDA kernels behind the C ABI of
-``include/attn.h``; this package is the thin PyTorch-facing binding.
+``include/attn.h``; this package is the thin PyTorch-facing binding.  Beside
+them: ``attn_fwd_varlen`` (packed sequences of different lengths, sliding
+windows), ``attn_fwd_qkvpacked`` (a [B, S, 3, H, D] projection read in place),
+``attn_bwd`` (dQ, dK, dV), ``attn_decode_paged`` (a paged KV cache),
+``attn_decode_fused`` (flash-decoding in one launch) and
+``attn_decode_noalloc`` (no allocation during the call).
 """
 
 from .binding import (  # noqa: F401
