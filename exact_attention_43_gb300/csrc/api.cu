@@ -318,6 +318,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   a.scale = scale;
   a.bf16 = dtype == ATTN_BF16;
   a.wait_limit_ns = g_wait_limit_ns;
+  a.debug_fault = g_fault;
   a.num_sms = g_num_sms[dev] > 0 ? g_num_sms[dev] : 1;
   const size_t rows = (size_t)B * Hq * Sq;
   if (Skv == 0) {
@@ -414,6 +415,7 @@ static int decode_contiguous_args(const void* q, const void* k_cache, const void
   a->scale = 1.0f / sqrtf((float)D);
   a->bf16 = dtype == ATTN_BF16;
   a->wait_limit_ns = g_wait_limit_ns;
+  a->debug_fault = g_fault;
   return ATTN_OK;
 }
 
@@ -488,6 +490,7 @@ int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
   a.scale = 1.0f / sqrtf((float)D);
   a.bf16 = dtype == ATTN_BF16;
   a.wait_limit_ns = g_wait_limit_ns;
+  a.debug_fault = g_fault;
   a.num_sms = g_num_sms[dev] > 0 ? g_num_sms[dev] : 1;
   a.block_table = max_S > 0 ? block_table : nullptr;
   a.page_size = page_size;
@@ -529,7 +532,7 @@ int attn_check_device_status(cudaStream_t stream) {
 }
 
 int attn_debug_set(int fault, unsigned wait_limit_us) {
-  if (fault < 0 || fault > 1) return ATTN_ERR_INVALID_ARG;
+  if (fault < 0 || fault > 3) return ATTN_ERR_INVALID_ARG;
   g_fault = fault;
   g_wait_limit_ns = wait_limit_us ? (uint64_t)wait_limit_us * 1000ull : kDefaultWaitNs;
   return ATTN_OK;

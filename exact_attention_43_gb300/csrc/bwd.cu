@@ -57,6 +57,7 @@ struct Params {
   float c2;     // scale * log2(e)
   float scale;
   uint64_t wait_limit_ns;
+  int debug_fault;  // 3: CTA (0, 0, 0) withholds the Q/dO loads of its iteration 1
 };
 
 template <int D>
@@ -215,8 +216,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       constexpr uint32_t idesc_kv = umma_idesc_f16(BF16, BN, D, false, true);
       constexpr uint32_t idesc_dq = umma_idesc_f16(BF16, BM, D, true, true);
       const uint32_t t_s = tmem, t_dp = tmem + 128, t_dv = tmem + 256, t_dk = tmem + 256 + D;
+      // bounded-wait test: one CTA never issues iteration 1's loads, so the waits run out
+      const int withheld =
+          (p.debug_fault == 3 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) ? 1 : -1;
       // Q, dO of iteration i go to buffer i & 1
       auto load_qd = [&](int i) {
+        if (i == withheld) return;
         const int h = hk * p.group + i / per_head, m = m_lo + i % per_head;
         const uint32_t fb = bar(L::QD_FULL + (i & 1));
         mbar_expect_tx(fb, 2 * L::TILE);
@@ -287,7 +292,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       // more commit, on a barrier of its own, tracks them all, also after an abort)
       drain_wait(bar(L::KV_FULL), 0, lim);
       for (int i = max(0, n_qd - 2); i < n_qd; ++i)
-        drain_wait(bar(L::QD_FULL + (i & 1)), (i >> 1) & 1, lim);
+        if (i != withheld) drain_wait(bar(L::QD_FULL + (i & 1)), (i >> 1) & 1, lim);
       umma_commit(bar(L::DRAIN));
       drain_wait(bar(L::DRAIN), 0, lim);
     }
@@ -469,6 +474,7 @@ static cudaError_t launch_t(const BwdArgs& a, cudaStream_t stream) {
     p.scale = a.scale;
     p.c2 = a.scale * 1.4426950408889634f;
     p.wait_limit_ns = a.wait_limit_ns;
+    p.debug_fault = a.debug_fault;
     // the longest CTA (key tile 0) against an SM's share of all (query head, Q tile)
     // iterations: above a fifth, start the long CTAs first
     const long long n_kt = (a.Skv + BN - 1) / BN, n_mt = (a.Sq + BM - 1) / BM;

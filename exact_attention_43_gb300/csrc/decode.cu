@@ -57,6 +57,7 @@ struct Params {
   int page_size, max_pages, num_pages;
   // single-launch decode: one zeroed counter per (sequence, head group) CTA row
   unsigned* tickets;
+  int debug_fault;  // 2: CTA (0, 0, 0) withholds load 1 (its first V sub-tile)
 };
 
 __device__ __forceinline__ int clamp_len(const Params& p, int b) {
@@ -176,11 +177,14 @@ __global__ void __launch_bounds__(THREADS) decode_split_kernel(const Params p) {
   // ---------------------- load stream (thread 0; all of warp 0 for the paged cache)
   int l_c = c0, l_off = 0, l_nload = 2 * ((chunk_rows(c0) + SUB - 1) / SUB), issued = 0;
   uint64_t pol = 0;
+  // bounded-wait test: one CTA never issues its load 1, so the waits on it run out
+  const int withheld = (p.debug_fault == 2 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) ? 1 : -1;
   auto issue_next = [&]() {  // the next K or V sub-tile of this CTA's chunks
     if (l_c >= c1) return;
     const int sub = l_off >> 1;
     const int rows = min(SUB, chunk_rows(l_c) - sub * SUB);
-    if constexpr (!PAGED) {
+    if (issued == withheld) {
+    } else if constexpr (!PAGED) {
       const size_t r = row0 + (size_t)l_c * p.chunk + (size_t)sub * SUB;
       const uint16_t* src = ((l_off & 1) ? p.v : p.k) + r * D;
       const uint32_t bar = ring_bar(issued);
@@ -462,7 +466,7 @@ __global__ void __launch_bounds__(THREADS) decode_split_kernel(const Params p) {
     // unwind: wait (bounded) for the copies still in flight, then leave
     const uint64_t t0 = global_timer_ns();
     for (int i = max(gl, issued - NST); i < issued; ++i)
-      while (!mbar_try_wait(ring_bar(i), (i / NST) & 1))
+      while (i != withheld && !mbar_try_wait(ring_bar(i), (i / NST) & 1))
         if (global_timer_ns() - t0 > p.wait_limit_ns) break;
   }
 
@@ -695,6 +699,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.max_pages = a.max_pages;
   p.num_pages = a.num_pages;
   p.tickets = a.tickets;
+  p.debug_fault = a.debug_fault;
   if (a.D == 64) return a.bf16 ? dec::launch_d<64, true>(a, p, stream) : dec::launch_d<64, false>(a, p, stream);
   return a.bf16 ? dec::launch_d<128, true>(a, p, stream) : dec::launch_d<128, false>(a, p, stream);
 }

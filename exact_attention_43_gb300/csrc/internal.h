@@ -52,6 +52,7 @@ struct DecodeArgs {
   float scale;
   int bf16;
   uint64_t wait_limit_ns;
+  int debug_fault;  // 2: split-kernel CTA (0, 0, 0) withholds its first V sub-tile (test only)
 };
 
 // Arguments of one backward call (attn_bwd), already validated.
@@ -73,6 +74,7 @@ struct BwdArgs {
   int bf16;
   uint64_t wait_limit_ns;
   int num_sms;  // multiprocessors of the device (CTA ordering)
+  int debug_fault;  // 3: CTA (0, 0, 0) withholds its second Q/dO tile pair (test only)
 };
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,

@@ -267,9 +267,13 @@ int attn_decode_chunk(int max_S, int num_splits);
 int attn_check_device_status(cudaStream_t stream);
 
 /* Test hooks for the bounded waits.  wait_limit_us sets how long any wait
- * may run before the kernel gives up (0 restores the default of 2 s);
- * fault = 1 makes the next attn_fwd launches withhold their first V tile so
- * that their waits run out.  Returns ATTN_OK or ATTN_ERR_INVALID_ARG. */
+ * may run before the kernel gives up (0 restores the default of 2 s).  A
+ * fault value makes later launches withhold one copy so that the waits on it
+ * run out: 1, attn_fwd withholds its first V tile; 2, the decode split kernel
+ * (attn_decode, attn_decode_fused, attn_decode_paged, attn_decode_noalloc)
+ * withholds the first V sub-tile of its CTA (0, 0, 0); 3, attn_bwd withholds
+ * the second Q/dO tile pair of its CTA (0, 0, 0).  0 turns the fault off.
+ * Returns ATTN_OK or ATTN_ERR_INVALID_ARG. */
 int attn_debug_set(int fault, unsigned wait_limit_us);
 
 /* Static description of a status code. */

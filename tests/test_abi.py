@@ -205,8 +205,11 @@ def test_decode_chunking_and_workspace(lib):
 
 
 def test_debug_hook_validation(lib):
-    assert lib.attn_debug_set(5, 0) == 1
-    assert lib.attn_debug_set(0, 0) == 0
+    # faults 1-3 withhold a copy in the prefill, decode and backward kernels
+    for bad in (-1, 4, 5):
+        assert lib.attn_debug_set(bad, 0) == 1
+    for good in (1, 2, 3, 0):
+        assert lib.attn_debug_set(good, 0) == 0
 
 
 def test_binding_fails_loudly_without_the_library(tmp_path):
