@@ -67,10 +67,13 @@ constexpr int NQ = 2;               // Q tiles per CTA
 constexpr int BN = 128;             // keys per KV tile
 constexpr int NS = 4;               // K/V ring stages
 constexpr int NITEM = 4;            // claimed work items queued from the loader to the others
-constexpr int NUM_THREADS = 384;    // warpgroups 0, 1: softmax; warp 8 loader, warps 9, 10 MMA
-                                    // (warp 11 only lends its registers to the softmax)
-constexpr int LOADER_WARP = 8;
-constexpr int MMA_WARP = 9;         // warp 9 + i issues the MMAs of Q tile i
+constexpr int NQS = 3;              // Q ring: single-tile slots
+constexpr int NUM_THREADS = 512;    // warpgroups 0, 1: softmax; warpgroup 2: epilogue; warp 12
+                                    // K/V loader, warps 13, 14 MMA, warp 15 work items and Q
+constexpr int EPI_WARP = 8;         // first warp of the epilogue warpgroup
+constexpr int KV_WARP = 12;
+constexpr int MMA_WARP = 13;        // warp 13 + i issues the MMAs of Q tile i
+constexpr int QLOAD_WARP = 15;
 constexpr float RESCALE_LOG2 = 8.0f;  // rescale O when the max grows by more than 2^8
 constexpr uint32_t TMEM_COLS = 512;
 // TMEM columns: S_i at 128 i (P_i overwrites its first 64 columns), O_i at 256 + 128 i
@@ -96,6 +99,7 @@ struct Params {
   int total_q, total_k;
   int win_left, win_right;  // sliding-window bounds (-1: none); causal is win_right = 0
   int o_rstride;            // elements between consecutive tokens of O
+  int o_align32;            // O is 32-byte aligned (so is every row): 32-byte stores
 };
 
 // Query and key rows of one sequence in the token-major layouts.
@@ -124,25 +128,31 @@ __device__ __forceinline__ Seq seq_of(const Params& p, int b) {
   return s;
 }
 
+// A claimed work item as queued in shared memory: its index (-1: no more work),
+// its KV steps n_kv (both Q tiles step through all of them), the steps [a, e) that
+// Q tile i multiplies, and the tensor-map coordinates of its Q tile 0 and K/V tile 0.
+struct ItemEntry {
+  int w, n_kv, a[2], e[2], q_y, q_z, k_y0, kv_z;
+};
+
 template <int D>
 struct Layout {
   static constexpr int REGION = 128 * 128;    // 128 rows x 128 bytes (64 columns), swizzled
   static constexpr int NREG = D / 64;
   static constexpr int TILE = NREG * REGION;  // a 128 x D 16-bit tile
-  static constexpr int Q_OFF = 0;             // Q_0, Q_1
-  static constexpr int RING_OFF = Q_OFF + NQ * TILE;
-  static constexpr int STAGE_OFF = RING_OFF + NS * TILE;  // O staging: one region per Q tile
-  static constexpr int BAR_OFF = STAGE_OFF + NQ * REGION;
+  static constexpr int Q_OFF = 0;             // Q ring: NQS single-tile slots
+  static constexpr int RING_OFF = Q_OFF + NQS * TILE;
+  static constexpr int INVL_OFF = RING_OFF + NS * TILE;  // 1 / l of each row, per Q tile
+  static constexpr int BAR_OFF = INVL_OFF + NQ * BM * 4;
   enum {
-    Q_FULL, Q_EMPTY, RING_FULL, RING_EMPTY = RING_FULL + NS, S_FULL = RING_EMPTY + NS,
-    P_FULL = S_FULL + NQ, O_DONE = P_FULL + NQ, O_FREE = O_DONE + NQ,
+    Q_FULL, Q_EMPTY = Q_FULL + NQS, RING_FULL = Q_EMPTY + NQS, RING_EMPTY = RING_FULL + NS,
+    S_FULL = RING_EMPTY + NS, P_FULL = S_FULL + NQ, O_DONE = P_FULL + NQ, O_FREE = O_DONE + NQ,
     ITEM_FULL = O_FREE + NQ, ITEM_EMPTY = ITEM_FULL + NITEM, TOK = ITEM_EMPTY + NITEM,
-    DRAIN = TOK + NQ,
-    STAGE_FREE = DRAIN + NQ, STAGE_FULL = STAGE_FREE + NQ, NUM_BARS = STAGE_FULL + NQ
+    DRAIN = TOK + NQ, INVL_FULL = DRAIN + NQ, INVL_EMPTY = INVL_FULL + NQ, NUM_BARS = INVL_EMPTY + NQ
   };
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;  // [0] TMEM base, [1] abort flag
-  static constexpr int ITEM_OFF = MISC_OFF + 16;           // NITEM claimed work items
-  static constexpr int BYTES = ITEM_OFF + NITEM * 4;
+  static constexpr int ITEM_OFF = MISC_OFF + 16;           // NITEM claimed work items (ItemEntry)
+  static constexpr int BYTES = ITEM_OFF + NITEM * (int)sizeof(ItemEntry);
   static constexpr int ALLOC = BYTES + 1024;  // slack to align the base to 1024 bytes
   static_assert(BAR_OFF % 8 == 0, "mbarriers need 8-byte alignment");
   static_assert(TILE % 1024 == 0 && RING_OFF % 1024 == 0,
@@ -268,8 +278,7 @@ __device__ __forceinline__ void decode_item(const Params& p, int w, int* mb, int
 template <int D, bool BF16, bool VL>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                    const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
-                    const Params p) {
+                    const __grid_constant__ CUtensorMap tmv, const Params p) {
   using L = Layout<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
@@ -282,8 +291,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int n_items = p.num_m_blocks * p.Hq * p.B;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(L::Q_FULL), 1);
-    mbar_init(bar(L::Q_EMPTY), NQ);  // one arrival per issuer
+    for (int s = 0; s < NQS; ++s) {
+      mbar_init(bar(L::Q_FULL + s), 1);
+      mbar_init(bar(L::Q_EMPTY + s), 1);  // the issuer of the tile in the slot
+    }
     for (int s = 0; s < NS; ++s) {
       mbar_init(bar(L::RING_FULL + s), 1);
       mbar_init(bar(L::RING_EMPTY + s), NQ);  // freed by both softmax warpgroups (see there)
@@ -293,28 +304,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(bar(L::P_FULL + i), BM);
       mbar_init(bar(L::O_DONE + i), 1);
       mbar_init(bar(L::O_FREE + i), BM);
+      mbar_init(bar(L::TOK + i), 1);  // issuer i finished issuing a batch
+      mbar_init(bar(L::DRAIN + i), 1);
+      mbar_init(bar(L::INVL_FULL + i), BM);   // written by softmax warpgroup i
+      mbar_init(bar(L::INVL_EMPTY + i), BM);  // read by the epilogue warpgroup
     }
     for (int q = 0; q < NITEM; ++q) {
       mbar_init(bar(L::ITEM_FULL + q), 1);
-      mbar_init(bar(L::ITEM_EMPTY + q), NQ + NQ * 4);  // the MMA issuers and the softmax warps
-    }
-    for (int i = 0; i < NQ; ++i) {
-      mbar_init(bar(L::TOK + i), 1);  // issuer i finished issuing a batch
-      mbar_init(bar(L::DRAIN + i), 1);
-    }
-    for (int i = 0; i < NQ; ++i) {
-      mbar_init(bar(L::STAGE_FREE + i), 1);   // the warpgroup's store thread
-      mbar_init(bar(L::STAGE_FULL + i), BM);  // every thread of the warpgroup
+      // the K/V loader, the MMA issuers, the softmax warps and the epilogue warps
+      mbar_init(bar(L::ITEM_EMPTY + q), 1 + NQ + NQ * 4 + 4);
     }
     *abort_flag = 0;
     fence_barrier_init();
   }
-  volatile int* item_q = reinterpret_cast<volatile int*>(smem + L::ITEM_OFF);
-  if (warp == LOADER_WARP && lane == 0) {
+  volatile ItemEntry* item_q = reinterpret_cast<volatile ItemEntry*>(smem + L::ITEM_OFF);
+  if (warp == QLOAD_WARP && lane == 0) {
     prefetch_tmap(&tmq);
     prefetch_tmap(&tmk);
     prefetch_tmap(&tmv);
-    prefetch_tmap(&tmo);
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(misc), TMEM_COLS);
@@ -326,59 +333,98 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem = misc[0];
   const uint64_t lim = p.wait_limit_ns;
 
-  if (warp >= NQ * 4) {
-    // register split: 128 threads x 88 + 256 threads x 208 = 384 threads x 168, the
-    // launch allotment (ptxas allocates each region within its new limit)
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 88;" ::: "memory");
-    if (warp == LOADER_WARP) {
-      // -------------------------------------------------------------- TMA loader
+  // Everything the loaders and issuers need about work item w, computed once by the
+  // thread that claims it.
+  auto fill_entry = [&](int w, volatile ItemEntry* q) {
+    int mb, hq, b;
+    decode_item(p, w, &mb, &hq, &b);
+    const int m_base = mb * (NQ * BM);
+    q->w = w;
+    if constexpr (VL) {
+      const Seq sq = seq_of(p, b);
+      const ItemTiles t0 = item_tiles(p, sq, m_base, 0), t1 = item_tiles(p, sq, m_base, 1);
+      q->n_kv = t0.n_kv;
+      q->a[0] = t0.a;
+      q->e[0] = t0.e;
+      q->a[1] = t1.a;
+      q->e[1] = t1.e;
+      q->q_y = sq.q0 + m_base;
+      q->q_z = hq;
+      q->k_y0 = sq.k0 + t0.t0 * BN;
+      q->kv_z = hq / p.group;
+    } else {
+      int n_t[NQ], mf[NQ];
+      for (int i = 0; i < NQ; ++i) tile_range(p, m_base + i * BM, &n_t[i], &mf[i]);
+      q->n_kv = max(n_t[0], n_t[1]);
+      q->a[0] = 0;
+      q->e[0] = n_t[0];
+      q->a[1] = 0;
+      q->e[1] = n_t[1];
+      q->q_y = m_base;
+      q->q_z = b * p.Hq + hq;
+      q->k_y0 = 0;
+      q->kv_z = b * p.Hkv + hq / p.group;
+    }
+  };
+
+  // register split: 128 threads x 72 (loaders, issuers) + 128 x 56 (epilogue) + 256 x 192
+  // (softmax) = 512 threads x 128, the launch allotment (ptxas allocates each region
+  // within its new limit)
+  if (warp >= KV_WARP) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;" ::: "memory");
+    if (warp == QLOAD_WARP) {
+      // ------------------------------------------ work items and Q tiles (one thread)
+      // Claims work items from the counter and queues them for every other role,
+      // then loads the item's two Q tiles into a ring of three single-tile slots;
+      // a slot is free once the last S MMA of its previous tile has completed, so
+      // the next item's first Q tile is usually resident long before it is needed.
       if (lane == 0) {
         const uint64_t pol_q = policy_evict_first();
-        const uint64_t pol_kv = policy_evict_last();
-        int ld = 0, k_item = 0;
+        int qt = 0;  // Q tiles loaded
         bool ok = true;
         for (int r = 0; ok; ++r) {
-          // claim the next work item and queue it for the MMA and softmax warps
           const int qs = r % NITEM;
           if (!(ok = mbar_wait(bar(L::ITEM_EMPTY + qs), ((r / NITEM) & 1) ^ 1, abort_flag,
                                &g_status, lim)))
             break;
           int w = atomicAdd(p.work_counter, 1);
           if (w >= n_items) w = -1;
-          item_q[qs] = w;
+          volatile ItemEntry* q = item_q + qs;
+          if (w >= 0) fill_entry(w, q);
+          else q->w = -1;
+          const int n_kv = w >= 0 ? q->n_kv : 0, q_y = q->q_y, q_z = q->q_z;
           mbar_arrive(bar(L::ITEM_FULL + qs));
           if (w < 0) break;
-          int mb, hq, b;
-          decode_item(p, w, &mb, &hq, &b);
-          const int m_base = mb * (NQ * BM);
-          int n_kv, q_y, q_z, k_y0, kv_z;  // tensor-map coordinates of Q and of K/V tile 0
-          if constexpr (VL) {
-            const Seq sq = seq_of(p, b);
-            const ItemTiles it = item_tiles(p, sq, m_base, 0);
-            n_kv = it.n_kv;
-            q_y = sq.q0 + m_base;
-            q_z = hq;
-            k_y0 = sq.k0 + it.t0 * BN;
-            kv_z = hq / p.group;
-          } else {
-            int n_t[NQ], mf[NQ];
-            for (int i = 0; i < NQ; ++i) tile_range(p, m_base + i * BM, &n_t[i], &mf[i]);
-            n_kv = max(n_t[0], n_t[1]);
-            q_y = m_base;
-            q_z = b * p.Hq + hq;
-            k_y0 = 0;
-            kv_z = b * p.Hkv + hq / p.group;
-          }
           if (n_kv == 0) continue;
-          // Q of this item may overwrite Q of the last one once its S MMAs are done
-          if (!(ok = mbar_wait(bar(L::Q_EMPTY), (k_item & 1) ^ 1, abort_flag, &g_status, lim)))
-            break;
-          mbar_expect_tx(bar(L::Q_FULL), NQ * L::TILE);
-          for (int i = 0; i < NQ; ++i)
+          for (int i = 0; i < NQ && ok; ++i, ++qt) {
+            const int s = qt % NQS;
+            if (!(ok = mbar_wait(bar(L::Q_EMPTY + s), ((qt / NQS) & 1) ^ 1, abort_flag, &g_status, lim)))
+              break;
+            mbar_expect_tx(bar(L::Q_FULL + s), L::TILE);
             for (int rr = 0; rr < L::NREG; ++rr)
-              tma_load_3d(sb + L::Q_OFF + i * L::TILE + rr * L::REGION, &tmq, bar(L::Q_FULL),
+              tma_load_3d(sb + L::Q_OFF + s * L::TILE + rr * L::REGION, &tmq, bar(L::Q_FULL + s),
                           rr * 64, q_y + i * BM, q_z, pol_q);
-          ++k_item;
+          }
+        }
+        // every copy issued must have landed before the CTA may exit
+        for (int t = max(0, qt - NQS); t < qt; ++t)
+          drain_wait(bar(L::Q_FULL + t % NQS), (t / NQS) & 1, lim);
+      }
+      __syncwarp();
+    } else if (warp == KV_WARP) {
+      // ---------------------------------------------------- K/V loader (one thread)
+      if (lane == 0) {
+        const uint64_t pol_kv = policy_evict_last();
+        int ld = 0;
+        bool ok = true;
+        for (int r = 0; ok; ++r) {
+          const int qs = r % NITEM;
+          if (!(ok = mbar_wait(bar(L::ITEM_FULL + qs), (r / NITEM) & 1, abort_flag, &g_status, lim)))
+            break;
+          const int w = item_q[qs].w;
+          const int n_kv = item_q[qs].n_kv, k_y0 = item_q[qs].k_y0, kv_z = item_q[qs].kv_z;
+          mbar_arrive(bar(L::ITEM_EMPTY + qs));
+          if (w < 0) break;
           for (int l = 0; l < 2 * n_kv; ++l, ++ld) {  // K_0, V_0, K_1, V_1, ...
             const int s = ld % NS;
             if (!(ok = mbar_wait(bar(L::RING_EMPTY + s), ((ld / NS) & 1) ^ 1, abort_flag, &g_status,
@@ -392,8 +438,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                           bar(L::RING_FULL + s), rr * 64, k_y0 + (l >> 1) * BN, kv_z, pol_kv);
           }
         }
-        // every copy issued must have landed before the CTA may exit
-        if (k_item > 0) drain_wait(bar(L::Q_FULL), (k_item - 1) & 1, lim);
         for (int l = max(0, ld - NS); l < ld; ++l) {
           if (p.debug_fault == 1 && l == 1) continue;
           drain_wait(bar(L::RING_FULL + l % NS), (l / NS) & 1, lim);
@@ -404,35 +448,54 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // ------------------------------------------------ MMA issuers, one per Q tile
       const int qi = warp - MMA_WARP;
       if (lane == 0) {
+        const uint32_t abort_s = smem_u32(misc + 1);
         constexpr uint32_t idesc_qk = umma_idesc_f16(BF16, BM, BN, false, false);
         constexpr uint32_t idesc_pv = umma_idesc_f16(BF16, BM, D, false, true);
         auto ring_wait = [&](int ld) -> bool {
-          return mbar_wait(bar(L::RING_FULL + ld % NS), (ld / NS) & 1, abort_flag, &g_status, lim);
+          return mbar_wait_s(bar(L::RING_FULL + ld % NS), (ld / NS) & 1, abort_s, &g_status, lim);
         };
-        // Shared-memory descriptors are built once; every MMA then only adds a
-        // compile-time offset to the 14-bit start-address field (addresses stay
-        // below 256 KB, so the addition never carries out of the field).
-        const uint64_t q_desc = sdesc_sw128(sb + L::Q_OFF + qi * L::TILE, 16, 1024);
-        const uint64_t k_desc = sdesc_sw128(sb + L::RING_OFF, 16, 1024);
-        const uint64_t v_desc = sdesc_sw128(sb + L::RING_OFF, L::REGION, 1024);
+        // Shared-memory descriptors are built once; every MMA then only adds an
+        // offset to the 14-bit start-address field (addresses stay below 256 KB,
+        // so the addition never carries out of the field).
+        // 128-byte-swizzle descriptors: the high half is one constant (stride 1024
+        // bytes); the low half holds the start address and the leading byte offset
+        // (16 bytes for the K-major Q and K, one 64-column region for the MN-major V)
+        const uint32_t d_hi = (uint32_t)(sdesc_sw128(sb, 16, 1024) >> 32);
+        const uint32_t q_lo = (uint32_t)sdesc_sw128(sb + L::Q_OFF, 16, 1024);
+        const uint32_t k_lo = (uint32_t)sdesc_sw128(sb + L::RING_OFF, 16, 1024);
+        const uint32_t v_lo = (uint32_t)sdesc_sw128(sb + L::RING_OFF, L::REGION, 1024);
         const uint32_t t_s = tmem + COL_S + 128u * qi, t_o = tmem + COL_O + 128u * qi;
-        auto issue_s = [&](int ld) {  // S = Q K^T, K in the ring slot of load ld
-          const uint64_t b0 = k_desc + (uint64_t)(((ld % NS) * L::TILE) >> 4);
+        // S = Q K^T with Q in slot qs and K in the ring slot of load ld (the start
+        // addresses stay below 256 KB, so the additions never leave their field)
+        auto issue_s = [&](int qs, int ld) {
+          const uint32_t a0 = q_lo + (uint32_t)((qs * L::TILE) >> 4);
+          const uint32_t b0 = k_lo + (uint32_t)(((ld % NS) * L::TILE) >> 4);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             // K-major operands: 16 columns = 32 bytes inside a 128-byte swizzled row
             const uint32_t off = ((kk >> 2) * L::REGION + (kk & 3) * 32) >> 4;
-            umma_ss(t_s, q_desc + off, b0 + off, idesc_qk, kk > 0 ? 1u : 0u);
+            umma_ss_lo(t_s, a0 + off, d_hi, b0 + off, d_hi, idesc_qk, kk > 0 ? 1u : 0u);
           }
           umma_commit(bar(L::S_FULL + qi));
         };
         auto issue_pv = [&](int ld, bool acc) {  // O += P V, V in the ring slot of ld
           // V is [key][d] (d contiguous): MN-major B, 16 keys = 2 swizzle atoms of 8 rows;
           // LBO steps to the next 64-column block of d, SBO to the next 8 keys.
-          const uint64_t b0 = v_desc + (uint64_t)(((ld % NS) * L::TILE) >> 4);
-          umma_ts(t_o, t_s, b0, idesc_pv, acc ? 1u : 0u);
+          const uint32_t b0 = v_lo + (uint32_t)(((ld % NS) * L::TILE) >> 4);
+          umma_ts_lo(t_o, t_s, b0, d_hi, idesc_pv, acc ? 1u : 0u);
 #pragma unroll
-          for (int kk = 1; kk < BN / 16; ++kk) umma_ts(t_o, t_s + kk * 8, b0 + kk * 128, idesc_pv, 1u);
+          for (int kk = 1; kk < BN / 16; ++kk) umma_ts_lo(t_o, t_s + kk * 8, b0 + kk * 128, d_hi, idesc_pv, 1u);
+        };
+        struct Steps {
+          int n_kv, a, e;  // the item's KV steps; this tile multiplies steps [a, e)
+        };
+        // An item's first batch: S(0), or only the commit of an empty step when this
+        // tile multiplies nothing there; the Q slot is released after the tile's last S.
+        auto first_s = [&](const Steps& it, int qs, int ld) {
+          if (it.a <= 0 && 0 < it.e) issue_s(qs, ld);
+          else umma_commit(bar(L::S_FULL + qi));
+          if (it.e == it.a) mbar_arrive(bar(L::Q_EMPTY + qs));
+          else if (it.e == 1) umma_commit(bar(L::Q_EMPTY + qs));  // this tile's last S
         };
         // The two issuers hand a token back and forth, so their batches reach the
         // tensor core in the order P_0 V(j), S_0(j+1), P_1 V(j), S_1(j+1): S_0 then
@@ -442,95 +505,194 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // between two batches, and the tensor core queues just a couple of MMAs.
         // Both Q tiles step through every KV tile of an item: the shorter one's
         // extra steps are empty batches (a commit, no MMA) that keep the two in
-        // step and release ring slots in order.
+        // step and release ring slots in order.  The batches run on across items:
+        // an item's last batch, P V(n_kv - 1) (or nothing, for the causal
+        // diagonal's shorter tile), carries the next item's S(0), so that S runs
+        // while the other tile finishes the item.  Both issuers therefore issue
+        // 1 + sum(n_kv) batches, and the token alternates to the end.
         int g = 0;  // batches issued
         auto token_wait = [&]() -> bool {
-          if (qi == 0) return g == 0 || mbar_wait(bar(L::TOK + 1), (g - 1) & 1, abort_flag, &g_status, lim);
-          return mbar_wait(bar(L::TOK + 0), g & 1, abort_flag, &g_status, lim);
+          if (qi == 0) return g == 0 || mbar_wait_s(bar(L::TOK + 1), (g - 1) & 1, abort_s, &g_status, lim);
+          return mbar_wait_s(bar(L::TOK + 0), g & 1, abort_s, &g_status, lim);
         };
         auto token_pass = [&]() {
           tc_fence_before();
           mbar_arrive(bar(L::TOK + qi));
           ++g;
         };
-        int ld = 0, k_item = 0, t_cnt = 0, n_items = 0;
-        bool ok = true;
-        for (int r = 0; ok; ++r) {
-          const int qs = r % NITEM;
-          if (!(ok = mbar_wait(bar(L::ITEM_FULL + qs), (r / NITEM) & 1, abort_flag, &g_status, lim)))
-            break;
-          const int w = item_q[qs];
-          mbar_arrive(bar(L::ITEM_EMPTY + qs));
-          if (w < 0) break;
-          int mb, hq, b;
-          decode_item(p, w, &mb, &hq, &b);
-          const int m_base = mb * (NQ * BM);
-          // this Q tile multiplies KV steps [a_own, e_own) of the item's n_kv
-          int n_kv, a_own, e_own;
-          if constexpr (VL) {
-            const ItemTiles it = item_tiles(p, seq_of(p, b), m_base, qi);
-            n_kv = it.n_kv;
-            a_own = it.a;
-            e_own = it.e;
-          } else {
-            int n_t[NQ], mf[NQ];
-            for (int i = 0; i < NQ; ++i) tile_range(p, m_base + i * BM, &n_t[i], &mf[i]);
-            n_kv = max(n_t[0], n_t[1]);
-            a_own = 0;
-            e_own = n_t[qi];
+        int r = 0;  // items taken from the queue
+        // the next queued item with keys (or w < 0: none left); false if a wait gave up
+        auto next_item = [&](int* w, Steps* it) -> bool {
+          for (;;) {
+            const int qs = r % NITEM;
+            if (!mbar_wait_s(bar(L::ITEM_FULL + qs), (r / NITEM) & 1, abort_s, &g_status, lim))
+              return false;
+            *w = item_q[qs].w;
+            it->n_kv = item_q[qs].n_kv;
+            it->a = item_q[qs].a[qi];
+            it->e = item_q[qs].e[qi];
+            mbar_arrive(bar(L::ITEM_EMPTY + qs));
+            ++r;
+            if (*w < 0 || it->n_kv > 0) return true;
           }
-          if (n_kv == 0) continue;
-          const int base = ld;
-          ld = base + 2 * n_kv;
-          // ---- first batch of the item: S(0)
-          if (!(ok = mbar_wait(bar(L::Q_FULL), k_item & 1, abort_flag, &g_status, lim))) break;
-          ++k_item;
-          if (!(ok = ring_wait(base))) break;
-          if (!(ok = token_wait())) break;
-          tc_fence_after();
-          // P of the last item lives in these columns, read by an MMA issued earlier
-          if (a_own <= 0 && 0 < e_own) issue_s(base);
-          else umma_commit(bar(L::S_FULL + qi));  // nothing to multiply for this tile
-          if (e_own == a_own) mbar_arrive(bar(L::Q_EMPTY));
-          else if (e_own == 1) umma_commit(bar(L::Q_EMPTY));  // this tile's last S
-          token_pass();
-          // ---- one batch per KV tile j: P V(j), then S(j+1)
-          for (int j = 0; j < n_kv && ok; ++j) {
+        };
+        // Q tile qi of the k-th item with keys sits in slot (2 k + qi) mod NQS
+        auto q_wait = [&](int k) -> bool {
+          const int t = 2 * k + qi;
+          return mbar_wait_s(bar(L::Q_FULL + t % NQS), (t / NQS) & 1, abort_s, &g_status, lim);
+        };
+        int t_cnt = 0, n_done = 0;
+        int w;
+        Steps cur;
+        bool ok = next_item(&w, &cur);
+        // ---- the first batch of all: S(0) of the first item
+        if (ok && w >= 0) {
+          ok = q_wait(0) && ring_wait(0) && token_wait();
+          if (ok) {
+            tc_fence_after();
+            first_s(cur, qi % NQS, 0);
+            token_pass();
+          }
+        }
+        for (int k = 0, base = 0; ok && w >= 0; ++k) {
+          const int qs = (2 * k + qi) % NQS;
+          const int ld_next = base + 2 * cur.n_kv;  // K_0 of the next item
+          int w_next = -1;
+          Steps nxt{};
+          // ---- one batch per KV tile j < n_kv - 1: P V(j), then S(j+1)
+          for (int j = 0; j + 1 < cur.n_kv; ++j) {
             const int ld_v = base + 2 * j + 1, ld_k = base + 2 * j + 2;
-            if (!(ok = ring_wait(ld_v))) break;
-            if (j + 1 < n_kv && !(ok = ring_wait(ld_k))) break;
-            if (!(ok = mbar_wait(bar(L::P_FULL + qi), t_cnt & 1, abort_flag, &g_status, lim))) break;
+            const bool has_pv = cur.a <= j && j < cur.e;
+            if (!(ok = ring_wait(ld_v) && ring_wait(ld_k))) break;
+            if (!(ok = mbar_wait_s(bar(L::P_FULL + qi), t_cnt & 1, abort_s, &g_status, lim))) break;
             ++t_cnt;
             // the first P V of an item overwrites O: the last epilogue must have read it
-            if (j == a_own && e_own > a_own && n_items > 0 &&
-                !(ok = mbar_wait(bar(L::O_FREE + qi), (n_items - 1) & 1, abort_flag, &g_status, lim)))
+            if (j == cur.a && has_pv && n_done > 0 &&
+                !(ok = mbar_wait_s(bar(L::O_FREE + qi), (n_done - 1) & 1, abort_s, &g_status, lim)))
               break;
             if (!(ok = token_wait())) break;
             tc_fence_after();
-            if (a_own <= j && j < e_own) issue_pv(ld_v, j > a_own);
-            if (j == n_kv - 1) {
-              umma_commit(bar(L::O_DONE + qi));
-              ++n_items;
-            }
-            if (j + 1 < n_kv) {
-              if (a_own <= j + 1 && j + 1 < e_own) {
-                issue_s(ld_k);  // after P V(j), which read P from these columns
-                if (j + 1 == e_own - 1) umma_commit(bar(L::Q_EMPTY));  // this tile's last S
-              } else {
-                umma_commit(bar(L::S_FULL + qi));  // an empty step for this tile
-              }
+            if (has_pv) issue_pv(ld_v, j > cur.a);
+            if (cur.a <= j + 1 && j + 1 < cur.e) {
+              issue_s(qs, ld_k);  // after P V(j), which read P from these columns
+              if (j + 1 == cur.e - 1) umma_commit(bar(L::Q_EMPTY + qs));  // this tile's last S
+            } else {
+              umma_commit(bar(L::S_FULL + qi));  // an empty step for this tile
             }
             token_pass();
           }
+          if (!ok) break;
+          // ---- the item's last batch: P V(n_kv - 1) (if this tile has it), then the
+          // next item's S(0)
+          {
+            const int j = cur.n_kv - 1, ld_v = base + 2 * j + 1;
+            const bool has_pv = cur.a <= j && j < cur.e;
+            if (!(ok = ring_wait(ld_v))) break;
+            if (!(ok = mbar_wait_s(bar(L::P_FULL + qi), t_cnt & 1, abort_s, &g_status, lim))) break;
+            ++t_cnt;
+            if (j == cur.a && has_pv && n_done > 0 &&
+                !(ok = mbar_wait_s(bar(L::O_FREE + qi), (n_done - 1) & 1, abort_s, &g_status, lim)))
+              break;
+            if (!(ok = next_item(&w_next, &nxt))) break;
+            if (w_next >= 0 && !(ok = q_wait(k + 1) && ring_wait(ld_next))) break;
+            if (!(ok = token_wait())) break;
+            tc_fence_after();
+            if (has_pv) issue_pv(ld_v, j > cur.a);
+            umma_commit(bar(L::O_DONE + qi));
+            ++n_done;
+            // after P V(j), which read P from these columns
+            if (w_next >= 0) first_s(nxt, (2 * (k + 1) + qi) % NQS, ld_next);
+            token_pass();
+          }
+          base = ld_next;
+          w = w_next;
+          cur = nxt;
         }
         umma_commit(bar(L::DRAIN + qi));  // fires once every MMA issued above has completed
         drain_wait(bar(L::DRAIN + qi), 0, lim);
       }
       __syncwarp();
     }
+  } else if (warp >= EPI_WARP) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
+    // ------------------------------------------------ epilogue (rows of both Q tiles)
+    // Thread r owns TMEM lane r, i.e. row r of either Q tile.  Once O_i of an item
+    // is complete it reads the row 32 columns at a time, hands O_i back to its
+    // issuer (O_FREE) as soon as the last piece is in registers, multiplies by the
+    // 1 / l the softmax warpgroup left in shared memory, rounds, and stores the
+    // row (rows past the queries are not written).  Nothing here is on the
+    // softmax warps' path.
+    const int r_lane = threadIdx.x & 127;
+    const uint32_t lane_t = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const float* inv_l_s = reinterpret_cast<const float*>(smem + L::INVL_OFF);
+    auto wait_warp = [&](uint32_t b_, uint32_t ph_) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(b_, ph_, abort_flag, &g_status, lim));
+    };
+    int u_cnt = 0;
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+      const int qs = r % NITEM;
+      if (!(ok = wait_warp(bar(L::ITEM_FULL + qs), (r / NITEM) & 1))) break;
+      const int w = item_q[qs].w, n_kv = item_q[qs].n_kv;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::ITEM_EMPTY + qs));
+      if (w < 0) break;
+      if (n_kv == 0) continue;  // no key for the item: the softmax wrote its rows
+      int mb, hq, b;
+      decode_item(p, w, &mb, &hq, &b);
+      const int m_base = mb * (NQ * BM);
+      int n_rows = p.Sq;  // query rows of the sequence
+      uint16_t* o_base = static_cast<uint16_t*>(p.o) + ((size_t)(b * p.Hq + hq) * p.Sq) * D;
+      size_t o_stride = D;
+      if constexpr (VL) {
+        const Seq sq = seq_of(p, b);
+        n_rows = sq.nq;
+        o_base = static_cast<uint16_t*>(p.o) + (size_t)sq.q0 * p.o_rstride + (size_t)hq * D;
+        o_stride = (size_t)p.o_rstride;
+      }
+      for (int qi = 0; qi < NQ; ++qi) {
+        const int row = m_base + qi * BM + r_lane;
+        if (!(ok = wait_warp(bar(L::INVL_FULL + qi), u_cnt & 1))) break;
+        const float inv_l = inv_l_s[qi * BM + r_lane];  // 0: no visible key, O = 0
+        mbar_arrive(bar(L::INVL_EMPTY + qi));
+        if (!(ok = wait_warp(bar(L::O_DONE + qi), u_cnt & 1))) break;
+        tc_fence_after();
+        const uint32_t t_o = lane_t + COL_O + 128u * qi;
+        uint16_t* dst = o_base + (size_t)row * o_stride;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(t_o + 32u * c, v);
+          if (c == D / 32 - 1) {  // the whole row is in registers: O_i may be overwritten
+            tc_fence_before();
+            mbar_arrive(bar(L::O_FREE + qi));
+          }
+          if (row < n_rows) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint32_t pk[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                pk[i] = inv_l > 0.f ? pack2<BF16>(__uint_as_float(v[16 * h + 2 * i]) * inv_l,
+                                                  __uint_as_float(v[16 * h + 2 * i + 1]) * inv_l)
+                                    : 0u;
+              uint16_t* d16 = dst + 32 * c + 16 * h;
+              if (p.o_align32) {
+                st_global_v8(d16, pk);  // whole 32-byte sectors in one store
+              } else {
+                reinterpret_cast<uint4*>(d16)[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                reinterpret_cast<uint4*>(d16)[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+              }
+            }
+          }
+        }
+      }
+      ++u_cnt;
+    }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 208;" ::: "memory");
-    // ------------------------------------------------ softmax + epilogue (rows)
+
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
+    // ------------------------------------------------ softmax (rows)
     const int qi = warp >> 2;             // Q tile of this warpgroup
     const int r_lane = threadIdx.x & 127; // TMEM lane == tile row
     const uint32_t lane_t = tmem + ((uint32_t)((warp & 3) * 32) << 16);
@@ -543,12 +705,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto wait_warp = [&](uint32_t b_, uint32_t ph_) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(b_, ph_, abort_flag, &g_status, lim));
     };
-    int t_cnt = 0, u_cnt = 0, k_stage = 0;
+    float* inv_l_s = reinterpret_cast<float*>(smem + L::INVL_OFF);
+    int t_cnt = 0, u_cnt = 0;
     bool ok = true;
     for (int r = 0; ok; ++r) {
       const int qs = r % NITEM;
       if (!(ok = wait_warp(bar(L::ITEM_FULL + qs), (r / NITEM) & 1))) break;
-      const int w = item_q[qs];
+      const int w = item_q[qs].w;
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::ITEM_EMPTY + qs));
       if (w < 0) break;
@@ -615,8 +778,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         float x[BN];
         {
+          static_assert(BN == 128, "one S row is two 64-column TMEM loads");
           uint32_t rr[BN];
-          tmem_ld(t_s, rr);  // the whole S row in one TMEM round trip
+          tmem_ld64x2(t_s, rr);  // the whole S row in one TMEM round trip
 #pragma unroll
           for (int i = 0; i < BN; ++i) x[i] = __uint_as_float(rr[i]);
         }
@@ -686,18 +850,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (o_scale) alpha_o = alpha;
           m_used = m_new;
         }
-        if (__any_sync(0xffffffffu, o_scale)) {
-          // S_i(t) completed, so every earlier MMA did: O_i holds P V up to tile t-1
-          // (rare; in 32-column pieces because the S row is still live in registers)
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t rr[32];
-            tmem_ld32(t_o + 32u * c, rr);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha_o);
-            tmem_st32(t_o + 32u * c, rr);
-          }
-        }
         const float mu = (m_used == -INFINITY) ? 0.f : m_used;
         const uint64_t c2p = f2_pack(c2, c2), nmu = f2_pack(-mu, -mu);
         uint64_t ls = f2_pack(0.f, 0.f);
@@ -719,77 +871,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           f2_unpack(ls, s0, s1);
           l_sum += s0 + s1;
         }
+        if (__any_sync(0xffffffffu, o_scale)) {
+          // S_i(t) completed, so every earlier MMA did: O_i holds P V up to tile t-1,
+          // and P V(t) waits for this warpgroup's P (rare; 32 columns at a time)
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t rr[32];
+            tmem_ld32(t_o + 32u * c, rr);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha_o);
+            tmem_st32(t_o + 32u * c, rr);
+          }
+        }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(L::P_FULL + qi));
       }
       if (!ok) break;
-      if (!(ok = wait_warp(bar(L::O_DONE + qi), u_cnt & 1))) break;
+      // 1 / l of this row for the epilogue warpgroup, once it has taken the last item's
+      // (a row with no visible key, or no P V at all, gets 0: O = 0)
+      if (!(ok = wait_warp(bar(L::INVL_EMPTY + qi), (u_cnt & 1) ^ 1))) break;
+      inv_l_s[qi * BM + r_lane] = l_sum > 0.f ? 1.f / l_sum : 0.f;
+      mbar_arrive(bar(L::INVL_FULL + qi));
       ++u_cnt;
-      tc_fence_after();
-      // read the whole O row, hand the accumulator back to the MMA warp, then store
-      uint32_t orow[D];
-      tmem_ld(t_o, orow);
-      tc_fence_before();
-      mbar_arrive(bar(L::O_FREE + qi));
-      const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
-      if (!(l_sum > 0.f)) {
-        // no visible key (or no P V at all for this tile): O = 0, not stale TMEM times 0
-#pragma unroll
-        for (int i = 0; i < D; ++i) orow[i] = 0u;
-      }
-      // O / l goes out through this warpgroup's staging region (128 rows x 64
-      // columns, the 128-byte swizzle of the tensor map: 16-byte chunk c of row r
-      // at chunk c ^ (r mod 8), so a warp's stores hit every bank once) and one
-      // TMA store per 64 columns; rows past Sq fall outside the tensor map and
-      // are not written.
-      const uint32_t stage = sb + L::STAGE_OFF + qi * L::REGION;
-      bool direct = false;
-      if constexpr (VL) direct = m0 + BM > sq.nq;  // rows past the sequence belong to the next one
-      if (direct) {
-        // a sequence's last, partial Q tile: each thread stores its own row
-        if (row < sq.nq) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
-                                                (size_t)(sq.q0 + row) * p.o_rstride + (size_t)hq * D);
-#pragma unroll
-          for (int c = 0; c < D / 8; ++c) {
-            const int col = 8 * c;
-            dst[c] = make_uint4(
-                pack2<BF16>(__uint_as_float(orow[col + 0]) * inv_l, __uint_as_float(orow[col + 1]) * inv_l),
-                pack2<BF16>(__uint_as_float(orow[col + 2]) * inv_l, __uint_as_float(orow[col + 3]) * inv_l),
-                pack2<BF16>(__uint_as_float(orow[col + 4]) * inv_l, __uint_as_float(orow[col + 5]) * inv_l),
-                pack2<BF16>(__uint_as_float(orow[col + 6]) * inv_l, __uint_as_float(orow[col + 7]) * inv_l));
-          }
-        }
-      } else {
-#pragma unroll
-        for (int h = 0; h < D / 64; ++h, ++k_stage) {
-          if (r_lane == 0) {
-            bulk_wait_read_all();  // the last store has read the region
-            mbar_arrive(bar(L::STAGE_FREE + qi));
-          }
-          if (!(ok = wait_warp(bar(L::STAGE_FREE + qi), k_stage & 1))) break;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const int col = 64 * h + 8 * c;
-            const uint4 v = make_uint4(
-                pack2<BF16>(__uint_as_float(orow[col + 0]) * inv_l, __uint_as_float(orow[col + 1]) * inv_l),
-                pack2<BF16>(__uint_as_float(orow[col + 2]) * inv_l, __uint_as_float(orow[col + 3]) * inv_l),
-                pack2<BF16>(__uint_as_float(orow[col + 4]) * inv_l, __uint_as_float(orow[col + 5]) * inv_l),
-                pack2<BF16>(__uint_as_float(orow[col + 6]) * inv_l, __uint_as_float(orow[col + 7]) * inv_l));
-            st_shared_v4(stage + r_lane * 128 + ((c ^ (r_lane & 7)) << 4), v);
-          }
-          fence_proxy_async_smem();
-          mbar_arrive(bar(L::STAGE_FULL + qi));
-          if (r_lane == 0) {
-            if (!(ok = mbar_wait(bar(L::STAGE_FULL + qi), k_stage & 1, abort_flag, &g_status, lim))) break;
-            if constexpr (VL) tma_store_3d(&tmo, stage, 64 * h, sq.q0 + m0, hq);
-            else tma_store_3d(&tmo, stage, 64 * h, m0, bh);
-            bulk_commit();
-          }
-        }
-      }
-      if (!ok) break;
       if constexpr (VL) {
         if (p.lse && row < sq.nq)
           p.lse[(size_t)hq * p.total_q + sq.q0 + row] =
@@ -799,7 +903,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             l_sum > 0.f ? (m_used + log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
       }
     }
-    if (r_lane == 0) bulk_wait_all();  // this warpgroup's O stores are complete
   }
 
   tc_fence_before();
@@ -843,7 +946,7 @@ static cudaError_t launch_t(const FwdArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, BF16, VL>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
-  CUtensorMap tq, tk, tv, to;
+  CUtensorMap tq, tk, tv;
   if (VL) {
     // [tokens, heads, D] with the given token strides; with no keys at all the K/V
     // maps cover one (never read) row of q, since a map cannot be empty
@@ -852,12 +955,10 @@ static cudaError_t launch_t(const FwdArgs& a, cudaStream_t stream) {
     const void* vb = a.total_k > 0 ? a.v : a.q;
     const long long kst = a.total_k > 0 ? a.k_rstride : a.q_rstride;
     if (!make_map(&tq, a.q, D, a.total_q, a.Hq, a.q_rstride, D, BF16) ||
-        !make_map(&to, a.o, D, a.total_q, a.Hq, a.o_rstride, D, BF16) ||
         !make_map(&tk, kb, D, tk_rows, a.total_k > 0 ? a.Hkv : 1, kst, D, BF16) ||
         !make_map(&tv, vb, D, tk_rows, a.total_k > 0 ? a.Hkv : 1, kst, D, BF16))
       return cudaErrorInvalidValue;
   } else if (!make_map(&tq, a.q, D, a.Sq, (long long)a.B * a.Hq, D, (long long)a.Sq * D, BF16) ||
-             !make_map(&to, a.o, D, a.Sq, (long long)a.B * a.Hq, D, (long long)a.Sq * D, BF16) ||
              !make_map(&tk, a.k, D, a.Skv, (long long)a.B * a.Hkv, D, (long long)a.Skv * D, BF16) ||
              !make_map(&tv, a.v, D, a.Skv, (long long)a.B * a.Hkv, D, (long long)a.Skv * D, BF16)) {
     return cudaErrorInvalidValue;
@@ -887,6 +988,8 @@ static cudaError_t launch_t(const FwdArgs& a, cudaStream_t stream) {
   p.win_left = a.win_left;
   p.win_right = a.causal ? 0 : a.win_right;
   p.o_rstride = (int)a.o_rstride;
+  // rows are multiples of 128 bytes apart in every layout, so the base decides
+  p.o_align32 = (reinterpret_cast<uintptr_t>(a.o) % 32) == 0 ? 1 : 0;
   // scheduling groups: as many (batch, head) rows as keep about 64 MB of K and V
   // in L2, rounded to whole GQA groups
   const double kv_head_bytes = 4.0 * (double)(a.Skv > 0 ? a.Skv : 1) * D;  // K and V of one KV head
@@ -898,7 +1001,7 @@ static cudaError_t launch_t(const FwdArgs& a, cudaStream_t stream) {
   // persistent: one CTA per SM (or one per work item when there are fewer)
   const long long n_items = (long long)p.num_m_blocks * a.Hq * a.B;
   const int grid = (int)(n_items < a.num_sms ? n_items : a.num_sms);
-  attn_fwd_kernel<D, BF16, VL><<<grid, NUM_THREADS, L::ALLOC, stream>>>(tq, tk, tv, to, p);
+  attn_fwd_kernel<D, BF16, VL><<<grid, NUM_THREADS, L::ALLOC, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 

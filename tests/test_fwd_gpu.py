@@ -158,3 +158,22 @@ def test_gqa_workload_full_size():
 def test_long_workload_full_size():
     # 512 seeded-random query rows per head plus rows 0 and S-1, full-length keys
     _full_size(wl.LONG, 512, seed=wl.SEED_BASE + 3)
+
+
+def test_output_only_16_byte_aligned():
+    # the C ABI promises 16-byte alignment only: an O that is not 32-byte aligned takes
+    # 16-byte stores (the check is on the host, per call)
+    import exact_attention_43_gb300 as ea
+
+    q, k, v = wl.fwd_inputs(1, 2, 2, 300, 300, 128, dtype=torch.bfloat16, seed=31)
+    shape = tuple(q.shape)
+    n = int(np.prod(shape))
+    buf = torch.full((n + 8,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    o = buf[8:].view(shape)
+    assert o.data_ptr() % 32 == 16
+    ea.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True, scale=128 ** -0.5, out=o)
+    torch.cuda.synchronize()
+    assert ea.check_device_status() == 0
+    assert bool(torch.isnan(buf[:8].float()).all())
+    ro, _ = oracle.sdpa(q, k, v, causal=True, scale=128 ** -0.5)
+    compare_o(o, ro, "16-byte aligned O")
