@@ -384,7 +384,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bool ok = true;
         for (int r = 0; ok; ++r) {
           const int qs = r % NITEM;
-          if (!(ok = mbar_wait(bar(L::ITEM_EMPTY + qs), ((r / NITEM) & 1) ^ 1, abort_flag,
+          if (!(ok = mbar_wait<false>(bar(L::ITEM_EMPTY + qs), ((r / NITEM) & 1) ^ 1, abort_flag,
                                &g_status, lim)))
             break;
           int w = atomicAdd(p.work_counter, 1);
@@ -398,7 +398,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (n_kv == 0) continue;
           for (int i = 0; i < NQ && ok; ++i, ++qt) {
             const int s = qt % NQS;
-            if (!(ok = mbar_wait(bar(L::Q_EMPTY + s), ((qt / NQS) & 1) ^ 1, abort_flag, &g_status, lim)))
+            if (!(ok = mbar_wait<false>(bar(L::Q_EMPTY + s), ((qt / NQS) & 1) ^ 1, abort_flag, &g_status, lim)))
               break;
             mbar_expect_tx(bar(L::Q_FULL + s), L::TILE);
             for (int rr = 0; rr < L::NREG; ++rr)
@@ -419,7 +419,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bool ok = true;
         for (int r = 0; ok; ++r) {
           const int qs = r % NITEM;
-          if (!(ok = mbar_wait(bar(L::ITEM_FULL + qs), (r / NITEM) & 1, abort_flag, &g_status, lim)))
+          if (!(ok = mbar_wait<false>(bar(L::ITEM_FULL + qs), (r / NITEM) & 1, abort_flag, &g_status, lim)))
             break;
           const int w = item_q[qs].w;
           const int n_kv = item_q[qs].n_kv, k_y0 = item_q[qs].k_y0, kv_z = item_q[qs].kv_z;
@@ -427,7 +427,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (w < 0) break;
           for (int l = 0; l < 2 * n_kv; ++l, ++ld) {  // K_0, V_0, K_1, V_1, ...
             const int s = ld % NS;
-            if (!(ok = mbar_wait(bar(L::RING_EMPTY + s), ((ld / NS) & 1) ^ 1, abort_flag, &g_status,
+            if (!(ok = mbar_wait<false>(bar(L::RING_EMPTY + s), ((ld / NS) & 1) ^ 1, abort_flag, &g_status,
                                  lim)))
               break;
             if (p.debug_fault == 1 && ld == 1) continue;  // withhold V_0: consumers must time out
@@ -626,7 +626,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t lane_t = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const float* inv_l_s = reinterpret_cast<const float*>(smem + L::INVL_OFF);
     auto wait_warp = [&](uint32_t b_, uint32_t ph_) -> bool {
-      return __all_sync(0xffffffffu, mbar_wait(b_, ph_, abort_flag, &g_status, lim));
+      return __all_sync(0xffffffffu, mbar_wait<false>(b_, ph_, abort_flag, &g_status, lim));
     };
     int u_cnt = 0;
     bool ok = true;
@@ -703,7 +703,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // tcgen05.ld/st are warp-collective: every wait outcome and every rescale
     // decision below is made uniform across the warp before TMEM is touched.
     auto wait_warp = [&](uint32_t b_, uint32_t ph_) -> bool {
-      return __all_sync(0xffffffffu, mbar_wait(b_, ph_, abort_flag, &g_status, lim));
+      return __all_sync(0xffffffffu, mbar_wait<false>(b_, ph_, abort_flag, &g_status, lim));
     };
     float* inv_l_s = reinterpret_cast<float*>(smem + L::INVL_OFF);
     int t_cnt = 0, u_cnt = 0;

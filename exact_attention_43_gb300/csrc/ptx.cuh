@@ -78,12 +78,17 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 // Wait for the phase of `bar` with the given parity to complete.  Gives up
 // after `limit_ns` (or as soon as another thread of the CTA raised `abort`),
 // recording a timeout in `status`.  Returns true when the phase completed.
+// SLEEP: the repeated tests may suspend the thread (up to 20 us, woken when the
+// phase completes), which frees issue slots for the warps that compute; without
+// it each test returns after the hardware's own short time limit, which reacts
+// sooner to a completion (the prefill kernel's hand-offs are latency-bound).
+template <bool SLEEP = true>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                           unsigned* status, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t n = 1;; ++n) {
-    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (SLEEP ? mbar_try_wait_sleep(bar, parity, 20000u) : mbar_try_wait(bar, parity)) return true;
     if ((n & 15u) == 0) {
       if (*abort) return false;
       if (global_timer_ns() - t0 > limit_ns) {
@@ -95,14 +100,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
-// The same wait with the abort flag given by its 32-bit shared-memory address,
-// for threads short of registers (a generic pointer takes two).
+// The same wait (without the suspend hint) with the abort flag given by its 32-bit
+// shared-memory address, for threads short of registers (a generic pointer takes two).
 __device__ __forceinline__ bool mbar_wait_s(uint32_t bar, uint32_t parity, uint32_t abort_smem,
                                             unsigned* status, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t n = 1;; ++n) {
-    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if ((n & 15u) == 0) {
       uint32_t a;
       asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(a) : "r"(abort_smem) : "memory");
