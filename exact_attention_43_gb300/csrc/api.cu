@@ -275,7 +275,7 @@ int attn_fwd_qkvpacked(const void* qkv, void* o, float* lse, int B, int S, int H
 size_t attn_bwd_workspace_bytes(int B, int Hq, int Sq, int D) {
   if (B < 0 || Hq < 0 || Sq < 0 || D <= 0) return 0;
   const size_t rows = (size_t)B * Hq * Sq;
-  return rows * sizeof(float) * (D + 1) + 256;  // dQ accumulator, row terms, alignment
+  return rows * sizeof(float) + 256;  // row terms, alignment
 }
 
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -332,13 +332,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
     if ((st = pool_for(dev, &pool)) != ATTN_OK) return st;
     cudaError_t e = cudaMallocFromPoolAsync(&ws, attn_bwd_workspace_bytes(B, Hq, Sq, D), pool, stream);
     if (e != cudaSuccess) return from_cuda(e);
-    a.dq_acc = static_cast<float*>(ws);
-    a.delta = a.dq_acc + rows * D;
-    e = cudaMemsetAsync(a.dq_acc, 0, rows * D * sizeof(float), stream);
-    if (e != cudaSuccess) {
-      cudaFreeAsync(ws, stream);
-      return from_cuda(e);
-    }
+    a.delta = static_cast<float*>(ws);
   }
   cudaError_t e = ea::launch_bwd(a, stream);
   if (ws) {

@@ -9,24 +9,27 @@
 // sum_j P dP because O = P V.  A K/V head shared by several query heads (GQA)
 // receives the sum of their gradients.
 //
-// GB300 design:
+// GB300 design, three kernels and no atomics (every gradient is reproducible bit
+// for bit):
 //  * a prep kernel forms the row term delta_i = sum_d dO_id O_id;
-//  * the main kernel keeps one 128-key tile of one KV head per CTA: K and V stay
+//  * the dK/dV kernel keeps one 128-key tile of one KV head per CTA: K and V stay
 //    in shared memory, and dK, dV accumulate in TMEM over every query head of the
 //    GQA group and every Q tile that sees the keys (causal tiles that see none are
-//    skipped), so K/V gradients need no atomics;
-//  * per Q tile one thread issues the tcgen05 MMAs: S^T = K Q^T and
-//    dP^T = V dO^T into TMEM; eight compute warps (two threads per key row, each
-//    with 64 of the tile's 128 queries; TMEM lane = key) form P^T = 2^(S^T c - LSE_2) and dS^T = P^T (dP^T - delta), write
-//    both to TMEM as 16-bit (over the columns they came from) and dS^T also to a
-//    128-byte-swizzled shared-memory tile; then dV += P^T dO and dK += dS^T Q (A
-//    from TMEM) and dQ_part = dS K (A: the dS^T tile read M-major) over dP^T's
-//    columns; the compute warps add scale * dQ_part (TMEM lane = query row) into
-//    an fp32 accumulator with 16-byte vector atomics;
-//  * Q and dO are double-buffered (the next Q tile's loads run during this one's
-//    MMAs) and the next S^T is issued before the compute warps have read this
-//    dQ_part, so the tensor core has work queued while they add it;
-//  * a last kernel rounds the dQ accumulator to the input type.
+//    skipped).  Per Q tile one thread issues S^T = K Q^T and dP^T = V dO^T into two
+//    TMEM regions, then dV += P^T dO and dK += dS^T Q with A read from TMEM.  Eight
+//    compute warps (two threads per key row, 64 queries each; TMEM lane = key)
+//    work in two phases, P^T = 2^(S^T c - LSE_2) and then dS^T = P^T (dP^T - delta),
+//    each written back over the columns it came from as 16-bit; the MMAs are
+//    ordered dV(i), S^T(i+1), dK(i), dP^T(i+1), so each phase runs while the
+//    tensor core works on two products of the tile before or after it;
+//  * the dQ kernel keeps one 128-row Q tile (and its dO) per CTA and streams the
+//    K/V tiles it sees through a 4-stage ring, like the forward: S = Q K^T (two
+//    TMEM buffers, so the next S is computed while this one is used), dP = dO V^T,
+//    dS = P (dP - delta) written over S as 16-bit, dQ += dS K accumulated in TMEM
+//    and stored once.  Recomputing S and dP costs two more products per (Q tile,
+//    KV tile) than one kernel that adds dQ into memory from the dK/dV kernel, but
+//    the eight compute warps then overlap the tensor core instead of waiting on
+//    it, and dQ needs no fp32 atomics.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -37,46 +40,71 @@ namespace bwd {
 
 __device__ unsigned g_status;
 
-constexpr int BM = 128;  // queries per Q tile
-constexpr int BN = 128;  // keys per K/V tile (= TMEM lanes)
-constexpr int THREADS = 288;  // warps 0-7 compute, warp 8 loads and issues
-constexpr int ISSUER_WARP = 8;
-constexpr int NCOMP = 256;    // compute threads: warps w and w + 4 share TMEM lanes 32 (w mod 4) ...
+constexpr int BM = 128;        // queries per Q tile
+constexpr int BN = 128;        // keys per K/V tile (= TMEM lanes in the dK/dV kernel)
+constexpr int THREADS = 320;   // warps 0-7 compute, warp 8 loads, warp 9 issues the MMAs
+constexpr int LOAD_WARP = 8;
+constexpr int MMA_WARP = 9;
+constexpr int NCOMP = 256;     // compute threads: warps w and w + 4 share TMEM lanes 32 (w mod 4) ...
+constexpr int NS = 4;          // dQ kernel: K/V ring stages
 constexpr uint32_t TMEM_COLS = 512;
-// TMEM columns: S^T at 0 (P^T over its first 64), dP^T at 128 (dS^T over its first
-// 64; dQ_part over its first D once dK has read dS^T), dV at 256, dK at 256 + D
 
 struct Params {
   const float* lse;    // [B, Hq, Sq], natural log
   const float* delta;  // [B, Hq, Sq]
-  float* dq_acc;       // [B, Hq, Sq, D], zero at launch
+  uint16_t* dq;        // [B, Hq, Sq, D]
   uint16_t* dk;        // [B, Hkv, Skv, D]
   uint16_t* dv;
   int B, Hq, Hkv, Sq, Skv, group, causal;
-  int kv_slowest;  // 1: grid (KV head, batch, key tile), 0: (key tile, KV head, batch)
-  float c2;     // scale * log2(e)
+  int kv_slowest;  // dK/dV kernel: 1: grid (KV head, batch, key tile), 0: (key tile, KV head, batch)
+  float c2;        // scale * log2(e)
   float scale;
   uint64_t wait_limit_ns;
-  int debug_fault;  // 3: CTA (0, 0, 0) withholds the Q/dO loads of its iteration 1
+  int debug_fault;  // 3: dK/dV CTA (0, 0, 0) withholds the Q/dO loads of its iteration 1
 };
 
+// dK/dV kernel shared memory: K, V, two Q and two dO buffers, the row vectors.
 template <int D>
-struct Layout {
+struct KVLayout {
   static constexpr int REGION = 128 * 128;  // 128 rows x 64 16-bit columns, 128-byte swizzle
   static constexpr int NREG = D / 64;
   static constexpr int TILE = NREG * REGION;  // 128 x D
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = TILE;
-  static constexpr int Q_OFF = 2 * TILE;                // two buffers
-  static constexpr int DO_OFF = 4 * TILE;               // two buffers
-  static constexpr int DS_OFF = 6 * TILE;               // dS^T: 128 keys x 128 queries
-  static constexpr int VEC_OFF = DS_OFF + 2 * REGION;   // LSE (log2 units), delta of the Q tile
-  static constexpr int BAR_OFF = VEC_OFF + 2 * BM * 4;
-  enum { KV_FULL, QD_FULL, S_FULL = QD_FULL + 2, P_FULL, DQ_FULL, DQ_FREE, VEC_READY, DRAIN, NUM_BARS };
+  static constexpr int Q_OFF = 2 * TILE;    // two buffers
+  static constexpr int DO_OFF = 4 * TILE;   // two buffers
+  static constexpr int VEC_OFF = 6 * TILE;  // [2 buffers][LSE_2, delta][BM] of the Q tile
+  static constexpr int BAR_OFF = VEC_OFF + 2 * 2 * BM * 4;
+  enum {
+    KV_FULL, Q_FULL, DO_FULL = Q_FULL + 2, Q_FREE = DO_FULL + 2, DO_FREE = Q_FREE + 2,
+    S_READY = DO_FREE + 2, DP_READY, P_READY, DS_READY, VEC_READY, DONE, DRAIN, NUM_BARS
+  };
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;  // [0] TMEM base, [1] abort flag
   static constexpr int BYTES = MISC_OFF + 16;
   static constexpr int ALLOC = BYTES + 1024;  // slack to align the base to 1024 bytes
-  static_assert(TILE % 1024 == 0 && DS_OFF % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+  static_assert(TILE % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+  static_assert(BAR_OFF % 8 == 0, "mbarriers need 8-byte alignment");
+  static_assert(ALLOC <= 227 * 1024, "shared memory per CTA");
+};
+
+// dQ kernel shared memory: the Q tile, its dO tile and a ring of K/V tiles.
+template <int D>
+struct QLayout {
+  static constexpr int REGION = 128 * 128;
+  static constexpr int NREG = D / 64;
+  static constexpr int TILE = NREG * REGION;
+  static constexpr int Q_OFF = 0;
+  static constexpr int DO_OFF = TILE;
+  static constexpr int RING_OFF = 2 * TILE;
+  static constexpr int BAR_OFF = RING_OFF + NS * TILE;
+  enum {
+    QD_FULL, RING_FULL, RING_EMPTY = RING_FULL + NS, S_READY = RING_EMPTY + NS, DP_READY,
+    DP_FREE, DS_READY, DONE, DRAIN, NUM_BARS
+  };
+  static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
+  static constexpr int BYTES = MISC_OFF + 16;
+  static constexpr int ALLOC = BYTES + 1024;
+  static_assert(TILE % 1024 == 0, "swizzled tiles need 1024-byte alignment");
   static_assert(BAR_OFF % 8 == 0, "mbarriers need 8-byte alignment");
   static_assert(ALLOC <= 227 * 1024, "shared memory per CTA");
 };
@@ -124,24 +152,41 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const uint16_t* o, const
   if (lane == 0) delta[row] = s;
 }
 
-// dq = dq_acc rounded to the input type, eight elements per thread.
-template <bool BF16>
-__global__ void bwd_dq_convert_kernel(const float* acc, uint16_t* dq, long long n8) {
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8;
-       i += (long long)gridDim.x * blockDim.x) {
-    const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
-    const float4 c = reinterpret_cast<const float4*>(acc)[2 * i + 1];
-    reinterpret_cast<uint4*>(dq)[i] = make_uint4(pack2<BF16>(a.x, a.y), pack2<BF16>(a.z, a.w),
-                                                 pack2<BF16>(c.x, c.y), pack2<BF16>(c.z, c.w));
+// S-like product D[tmem] = A B^T over the head dimension, both operands K-major
+// 128 x D tiles in shared memory (16 columns = 32 bytes of a 128-byte swizzled row).
+template <int D, bool BF16>
+__device__ __forceinline__ void mma_kmajor(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc) {
+  constexpr uint32_t idesc = umma_idesc_f16(BF16, 128, 128, false, false);
+  constexpr int REGION = 128 * 128;
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = ((kk >> 2) * REGION + (kk & 3) * 32) >> 4;
+    umma_ss(d_tmem, a_desc + off, b_desc + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
+// D[tmem] (+)= A B over 128 K-rows: A is 128 x 128 16-bit in TMEM (two values per
+// column), B a 128 x D tile in shared memory read MN-major (16 rows = two swizzle
+// atoms of 8 rows per MMA; LBO steps to the next 64 columns, SBO to the next 8 rows).
+// The two compute threads of a TMEM lane each write their 64 values inside the 64
+// columns they read (K-rows 0-63 at columns 0-31, K-rows 64-127 at 64-95), so
+// neither overwrites columns the other may still be loading.
+template <int D, bool BF16>
+__device__ __forceinline__ void mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, bool acc) {
+  constexpr uint32_t idesc = umma_idesc_f16(BF16, 128, D, false, true);
+#pragma unroll
+  for (int kk = 0; kk < 128 / 16; ++kk)
+    umma_ts(d_tmem, a_tmem + kk * 8 + (kk >= 4 ? 32 : 0), b_desc + kk * 128, idesc,
+            (acc || kk > 0) ? 1u : 0u);
+}
+
+// ============================================================================ dK, dV
 template <int D, bool BF16>
 __global__ void __launch_bounds__(THREADS, 1)
-    attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
                     const Params p) {
-  using L = Layout<D>;
+  using L = KVLayout<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
@@ -152,10 +197,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t lim = p.wait_limit_ns;
 
-  // Key tiles vary fastest: CTAs that run at the same time share a few heads, whose
-  // fp32 dQ rows then stay in L2 for their atomics, and within a head the causal
-  // tiles that most Q tiles see start first.  When one CTA's work is a large share
-  // of an SM's, key tiles vary slowest instead, so those long CTAs start first.
+  // Key tiles vary fastest: CTAs that run at the same time share a few heads (their
+  // Q, dO rows stay in L2), and within a head the causal tiles that most Q tiles see
+  // start first.  When one CTA's work is a large share of an SM's, key tiles vary
+  // slowest instead, so those long CTAs start first.
   const int n0 = (p.kv_slowest ? blockIdx.z : blockIdx.x) * BN;
   const int hk = p.kv_slowest ? blockIdx.x : blockIdx.y, b = p.kv_slowest ? blockIdx.y : blockIdx.z;
   const int dlen = p.Skv - p.Sq;  // key j is visible to query i iff j <= i + dlen (causal)
@@ -170,13 +215,18 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::KV_FULL), 1);
-    mbar_init(bar(L::QD_FULL), 1);
-    mbar_init(bar(L::QD_FULL + 1), 1);
-    mbar_init(bar(L::S_FULL), 1);
-    mbar_init(bar(L::P_FULL), NCOMP);
-    mbar_init(bar(L::DQ_FULL), 1);
-    mbar_init(bar(L::DQ_FREE), NCOMP);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(L::Q_FULL + i), 1);
+      mbar_init(bar(L::DO_FULL + i), 1);
+      mbar_init(bar(L::Q_FREE + i), 1);
+      mbar_init(bar(L::DO_FREE + i), 1);
+    }
+    mbar_init(bar(L::S_READY), 1);
+    mbar_init(bar(L::DP_READY), 1);
+    mbar_init(bar(L::P_READY), NCOMP);
+    mbar_init(bar(L::DS_READY), NCOMP);
     mbar_init(bar(L::VEC_READY), NCOMP);
+    mbar_init(bar(L::DONE), 1);
     mbar_init(bar(L::DRAIN), 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -189,9 +239,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
+  // TMEM columns: S^T (P^T over columns 0-31 and 64-95) at 0, dP^T (dS^T likewise)
+  // at 128, dV at 256, dK at 384
+  constexpr uint32_t C_S = 0, C_DP = 128, C_DV = 256, C_DK = 384;
 
-  if (warp == ISSUER_WARP) {
-    // ------------------------------------------------ loads and MMAs (one thread)
+  if (warp == LOAD_WARP) {
+    // ------------------------------------------------------------ loads (one thread)
     if (lane == 0 && n_iter > 0) {
       prefetch_tmap(&tmq);
       prefetch_tmap(&tmk);
@@ -205,109 +258,108 @@ __global__ void __launch_bounds__(THREADS, 1)
         tma_load_3d(sb + L::K_OFF + rr * L::REGION, &tmk, bar(L::KV_FULL), rr * 64, n0, kv_z, pol_kv);
         tma_load_3d(sb + L::V_OFF + rr * L::REGION, &tmv, bar(L::KV_FULL), rr * 64, n0, kv_z, pol_kv);
       }
-      // K-major operands (S^T = K Q^T, dP^T = V dO^T): 16 columns = 32 bytes of a
-      // 128-byte swizzled row; M/N-major operands (dO, Q, K as B and dS^T as A):
-      // rows are the K dimension, LBO steps to the next 64 columns, SBO to the next 8 rows
-      const uint64_t k_km = sdesc_sw128(sb + L::K_OFF, 16, 1024);
-      const uint64_t v_km = sdesc_sw128(sb + L::V_OFF, 16, 1024);
-      const uint64_t k_mn = sdesc_sw128(sb + L::K_OFF, L::REGION, 1024);
-      const uint64_t ds_mn = sdesc_sw128(sb + L::DS_OFF, L::REGION, 1024);
-      constexpr uint32_t idesc_s = umma_idesc_f16(BF16, BN, BM, false, false);
-      constexpr uint32_t idesc_kv = umma_idesc_f16(BF16, BN, D, false, true);
-      constexpr uint32_t idesc_dq = umma_idesc_f16(BF16, BM, D, true, true);
-      const uint32_t t_s = tmem, t_dp = tmem + 128, t_dv = tmem + 256, t_dk = tmem + 256 + D;
       // bounded-wait test: one CTA never issues iteration 1's loads, so the waits run out
       const int withheld =
           (p.debug_fault == 3 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) ? 1 : -1;
-      // Q, dO of iteration i go to buffer i & 1
-      auto load_qd = [&](int i) {
-        if (i == withheld) return;
-        const int h = hk * p.group + i / per_head, m = m_lo + i % per_head;
-        const uint32_t fb = bar(L::QD_FULL + (i & 1));
-        mbar_expect_tx(fb, 2 * L::TILE);
-        for (int rr = 0; rr < L::NREG; ++rr) {
-          tma_load_3d(sb + L::Q_OFF + (i & 1) * L::TILE + rr * L::REGION, &tmq, fb, rr * 64, m * BM,
-                      b * p.Hq + h, pol_q);
-          tma_load_3d(sb + L::DO_OFF + (i & 1) * L::TILE + rr * L::REGION, &tmdo, fb, rr * 64, m * BM,
-                      b * p.Hq + h, pol_q);
-        }
-      };
-      int n_qd = 0;  // Q/dO loads issued
-      load_qd(0);
-      ++n_qd;
-      if (n_iter > 1) {
-        load_qd(1);
-        ++n_qd;
-      }
+      // iteration i's Q and dO go to buffer i & 1, once iteration i - 2's last products
+      // that read them (dV for dO, dK for Q) have completed
       bool ok = true;
-      for (int it = 0; it < n_iter && ok; ++it) {
-        const uint32_t qo = (it & 1) * L::TILE;
-        const uint64_t q_km = sdesc_sw128(sb + L::Q_OFF + qo, 16, 1024);
-        const uint64_t do_km = sdesc_sw128(sb + L::DO_OFF + qo, 16, 1024);
-        const uint64_t q_mn = sdesc_sw128(sb + L::Q_OFF + qo, L::REGION, 1024);
-        const uint64_t do_mn = sdesc_sw128(sb + L::DO_OFF + qo, L::REGION, 1024);
-        if (!(ok = mbar_wait(bar(L::QD_FULL + (it & 1)), (it >> 1) & 1, abort_flag, &g_status, lim)))
+      int n_do = 0, n_q = 0;  // the dO and Q loads of iterations [0, n_do), [0, n_q) are issued
+      for (int i = 0; i < n_iter && ok; ++i) {
+        const int bi = i & 1, h = hk * p.group + i / per_head, m = m_lo + i % per_head;
+        if (i >= 2 && !(ok = mbar_wait(bar(L::DO_FREE + bi), ((i - 2) >> 1) & 1, abort_flag, &g_status, lim)))
           break;
-        if (it == 0 && !(ok = mbar_wait(bar(L::KV_FULL), 0, abort_flag, &g_status, lim))) break;
-        tc_fence_after();
-        // S^T = K Q^T: its columns' last P^T was read by the last dV, issued before
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * L::REGION + (kk & 3) * 32) >> 4;
-          umma_ss(t_s, k_km + off, q_km + off, idesc_s, kk > 0 ? 1u : 0u);
+        if (i != withheld) {
+          mbar_expect_tx(bar(L::DO_FULL + bi), L::TILE);
+          for (int rr = 0; rr < L::NREG; ++rr)
+            tma_load_3d(sb + L::DO_OFF + bi * L::TILE + rr * L::REGION, &tmdo, bar(L::DO_FULL + bi),
+                        rr * 64, m * BM, b * p.Hq + h, pol_q);
         }
-        // dP^T's columns held the last dQ_part: the compute warps must have read it
-        if (it > 0 && !(ok = mbar_wait(bar(L::DQ_FREE), (it - 1) & 1, abort_flag, &g_status, lim)))
+        n_do = i + 1;
+        if (i >= 2 && !(ok = mbar_wait(bar(L::Q_FREE + bi), ((i - 2) >> 1) & 1, abort_flag, &g_status, lim)))
           break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * L::REGION + (kk & 3) * 32) >> 4;
-          umma_ss(t_dp, v_km + off, do_km + off, idesc_s, kk > 0 ? 1u : 0u);
+        if (i != withheld) {
+          mbar_expect_tx(bar(L::Q_FULL + bi), L::TILE);
+          for (int rr = 0; rr < L::NREG; ++rr)
+            tma_load_3d(sb + L::Q_OFF + bi * L::TILE + rr * L::REGION, &tmq, bar(L::Q_FULL + bi),
+                        rr * 64, m * BM, b * p.Hq + h, pol_q);
         }
-        umma_commit(bar(L::S_FULL));
-        // the other buffer's last reader, iteration it - 1, has completed (its DQ_FULL
-        // preceded DQ_FREE): load iteration it + 1 into it
-        if (it > 0 && it + 1 < n_iter) {
-          load_qd(it + 1);
-          ++n_qd;
-        }
-        if (!(ok = mbar_wait(bar(L::P_FULL), it & 1, abort_flag, &g_status, lim))) break;
-        tc_fence_after();
-        // dV += P^T dO and dK += dS^T Q over the tile's 128 queries, 16 per MMA
-#pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk)
-          umma_ts(t_dv, t_s + kk * 8, do_mn + kk * 128, idesc_kv, (it > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk)
-          umma_ts(t_dk, t_dp + kk * 8, q_mn + kk * 128, idesc_kv, (it > 0 || kk > 0) ? 1u : 0u);
-        // dQ_part = dS K over the tile's 128 keys, into dP^T's columns (after dK read dS^T)
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          umma_ss(t_dp, ds_mn + kk * 128, k_mn + kk * 128, idesc_dq, kk > 0 ? 1u : 0u);
-        umma_commit(bar(L::DQ_FULL));
+        n_q = i + 1;
       }
-      // nothing may be in flight when the CTA exits: the last load into each buffer
-      // (no later phase follows, so none is missed) and every MMA issued above (one
-      // more commit, on a barrier of its own, tracks them all, also after an abort)
+      // nothing may be in flight when the CTA exits: the last loads into each buffer
+      // (a withheld pair was never issued, and no later load of its buffer is reached)
       drain_wait(bar(L::KV_FULL), 0, lim);
-      for (int i = max(0, n_qd - 2); i < n_qd; ++i)
-        if (i != withheld) drain_wait(bar(L::QD_FULL + (i & 1)), (i >> 1) & 1, lim);
+      for (int i = max(0, n_do - 2); i < n_do; ++i)
+        if (i != withheld) drain_wait(bar(L::DO_FULL + (i & 1)), (i >> 1) & 1, lim);
+      for (int i = max(0, n_q - 2); i < n_q; ++i)
+        if (i != withheld) drain_wait(bar(L::Q_FULL + (i & 1)), (i >> 1) & 1, lim);
+    }
+    __syncwarp();
+  } else if (warp == MMA_WARP) {
+    // ------------------------------------------------------------ MMAs (one thread)
+    if (lane == 0 && n_iter > 0) {
+      const uint64_t k_km = sdesc_sw128(sb + L::K_OFF, 16, 1024);
+      const uint64_t v_km = sdesc_sw128(sb + L::V_OFF, 16, 1024);
+      auto q_km = [&](int bi) { return sdesc_sw128(sb + L::Q_OFF + bi * L::TILE, 16, 1024); };
+      auto do_km = [&](int bi) { return sdesc_sw128(sb + L::DO_OFF + bi * L::TILE, 16, 1024); };
+      auto q_mn = [&](int bi) { return sdesc_sw128(sb + L::Q_OFF + bi * L::TILE, L::REGION, 1024); };
+      auto do_mn = [&](int bi) { return sdesc_sw128(sb + L::DO_OFF + bi * L::TILE, L::REGION, 1024); };
+      auto wait = [&](int bar_i, int parity) -> bool {
+        return mbar_wait(bar(bar_i), parity & 1, abort_flag, &g_status, lim);
+      };
+      // S^T(0), dP^T(0); then per iteration i: dV(i), S^T(i+1), dK(i), dP^T(i+1), so
+      // that the compute warps' P phase of i + 1 runs during dK(i), dP^T(i+1) and
+      // their dS phase of i during dV(i), S^T(i+1)
+      bool ok = wait(L::KV_FULL, 0) && wait(L::Q_FULL, 0);
+      if (ok) {
+        tc_fence_after();
+        mma_kmajor<D, BF16>(tmem + C_S, k_km, q_km(0));
+        umma_commit(bar(L::S_READY));
+        ok = wait(L::DO_FULL, 0);
+        if (ok) {
+          tc_fence_after();
+          mma_kmajor<D, BF16>(tmem + C_DP, v_km, do_km(0));
+          umma_commit(bar(L::DP_READY));
+        }
+      }
+      for (int i = 0; i < n_iter && ok; ++i) {
+        const int bi = i & 1, bn = bi ^ 1;
+        if (!(ok = wait(L::P_READY, i))) break;
+        tc_fence_after();
+        mma_tmem_a<D, BF16>(tmem + C_DV, tmem + C_S, do_mn(bi), i > 0);  // dV += P^T dO
+        umma_commit(bar(L::DO_FREE + bi));
+        if (i + 1 < n_iter) {
+          if (!(ok = wait(L::Q_FULL + bn, (i + 1) >> 1))) break;
+          tc_fence_after();
+          mma_kmajor<D, BF16>(tmem + C_S, k_km, q_km(bn));  // after dV read P^T there
+          umma_commit(bar(L::S_READY));
+        }
+        if (!(ok = wait(L::DS_READY, i))) break;
+        tc_fence_after();
+        mma_tmem_a<D, BF16>(tmem + C_DK, tmem + C_DP, q_mn(bi), i > 0);  // dK += dS^T Q
+        umma_commit(bar(L::Q_FREE + bi));
+        if (i + 1 < n_iter) {
+          if (!(ok = wait(L::DO_FULL + bn, (i + 1) >> 1))) break;
+          tc_fence_after();
+          mma_kmajor<D, BF16>(tmem + C_DP, v_km, do_km(bn));  // after dK read dS^T there
+          umma_commit(bar(L::DP_READY));
+        }
+      }
+      umma_commit(bar(L::DONE));  // dK and dV complete (also after an abort: a tracked commit)
       umma_commit(bar(L::DRAIN));
       drain_wait(bar(L::DRAIN), 0, lim);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------ compute warps: two threads per key row
-    // TMEM lane r: key n0 + r (S^T, dP^T, dK, dV), query m0 + r (dQ_part); warps w and
-    // w + 4 share the lanes of quarter w and split the columns between them
+    // TMEM lane r: key n0 + r; warps w and w + 4 share the lanes of quarter w and
+    // take queries [0, 64) and [64, 128) of each Q tile
     const int quarter = warp & 3, half = warp >> 2;
     const int r = quarter * 32 + lane;
     const uint32_t lane_t = tmem + ((uint32_t)(quarter * 32) << 16);
-    float* v_lse = reinterpret_cast<float*>(smem + L::VEC_OFF);
-    float* v_dl = v_lse + BM;
+    float* vec = reinterpret_cast<float*>(smem + L::VEC_OFF);  // [buffer][LSE_2, delta][BM]
     const int key = n0 + r;
-    const int c0 = half * 64;  // this thread's 64 of the tile's 128 queries
+    const int c0 = half * 64;
     auto wait_warp = [&](uint32_t b_, uint32_t ph_) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(b_, ph_, abort_flag, &g_status, lim));
     };
@@ -322,77 +374,60 @@ __global__ void __launch_bounds__(THREADS, 1)
     float next_v = n_iter > 0 ? row_value(0) : 0.f;
     bool ok = true;
     for (int it = 0; it < n_iter && ok; ++it) {
-      const int h = hk * p.group + it / per_head, m = m_lo + it % per_head;
-      const int m0 = m * BM;
-      const size_t bh = (size_t)b * p.Hq + h;
-      // the row vectors of this Q tile: every thread read the last ones before P_FULL
-      // completed, which the last DQ_FULL implies
+      const int m0 = (m_lo + it % per_head) * BM;
+      // the row vectors of this Q tile, in buffer it & 1: every thread finished
+      // iteration it - 2's reads before it arrived on iteration it - 1's VEC_READY
+      float* v_lse = vec + (it & 1) * 2 * BM;
+      float* v_dl = v_lse + BM;
       (half == 0 ? v_lse : v_dl)[r] = next_v;
       mbar_arrive(bar(L::VEC_READY));
       if (it + 1 < n_iter) next_v = row_value(it + 1);
       if (!(ok = wait_warp(bar(L::VEC_READY), it & 1))) break;
-      if (!(ok = wait_warp(bar(L::S_FULL), it & 1))) break;
+      // ---- P phase: P^T = 2^(S^T c - LSE_2) on the visible (key, query) pairs
+      if (!(ok = wait_warp(bar(L::S_READY), it & 1))) break;
       tc_fence_after();
+      float pv[64];
       {
-        uint32_t pp[32], dd[32];  // this thread's 64 queries of P^T, dS^T as 16-bit pairs
+        uint32_t sr[64];
+        tmem_ld32(lane_t + C_S + c0, *reinterpret_cast<uint32_t(*)[32]>(sr));
+        tmem_ld32(lane_t + C_S + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+        uint32_t pk[32];
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {  // 32 queries at a time
-          uint32_t sr[32], dr[32];
-          tmem_ld32(lane_t + c0 + 32 * g, sr);
-          tmem_ld32(lane_t + 128 + c0 + 32 * g, dr);
-#pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            float pv[2], dsv[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int cq = c0 + 32 * g + j + u;  // query column in the tile
-              const int q = m0 + cq;
-              const bool vis = q < p.Sq && key < p.Skv && (!p.causal || key <= q + dlen);
-              const float x = fmaf(__uint_as_float(sr[j + u]), p.c2, -v_lse[cq]);
-              pv[u] = vis ? ex2(x) : 0.f;
-              dsv[u] = pv[u] * (__uint_as_float(dr[j + u]) - v_dl[cq]);
-            }
-            pp[16 * g + (j >> 1)] = pack2<BF16>(pv[0], pv[1]);
-            dd[16 * g + (j >> 1)] = pack2<BF16>(dsv[0], dsv[1]);
-          }
+        for (int j = 0; j < 64; ++j) {
+          const int cq = c0 + j, q = m0 + cq;
+          const bool vis = q < p.Sq && key < p.Skv && (!p.causal || key <= q + dlen);
+          pv[j] = vis ? ex2(fmaf(__uint_as_float(sr[j]), p.c2, -v_lse[cq])) : 0.f;
         }
-        tmem_st32(lane_t + (c0 >> 1), pp);        // P^T over S^T's columns
-        tmem_st32(lane_t + 128 + (c0 >> 1), dd);  // dS^T over dP^T's columns
-        // dS^T row r, queries c0 .. c0 + 63: 16-byte chunk c at chunk c ^ (r mod 8)
-        const uint32_t reg = sb + L::DS_OFF + half * L::REGION + r * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          st_shared_v4(reg + ((c ^ (r & 7)) << 4),
-                       make_uint4(dd[4 * c], dd[4 * c + 1], dd[4 * c + 2], dd[4 * c + 3]));
+        for (int j = 0; j < 32; ++j) pk[j] = pack2<BF16>(pv[2 * j], pv[2 * j + 1]);
+        tmem_st32(lane_t + C_S + c0, pk);  // P^T over the S^T columns this thread read
       }
       tmem_wait_st();
-      fence_proxy_async_smem();  // dS^T in shared memory, for the MMA that reads it
       tc_fence_before();
-      mbar_arrive(bar(L::P_FULL));
-      if (!(ok = wait_warp(bar(L::DQ_FULL), it & 1))) break;
+      mbar_arrive(bar(L::P_READY));
+      // ---- dS phase: dS^T = P^T (dP^T - delta)
+      if (!(ok = wait_warp(bar(L::DP_READY), it & 1))) break;
       tc_fence_after();
-      // dQ_part row r (query m0 + r), this half's D / 2 columns, into the fp32 accumulator
-      const bool live = m0 + r < p.Sq;
-      float* dst = p.dq_acc + (bh * p.Sq + (live ? m0 + r : 0)) * D + half * (D / 2);
+      {
+        uint32_t dr[64];
+        tmem_ld32(lane_t + C_DP + c0, *reinterpret_cast<uint32_t(*)[32]>(dr));
+        tmem_ld32(lane_t + C_DP + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(dr + 32));
+        uint32_t dk2[32];
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        uint32_t v[32];
-        tmem_ld32(lane_t + 128 + half * (D / 2) + 32 * c, v);
-        if (live) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            atomicAdd(reinterpret_cast<float4*>(dst + 32 * c + 4 * i),
-                      make_float4(__uint_as_float(v[4 * i]) * p.scale,
-                                  __uint_as_float(v[4 * i + 1]) * p.scale,
-                                  __uint_as_float(v[4 * i + 2]) * p.scale,
-                                  __uint_as_float(v[4 * i + 3]) * p.scale));
+        for (int j = 0; j < 32; ++j) {
+          const float d0 = pv[2 * j] * (__uint_as_float(dr[2 * j]) - v_dl[c0 + 2 * j]);
+          const float d1 = pv[2 * j + 1] * (__uint_as_float(dr[2 * j + 1]) - v_dl[c0 + 2 * j + 1]);
+          dk2[j] = pack2<BF16>(d0, d1);
         }
+        tmem_st32(lane_t + C_DP + c0, dk2);  // dS^T over the dP^T columns this thread read
       }
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(L::DQ_FREE));
+      mbar_arrive(bar(L::DS_READY));
     }
     // this tile's dV rows (half 0) and dK rows (half 1); zero when no query sees the key
-    if (ok) {
+    if (ok && (n_iter == 0 || wait_warp(bar(L::DONE), 0))) {
+      tc_fence_after();
       const float f = half == 0 ? 1.f : p.scale;
       uint16_t* grad = half == 0 ? p.dv : p.dk;
       uint4* row = reinterpret_cast<uint4*>(grad + (((size_t)b * p.Hkv + hk) * p.Skv + key) * D);
@@ -403,11 +438,223 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t v[32];
-          tmem_ld32(lane_t + 256 + half * D + 32 * c, v);
+          tmem_ld32(lane_t + (half == 0 ? C_DV : C_DK) + 32 * c, v);
           if (key < p.Skv) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) row[4 * c + i] = pack8<BF16>(v + 8 * i, f);
           }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ============================================================================ dQ
+template <int D, bool BF16>
+__global__ void __launch_bounds__(THREADS, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                  const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
+                  const Params p) {
+  using L = QLayout<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw_s = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+  const uint32_t sb = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sb + L::BAR_OFF + 8u * i; };
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t lim = p.wait_limit_ns;
+
+  // CTA (m tile, query head, batch); the causal tiles with the most keys run first
+  const int n_mt = (p.Sq + BM - 1) / BM;
+  const int m0 = (p.causal ? n_mt - 1 - (int)blockIdx.x : (int)blockIdx.x) * BM;
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int hk = h / p.group;
+  const int dlen = p.Skv - p.Sq;
+  int n_kv = (p.Skv + BN - 1) / BN;  // K/V tiles this Q tile sees
+  if (p.causal) {
+    const long long last = min((long long)p.Skv - 1, (long long)min(m0 + BM, p.Sq) - 1 + dlen);
+    n_kv = last < 0 ? 0 : (int)(last / BN + 1);
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(L::QD_FULL), 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(bar(L::RING_FULL + s), 1);
+      mbar_init(bar(L::RING_EMPTY + s), 1);
+    }
+    mbar_init(bar(L::S_READY), 1);
+    mbar_init(bar(L::DP_READY), 1);
+    mbar_init(bar(L::DP_FREE), NCOMP);
+    mbar_init(bar(L::DS_READY), NCOMP);
+    mbar_init(bar(L::DONE), 1);
+    mbar_init(bar(L::DRAIN), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(misc), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  // TMEM columns: S of even K/V tiles at 0, of odd ones at 128 (dS over columns 0-31
+  // and 64-95), dP at 256, dQ at 384
+  constexpr uint32_t C_S = 0, C_DP = 256, C_DQ = 384;
+
+  if (warp == LOAD_WARP) {
+    // ------------------------------------------------------------ loads (one thread)
+    if (lane == 0 && n_kv > 0) {
+      prefetch_tmap(&tmq);
+      prefetch_tmap(&tmk);
+      prefetch_tmap(&tmv);
+      prefetch_tmap(&tmdo);
+      const uint64_t pol_q = policy_evict_first();
+      const uint64_t pol_kv = policy_evict_last();
+      mbar_expect_tx(bar(L::QD_FULL), 2 * L::TILE);
+      for (int rr = 0; rr < L::NREG; ++rr) {
+        tma_load_3d(sb + L::Q_OFF + rr * L::REGION, &tmq, bar(L::QD_FULL), rr * 64, m0, b * p.Hq + h, pol_q);
+        tma_load_3d(sb + L::DO_OFF + rr * L::REGION, &tmdo, bar(L::QD_FULL), rr * 64, m0, b * p.Hq + h,
+                    pol_q);
+      }
+      const int kv_z = b * p.Hkv + hk;
+      bool ok = true;
+      int ld = 0;
+      for (; ld < 2 * n_kv && ok; ++ld) {  // K_0, V_0, K_1, V_1, ...
+        const int s = ld % NS;
+        if (ld >= NS && !(ok = mbar_wait(bar(L::RING_EMPTY + s), ((ld / NS) - 1) & 1, abort_flag,
+                                         &g_status, lim)))
+          break;
+        mbar_expect_tx(bar(L::RING_FULL + s), L::TILE);
+        const CUtensorMap* tm = (ld & 1) ? &tmv : &tmk;
+        for (int rr = 0; rr < L::NREG; ++rr)
+          tma_load_3d(sb + L::RING_OFF + s * L::TILE + rr * L::REGION, tm, bar(L::RING_FULL + s), rr * 64,
+                      (ld >> 1) * BN, kv_z, pol_kv);
+      }
+      drain_wait(bar(L::QD_FULL), 0, lim);
+      for (int l = max(0, ld - NS); l < ld; ++l) drain_wait(bar(L::RING_FULL + l % NS), (l / NS) & 1, lim);
+    }
+    __syncwarp();
+  } else if (warp == MMA_WARP) {
+    // ------------------------------------------------------------ MMAs (one thread)
+    if (lane == 0 && n_kv > 0) {
+      const uint64_t q_km = sdesc_sw128(sb + L::Q_OFF, 16, 1024);
+      const uint64_t do_km = sdesc_sw128(sb + L::DO_OFF, 16, 1024);
+      auto ring_km = [&](int ld) { return sdesc_sw128(sb + L::RING_OFF + (ld % NS) * L::TILE, 16, 1024); };
+      auto ring_mn = [&](int ld) {
+        return sdesc_sw128(sb + L::RING_OFF + (ld % NS) * L::TILE, L::REGION, 1024);
+      };
+      auto wait = [&](int bar_i, int parity) -> bool {
+        return mbar_wait(bar(bar_i), parity & 1, abort_flag, &g_status, lim);
+      };
+      auto ring_wait = [&](int ld) -> bool { return wait(L::RING_FULL + ld % NS, ld / NS); };
+      // S(0), dP(0); then per K/V tile j: S(j+1) into the other S buffer, dP(j+1) once
+      // the compute warps hold dP(j), dQ += dS(j) K(j) once they wrote dS(j)
+      bool ok = wait(L::QD_FULL, 0) && ring_wait(0);
+      if (ok) {
+        tc_fence_after();
+        mma_kmajor<D, BF16>(tmem + C_S, q_km, ring_km(0));
+        umma_commit(bar(L::S_READY));
+        ok = ring_wait(1);
+        if (ok) {
+          tc_fence_after();
+          mma_kmajor<D, BF16>(tmem + C_DP, do_km, ring_km(1));
+          umma_commit(bar(L::DP_READY));
+        }
+      }
+      for (int j = 0; j < n_kv && ok; ++j) {
+        if (j + 1 < n_kv) {
+          if (!(ok = ring_wait(2 * j + 2))) break;
+          tc_fence_after();
+          // the other buffer held dS(j-1), read by dQ(j-1), issued before
+          mma_kmajor<D, BF16>(tmem + C_S + 128u * ((j + 1) & 1), q_km, ring_km(2 * j + 2));
+          umma_commit(bar(L::S_READY));
+        }
+        if (!(ok = wait(L::DP_FREE, j))) break;
+        if (j + 1 < n_kv) {
+          if (!(ok = ring_wait(2 * j + 3))) break;
+          tc_fence_after();
+          mma_kmajor<D, BF16>(tmem + C_DP, do_km, ring_km(2 * j + 3));
+          umma_commit(bar(L::DP_READY));
+        }
+        if (!(ok = wait(L::DS_READY, j))) break;
+        tc_fence_after();
+        mma_tmem_a<D, BF16>(tmem + C_DQ, tmem + C_S + 128u * (j & 1), ring_mn(2 * j), j > 0);  // dQ += dS K
+        umma_commit(bar(L::RING_EMPTY + (2 * j) % NS));      // K(j): read by S(j) and dQ(j)
+        umma_commit(bar(L::RING_EMPTY + (2 * j + 1) % NS));  // V(j): read by dP(j)
+      }
+      umma_commit(bar(L::DONE));
+      umma_commit(bar(L::DRAIN));
+      drain_wait(bar(L::DRAIN), 0, lim);
+    }
+    __syncwarp();
+  } else if (warp < 8) {
+    // ------------------------------------------------ compute warps: two threads per query row
+    const int quarter = warp & 3, half = warp >> 2;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_t = tmem + ((uint32_t)(quarter * 32) << 16);
+    const int row = m0 + r;
+    const int c0 = half * 64;  // this thread's 64 of a K/V tile's 128 keys
+    const size_t ridx = ((size_t)b * p.Hq + h) * p.Sq + row;
+    const float lse2 = row < p.Sq ? p.lse[ridx] * 1.4426950408889634f : INFINITY;
+    const float dlt = row < p.Sq ? p.delta[ridx] : 0.f;
+    const int last_key = p.causal ? row + dlen : p.Skv - 1;  // keys of this row: [0, last_key]
+    auto wait_warp = [&](uint32_t b_, uint32_t ph_) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(b_, ph_, abort_flag, &g_status, lim));
+    };
+    bool ok = true;
+    for (int j = 0; j < n_kv && ok; ++j) {
+      if (!(ok = wait_warp(bar(L::S_READY), j & 1))) break;
+      if (!(ok = wait_warp(bar(L::DP_READY), j & 1))) break;
+      tc_fence_after();
+      const uint32_t t_s = lane_t + C_S + 128u * (j & 1);
+      uint32_t sr[64], dr[64];
+      tmem_ld32(t_s + c0, *reinterpret_cast<uint32_t(*)[32]>(sr));
+      tmem_ld32(t_s + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+      tmem_ld32(lane_t + C_DP + c0, *reinterpret_cast<uint32_t(*)[32]>(dr));
+      tmem_ld32(lane_t + C_DP + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(dr + 32));
+      tc_fence_before();
+      mbar_arrive(bar(L::DP_FREE));  // dP(j + 1) may overwrite dP(j)
+      // keys j BN + c0 + u, u < vis, are visible to this row (none for rows past Sq)
+      const int vis = row < p.Sq ? min(last_key + 1, p.Skv) - (j * BN + c0) : 0;
+      uint32_t pk[32];
+#pragma unroll
+      for (int u = 0; u < 32; ++u) {
+        const float p0 = 2 * u < vis ? ex2(fmaf(__uint_as_float(sr[2 * u]), p.c2, -lse2)) : 0.f;
+        const float p1 = 2 * u + 1 < vis ? ex2(fmaf(__uint_as_float(sr[2 * u + 1]), p.c2, -lse2)) : 0.f;
+        pk[u] = pack2<BF16>(p0 * (__uint_as_float(dr[2 * u]) - dlt), p1 * (__uint_as_float(dr[2 * u + 1]) - dlt));
+      }
+      tmem_st32(t_s + c0, pk);  // dS over the S columns this thread read
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(L::DS_READY));
+    }
+    // dQ = scale * (dS K) summed over the K/V tiles; rows that see no key get 0
+    if (ok && (n_kv == 0 || wait_warp(bar(L::DONE), 0))) {
+      tc_fence_after();
+      uint4* dst = reinterpret_cast<uint4*>(p.dq + ridx * D + half * (D / 2));
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t v[32];
+        if (n_kv > 0) {
+          tmem_ld32(lane_t + C_DQ + half * (D / 2) + 32 * c, v);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0u;
+        }
+        if (row < p.Sq) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[4 * c + i] = pack8<BF16>(v + 8 * i, p.scale);
         }
       }
     }
@@ -436,7 +683,6 @@ static bool make_map(CUtensorMap* map, const void* base, int D, int S, long long
 
 template <int D, bool BF16>
 static cudaError_t launch_t(const BwdArgs& a, cudaStream_t stream) {
-  using L = Layout<D>;
   const long long rows = (long long)a.B * a.Hq * a.Sq;
   if (rows > 0) {
     bwd_delta_kernel<D, BF16><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
@@ -444,40 +690,41 @@ static cudaError_t launch_t(const BwdArgs& a, cudaStream_t stream) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
+  // with no query rows the Q/dO maps cover one (never read) row of k
+  const int sq_map = a.Sq > 0 ? a.Sq : 1;
+  const void* qb = a.Sq > 0 ? a.q : a.k;
+  const void* gb = a.Sq > 0 ? a.dout : a.k;
+  CUtensorMap tq, tk, tv, tg;
+  if (!make_map(&tq, qb, D, sq_map, a.Sq > 0 ? (long long)a.B * a.Hq : 1, BF16) ||
+      !make_map(&tg, gb, D, sq_map, a.Sq > 0 ? (long long)a.B * a.Hq : 1, BF16) ||
+      !make_map(&tk, a.k, D, a.Skv, (long long)a.B * a.Hkv, BF16) ||
+      !make_map(&tv, a.v, D, a.Skv, (long long)a.B * a.Hkv, BF16))
+    return cudaErrorInvalidValue;
+  Params p{};
+  p.lse = a.lse;
+  p.delta = a.delta;
+  p.dq = static_cast<uint16_t*>(a.dq);
+  p.dk = static_cast<uint16_t*>(a.dk);
+  p.dv = static_cast<uint16_t*>(a.dv);
+  p.B = a.B;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.Sq = a.Sq;
+  p.Skv = a.Skv;
+  p.group = a.Hq / a.Hkv;
+  p.causal = a.causal ? 1 : 0;
+  p.scale = a.scale;
+  p.c2 = a.scale * 1.4426950408889634f;
+  p.wait_limit_ns = a.wait_limit_ns;
+  p.debug_fault = a.debug_fault;
+  const long long n_kt = (a.Skv + BN - 1) / BN, n_mt = (a.Sq + BM - 1) / BM;
   if (a.Skv > 0) {
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D, BF16>,
+    using L = KVLayout<D>;
+    cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, BF16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
-    // with no query rows the maps cover one (never read) row of k
-    const int sq_map = a.Sq > 0 ? a.Sq : 1;
-    const void* qb = a.Sq > 0 ? a.q : a.k;
-    const void* gb = a.Sq > 0 ? a.dout : a.k;
-    CUtensorMap tq, tk, tv, tg;
-    if (!make_map(&tq, qb, D, sq_map, a.Sq > 0 ? (long long)a.B * a.Hq : 1, BF16) ||
-        !make_map(&tg, gb, D, sq_map, a.Sq > 0 ? (long long)a.B * a.Hq : 1, BF16) ||
-        !make_map(&tk, a.k, D, a.Skv, (long long)a.B * a.Hkv, BF16) ||
-        !make_map(&tv, a.v, D, a.Skv, (long long)a.B * a.Hkv, BF16))
-      return cudaErrorInvalidValue;
-    Params p{};
-    p.lse = a.lse;
-    p.delta = a.delta;
-    p.dq_acc = a.dq_acc;
-    p.dk = static_cast<uint16_t*>(a.dk);
-    p.dv = static_cast<uint16_t*>(a.dv);
-    p.B = a.B;
-    p.Hq = a.Hq;
-    p.Hkv = a.Hkv;
-    p.Sq = a.Sq;
-    p.Skv = a.Skv;
-    p.group = a.Hq / a.Hkv;
-    p.causal = a.causal ? 1 : 0;
-    p.scale = a.scale;
-    p.c2 = a.scale * 1.4426950408889634f;
-    p.wait_limit_ns = a.wait_limit_ns;
-    p.debug_fault = a.debug_fault;
     // the longest CTA (key tile 0) against an SM's share of all (query head, Q tile)
     // iterations: above a fifth, start the long CTAs first
-    const long long n_kt = (a.Skv + BN - 1) / BN, n_mt = (a.Sq + BM - 1) / BM;
     long long total = 0;
     for (long long t = 0; t < n_kt; ++t) {
       long long m_lo = 0;
@@ -491,15 +738,16 @@ static cudaError_t launch_t(const BwdArgs& a, cudaStream_t stream) {
     const long long longest = n_mt * (a.Hq / a.Hkv);
     p.kv_slowest = longest * 5 * (a.num_sms > 0 ? a.num_sms : 1) > total ? 1 : 0;
     const dim3 grid = p.kv_slowest ? dim3(a.Hkv, a.B, (unsigned)n_kt) : dim3((unsigned)n_kt, a.Hkv, a.B);
-    attn_bwd_kernel<D, BF16><<<grid, THREADS, L::ALLOC, stream>>>(tq, tk, tv, tg, p);
+    bwd_dkdv_kernel<D, BF16><<<grid, THREADS, L::ALLOC, stream>>>(tq, tk, tv, tg, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   if (rows > 0) {
-    const long long n8 = rows * D / 8;
-    const long long blocks = (n8 + 255) / 256 < 4096 ? (n8 + 255) / 256 : 4096;
-    bwd_dq_convert_kernel<BF16><<<(unsigned)blocks, 256, 0, stream>>>(
-        a.dq_acc, static_cast<uint16_t*>(a.dq), n8);
+    using L = QLayout<D>;
+    cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<D, BF16>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+    if (e != cudaSuccess) return e;
+    bwd_dq_kernel<D, BF16><<<dim3((unsigned)n_mt, a.Hq, a.B), THREADS, L::ALLOC, stream>>>(tq, tk, tv, tg, p);
     return cudaGetLastError();
   }
   return cudaSuccess;

@@ -66,8 +66,7 @@ struct BwdArgs {
   void* dq;
   void* dk;
   void* dv;
-  float* delta;   // [B, Hq, Sq] fp32 workspace
-  float* dq_acc;  // [B, Hq, Sq, D] fp32 workspace, zeroed before the launch
+  float* delta;   // [B, Hq, Sq] fp32 workspace (the row terms)
   int B, Hq, Hkv, Sq, Skv, D;
   int causal;
   float scale;

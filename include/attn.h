@@ -134,8 +134,9 @@ int attn_fwd_qkvpacked(const void* qkv, void* o, float* lse, int B, int S, int H
  * k, v, dk, dv     device, [B, Hkv, Skv, D], 16-byte aligned.
  * lse              device, [B, Hq, Sq] float32, the forward's (natural log).
  * o, lse must be attn_fwd's outputs for these q, k, v, causal and scale.
- * A workspace of attn_bwd_workspace_bytes(B, Hq, Sq, D) bytes (fp32 dQ
- * accumulator and row terms) is taken from the library's stream-ordered pool.
+ * A workspace of attn_bwd_workspace_bytes(B, Hq, Sq, D) bytes (the fp32 row
+ * terms) is taken from the library's stream-ordered pool.  No gradient is
+ * accumulated with atomics: two calls give identical bits.
  * D 64 or 128; B, Hq, Hkv <= 65535; scale finite.  With Skv == 0, dq = 0.
  */
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,

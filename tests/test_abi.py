@@ -144,7 +144,7 @@ def test_backward_argument_errors(lib):
     assert bw(D=32) == 2 and bw(dtype=7) == 2
     assert bw(B=0) == 0 and bw(Sq=0, Skv=0) == 0
     # fp32 dQ accumulator and row terms, plus alignment slack
-    assert lib.attn_bwd_workspace_bytes(2, 8, 64, 128) == 2 * 8 * 64 * 4 * 129 + 256
+    assert lib.attn_bwd_workspace_bytes(2, 8, 64, 128) == 2 * 8 * 64 * 4 + 256
     assert lib.attn_bwd_workspace_bytes(-1, 8, 64, 128) == 0
 
 

@@ -75,9 +75,10 @@ def test_bwd_cases(case):
         compare_grad(got, w, f"{name} {case}")
 
 
-def test_bwd_mha_workload_two_heads():
+def test_bwd_mha_workload_sampled_heads():
     """B4 H32 S2048 D128 bf16 causal (the MHA workload) end to end; every gradient of
-    two (batch 0) heads against the oracle, and all of them finite."""
+    a seeded sample of (batch, head) pairs spread over the launch -- the first and
+    the last included -- against the oracle, and all gradients finite."""
     import exact_attention_43_gb300 as ea
 
     w = wl.MHA
@@ -89,15 +90,43 @@ def test_bwd_mha_workload_two_heads():
     assert ea.check_device_status() == 0
     for t in (dq, dk, dv):
         assert bool(torch.isfinite(t.float()).all())
-    sl = slice(0, 2)
-    want = oracle.sdpa_backward(q[:1, sl].cpu(), k[:1, sl].cpu(), v[:1, sl].cpu(), do[:1, sl].cpu(),
-                                causal=True, scale=w.scale)
-    for name, got, wgt in zip(("dQ", "dK", "dV"), (dq[:1, sl], dk[:1, sl], dv[:1, sl]), want):
-        compare_grad(got, wgt, f"{name} MHA heads 0-1")
+    g = torch.Generator().manual_seed(4201)
+    pick = torch.randperm(w.B * w.Hq, generator=g)[:4].tolist()
+    pairs = sorted({(0, 0), (w.B - 1, w.Hq - 1)} | {(i // w.Hq, i % w.Hq) for i in pick})
+    for b, h in pairs:
+        sl = slice(h, h + 1)
+        want = oracle.sdpa_backward(q[b:b + 1, sl].cpu(), k[b:b + 1, sl].cpu(), v[b:b + 1, sl].cpu(),
+                                    do[b:b + 1, sl].cpu(), causal=True, scale=w.scale)
+        for name, got, wgt in zip(("dQ", "dK", "dV"), (dq[b:b + 1, sl], dk[b:b + 1, sl], dv[b:b + 1, sl]),
+                                  want):
+            compare_grad(got, wgt, f"{name} MHA batch {b} head {h}")
 
 
-def test_bwd_deterministic_kv_gradients():
-    """dK and dV need no atomics: two calls agree bit for bit."""
+def test_bwd_gqa_workload_sampled_heads():
+    """B2 Hq32 Hkv8 S8192 (the GQA workload, peaked rows): the gradients of one whole
+    GQA group in each batch against the oracle (dK, dV summed over the group's four
+    query heads)."""
+    import exact_attention_43_gb300 as ea
+
+    w = wl.GQA
+    q, k, v = wl.workload_fwd_inputs(w, device="cuda")
+    do = wl.normal(tuple(q.shape), seed=4202, dtype=q.dtype, device="cuda")
+    o, lse = ea.attn_fwd(q, k, v, causal=True, scale=w.scale)
+    dq, dk, dv = ea.attn_bwd(q, k, v, o, lse, do, causal=True, scale=w.scale)
+    torch.cuda.synchronize()
+    assert ea.check_device_status() == 0
+    G = w.Hq // w.Hkv
+    for b, g in ((0, 0), (w.B - 1, w.Hkv - 1)):
+        qs, ks = slice(g * G, (g + 1) * G), slice(g, g + 1)
+        want = oracle.sdpa_backward(q[b:b + 1, qs].cpu(), k[b:b + 1, ks].cpu(), v[b:b + 1, ks].cpu(),
+                                    do[b:b + 1, qs].cpu(), causal=True, scale=w.scale)
+        for name, got, wgt in zip(("dQ", "dK", "dV"), (dq[b:b + 1, qs], dk[b:b + 1, ks], dv[b:b + 1, ks]),
+                                  want):
+            compare_grad(got, wgt, f"{name} GQA batch {b} group {g}")
+
+
+def test_bwd_deterministic():
+    """No gradient is accumulated with atomics: two calls agree bit for bit."""
     import exact_attention_43_gb300 as ea
 
     q, k, v = wl.fwd_inputs(1, 8, 2, 512, 512, 128, seed=4300, device="cuda")
@@ -106,5 +135,5 @@ def test_bwd_deterministic_kv_gradients():
     a = ea.attn_bwd(q, k, v, o, lse, do, causal=True)
     b = ea.attn_bwd(q, k, v, o, lse, do, causal=True)
     torch.cuda.synchronize()
-    assert torch.equal(a[1].view(torch.int16), b[1].view(torch.int16))
-    assert torch.equal(a[2].view(torch.int16), b[2].view(torch.int16))
+    for x, y in zip(a, b):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
