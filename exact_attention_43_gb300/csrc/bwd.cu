@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       int n_do = 0, n_q = 0;  // the dO and Q loads of iterations [0, n_do), [0, n_q) are issued
       for (int i = 0; i < n_iter && ok; ++i) {
         const int bi = i & 1, h = hk * p.group + i / per_head, m = m_lo + i % per_head;
-        if (i >= 2 && !(ok = mbar_wait(bar(L::DO_FREE + bi), ((i - 2) >> 1) & 1, abort_flag, &g_status, lim)))
+        if (i >= 2 && !(ok = mbar_wait<false>(bar(L::DO_FREE + bi), ((i - 2) >> 1) & 1, abort_flag, &g_status, lim)))
           break;
         if (i != withheld) {
           mbar_expect_tx(bar(L::DO_FULL + bi), L::TILE);
@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         rr * 64, m * BM, b * p.Hq + h, pol_q);
         }
         n_do = i + 1;
-        if (i >= 2 && !(ok = mbar_wait(bar(L::Q_FREE + bi), ((i - 2) >> 1) & 1, abort_flag, &g_status, lim)))
+        if (i >= 2 && !(ok = mbar_wait<false>(bar(L::Q_FREE + bi), ((i - 2) >> 1) & 1, abort_flag, &g_status, lim)))
           break;
         if (i != withheld) {
           mbar_expect_tx(bar(L::Q_FULL + bi), L::TILE);
@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       auto q_mn = [&](int bi) { return sdesc_sw128(sb + L::Q_OFF + bi * L::TILE, L::REGION, 1024); };
       auto do_mn = [&](int bi) { return sdesc_sw128(sb + L::DO_OFF + bi * L::TILE, L::REGION, 1024); };
       auto wait = [&](int bar_i, int parity) -> bool {
-        return mbar_wait(bar(bar_i), parity & 1, abort_flag, &g_status, lim);
+        return mbar_wait<false>(bar(bar_i), parity & 1, abort_flag, &g_status, lim);
       };
       // S^T(0), dP^T(0); then per iteration i: dV(i), S^T(i+1), dK(i), dP^T(i+1), so
       // that the compute warps' P phase of i + 1 runs during dK(i), dP^T(i+1) and
@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int key = n0 + r;
     const int c0 = half * 64;
     auto wait_warp = [&](uint32_t b_, uint32_t ph_) -> bool {
-      return __all_sync(0xffffffffu, mbar_wait(b_, ph_, abort_flag, &g_status, lim));
+      return __all_sync(0xffffffffu, mbar_wait<false>(b_, ph_, abort_flag, &g_status, lim));
     };
     // row r's LSE (half 0, log2 units) or delta (half 1) for iteration i, loaded one
     // iteration ahead so its latency hides behind the current one
@@ -392,11 +392,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_ld32(lane_t + C_S + c0, *reinterpret_cast<uint32_t(*)[32]>(sr));
         tmem_ld32(lane_t + C_S + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
         uint32_t pk[32];
+        // query columns [lo, hi) of this thread's 64 see key n0 + r; a tile whose every
+        // query sees every key (all but the causal diagonal and the ragged ends) needs no test
+        const int lo = p.causal ? key - dlen - m0 - c0 : 0;
+        const int hi = key < p.Skv ? p.Sq - m0 - c0 : 0;
+        if (__all_sync(0xffffffffu, lo <= 0 && hi >= 64)) {
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const int cq = c0 + j, q = m0 + cq;
-          const bool vis = q < p.Sq && key < p.Skv && (!p.causal || key <= q + dlen);
-          pv[j] = vis ? ex2(fmaf(__uint_as_float(sr[j]), p.c2, -v_lse[cq])) : 0.f;
+          for (int j = 0; j < 64; ++j) pv[j] = ex2(fmaf(__uint_as_float(sr[j]), p.c2, -v_lse[c0 + j]));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 64; ++j)
+            pv[j] = (j >= lo && j < hi) ? ex2(fmaf(__uint_as_float(sr[j]), p.c2, -v_lse[c0 + j])) : 0.f;
         }
 #pragma unroll
         for (int j = 0; j < 32; ++j) pk[j] = pack2<BF16>(pv[2 * j], pv[2 * j + 1]);
@@ -532,7 +538,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       int ld = 0;
       for (; ld < 2 * n_kv && ok; ++ld) {  // K_0, V_0, K_1, V_1, ...
         const int s = ld % NS;
-        if (ld >= NS && !(ok = mbar_wait(bar(L::RING_EMPTY + s), ((ld / NS) - 1) & 1, abort_flag,
+        if (ld >= NS && !(ok = mbar_wait<false>(bar(L::RING_EMPTY + s), ((ld / NS) - 1) & 1, abort_flag,
                                          &g_status, lim)))
           break;
         mbar_expect_tx(bar(L::RING_FULL + s), L::TILE);
@@ -555,7 +561,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         return sdesc_sw128(sb + L::RING_OFF + (ld % NS) * L::TILE, L::REGION, 1024);
       };
       auto wait = [&](int bar_i, int parity) -> bool {
-        return mbar_wait(bar(bar_i), parity & 1, abort_flag, &g_status, lim);
+        return mbar_wait<false>(bar(bar_i), parity & 1, abort_flag, &g_status, lim);
       };
       auto ring_wait = [&](int ld) -> bool { return wait(L::RING_FULL + ld % NS, ld / NS); };
       // S(0), dP(0); then per K/V tile j: S(j+1) into the other S buffer, dP(j+1) once
@@ -610,7 +616,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const float dlt = row < p.Sq ? p.delta[ridx] : 0.f;
     const int last_key = p.causal ? row + dlen : p.Skv - 1;  // keys of this row: [0, last_key]
     auto wait_warp = [&](uint32_t b_, uint32_t ph_) -> bool {
-      return __all_sync(0xffffffffu, mbar_wait(b_, ph_, abort_flag, &g_status, lim));
+      return __all_sync(0xffffffffu, mbar_wait<false>(b_, ph_, abort_flag, &g_status, lim));
     };
     bool ok = true;
     for (int j = 0; j < n_kv && ok; ++j) {
