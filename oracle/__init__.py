@@ -20,13 +20,16 @@ sliding windows against a brute force with explicit key sets, the diagonal
 window's closed form and PyTorch SDPA on the explicit key slice; packed
 variable-length batches against the batched definition (equal lengths) and
 PyTorch SDPA per sequence; the backward against PyTorch float64 autograd,
-central finite differences of the forward and a single-key closed form.
+central finite differences of the forward and a single-key closed form, its
+sliding windows against autograd through SDPA with explicitly enumerated key
+masks and finite differences, and packed batches against autograd per sequence.
 No function here is "parity unpinned".
 """
 
 from .attention import (  # noqa: F401
     sdpa,
     sdpa_backward,
+    sdpa_backward_varlen,
     sdpa_varlen,
     softmax_probs,
     decode,

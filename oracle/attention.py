@@ -198,16 +198,18 @@ def sdpa_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, *, causal: bool, scale: flo
     return out, lse
 
 
-def sdpa_backward(q, k, v, dout, *, causal: bool, scale: float):
+def sdpa_backward(q, k, v, dout, *, causal: bool, scale: float, window_left: int = -1,
+                  window_right: int = -1):
     """Gradients of O = sdpa(q, k, v) for an incoming dO, as the llm.c page's
     ``attention_backward`` computes them for each (batch, query head):
 
     datt = dO V^T; dV += att^T dO; local = sum_j att * datt (per row);
     dpreatt = scale * att * (datt - local); dQ = dpreatt K; dK += dpreatt^T Q,
 
-    att being the materialised probabilities (bottom-right causal mask as in
-    ``sdpa``).  Shapes as ``sdpa``; dout [B, Hq, Sq, D].  Returns (dQ, dK, dV)
-    in float64, dK and dV summed over the query heads of each KV head.
+    att being the materialised probabilities (bottom-right causal mask and the
+    sliding-window bounds of ``sdpa``).  Shapes as ``sdpa``; dout [B, Hq, Sq, D].
+    Returns (dQ, dK, dV) in float64, dK and dV summed over the query heads of
+    each KV head.
     """
     q = _f64(q)
     k = _f64(k)
@@ -222,13 +224,43 @@ def sdpa_backward(q, k, v, dout, *, causal: bool, scale: float):
     for b in range(B):
         for h in range(Hq):
             kv = h // group
-            att, _, _ = softmax_probs(q[b, h], k[b, kv], causal=causal, scale=scale)
+            att, _, _ = softmax_probs(q[b, h], k[b, kv], causal=causal, scale=scale,
+                                      window_left=window_left, window_right=window_right)
             datt = do[b, h] @ v[b, kv].T                    # [Sq, Skv]
             dv[b, kv] += att.T @ do[b, h]
             local = (att * datt).sum(axis=1, keepdims=True)
             dpre = scale * att * (datt - local)
             dq[b, h] = dpre @ k[b, kv]
             dk[b, kv] += dpre.T @ q[b, h]
+    return dq, dk, dv
+
+
+def sdpa_backward_varlen(q, k, v, dout, cu_seqlens_q, cu_seqlens_k, *, causal: bool,
+                         scale: float, window_left: int = -1, window_right: int = -1):
+    """Gradients of ``sdpa_varlen`` for an incoming dO: each packed sequence is the
+    plain ``sdpa_backward`` of its own rows (layouts of ``sdpa_varlen``; dout like
+    q).  Returns (dQ [total_q, Hq, D], dK, dV [total_k, Hkv, D]) float64; rows
+    outside every sequence get zero gradients.
+    """
+    q = _f64(q)
+    k = _f64(k)
+    v = _f64(v)
+    do = _f64(dout)
+    cq = [int(x) for x in np.asarray(_f64(cu_seqlens_q)).reshape(-1)]
+    ck = [int(x) for x in np.asarray(_f64(cu_seqlens_k)).reshape(-1)]
+    if len(cq) != len(ck):
+        raise ValueError("cu_seqlens_q and cu_seqlens_k need the same length")
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for b in range(len(cq) - 1):
+        q0, q1, k0, k1 = cq[b], cq[b + 1], ck[b], ck[b + 1]
+        if q1 <= q0 or k1 <= k0:
+            continue                                  # no query, or no key: zero gradients
+        t = lambda x, a, e: x[a:e].transpose(1, 0, 2)[None]   # [1, H, S_b, D]
+        g = sdpa_backward(t(q, q0, q1), t(k, k0, k1), t(v, k0, k1), t(do, q0, q1), causal=causal,
+                          scale=scale, window_left=window_left, window_right=window_right)
+        dq[q0:q1] = g[0][0].transpose(1, 0, 2)
+        dk[k0:k1] = g[1][0].transpose(1, 0, 2)
+        dv[k0:k1] = g[2][0].transpose(1, 0, 2)
     return dq, dk, dv
 
 

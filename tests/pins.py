@@ -2,6 +2,7 @@
 
 Each pin is a function ``pin_*(impl)`` that raises AssertionError when the
 implementation ``impl`` (a namespace with ``sdpa``, ``sdpa_varlen``, ``sdpa_backward``,
+``sdpa_backward_varlen``,
 ``softmax_probs``, ``decode``, ``decode_partials`` and ``merge_partials``)
 disagrees with a fact
 that does not depend on the oracle: a closed form, an invariant, a hand-worked
@@ -379,6 +380,99 @@ def pin_backward_single_key(impl):
     _close(dv[0, :, 0], do[0].sum(axis=1), 1e-12, "single key dV")
 
 
+def _mask_from_keys(Sq, Skv, causal, wl, wr):
+    """Boolean [Sq, Skv] mask of the keys each query keeps, from the window's wording."""
+    m = np.zeros((Sq, Skv), dtype=bool)
+    for i in range(Sq):
+        for j in _window_keys(i, Sq, Skv, causal, wl, wr):
+            m[i, j] = True
+    return m
+
+
+def _torch_grads(q, k, v, do, mask, scale):
+    """PyTorch float64 autograd through its SDPA with an explicit boolean mask [Sq, Skv]
+    (GQA by repeating K and V heads); every row must keep at least one key."""
+    tq, tk, tv = (torch.from_numpy(x).requires_grad_() for x in (q, k, v))
+    G = q.shape[1] // k.shape[1]
+    o = torch.nn.functional.scaled_dot_product_attention(
+        tq, tk.repeat_interleave(G, dim=1), tv.repeat_interleave(G, dim=1),
+        attn_mask=torch.from_numpy(mask), scale=scale)
+    o.backward(torch.from_numpy(do))
+    return tq.grad.numpy(), tk.grad.numpy(), tv.grad.numpy()
+
+
+BWD_WINDOW_CASES = [  # (Sq, Skv, causal, window_left, window_right, Hq, Hkv); every row keeps a key
+    (9, 9, True, 2, -1, 4, 2),
+    (6, 10, True, 3, -1, 2, 1),
+    (8, 8, False, 1, 2, 2, 2),
+    (7, 5, False, -1, 2, 3, 1),
+]
+
+
+def pin_backward_window_autograd(impl):
+    """Sliding windows: PyTorch float64 autograd through SDPA with the window's key
+    sets enumerated one by one (bottom-right alignment, GQA, Sq != Skv both ways)."""
+    for n, (Sq, Skv, causal, wl, wr, Hq, Hkv) in enumerate(BWD_WINDOW_CASES):
+        q, k, v = _rand((1, Hq, Sq, 5), 540 + n), _rand((1, Hkv, Skv, 5), 550 + n), _rand((1, Hkv, Skv, 5), 560 + n)
+        do = _rand((1, Hq, Sq, 5), 570 + n)
+        mask = _mask_from_keys(Sq, Skv, causal, wl, wr)
+        assert mask.any(axis=1).all(), "every row of a pin case keeps a key"
+        want = _torch_grads(q, k, v, do, mask, 0.55)
+        got = impl.sdpa_backward(q, k, v, do, causal=causal, scale=0.55, window_left=wl, window_right=wr)
+        for name, g, w in zip(("dQ", "dK", "dV"), got, want):
+            _close(g, w, 1e-10, f"window backward case {n} {name}")
+
+
+def pin_backward_window_finite_differences(impl):
+    """Central differences of sum(dO * O) through the windowed forward."""
+    q, k, v = _rand((1, 2, 5, 3), 580), _rand((1, 1, 7, 3), 581), _rand((1, 1, 7, 3), 582)
+    do = _rand((1, 2, 5, 3), 583)
+    kw = dict(causal=True, scale=0.8, window_left=2, window_right=-1)
+    dq, dk, dv = impl.sdpa_backward(q, k, v, do, **kw)
+    eps = 1e-6
+
+    def loss(q_, k_, v_):
+        o, _ = impl.sdpa(q_, k_, v_, **kw)
+        return float((o * do).sum())
+
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(*x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args_p = {"q": (xp, k, v), "k": (q, xp, v), "v": (q, k, xp)}[name]
+            args_m = {"q": (xm, k, v), "k": (q, xm, v), "v": (q, k, xm)}[name]
+            num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+        _close(g, num, 1e-7, f"window finite differences d{name}")
+
+
+def pin_backward_varlen_per_sequence(impl):
+    """Packed batches: each sequence's gradients equal PyTorch autograd on its own rows
+    (bottom-right causal window, GQA 2, query and key lengths differing per sequence);
+    rows outside every sequence get zero gradients."""
+    lq, lk = [4, 0, 6, 3], [5, 3, 6, 7]
+    cq, ck = _cu(lq), _cu(lk)
+    Hq, Hkv, D = 2, 1, 4
+    q, do = _rand((int(cq[-1]) + 2, Hq, D), 590), _rand((int(cq[-1]) + 2, Hq, D), 593)
+    k, v = _rand((int(ck[-1]) + 1, Hkv, D), 591), _rand((int(ck[-1]) + 1, Hkv, D), 592)
+    wl = 3
+    dq, dk, dv = impl.sdpa_backward_varlen(q, k, v, do, cq, ck, causal=True, scale=0.6, window_left=wl)
+    for b in range(4):
+        if lq[b] == 0:
+            continue
+        t = lambda x, a, e: np.ascontiguousarray(x[a:e].transpose(1, 0, 2)[None])
+        mask = _mask_from_keys(lq[b], lk[b], True, wl, -1)
+        want = _torch_grads(t(q, cq[b], cq[b + 1]), t(k, ck[b], ck[b + 1]), t(v, ck[b], ck[b + 1]),
+                            t(do, cq[b], cq[b + 1]), mask, 0.6)
+        _close(dq[cq[b]:cq[b + 1]], want[0][0].transpose(1, 0, 2), 1e-10, f"varlen backward seq {b} dQ")
+        _close(dk[ck[b]:ck[b + 1]], want[1][0].transpose(1, 0, 2), 1e-10, f"varlen backward seq {b} dK")
+        _close(dv[ck[b]:ck[b + 1]], want[2][0].transpose(1, 0, 2), 1e-10, f"varlen backward seq {b} dV")
+    # sequence 1 has no query: its keys get no gradient; nor do rows outside every sequence
+    assert np.all(dk[ck[1]:ck[2]] == 0) and np.all(dv[ck[1]:ck[2]] == 0), "keys of a query-less sequence"
+    assert np.all(dq[int(cq[-1]):] == 0) and np.all(dk[int(ck[-1]):] == 0), "rows outside every sequence"
+
+
 # ----------------------------------------------------------------- decode pins
 
 def _decode_case(seed, B=3, Hq=4, Hkv=2, max_S=40, D=8):
@@ -444,6 +538,8 @@ ALL_PINS = [
     pin_window_brute_force, pin_window_diagonal, pin_window_torch_slice, pin_window_wide_is_plain,
     pin_varlen_equal_lengths, pin_varlen_torch_per_sequence,
     pin_backward_torch_autograd, pin_backward_finite_differences, pin_backward_single_key,
+    pin_backward_window_autograd, pin_backward_window_finite_differences,
+    pin_backward_varlen_per_sequence,
 ]
 
 

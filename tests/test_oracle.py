@@ -9,6 +9,7 @@ from tests import pins
 
 IMPL = types.SimpleNamespace(
     sdpa=oracle.sdpa, sdpa_varlen=oracle.sdpa_varlen, sdpa_backward=oracle.sdpa_backward,
+    sdpa_backward_varlen=oracle.sdpa_backward_varlen,
     softmax_probs=oracle.softmax_probs,
     decode=oracle.decode,
     decode_partials=oracle.decode_partials, merge_partials=oracle.merge_partials)

@@ -13,6 +13,7 @@ from oracle import attention as A
 from tests import pins
 
 BASE = dict(sdpa=oracle.sdpa, sdpa_varlen=oracle.sdpa_varlen, sdpa_backward=oracle.sdpa_backward,
+    sdpa_backward_varlen=oracle.sdpa_backward_varlen,
             softmax_probs=oracle.softmax_probs,
             decode=oracle.decode, decode_partials=oracle.decode_partials,
             merge_partials=oracle.merge_partials)
@@ -198,14 +199,14 @@ def _merge_drops_l_weight(partials, seq_lens, *, chunk):
     return out
 
 
-def _bwd_without_local_sum(q, k, v, dout, *, causal, scale):
+def _bwd_without_local_sum(q, k, v, dout, *, causal, scale, **win):
     # mistake: dpreatt = scale * att * datt, the row term sum_j att * datt dropped
     q, k, v, do = (A._f64(x) for x in (q, k, v, dout))
     dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
     G = q.shape[1] // k.shape[1]
     for b in range(q.shape[0]):
         for h in range(q.shape[1]):
-            att, _, _ = oracle.softmax_probs(q[b, h], k[b, h // G], causal=causal, scale=scale)
+            att, _, _ = oracle.softmax_probs(q[b, h], k[b, h // G], causal=causal, scale=scale, **win)
             datt = do[b, h] @ v[b, h // G].T
             dv[b, h // G] += att.T @ do[b, h]
             dpre = scale * att * datt
@@ -214,15 +215,25 @@ def _bwd_without_local_sum(q, k, v, dout, *, causal, scale):
     return dq, dk, dv
 
 
-def _bwd_dk_not_summed_over_group(q, k, v, dout, *, causal, scale):
-    dq, dk, dv = oracle.sdpa_backward(q, k, v, dout, causal=causal, scale=scale)
+def _bwd_dk_not_summed_over_group(q, k, v, dout, *, causal, scale, **win):
+    dq, dk, dv = oracle.sdpa_backward(q, k, v, dout, causal=causal, scale=scale, **win)
     G = A._f64(q).shape[1] // A._f64(k).shape[1]
     return dq, dk / G, dv                           # mistake: an average, not the sum
 
 
-def _bwd_unscaled(q, k, v, dout, *, causal, scale):
-    dq, dk, dv = oracle.sdpa_backward(q, k, v, dout, causal=causal, scale=scale)
+def _bwd_unscaled(q, k, v, dout, *, causal, scale, **win):
+    dq, dk, dv = oracle.sdpa_backward(q, k, v, dout, causal=causal, scale=scale, **win)
     return dq / scale, dk / scale, dv               # mistake: the chain rule's scale dropped
+
+
+def _bwd_window_ignored(q, k, v, dout, *, causal, scale, **win):
+    # mistake: the backward re-forms P without the window's bounds
+    return oracle.sdpa_backward(q, k, v, dout, causal=causal, scale=scale)
+
+
+def _bwd_varlen_key_offsets_from_queries(q, k, v, dout, cu_q, cu_k, **kw):
+    # mistake: the keys of sequence b taken at the query offsets
+    return oracle.sdpa_backward_varlen(q, k, v, dout, cu_q, cu_q, **kw)
 
 
 MUTANTS = {
@@ -245,6 +256,9 @@ MUTANTS = {
     "backward_row_term_dropped": _impl(sdpa_backward=_bwd_without_local_sum),
     "backward_group_average": _impl(sdpa_backward=_bwd_dk_not_summed_over_group),
     "backward_unscaled": _impl(sdpa_backward=_bwd_unscaled),
+    "backward_window_ignored": _impl(sdpa_backward=_bwd_window_ignored),
+    "backward_varlen_key_offsets_from_queries":
+        _impl(sdpa_backward_varlen=_bwd_varlen_key_offsets_from_queries),
 }
 
 
