@@ -25,8 +25,9 @@ ATTN_ERR_DEVICE_TIMEOUT = 4
 ATTN_BF16 = 0
 ATTN_FP16 = 1
 
-EXPORTS = ("attn_fwd", "attn_fwd_varlen", "attn_fwd_qkvpacked", "attn_bwd",
-           "attn_bwd_workspace_bytes", "attn_decode", "attn_decode_fused", "attn_decode_paged",
+EXPORTS = ("attn_fwd", "attn_fwd_varlen", "attn_fwd_qkvpacked", "attn_bwd", "attn_bwd_varlen",
+           "attn_bwd_qkvpacked", "attn_bwd_workspace_bytes", "attn_decode", "attn_decode_fused",
+           "attn_decode_paged",
            "attn_decode_noalloc",
            "attn_decode_workspace_bytes",
            "attn_decode_chunk", "attn_check_device_status", "attn_debug_set",
@@ -67,6 +68,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_fwd_qkvpacked.restype = i
     lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
     lib.attn_bwd.restype = i
+    lib.attn_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i,
+                                    i, i, i, f, i, vp]
+    lib.attn_bwd_varlen.restype = i
+    lib.attn_bwd_qkvpacked.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
+    lib.attn_bwd_qkvpacked.restype = i
     lib.attn_bwd_workspace_bytes.argtypes = [i, i, i, i]
     lib.attn_bwd_workspace_bytes.restype = sz
     lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
@@ -259,6 +265,69 @@ def attn_bwd(q, k, v, o, lse, dout, *, causal: bool = True, scale=None, dq=None,
                       _dtype_code(q), _stream(stream))
     _check(st, "attn_bwd")
     return dq, dk, dv
+
+
+def attn_bwd_varlen(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
+                    max_seqlen_k: int, *, causal: bool = True, window=(-1, -1), scale=None, dq=None,
+                    dk=None, dv=None, stream=None):
+    """Gradients of attn_fwd_varlen: q, o, dout [total_q,Hq,D], k, v [total_k,Hkv,D], lse
+    [Hq,total_q] float32 (the forward's outputs), cu_seqlens_* [B+1] int32.  Returns
+    (dQ, dK, dV); rows of tokens outside every sequence are not written."""
+    lib = load()
+    dev = _cuda16(q, "q")
+    total_q, Hq, D = q.shape
+    total_k, Hkv = k.shape[0], k.shape[1]
+    for t, name in ((q, "q"), (o, "o"), (dout, "dout")):
+        _expect(t, name, (total_q, Hq, D), q.dtype, dev)
+    for t, name in ((k, "k"), (v, "v")):
+        _expect(t, name, (total_k, Hkv, D), q.dtype, dev)
+    _expect(lse, "lse", (Hq, total_q), torch.float32, dev)
+    if cu_seqlens_q.dim() != 1 or cu_seqlens_q.numel() < 1:
+        raise ValueError("cu_seqlens_q must hold B + 1 offsets")
+    B = cu_seqlens_q.numel() - 1
+    _expect(cu_seqlens_q, "cu_seqlens_q", (B + 1,), torch.int32, dev)
+    _expect(cu_seqlens_k, "cu_seqlens_k", (B + 1,), torch.int32, dev)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _expect(dq, "dq", q.shape, q.dtype, dev)
+    _expect(dk, "dk", k.shape, q.dtype, dev)
+    _expect(dv, "dv", v.shape, q.dtype, dev)
+    wl, wr = window
+    st = lib.attn_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                             _ptr(dk), _ptr(dv), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B, Hq, Hkv,
+                             total_q, total_k, int(max_seqlen_q), int(max_seqlen_k), D,
+                             1 if causal else 0, int(wl), int(wr), float(scale), _dtype_code(q),
+                             _stream(stream))
+    _check(st, "attn_bwd_varlen")
+    return dq, dk, dv
+
+
+def attn_bwd_qkvpacked(qkv, o, lse, dout, *, causal: bool = True, window=(-1, -1), scale=None,
+                       dqkv=None, stream=None):
+    """Gradient of attn_fwd_qkvpacked: qkv [B,S,3,H,D], o and dout [B,S,H,D], lse [H,B,S]
+    float32.  Returns dqkv [B,S,3,H,D] (dQ, dK, dV at the places of Q, K, V)."""
+    lib = load()
+    dev = _cuda16(qkv, "qkv")
+    if qkv.dim() != 5 or qkv.shape[2] != 3:
+        raise ValueError("qkv must be [B, S, 3, H, D]")
+    B, S, _, H, D = qkv.shape
+    _expect(qkv, "qkv", (B, S, 3, H, D), qkv.dtype, dev)
+    _expect(o, "o", (B, S, H, D), qkv.dtype, dev)
+    _expect(dout, "dout", (B, S, H, D), qkv.dtype, dev)
+    _expect(lse, "lse", (H, B, S), torch.float32, dev)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dqkv = torch.empty_like(qkv) if dqkv is None else dqkv
+    _expect(dqkv, "dqkv", qkv.shape, qkv.dtype, dev)
+    wl, wr = window
+    st = lib.attn_bwd_qkvpacked(_ptr(qkv), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dqkv), B, S, H, D,
+                                1 if causal else 0, int(wl), int(wr), float(scale),
+                                _dtype_code(qkv), _stream(stream))
+    _check(st, "attn_bwd_qkvpacked")
+    return dqkv
 
 
 def _decode_shapes(q, k_cache, v_cache, seq_lens, out):

@@ -272,6 +272,53 @@ int attn_fwd_qkvpacked(const void* qkv, void* o, float* lse, int B, int S, int H
   return run_fwd_tm(a, S, S, window_left, window_right, stream);
 }
 
+}  // extern "C"
+
+// The backward's row-term workspace from the library pool, stream-ordered around the
+// kernels.  rows: (query token, head) pairs.
+static int run_bwd(ea::BwdArgs& a, int dev, size_t rows, cudaStream_t stream) {
+  int st;
+  void* ws = nullptr;
+  if (rows > 0) {
+    cudaMemPool_t pool;
+    if ((st = pool_for(dev, &pool)) != ATTN_OK) return st;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, rows * sizeof(float) + 256, pool, stream);
+    if (e != cudaSuccess) return from_cuda(e);
+    a.delta = static_cast<float*>(ws);
+  }
+  cudaError_t e = ea::launch_bwd(a, stream);
+  if (ws) {
+    cudaError_t f = cudaFreeAsync(ws, stream);
+    if (e == cudaSuccess) e = f;
+  }
+  if (e == cudaErrorInvalidValue && !ea::encode_tiled_fn()) return ATTN_ERR_UNSUPPORTED;
+  return from_cuda(e);
+}
+
+// Token-major backward (attn_bwd_varlen, attn_bwd_qkvpacked): the checks of the
+// window and the longest lengths, then the launch.
+static int run_bwd_tm(ea::BwdArgs& a, int max_q, int max_k, int window_left, int window_right,
+                      cudaStream_t stream) {
+  if (window_left < -1 || window_right < -1) return ATTN_ERR_INVALID_ARG;
+  if (!isfinite(a.scale)) return ATTN_ERR_INVALID_ARG;
+  if ((long long)max_q + max_k > 0x3fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  int dev = 0;
+  int st = check_device(&dev);
+  if (st != ATTN_OK) return st;
+  a.vl = 1;
+  a.Sq = max_q;
+  a.Skv = max_k;
+  // a bound at least max_q + max_k away from every diagonal excludes no key
+  a.win_left = window_left > max_q + max_k ? -1 : window_left;
+  a.win_right = window_right > max_q + max_k ? -1 : window_right;
+  a.wait_limit_ns = g_wait_limit_ns;
+  a.debug_fault = 0;
+  a.num_sms = g_num_sms[dev] > 0 ? g_num_sms[dev] : 1;
+  return run_bwd(a, dev, (size_t)a.total_q * a.Hq, stream);
+}
+
+extern "C" {
+
 size_t attn_bwd_workspace_bytes(int B, int Hq, int Sq, int D) {
   if (B < 0 || Hq < 0 || Sq < 0 || D <= 0) return 0;
   const size_t rows = (size_t)B * Hq * Sq;
@@ -320,27 +367,103 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   a.wait_limit_ns = g_wait_limit_ns;
   a.debug_fault = g_fault;
   a.num_sms = g_num_sms[dev] > 0 ? g_num_sms[dev] : 1;
+  a.win_left = -1;
+  a.win_right = -1;
   const size_t rows = (size_t)B * Hq * Sq;
   if (Skv == 0) {
     // no key: O was 0 whatever Q, K, V were, so every gradient is 0 (dK, dV are empty)
     cudaError_t e = cudaMemsetAsync(dq, 0, rows * D * 2, stream);
     return from_cuda(e);
   }
-  void* ws = nullptr;
-  if (rows > 0) {
-    cudaMemPool_t pool;
-    if ((st = pool_for(dev, &pool)) != ATTN_OK) return st;
-    cudaError_t e = cudaMallocFromPoolAsync(&ws, attn_bwd_workspace_bytes(B, Hq, Sq, D), pool, stream);
-    if (e != cudaSuccess) return from_cuda(e);
-    a.delta = static_cast<float*>(ws);
-  }
-  cudaError_t e = ea::launch_bwd(a, stream);
-  if (ws) {
-    cudaError_t f = cudaFreeAsync(ws, stream);
-    if (e == cudaSuccess) e = f;
-  }
-  if (e == cudaErrorInvalidValue && !ea::encode_tiled_fn()) return ATTN_ERR_UNSUPPORTED;
-  return from_cuda(e);
+  return run_bwd(a, dev, rows, stream);
+}
+
+int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dout, void* dq, void* dk, void* dv, const int32_t* cu_seqlens_q,
+                    const int32_t* cu_seqlens_k, int B, int Hq, int Hkv, int total_q, int total_k,
+                    int max_seqlen_q, int max_seqlen_k, int D, int causal, int window_left,
+                    int window_right, float scale, int dtype, cudaStream_t stream) {
+  if (B < 0 || Hq < 0 || Hkv < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 ||
+      max_seqlen_k < 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || Hq == 0 || ((total_q == 0 || max_seqlen_q == 0) && (total_k == 0 || max_seqlen_k == 0)))
+    return ATTN_OK;  // no query and no key: nothing to compute
+  if (Hkv == 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (B > 65535 || Hq > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (!cu_seqlens_q || !cu_seqlens_k) return ATTN_ERR_INVALID_ARG;
+  if (total_q > 0 && (!q || !o || !lse || !dout || !dq)) return ATTN_ERR_INVALID_ARG;
+  if (total_k > 0 && (!k || !v || !dk || !dv)) return ATTN_ERR_INVALID_ARG;
+  const void* a16[] = {q, k, v, o, dout, dq, dk, dv};
+  for (const void* ptr : a16)
+    if (ptr && !aligned(ptr, 16)) return ATTN_ERR_INVALID_ARG;
+  if ((lse && !aligned(lse, 4)) || !aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4))
+    return ATTN_ERR_INVALID_ARG;
+  ea::BwdArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.dout = dout;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.causal = causal != 0;
+  a.scale = scale;
+  a.bf16 = dtype == ATTN_BF16;
+  a.cu_q = cu_seqlens_q;
+  a.cu_k = cu_seqlens_k;
+  a.total_q = total_q;
+  a.total_k = total_k;
+  a.q_rstride = a.do_rstride = a.dq_rstride = (long long)Hq * D;
+  a.k_rstride = a.dk_rstride = (long long)Hkv * D;
+  return run_bwd_tm(a, max_seqlen_q, max_seqlen_k, window_left, window_right, stream);
+}
+
+int attn_bwd_qkvpacked(const void* qkv, const void* o, const float* lse, const void* dout, void* dqkv,
+                       int B, int S, int H, int D, int causal, int window_left, int window_right,
+                       float scale, int dtype, cudaStream_t stream) {
+  if (B < 0 || S < 0 || H < 0) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if ((long long)B * S * H == 0) return ATTN_OK;
+  if (B > 65535 || H > 65535) return ATTN_ERR_UNSUPPORTED;
+  if ((long long)B * S > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  if (!qkv || !o || !lse || !dout || !dqkv) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(qkv, 16) || !aligned(o, 16) || !aligned(dout, 16) || !aligned(dqkv, 16) ||
+      !aligned(lse, 4))
+    return ATTN_ERR_INVALID_ARG;
+  const size_t plane = (size_t)H * D;  // elements of one of Q, K, V of one token
+  ea::BwdArgs a{};
+  a.q = qkv;
+  a.k = static_cast<const uint16_t*>(qkv) + plane;
+  a.v = static_cast<const uint16_t*>(qkv) + 2 * plane;
+  a.o = o;
+  a.lse = lse;
+  a.dout = dout;
+  a.dq = dqkv;
+  a.dk = static_cast<uint16_t*>(dqkv) + plane;
+  a.dv = static_cast<uint16_t*>(dqkv) + 2 * plane;
+  a.B = B;
+  a.Hq = H;
+  a.Hkv = H;
+  a.D = D;
+  a.causal = causal != 0;
+  a.scale = scale;
+  a.bf16 = dtype == ATTN_BF16;
+  a.cu_q = nullptr;  // sequence b starts at token b * S
+  a.cu_k = nullptr;
+  a.total_q = B * S;
+  a.total_k = B * S;
+  a.q_rstride = a.k_rstride = a.dq_rstride = a.dk_rstride = 3 * (long long)plane;
+  a.do_rstride = (long long)plane;
+  return run_bwd_tm(a, S, S, window_left, window_right, stream);
 }
 
 int attn_decode_chunk(int max_S, int num_splits) { return chunk_for(max_S, num_splits); }

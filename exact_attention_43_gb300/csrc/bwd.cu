@@ -61,7 +61,48 @@ struct Params {
   float scale;
   uint64_t wait_limit_ns;
   int debug_fault;  // 3: dK/dV CTA (0, 0, 0) withholds the Q/dO loads of its iteration 1
+  // visible keys: key j to query i iff j <= i + d + win_right (win_right >= 0) and
+  // j >= i + d - win_left (win_left >= 0), d = (keys) - (queries); causal is win_right 0
+  int win_left, win_right;
+  // token-major layouts (attn_bwd_varlen, attn_bwd_qkvpacked; the VL kernels): q, o, dO
+  // and dq are [tokens, Hq, D], k, v, dk, dv [tokens, Hkv, D] with the row strides
+  // below (elements); sequence b's queries are tokens [cu_q[b], cu_q[b+1]) and its
+  // keys [cu_k[b], cu_k[b+1]), or b * Sq and b * Skv onwards when cu_q is null; Sq and
+  // Skv are then the longest lengths.  LSE and the row terms are [Hq, total_q].
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int total_q, total_k;
+  long long dq_rstride, dk_rstride;
 };
+
+// Query and key tokens of one sequence (the token-major layouts), or the dense
+// layout's one sequence per (batch, head) plane.
+struct Seq {
+  int q0, nq;  // first query token, query count
+  int k0, nk;  // first key token, key count
+};
+
+// Offsets outside the arrays, decreasing offsets and lengths above the longest
+// length are clamped (no access leaves the arrays) and reported in the status word.
+template <bool VL>
+__device__ __forceinline__ Seq seq_of(const Params& p, int b) {
+  Seq s;
+  if (!VL || !p.cu_q) {
+    s.q0 = VL ? b * p.Sq : 0;
+    s.nq = p.Sq;
+    s.k0 = VL ? b * p.Skv : 0;
+    s.nk = p.Skv;
+    return s;
+  }
+  const int a = p.cu_q[b], e = p.cu_q[b + 1], c = p.cu_k[b], f = p.cu_k[b + 1];
+  s.q0 = min(max(a, 0), p.total_q);
+  s.nq = min(min(max(e, s.q0), p.total_q) - s.q0, p.Sq);
+  s.k0 = min(max(c, 0), p.total_k);
+  s.nk = min(min(max(f, s.k0), p.total_k) - s.k0, p.Skv);
+  if ((s.q0 != a || s.nq != e - a || s.k0 != c || s.nk != f - c) && threadIdx.x == 0)
+    atomicOr(&g_status, kStatusSeqLenClamped);
+  return s;
+}
 
 // dK/dV kernel shared memory: K, V, two Q and two dO buffers, the row vectors.
 template <int D>
@@ -129,10 +170,13 @@ __device__ __forceinline__ uint4 pack8(const uint32_t* r, float f) {
                     pack2<BF16>(__uint_as_float(r[6]) * f, __uint_as_float(r[7]) * f));
 }
 
-// delta_i = sum_d dO_id O_id, one warp per row.
+// delta_i = sum_d dO_id O_id, one warp per row (rows of D contiguous elements).  With
+// hq_tm > 0 the rows are token-major ([tokens, hq_tm, D]) and the result goes to the
+// [Hq, total_q] layout of the LSE; otherwise to row order.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_delta_kernel(const uint16_t* o, const uint16_t* dout,
-                                                        float* delta, long long rows) {
+                                                        float* delta, long long rows, int hq_tm,
+                                                        long long total_q) {
   constexpr int EPL = D / 32;  // elements per lane
   const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (row >= rows) return;
@@ -149,7 +193,7 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const uint16_t* o, const
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-  if (lane == 0) delta[row] = s;
+  if (lane == 0) delta[hq_tm > 0 ? (row % hq_tm) * total_q + row / hq_tm : row] = s;
 }
 
 // S-like product D[tmem] = A B^T over the head dimension, both operands K-major
@@ -181,7 +225,7 @@ __device__ __forceinline__ void mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uin
 }
 
 // ============================================================================ dK, dV
-template <int D, bool BF16>
+template <int D, bool BF16, bool VL>
 __global__ void __launch_bounds__(THREADS, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
@@ -203,14 +247,15 @@ __global__ void __launch_bounds__(THREADS, 1)
   // slowest instead, so those long CTAs start first.
   const int n0 = (p.kv_slowest ? blockIdx.z : blockIdx.x) * BN;
   const int hk = p.kv_slowest ? blockIdx.x : blockIdx.y, b = p.kv_slowest ? blockIdx.y : blockIdx.z;
-  const int dlen = p.Skv - p.Sq;  // key j is visible to query i iff j <= i + dlen (causal)
-  const int n_mt = (p.Sq + BM - 1) / BM;
-  int m_lo = 0;  // first Q tile with a row that sees a key of this tile
-  if (p.causal) {
-    const long long lo = (long long)n0 - dlen - (BM - 1);
-    m_lo = lo <= 0 ? 0 : (int)min((lo + BM - 1) / BM, (long long)n_mt);
-  }
-  const int per_head = n_mt - m_lo;
+  const Seq sq = seq_of<VL>(p, b);
+  if (n0 >= sq.nk) return;  // past the sequence's keys (packed batches): nothing to do
+  const int dlen = sq.nk - sq.nq;  // the bottom-right alignment of the mask
+  // the queries [i_min, i_max] that see a key of this tile, in Q tiles m_lo ...
+  int i_min = 0, i_max = sq.nq - 1;
+  if (p.win_right >= 0) i_min = max(0, n0 - dlen - p.win_right);
+  if (p.win_left >= 0) i_max = min(i_max, n0 + BN - 1 - dlen + p.win_left);
+  const int m_lo = i_min / BM;
+  const int per_head = i_min <= i_max ? i_max / BM + 1 - m_lo : 0;
   const int n_iter = p.group * per_head;  // (query head, Q tile) pairs of this CTA
 
   if (threadIdx.x == 0) {
@@ -252,11 +297,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       prefetch_tmap(&tmdo);
       const uint64_t pol_kv = policy_evict_first();
       const uint64_t pol_q = policy_evict_last();
-      const int kv_z = b * p.Hkv + hk;
+      const int kv_y = VL ? sq.k0 + n0 : n0, kv_z = VL ? hk : b * p.Hkv + hk;
       mbar_expect_tx(bar(L::KV_FULL), 2 * L::TILE);
       for (int rr = 0; rr < L::NREG; ++rr) {
-        tma_load_3d(sb + L::K_OFF + rr * L::REGION, &tmk, bar(L::KV_FULL), rr * 64, n0, kv_z, pol_kv);
-        tma_load_3d(sb + L::V_OFF + rr * L::REGION, &tmv, bar(L::KV_FULL), rr * 64, n0, kv_z, pol_kv);
+        tma_load_3d(sb + L::K_OFF + rr * L::REGION, &tmk, bar(L::KV_FULL), rr * 64, kv_y, kv_z, pol_kv);
+        tma_load_3d(sb + L::V_OFF + rr * L::REGION, &tmv, bar(L::KV_FULL), rr * 64, kv_y, kv_z, pol_kv);
       }
       // bounded-wait test: one CTA never issues iteration 1's loads, so the waits run out
       const int withheld =
@@ -267,13 +312,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       int n_do = 0, n_q = 0;  // the dO and Q loads of iterations [0, n_do), [0, n_q) are issued
       for (int i = 0; i < n_iter && ok; ++i) {
         const int bi = i & 1, h = hk * p.group + i / per_head, m = m_lo + i % per_head;
+        const int q_y = VL ? sq.q0 + m * BM : m * BM, q_z = VL ? h : b * p.Hq + h;
         if (i >= 2 && !(ok = mbar_wait<false>(bar(L::DO_FREE + bi), ((i - 2) >> 1) & 1, abort_flag, &g_status, lim)))
           break;
         if (i != withheld) {
           mbar_expect_tx(bar(L::DO_FULL + bi), L::TILE);
           for (int rr = 0; rr < L::NREG; ++rr)
             tma_load_3d(sb + L::DO_OFF + bi * L::TILE + rr * L::REGION, &tmdo, bar(L::DO_FULL + bi),
-                        rr * 64, m * BM, b * p.Hq + h, pol_q);
+                        rr * 64, q_y, q_z, pol_q);
         }
         n_do = i + 1;
         if (i >= 2 && !(ok = mbar_wait<false>(bar(L::Q_FREE + bi), ((i - 2) >> 1) & 1, abort_flag, &g_status, lim)))
@@ -282,7 +328,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_expect_tx(bar(L::Q_FULL + bi), L::TILE);
           for (int rr = 0; rr < L::NREG; ++rr)
             tma_load_3d(sb + L::Q_OFF + bi * L::TILE + rr * L::REGION, &tmq, bar(L::Q_FULL + bi),
-                        rr * 64, m * BM, b * p.Hq + h, pol_q);
+                        rr * 64, q_y, q_z, pol_q);
         }
         n_q = i + 1;
       }
@@ -367,8 +413,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     // iteration ahead so its latency hides behind the current one
     auto row_value = [&](int i) -> float {
       const int hi = hk * p.group + i / per_head, qi = (m_lo + i % per_head) * BM + r;
-      if (qi >= p.Sq) return half == 0 ? INFINITY : 0.f;
-      const size_t idx = ((size_t)b * p.Hq + hi) * p.Sq + qi;
+      if (qi >= sq.nq) return half == 0 ? INFINITY : 0.f;
+      const size_t idx = VL ? (size_t)hi * p.total_q + sq.q0 + qi : ((size_t)b * p.Hq + hi) * p.Sq + qi;
       return half == 0 ? p.lse[idx] * 1.4426950408889634f : p.delta[idx];
     };
     float next_v = n_iter > 0 ? row_value(0) : 0.f;
@@ -393,9 +439,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_ld32(lane_t + C_S + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
         uint32_t pk[32];
         // query columns [lo, hi) of this thread's 64 see key n0 + r; a tile whose every
-        // query sees every key (all but the causal diagonal and the ragged ends) needs no test
-        const int lo = p.causal ? key - dlen - m0 - c0 : 0;
-        const int hi = key < p.Skv ? p.Sq - m0 - c0 : 0;
+        // query sees every key (all but the window's edges and the ragged ends) needs no test
+        const int lo = p.win_right >= 0 ? key - dlen - p.win_right - m0 - c0 : 0;
+        int hi = key < sq.nk ? sq.nq - m0 - c0 : 0;
+        if (p.win_left >= 0) hi = min(hi, key - dlen + p.win_left - m0 - c0 + 1);
         if (__all_sync(0xffffffffu, lo <= 0 && hi >= 64)) {
 #pragma unroll
           for (int j = 0; j < 64; ++j) pv[j] = ex2(fmaf(__uint_as_float(sr[j]), p.c2, -v_lse[c0 + j]));
@@ -436,16 +483,18 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const float f = half == 0 ? 1.f : p.scale;
       uint16_t* grad = half == 0 ? p.dv : p.dk;
-      uint4* row = reinterpret_cast<uint4*>(grad + (((size_t)b * p.Hkv + hk) * p.Skv + key) * D);
+      uint4* row = reinterpret_cast<uint4*>(
+          VL ? grad + (size_t)(sq.k0 + key) * p.dk_rstride + (size_t)hk * D
+             : grad + (((size_t)b * p.Hkv + hk) * p.Skv + key) * D);
       if (n_iter == 0) {
-        if (key < p.Skv)
+        if (key < sq.nk)
           for (int i = 0; i < D / 8; ++i) row[i] = make_uint4(0, 0, 0, 0);
       } else {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t v[32];
           tmem_ld32(lane_t + (half == 0 ? C_DV : C_DK) + 32 * c, v);
-          if (key < p.Skv) {
+          if (key < sq.nk) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) row[4 * c + i] = pack8<BF16>(v + 8 * i, f);
           }
@@ -463,7 +512,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // ============================================================================ dQ
-template <int D, bool BF16>
+template <int D, bool BF16, bool VL>
 __global__ void __launch_bounds__(THREADS, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
@@ -481,15 +530,19 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   // CTA (m tile, query head, batch); the causal tiles with the most keys run first
   const int n_mt = (p.Sq + BM - 1) / BM;
-  const int m0 = (p.causal ? n_mt - 1 - (int)blockIdx.x : (int)blockIdx.x) * BM;
+  const int m0 = (p.win_right >= 0 ? n_mt - 1 - (int)blockIdx.x : (int)blockIdx.x) * BM;
   const int h = blockIdx.y, b = blockIdx.z;
   const int hk = h / p.group;
-  const int dlen = p.Skv - p.Sq;
-  int n_kv = (p.Skv + BN - 1) / BN;  // K/V tiles this Q tile sees
-  if (p.causal) {
-    const long long last = min((long long)p.Skv - 1, (long long)min(m0 + BM, p.Sq) - 1 + dlen);
-    n_kv = last < 0 ? 0 : (int)(last / BN + 1);
-  }
+  const Seq sq = seq_of<VL>(p, b);
+  if (m0 >= sq.nq) return;  // past the sequence's queries (packed batches): nothing to do
+  const int dlen = sq.nk - sq.nq;
+  // the keys [k_lo, k_hi] some row of this tile sees, K/V tiles t_lo ... t_lo + n_kv - 1
+  const int last_row = min(m0 + BM, sq.nq) - 1;
+  int k_lo = 0, k_hi = sq.nk - 1;
+  if (p.win_right >= 0) k_hi = min(k_hi, last_row + dlen + p.win_right);
+  if (p.win_left >= 0) k_lo = max(0, m0 + dlen - p.win_left);
+  const int t_lo = k_lo / BN;
+  const int n_kv = k_lo <= k_hi ? k_hi / BN + 1 - t_lo : 0;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::QD_FULL), 1);
@@ -528,12 +581,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint64_t pol_q = policy_evict_first();
       const uint64_t pol_kv = policy_evict_last();
       mbar_expect_tx(bar(L::QD_FULL), 2 * L::TILE);
+      const int q_y = VL ? sq.q0 + m0 : m0, q_z = VL ? h : b * p.Hq + h;
       for (int rr = 0; rr < L::NREG; ++rr) {
-        tma_load_3d(sb + L::Q_OFF + rr * L::REGION, &tmq, bar(L::QD_FULL), rr * 64, m0, b * p.Hq + h, pol_q);
-        tma_load_3d(sb + L::DO_OFF + rr * L::REGION, &tmdo, bar(L::QD_FULL), rr * 64, m0, b * p.Hq + h,
-                    pol_q);
+        tma_load_3d(sb + L::Q_OFF + rr * L::REGION, &tmq, bar(L::QD_FULL), rr * 64, q_y, q_z, pol_q);
+        tma_load_3d(sb + L::DO_OFF + rr * L::REGION, &tmdo, bar(L::QD_FULL), rr * 64, q_y, q_z, pol_q);
       }
-      const int kv_z = b * p.Hkv + hk;
+      const int kv_y0 = (VL ? sq.k0 : 0) + t_lo * BN, kv_z = VL ? hk : b * p.Hkv + hk;
       bool ok = true;
       int ld = 0;
       for (; ld < 2 * n_kv && ok; ++ld) {  // K_0, V_0, K_1, V_1, ...
@@ -545,7 +598,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const CUtensorMap* tm = (ld & 1) ? &tmv : &tmk;
         for (int rr = 0; rr < L::NREG; ++rr)
           tma_load_3d(sb + L::RING_OFF + s * L::TILE + rr * L::REGION, tm, bar(L::RING_FULL + s), rr * 64,
-                      (ld >> 1) * BN, kv_z, pol_kv);
+                      kv_y0 + (ld >> 1) * BN, kv_z, pol_kv);
       }
       drain_wait(bar(L::QD_FULL), 0, lim);
       for (int l = max(0, ld - NS); l < ld; ++l) drain_wait(bar(L::RING_FULL + l % NS), (l / NS) & 1, lim);
@@ -611,10 +664,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t lane_t = tmem + ((uint32_t)(quarter * 32) << 16);
     const int row = m0 + r;
     const int c0 = half * 64;  // this thread's 64 of a K/V tile's 128 keys
-    const size_t ridx = ((size_t)b * p.Hq + h) * p.Sq + row;
-    const float lse2 = row < p.Sq ? p.lse[ridx] * 1.4426950408889634f : INFINITY;
-    const float dlt = row < p.Sq ? p.delta[ridx] : 0.f;
-    const int last_key = p.causal ? row + dlen : p.Skv - 1;  // keys of this row: [0, last_key]
+    const bool live = row < sq.nq;
+    const size_t ridx = VL ? (size_t)h * p.total_q + sq.q0 + row : ((size_t)b * p.Hq + h) * p.Sq + row;
+    const float lse2 = live ? p.lse[ridx] * 1.4426950408889634f : INFINITY;
+    const float dlt = live ? p.delta[ridx] : 0.f;
+    // keys of this row: [key_lo, key_hi] (none for rows past the sequence)
+    int key_lo = 0, key_hi = live ? sq.nk - 1 : -1;
+    if (p.win_right >= 0) key_hi = min(key_hi, row + dlen + p.win_right);
+    if (p.win_left >= 0) key_lo = row + dlen - p.win_left;
     auto wait_warp = [&](uint32_t b_, uint32_t ph_) -> bool {
       return __all_sync(0xffffffffu, mbar_wait<false>(b_, ph_, abort_flag, &g_status, lim));
     };
@@ -631,13 +688,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       tmem_ld32(lane_t + C_DP + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(dr + 32));
       tc_fence_before();
       mbar_arrive(bar(L::DP_FREE));  // dP(j + 1) may overwrite dP(j)
-      // keys j BN + c0 + u, u < vis, are visible to this row (none for rows past Sq)
-      const int vis = row < p.Sq ? min(last_key + 1, p.Skv) - (j * BN + c0) : 0;
+      // keys kb + u, ulo <= u < uhi, are visible to this row
+      const int kb = (t_lo + j) * BN + c0, ulo = key_lo - kb, uhi = key_hi + 1 - kb;
       uint32_t pk[32];
 #pragma unroll
       for (int u = 0; u < 32; ++u) {
-        const float p0 = 2 * u < vis ? ex2(fmaf(__uint_as_float(sr[2 * u]), p.c2, -lse2)) : 0.f;
-        const float p1 = 2 * u + 1 < vis ? ex2(fmaf(__uint_as_float(sr[2 * u + 1]), p.c2, -lse2)) : 0.f;
+        const float p0 = (2 * u >= ulo && 2 * u < uhi) ? ex2(fmaf(__uint_as_float(sr[2 * u]), p.c2, -lse2)) : 0.f;
+        const float p1 = (2 * u + 1 >= ulo && 2 * u + 1 < uhi)
+                             ? ex2(fmaf(__uint_as_float(sr[2 * u + 1]), p.c2, -lse2)) : 0.f;
         pk[u] = pack2<BF16>(p0 * (__uint_as_float(dr[2 * u]) - dlt), p1 * (__uint_as_float(dr[2 * u + 1]) - dlt));
       }
       tmem_st32(t_s + c0, pk);  // dS over the S columns this thread read
@@ -648,7 +706,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     // dQ = scale * (dS K) summed over the K/V tiles; rows that see no key get 0
     if (ok && (n_kv == 0 || wait_warp(bar(L::DONE), 0))) {
       tc_fence_after();
-      uint4* dst = reinterpret_cast<uint4*>(p.dq + ridx * D + half * (D / 2));
+      uint4* dst = reinterpret_cast<uint4*>(
+          (VL ? p.dq + (size_t)(sq.q0 + row) * p.dq_rstride + (size_t)h * D : p.dq + ridx * D) + half * (D / 2));
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
         uint32_t v[32];
@@ -658,7 +717,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0u;
         }
-        if (row < p.Sq) {
+        if (live) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) dst[4 * c + i] = pack8<BF16>(v + 8 * i, p.scale);
         }
@@ -674,11 +733,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-static bool make_map(CUtensorMap* map, const void* base, int D, int S, long long planes, bool bf16) {
+// 3-D tensor map over 16-bit elements: D contiguous, then n1 rows s1 elements apart,
+// then n2 planes s2 elements apart; 64 x 128 x 1 boxes, 128-byte swizzle.
+static bool make_map(CUtensorMap* map, const void* base, int D, long long n1, long long n2, long long s1,
+                     long long s2, bool bf16) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return false;
-  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)planes};
-  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)S * D * 2};
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)n1, (cuuint64_t)n2};
+  const cuuint64_t strides[2] = {(cuuint64_t)s1 * 2, (cuuint64_t)s2 * 2};
   const cuuint32_t box[3] = {64, 128, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
@@ -687,25 +749,43 @@ static bool make_map(CUtensorMap* map, const void* base, int D, int S, long long
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool VL>
 static cudaError_t launch_t(const BwdArgs& a, cudaStream_t stream) {
-  const long long rows = (long long)a.B * a.Hq * a.Sq;
+  // row terms: one per (query token, head) in either layout
+  const long long rows = VL ? (long long)a.total_q * a.Hq : (long long)a.B * a.Hq * a.Sq;
   if (rows > 0) {
     bwd_delta_kernel<D, BF16><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
-        static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.delta, rows);
+        static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.delta, rows,
+        VL ? a.Hq : 0, (long long)a.total_q);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  // with no query rows the Q/dO maps cover one (never read) row of k
-  const int sq_map = a.Sq > 0 ? a.Sq : 1;
-  const void* qb = a.Sq > 0 ? a.q : a.k;
-  const void* gb = a.Sq > 0 ? a.dout : a.k;
   CUtensorMap tq, tk, tv, tg;
-  if (!make_map(&tq, qb, D, sq_map, a.Sq > 0 ? (long long)a.B * a.Hq : 1, BF16) ||
-      !make_map(&tg, gb, D, sq_map, a.Sq > 0 ? (long long)a.B * a.Hq : 1, BF16) ||
-      !make_map(&tk, a.k, D, a.Skv, (long long)a.B * a.Hkv, BF16) ||
-      !make_map(&tv, a.v, D, a.Skv, (long long)a.B * a.Hkv, BF16))
-    return cudaErrorInvalidValue;
+  if (VL) {
+    // [tokens, heads, D] with the given token strides; with no keys (or no queries) a
+    // map covers one never-read row of an array that has one
+    const bool nk = a.total_k > 0, nq = a.total_q > 0;
+    const void* qb = nq ? a.q : a.k;
+    const void* gb = nq ? a.dout : a.k;
+    const void* kb = nk ? a.k : a.q;
+    const void* vb = nk ? a.v : a.q;
+    if (!make_map(&tq, qb, D, nq ? a.total_q : 1, nq ? a.Hq : 1, nq ? a.q_rstride : a.k_rstride, D, BF16) ||
+        !make_map(&tg, gb, D, nq ? a.total_q : 1, nq ? a.Hq : 1, nq ? a.do_rstride : a.k_rstride, D, BF16) ||
+        !make_map(&tk, kb, D, nk ? a.total_k : 1, nk ? a.Hkv : 1, nk ? a.k_rstride : a.q_rstride, D, BF16) ||
+        !make_map(&tv, vb, D, nk ? a.total_k : 1, nk ? a.Hkv : 1, nk ? a.k_rstride : a.q_rstride, D, BF16))
+      return cudaErrorInvalidValue;
+  } else {
+    // with no query rows the Q/dO maps cover one (never read) row of k
+    const int sq_map = a.Sq > 0 ? a.Sq : 1;
+    const void* qb = a.Sq > 0 ? a.q : a.k;
+    const void* gb = a.Sq > 0 ? a.dout : a.k;
+    const long long qp = a.Sq > 0 ? (long long)a.B * a.Hq : 1;
+    if (!make_map(&tq, qb, D, sq_map, qp, D, (long long)sq_map * D, BF16) ||
+        !make_map(&tg, gb, D, sq_map, qp, D, (long long)sq_map * D, BF16) ||
+        !make_map(&tk, a.k, D, a.Skv, (long long)a.B * a.Hkv, D, (long long)a.Skv * D, BF16) ||
+        !make_map(&tv, a.v, D, a.Skv, (long long)a.B * a.Hkv, D, (long long)a.Skv * D, BF16))
+      return cudaErrorInvalidValue;
+  }
   Params p{};
   p.lse = a.lse;
   p.delta = a.delta;
@@ -723,37 +803,48 @@ static cudaError_t launch_t(const BwdArgs& a, cudaStream_t stream) {
   p.c2 = a.scale * 1.4426950408889634f;
   p.wait_limit_ns = a.wait_limit_ns;
   p.debug_fault = a.debug_fault;
+  p.win_left = a.win_left;
+  p.win_right = a.causal ? 0 : a.win_right;
+  p.cu_q = a.cu_q;
+  p.cu_k = a.cu_k;
+  p.total_q = a.total_q;
+  p.total_k = a.total_k;
+  p.dq_rstride = a.dq_rstride;
+  p.dk_rstride = a.dk_rstride;
   const long long n_kt = (a.Skv + BN - 1) / BN, n_mt = (a.Sq + BM - 1) / BM;
-  if (a.Skv > 0) {
+  if (n_kt > 0) {
     using L = KVLayout<D>;
-    cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, BF16>,
+    cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, BF16, VL>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
-    // the longest CTA (key tile 0) against an SM's share of all (query head, Q tile)
-    // iterations: above a fifth, start the long CTAs first
-    long long total = 0;
-    for (long long t = 0; t < n_kt; ++t) {
-      long long m_lo = 0;
-      if (a.causal) {
-        const long long lo = t * BN - (a.Skv - a.Sq) - (BM - 1);
-        m_lo = lo <= 0 ? 0 : ((lo + BM - 1) / BM < n_mt ? (lo + BM - 1) / BM : n_mt);
+    p.kv_slowest = 0;
+    if (!VL && a.win_left < 0) {
+      // the longest CTA (key tile 0) against an SM's share of all (query head, Q tile)
+      // iterations: above a fifth, start the long CTAs first
+      long long total = 0;
+      for (long long t = 0; t < n_kt; ++t) {
+        long long m_lo = 0;
+        if (a.causal) {
+          const long long lo = t * BN - (a.Skv - a.Sq) - (BM - 1);
+          m_lo = lo <= 0 ? 0 : ((lo + BM - 1) / BM < n_mt ? (lo + BM - 1) / BM : n_mt);
+        }
+        total += n_mt - m_lo;
       }
-      total += n_mt - m_lo;
+      total *= (long long)a.B * a.Hq;
+      const long long longest = n_mt * (a.Hq / a.Hkv);
+      p.kv_slowest = longest * 5 * (a.num_sms > 0 ? a.num_sms : 1) > total ? 1 : 0;
     }
-    total *= (long long)a.B * a.Hq;
-    const long long longest = n_mt * (a.Hq / a.Hkv);
-    p.kv_slowest = longest * 5 * (a.num_sms > 0 ? a.num_sms : 1) > total ? 1 : 0;
     const dim3 grid = p.kv_slowest ? dim3(a.Hkv, a.B, (unsigned)n_kt) : dim3((unsigned)n_kt, a.Hkv, a.B);
-    bwd_dkdv_kernel<D, BF16><<<grid, THREADS, L::ALLOC, stream>>>(tq, tk, tv, tg, p);
+    bwd_dkdv_kernel<D, BF16, VL><<<grid, THREADS, L::ALLOC, stream>>>(tq, tk, tv, tg, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  if (rows > 0) {
+  if (n_mt > 0 && rows > 0) {
     using L = QLayout<D>;
-    cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<D, BF16>,
+    cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<D, BF16, VL>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
-    bwd_dq_kernel<D, BF16><<<dim3((unsigned)n_mt, a.Hq, a.B), THREADS, L::ALLOC, stream>>>(tq, tk, tv, tg, p);
+    bwd_dq_kernel<D, BF16, VL><<<dim3((unsigned)n_mt, a.Hq, a.B), THREADS, L::ALLOC, stream>>>(tq, tk, tv, tg, p);
     return cudaGetLastError();
   }
   return cudaSuccess;
@@ -762,8 +853,14 @@ static cudaError_t launch_t(const BwdArgs& a, cudaStream_t stream) {
 }  // namespace bwd
 
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
-  if (a.D == 64) return a.bf16 ? bwd::launch_t<64, true>(a, stream) : bwd::launch_t<64, false>(a, stream);
-  return a.bf16 ? bwd::launch_t<128, true>(a, stream) : bwd::launch_t<128, false>(a, stream);
+  if (a.vl) {
+    if (a.D == 64)
+      return a.bf16 ? bwd::launch_t<64, true, true>(a, stream) : bwd::launch_t<64, false, true>(a, stream);
+    return a.bf16 ? bwd::launch_t<128, true, true>(a, stream) : bwd::launch_t<128, false, true>(a, stream);
+  }
+  if (a.D == 64)
+    return a.bf16 ? bwd::launch_t<64, true, false>(a, stream) : bwd::launch_t<64, false, false>(a, stream);
+  return a.bf16 ? bwd::launch_t<128, true, false>(a, stream) : bwd::launch_t<128, false, false>(a, stream);
 }
 
 cudaError_t read_bwd_status(unsigned* out, cudaStream_t stream) {

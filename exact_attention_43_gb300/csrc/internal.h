@@ -74,6 +74,16 @@ struct BwdArgs {
   uint64_t wait_limit_ns;
   int num_sms;  // multiprocessors of the device (CTA ordering)
   int debug_fault;  // 3: CTA (0, 0, 0) withholds its second Q/dO tile pair (test only)
+  int win_left, win_right;  // sliding-window bounds, -1: none (causal: the right bound is 0)
+  // token-major layouts (attn_bwd_varlen, attn_bwd_qkvpacked): vl = 1; q, o, dout, dq are
+  // [tokens, Hq, D] and k, v, dk, dv [tokens, Hkv, D] with the token strides below
+  // (elements); sequence b's offsets come from cu_q / cu_k ([B + 1]), or are b * Sq /
+  // b * Skv when cu_q is null; Sq and Skv are the longest lengths; LSE is [Hq, total_q]
+  int vl;
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int total_q, total_k;
+  long long q_rstride, k_rstride, do_rstride, dq_rstride, dk_rstride;
 };
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,

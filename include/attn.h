@@ -143,8 +143,51 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
              const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq, int Skv,
              int D, int causal, float scale, int dtype, cudaStream_t stream);
 
-/* Bytes of workspace attn_bwd allocates for these sizes; 0 on invalid sizes. */
+/* Bytes of workspace attn_bwd allocates for these sizes; 0 on invalid sizes.  The
+ * token-major entry points below allocate the same for B = 1, Sq = total_q. */
 size_t attn_bwd_workspace_bytes(int B, int Hq, int Sq, int D);
+
+/*
+ * attn_bwd_varlen -- attn_bwd for attn_fwd_varlen: packed sequences of different
+ * lengths and sliding windows, in the token-major layout.
+ *
+ * The flash-attention backward page's kernel class takes the same `Varlen` and
+ * `Is_local` switches as the forward; the readings are attn_fwd_varlen's: each
+ * sequence's gradients are those of its own rows, with its own bottom-right
+ * alignment and the window's bounds.
+ *
+ * q, o, dout, dq   device, [total_q, Hq, D], dtype `dtype`, 16-byte aligned.
+ * k, v, dk, dv     device, [total_k, Hkv, D], 16-byte aligned.
+ * lse              device, [Hq, total_q] float32: attn_fwd_varlen's, for the same
+ *                  inputs, offsets, causal flag, window and scale (as is o).
+ * cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, causal, window_left,
+ * window_right, scale, D, dtype, B, Hq, Hkv: as in attn_fwd_varlen (offsets
+ * outside their ranges are clamped on the device and reported by
+ * attn_check_device_status as ATTN_ERR_INVALID_ARG).  Gradient rows of tokens
+ * outside every sequence are not written; a sequence's keys that no query sees
+ * get dK = dV = 0, its queries that see no key dQ = 0.  Every element of q, k, v
+ * and dout must be finite (a tile that ends inside a sequence also reads the
+ * next sequence's rows, with weight exactly 0).
+ */
+int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dout, void* dq, void* dk, void* dv, const int32_t* cu_seqlens_q,
+                    const int32_t* cu_seqlens_k, int B, int Hq, int Hkv, int total_q, int total_k,
+                    int max_seqlen_q, int max_seqlen_k, int D, int causal, int window_left,
+                    int window_right, float scale, int dtype, cudaStream_t stream);
+
+/*
+ * attn_bwd_qkvpacked -- attn_bwd for attn_fwd_qkvpacked: the gradient of one packed
+ * projection, written in place into the same layout.
+ *
+ * qkv    device, [B, S, 3, H, D] (attn_fwd_qkvpacked's input), 16-byte aligned.
+ * o      device, [B, S, H, D], lse [H, B, S] float32: attn_fwd_qkvpacked's outputs.
+ * dout   device, [B, S, H, D].
+ * dqkv   device, [B, S, 3, H, D]: dQ, dK, dV at the places of Q, K, V.
+ * causal, window_left, window_right, scale as in attn_fwd_qkvpacked.
+ */
+int attn_bwd_qkvpacked(const void* qkv, const void* o, const float* lse, const void* dout, void* dqkv,
+                       int B, int S, int H, int D, int causal, int window_left, int window_right,
+                       float scale, int dtype, cudaStream_t stream);
 
 /*
  * attn_decode -- flash-decoding: one query token per sequence against a KV cache.

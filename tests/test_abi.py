@@ -143,9 +143,42 @@ def test_backward_argument_errors(lib):
     assert bw(scale=float("nan")) == 1
     assert bw(D=32) == 2 and bw(dtype=7) == 2
     assert bw(B=0) == 0 and bw(Sq=0, Skv=0) == 0
-    # fp32 dQ accumulator and row terms, plus alignment slack
+    # fp32 row terms, plus alignment slack
     assert lib.attn_bwd_workspace_bytes(2, 8, 64, 128) == 2 * 8 * 64 * 4 + 256
     assert lib.attn_bwd_workspace_bytes(-1, 8, 64, 128) == 0
+
+
+def test_backward_token_major_argument_errors(lib):
+    def vb(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, do=FAKE, dq=FAKE, dk=FAKE, dv=FAKE,
+                 cq=FAKE, ck=FAKE, B=2, Hq=8, Hkv=2, tq=100, tk=120, mq=60, mk=70, D=128, causal=1,
+                 wl=-1, wr=-1, scale=0.1, dtype=0)
+        a.update(kw)
+        return lib.attn_bwd_varlen(a["q"], a["k"], a["v"], a["o"], a["lse"], a["do"], a["dq"],
+                                   a["dk"], a["dv"], a["cq"], a["ck"], a["B"], a["Hq"], a["Hkv"],
+                                   a["tq"], a["tk"], a["mq"], a["mk"], a["D"], a["causal"], a["wl"],
+                                   a["wr"], a["scale"], a["dtype"], None)
+
+    assert vb(cq=None) == 1 and vb(ck=None) == 1
+    assert vb(lse=None) == 1 and vb(dv=None) == 1
+    assert vb(dk=FAKE + 8) == 1 and vb(cq=FAKE + 2) == 1
+    assert vb(Hkv=3) == 1 and vb(wl=-2) == 1 and vb(tq=-1) == 1
+    assert vb(scale=float("inf")) == 1
+    assert vb(D=96) == 2 and vb(dtype=4) == 2
+    assert vb(B=0) == 0 and vb(tq=0, tk=0) == 0
+
+    def pk(**kw):
+        a = dict(qkv=FAKE, o=FAKE, lse=FAKE, do=FAKE, dqkv=FAKE, B=2, S=64, H=4, D=64, causal=1,
+                 wl=-1, wr=-1, scale=0.1, dtype=1)
+        a.update(kw)
+        return lib.attn_bwd_qkvpacked(a["qkv"], a["o"], a["lse"], a["do"], a["dqkv"], a["B"],
+                                      a["S"], a["H"], a["D"], a["causal"], a["wl"], a["wr"],
+                                      a["scale"], a["dtype"], None)
+
+    assert pk(dqkv=None) == 1 and pk(lse=None) == 1
+    assert pk(do=FAKE + 8) == 1 and pk(wr=-5) == 1
+    assert pk(D=80) == 2
+    assert pk(S=0) == 0
 
 
 def test_fused_decode_argument_errors(lib):
