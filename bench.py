@@ -26,7 +26,9 @@ Inputs are resident in HBM when the timed region starts; the e2e figure
 repeats the step from pinned host buffers with the copies inside its timed
 region: every prefill's Q, K, V, the decode queries, the valid prefix
 (seq_lens rows) of every (sequence, KV head) of the K and V caches, and
-seq_lens in; every O, LSE and the decode output back.
+seq_lens in; every O, LSE and the decode output back.  The backward (attn_bwd)
+of the three prefill workloads is timed after the step, in a loop of its own,
+and reported under "backward"; it is not part of the metric.
 """
 
 from __future__ import annotations
@@ -286,6 +288,8 @@ def main():
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=2, help="0 skips the end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--bwd-steps", type=int, default=5,
+                    help="timed backward steps after the main loop (0 skips them)")
     ap.add_argument("--clock-soak", type=float, default=1.5,
                     help="seconds of untimed steps before the warm-up, for clock sampling")
     args = ap.parse_args()
@@ -439,6 +443,45 @@ def main():
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": args.e2e_steps, "ms_per_step": 1e3 * e2e_s / args.e2e_steps}
 
+    # ------------------------------------------------ backward of the three prefill workloads
+    # (reported beside the step, timed in a loop of its own after it; not in the metric)
+    bwd_legs = None
+    if args.bwd_steps > 0:
+        grads = []
+        for name, w, q, k, v, o, lse in fwd_legs:
+            do_ = wl.normal(tuple(q.shape), seed=wl.SEED_BASE + 50 + w.index, dtype=q.dtype, device=dev)
+            grads.append((name, w, q, k, v, o, lse, do_, torch.empty_like(q), torch.empty_like(k),
+                          torch.empty_like(v)))
+
+        def run_bwd(g):
+            name, w, q, k, v, o, lse, do_, gq, gk, gv = g
+            ea.attn_bwd(q, k, v, o, lse, do_, causal=True, scale=w.scale, dq=gq, dk=gk, dv=gv,
+                        stream=stream)
+
+        for g in grads:
+            run_bwd(g)
+        torch.cuda.synchronize()
+        bev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(grads) + 1)]
+               for _ in range(args.bwd_steps)]
+        for i in range(args.bwd_steps):
+            bev[i][0].record(stream)
+            for j, g in enumerate(grads):
+                run_bwd(g)
+                bev[i][j + 1].record(stream)
+        torch.cuda.synchronize()
+        if ea.check_device_status() != 0:
+            raise RuntimeError("device status error in the backward loop")
+        bwd_legs = {}
+        for j, (name, w, *_r) in enumerate(grads):
+            t = statistics.mean(e[j].elapsed_time(e[j + 1]) for e in bev) / 1e3
+            fl = 2.5 * w.flops()  # dQ, dK, dV: five products per visible pair against the forward's two
+            bwd_legs[name.replace("fwd", "bwd")] = {
+                "ms": 1e3 * t, "tflops": fl / t / 1e12, "gflop": fl / 1e9,
+                "frac": fl / t / 1e12 / peaks["bf16_tflops"], "frac_of": "measured dense bf16 peak (burst)",
+                "note": "flops counted as 2.5x the forward's; the kernels execute 3.5x (dS, dP recomputed "
+                        "for dQ)"}
+        del grads
+
     rt = roofline_time(total_flops, dec_bytes, peaks)
     value = whole_job_value(rt, args.steps, world, total_s)
 
@@ -476,6 +519,7 @@ def main():
                        "l2": "inputs larger than L2 (the long prefill reads 0.8 GB and the decode "
                              "leg streams ~4.3 GB between the other legs)"},
             "legs": legs,
+            "backward": bwd_legs,
             # the dominant kernel: the prefill kernel over the step's three launches
             # (flops and DRAM bytes per launch averaged over them)
             "roofline": {"kernel": "attn_fwd_kernel<128, bf16> (MHA, GQA and long-context "
