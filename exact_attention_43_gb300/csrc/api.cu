@@ -279,18 +279,17 @@ int attn_fwd_qkvpacked(const void* qkv, void* o, float* lse, int B, int S, int H
 static int run_bwd(ea::BwdArgs& a, int dev, size_t rows, cudaStream_t stream) {
   int st;
   void* ws = nullptr;
-  if (rows > 0) {
-    cudaMemPool_t pool;
-    if ((st = pool_for(dev, &pool)) != ATTN_OK) return st;
-    cudaError_t e = cudaMallocFromPoolAsync(&ws, rows * sizeof(float) + 256, pool, stream);
-    if (e != cudaSuccess) return from_cuda(e);
-    a.delta = static_cast<float*>(ws);
-  }
-  cudaError_t e = ea::launch_bwd(a, stream);
-  if (ws) {
-    cudaError_t f = cudaFreeAsync(ws, stream);
-    if (e == cudaSuccess) e = f;
-  }
+  cudaMemPool_t pool;
+  if ((st = pool_for(dev, &pool)) != ATTN_OK) return st;
+  // the row terms, then (16-byte aligned) the two work-item counters
+  const size_t vec_bytes = (rows * sizeof(float) + 15) / 16 * 16;
+  cudaError_t e = cudaMallocFromPoolAsync(&ws, rows * sizeof(float) + 256, pool, stream);
+  if (e != cudaSuccess) return from_cuda(e);
+  a.delta = static_cast<float*>(ws);
+  a.work_counter = reinterpret_cast<int*>(static_cast<char*>(ws) + vec_bytes);
+  e = ea::launch_bwd(a, stream);
+  cudaError_t f = cudaFreeAsync(ws, stream);
+  if (e == cudaSuccess) e = f;
   if (e == cudaErrorInvalidValue && !ea::encode_tiled_fn()) return ATTN_ERR_UNSUPPORTED;
   return from_cuda(e);
 }
@@ -322,7 +321,7 @@ extern "C" {
 size_t attn_bwd_workspace_bytes(int B, int Hq, int Sq, int D) {
   if (B < 0 || Hq < 0 || Sq < 0 || D <= 0) return 0;
   const size_t rows = (size_t)B * Hq * Sq;
-  return rows * sizeof(float) + 256;  // row terms, alignment
+  return rows * sizeof(float) + 256;  // row terms, then (16-byte aligned) two work counters
 }
 
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,

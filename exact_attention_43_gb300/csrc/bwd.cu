@@ -46,7 +46,7 @@ constexpr int THREADS = 320;   // warps 0-7 compute, warp 8 loads, warp 9 issues
 constexpr int LOAD_WARP = 8;
 constexpr int MMA_WARP = 9;
 constexpr int NCOMP = 256;     // compute threads: warps w and w + 4 share TMEM lanes 32 (w mod 4) ...
-constexpr int NS = 4;          // dQ kernel: K/V ring stages
+constexpr int NS = 5;          // dQ kernel: K/V ring stages (two and a half K/V steps)
 constexpr uint32_t TMEM_COLS = 512;
 
 struct Params {
@@ -56,11 +56,13 @@ struct Params {
   uint16_t* dk;        // [B, Hkv, Skv, D]
   uint16_t* dv;
   int B, Hq, Hkv, Sq, Skv, group, causal;
-  int kv_slowest;  // dK/dV kernel: 1: grid (KV head, batch, key tile), 0: (key tile, KV head, batch)
+  int* work_counter;  // [0] dK/dV, [1] dQ work items claimed; zeroed before the launches
+  int per_group;      // dK/dV items: (batch, KV head) planes per scheduling group
+  int per_group_q;    // dQ items: (batch, query head) planes per scheduling group
   float c2;        // scale * log2(e)
   float scale;
   uint64_t wait_limit_ns;
-  int debug_fault;  // 3: dK/dV CTA (0, 0, 0) withholds the Q/dO loads of its iteration 1
+  int debug_fault;  // 3: the dK/dV CTA of work item 0 withholds that item's second Q/dO loads
   // visible keys: key j to query i iff j <= i + d + win_right (win_right >= 0) and
   // j >= i + d - win_left (win_left >= 0), d = (keys) - (queries); causal is win_right 0
   int win_left, win_right;
@@ -117,10 +119,12 @@ struct KVLayout {
   static constexpr int VEC_OFF = 6 * TILE;  // [2 buffers][LSE_2, delta][BM] of the Q tile
   static constexpr int BAR_OFF = VEC_OFF + 2 * 2 * BM * 4;
   enum {
-    KV_FULL, Q_FULL, DO_FULL = Q_FULL + 2, Q_FREE = DO_FULL + 2, DO_FREE = Q_FREE + 2,
-    S_READY = DO_FREE + 2, DP_READY, P_READY, DS_READY, VEC_READY, DONE, DRAIN, NUM_BARS
+    KV_FULL, KV_EMPTY, Q_FULL, DO_FULL = Q_FULL + 2, Q_FREE = DO_FULL + 2, DO_FREE = Q_FREE + 2,
+    S_READY = DO_FREE + 2, DP_READY, P_READY, DS_READY, VEC_READY, DONE, ACC_FREE, ITEM_FULL,
+    ITEM_EMPTY = ITEM_FULL + 2, DRAIN = ITEM_EMPTY + 2, NUM_BARS
   };
-  static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;  // [0] TMEM base, [1] abort flag
+  // [0] TMEM base, [1] abort flag, [2], [3] the two queued work items
+  static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int BYTES = MISC_OFF + 16;
   static constexpr int ALLOC = BYTES + 1024;  // slack to align the base to 1024 bytes
   static_assert(TILE % 1024 == 0, "swizzled tiles need 1024-byte alignment");
@@ -139,16 +143,98 @@ struct QLayout {
   static constexpr int RING_OFF = 2 * TILE;
   static constexpr int BAR_OFF = RING_OFF + NS * TILE;
   enum {
-    QD_FULL, RING_FULL, RING_EMPTY = RING_FULL + NS, S_READY = RING_EMPTY + NS, DP_READY,
-    DP_FREE, DS_READY, DONE, DRAIN, NUM_BARS
+    // S_READY + b, DS_READY + b: S, dS of a step in TMEM buffer b.  One barrier per
+    // buffer: S of the next step is issued before the compute warps wait for this one
+    // (at an item's start even two), and they may write dS of the next step before the
+    // issuer waits for this one; a barrier must never complete two phases ahead of a
+    // waiter, and the step after next needs a hand-off from the waiter first.
+    QD_FULL, QD_EMPTY, RING_FULL, RING_EMPTY = RING_FULL + NS, S_READY = RING_EMPTY + NS,
+    DP_READY = S_READY + 2, DP_FREE, DS_READY, DONE = DS_READY + 2, ACC_FREE, ITEM_FULL,
+    ITEM_EMPTY = ITEM_FULL + 2, DRAIN = ITEM_EMPTY + 2, NUM_BARS
   };
-  static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
+  static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;  // as KVLayout
   static constexpr int BYTES = MISC_OFF + 16;
   static constexpr int ALLOC = BYTES + 1024;
   static_assert(TILE % 1024 == 0, "swizzled tiles need 1024-byte alignment");
   static_assert(BAR_OFF % 8 == 0, "mbarriers need 8-byte alignment");
   static_assert(ALLOC <= 227 * 1024, "shared memory per CTA");
 };
+
+// Work item w -> (tile, head, batch).  Items are grouped by `per_group` consecutive
+// (batch, head) planes, chosen on the host so that the rows a group streams stay in
+// L2; inside a group the tiles go in the order the caller gives (the longest items
+// first), heads innermost.  Returns the tile's position in that order.
+__device__ __forceinline__ int decode_item(int w, int n_tiles, int planes, int per_group, int* plane) {
+  const int full = n_tiles * per_group;
+  const int gi = w / full;
+  const int g0 = gi * per_group;
+  const int size = min(per_group, planes - g0);
+  const int off = w - gi * full;
+  *plane = g0 + off % size;
+  return off / size;
+}
+
+// One key tile of one KV head (the dK/dV kernel's work item) and the (query head,
+// Q tile) iterations that see it.
+struct KVItem {
+  int n0, hk, b;
+  Seq sq;
+  int dlen;              // the bottom-right alignment of the mask
+  int m_lo, per_head;    // Q tiles m_lo ... m_lo + per_head - 1 of each query head
+  int n_iter;            // group * per_head
+  bool skip;             // past the sequence's keys: nothing to compute or write
+};
+
+template <bool VL>
+__device__ __forceinline__ KVItem kv_item(const Params& p, int n_kt, int w) {
+  KVItem it;
+  int hb;
+  it.n0 = decode_item(w, n_kt, p.B * p.Hkv, p.per_group, &hb) * BN;  // key tiles from the first
+  it.b = hb / p.Hkv;
+  it.hk = hb % p.Hkv;
+  it.sq = seq_of<VL>(p, it.b);
+  it.skip = it.n0 >= it.sq.nk;
+  it.dlen = it.sq.nk - it.sq.nq;
+  // the queries [i_min, i_max] that see a key of this tile
+  int i_min = 0, i_max = it.sq.nq - 1;
+  if (p.win_right >= 0) i_min = max(0, it.n0 - it.dlen - p.win_right);
+  if (p.win_left >= 0) i_max = min(i_max, it.n0 + BN - 1 - it.dlen + p.win_left);
+  it.m_lo = i_min / BM;
+  it.per_head = i_min <= i_max ? i_max / BM + 1 - it.m_lo : 0;
+  it.n_iter = it.skip ? 0 : p.group * it.per_head;
+  return it;
+}
+
+// One Q tile of one query head (the dQ kernel's work item) and the K/V tiles it sees.
+struct QItem {
+  int m0, h, b;
+  Seq sq;
+  int dlen;
+  int t_lo, n_kv;  // K/V tiles t_lo ... t_lo + n_kv - 1
+  bool skip;       // past the sequence's queries: nothing to compute or write
+};
+
+template <bool VL>
+__device__ __forceinline__ QItem q_item(const Params& p, int n_mt, int w) {
+  QItem it;
+  int hb;
+  const int mi = decode_item(w, n_mt, p.B * p.Hq, p.per_group_q, &hb);
+  // with a right bound (causal) the last Q tiles see the most keys: they go first
+  it.m0 = (p.win_right >= 0 ? n_mt - 1 - mi : mi) * BM;
+  it.b = hb / p.Hq;
+  it.h = hb % p.Hq;
+  it.sq = seq_of<VL>(p, it.b);
+  it.skip = it.m0 >= it.sq.nq;
+  it.dlen = it.sq.nk - it.sq.nq;
+  // the keys [k_lo, k_hi] some row of this tile sees
+  const int last_row = min(it.m0 + BM, it.sq.nq) - 1;
+  int k_lo = 0, k_hi = it.sq.nk - 1;
+  if (p.win_right >= 0) k_hi = min(k_hi, last_row + it.dlen + p.win_right);
+  if (p.win_left >= 0) k_lo = max(0, it.m0 + it.dlen - p.win_left);
+  it.t_lo = k_lo / BN;
+  it.n_kv = (!it.skip && k_lo <= k_hi) ? k_hi / BN + 1 - it.t_lo : 0;
+  return it;
+}
 
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return;
@@ -196,16 +282,28 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const uint16_t* o, const
   if (lane == 0) delta[hq_tm > 0 ? (row % hq_tm) * total_q + row / hq_tm : row] = s;
 }
 
+// Shared-memory descriptors of 128-byte-swizzled tiles as two 32-bit halves: the high
+// half (stride 1024 bytes, version, layout) is one constant, the low half holds the
+// start address and the leading byte offset (16 bytes for K-major operands, one
+// 64-column region for MN-major ones).  The issuing thread keeps one word per operand
+// and adds offsets to the 14-bit address field (addresses stay below 256 KB, so the
+// addition never carries out of it).
+__device__ __forceinline__ uint32_t desc_hi() { return (uint32_t)(sdesc_sw128(0, 16, 1024) >> 32); }
+__device__ __forceinline__ uint32_t desc_km(uint32_t saddr) { return (uint32_t)sdesc_sw128(saddr, 16, 1024); }
+__device__ __forceinline__ uint32_t desc_mn(uint32_t saddr) {
+  return (uint32_t)sdesc_sw128(saddr, 128 * 128, 1024);
+}
+
 // S-like product D[tmem] = A B^T over the head dimension, both operands K-major
 // 128 x D tiles in shared memory (16 columns = 32 bytes of a 128-byte swizzled row).
 template <int D, bool BF16>
-__device__ __forceinline__ void mma_kmajor(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc) {
+__device__ __forceinline__ void mma_kmajor(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi) {
   constexpr uint32_t idesc = umma_idesc_f16(BF16, 128, 128, false, false);
   constexpr int REGION = 128 * 128;
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = ((kk >> 2) * REGION + (kk & 3) * 32) >> 4;
-    umma_ss(d_tmem, a_desc + off, b_desc + off, idesc, kk > 0 ? 1u : 0u);
+    umma_ss_lo(d_tmem, a_lo + off, hi, b_lo + off, hi, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -216,15 +314,21 @@ __device__ __forceinline__ void mma_kmajor(uint32_t d_tmem, uint64_t a_desc, uin
 // columns they read (K-rows 0-63 at columns 0-31, K-rows 64-127 at 64-95), so
 // neither overwrites columns the other may still be loading.
 template <int D, bool BF16>
-__device__ __forceinline__ void mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, bool acc) {
+__device__ __forceinline__ void mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
+                                           bool acc) {
   constexpr uint32_t idesc = umma_idesc_f16(BF16, 128, D, false, true);
 #pragma unroll
   for (int kk = 0; kk < 128 / 16; ++kk)
-    umma_ts(d_tmem, a_tmem + kk * 8 + (kk >= 4 ? 32 : 0), b_desc + kk * 128, idesc,
-            (acc || kk > 0) ? 1u : 0u);
+    umma_ts_lo(d_tmem, a_tmem + kk * 8 + (kk >= 4 ? 32 : 0), b_lo + kk * 128, hi, idesc,
+               (acc || kk > 0) ? 1u : 0u);
 }
 
 // ============================================================================ dK, dV
+// Persistent: one CTA per SM claims work items (key tile, KV head, batch) from a
+// counter, longest first within each group of heads.  K and V of the next item load
+// as soon as the current item's last S^T and dP^T (their only readers) complete, its
+// first S^T and dP^T run while the compute warps store the current dK and dV, and its
+// first dV waits only for those warps to have read the accumulators.
 template <int D, bool BF16, bool VL>
 __global__ void __launch_bounds__(THREADS, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -238,33 +342,22 @@ __global__ void __launch_bounds__(THREADS, 1)
   auto bar = [&](int i) -> uint32_t { return sb + L::BAR_OFF + 8u * i; };
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+  volatile int* item_q = reinterpret_cast<volatile int*>(misc + 2);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t lim = p.wait_limit_ns;
-
-  // Key tiles vary fastest: CTAs that run at the same time share a few heads (their
-  // Q, dO rows stay in L2), and within a head the causal tiles that most Q tiles see
-  // start first.  When one CTA's work is a large share of an SM's, key tiles vary
-  // slowest instead, so those long CTAs start first.
-  const int n0 = (p.kv_slowest ? blockIdx.z : blockIdx.x) * BN;
-  const int hk = p.kv_slowest ? blockIdx.x : blockIdx.y, b = p.kv_slowest ? blockIdx.y : blockIdx.z;
-  const Seq sq = seq_of<VL>(p, b);
-  if (n0 >= sq.nk) return;  // past the sequence's keys (packed batches): nothing to do
-  const int dlen = sq.nk - sq.nq;  // the bottom-right alignment of the mask
-  // the queries [i_min, i_max] that see a key of this tile, in Q tiles m_lo ...
-  int i_min = 0, i_max = sq.nq - 1;
-  if (p.win_right >= 0) i_min = max(0, n0 - dlen - p.win_right);
-  if (p.win_left >= 0) i_max = min(i_max, n0 + BN - 1 - dlen + p.win_left);
-  const int m_lo = i_min / BM;
-  const int per_head = i_min <= i_max ? i_max / BM + 1 - m_lo : 0;
-  const int n_iter = p.group * per_head;  // (query head, Q tile) pairs of this CTA
+  const int n_kt = (p.Skv + BN - 1) / BN;
+  const int n_items = n_kt * p.Hkv * p.B;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::KV_FULL), 1);
+    mbar_init(bar(L::KV_EMPTY), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(L::Q_FULL + i), 1);
       mbar_init(bar(L::DO_FULL + i), 1);
       mbar_init(bar(L::Q_FREE + i), 1);
       mbar_init(bar(L::DO_FREE + i), 1);
+      mbar_init(bar(L::ITEM_FULL + i), 1);
+      mbar_init(bar(L::ITEM_EMPTY + i), 1 + NCOMP);  // the issuer and every compute thread
     }
     mbar_init(bar(L::S_READY), 1);
     mbar_init(bar(L::DP_READY), 1);
@@ -272,6 +365,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(bar(L::DS_READY), NCOMP);
     mbar_init(bar(L::VEC_READY), NCOMP);
     mbar_init(bar(L::DONE), 1);
+    mbar_init(bar(L::ACC_FREE), NCOMP);
     mbar_init(bar(L::DRAIN), 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -289,110 +383,152 @@ __global__ void __launch_bounds__(THREADS, 1)
   constexpr uint32_t C_S = 0, C_DP = 128, C_DV = 256, C_DK = 384;
 
   if (warp == LOAD_WARP) {
-    // ------------------------------------------------------------ loads (one thread)
-    if (lane == 0 && n_iter > 0) {
+    // ------------------------------------------------ work items and loads (one thread)
+    if (lane == 0) {
       prefetch_tmap(&tmq);
       prefetch_tmap(&tmk);
       prefetch_tmap(&tmv);
       prefetch_tmap(&tmdo);
       const uint64_t pol_kv = policy_evict_first();
       const uint64_t pol_q = policy_evict_last();
-      const int kv_y = VL ? sq.k0 + n0 : n0, kv_z = VL ? hk : b * p.Hkv + hk;
-      mbar_expect_tx(bar(L::KV_FULL), 2 * L::TILE);
-      for (int rr = 0; rr < L::NREG; ++rr) {
-        tma_load_3d(sb + L::K_OFF + rr * L::REGION, &tmk, bar(L::KV_FULL), rr * 64, kv_y, kv_z, pol_kv);
-        tma_load_3d(sb + L::V_OFF + rr * L::REGION, &tmv, bar(L::KV_FULL), rr * 64, kv_y, kv_z, pol_kv);
-      }
-      // bounded-wait test: one CTA never issues iteration 1's loads, so the waits run out
-      const int withheld =
-          (p.debug_fault == 3 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) ? 1 : -1;
-      // iteration i's Q and dO go to buffer i & 1, once iteration i - 2's last products
-      // that read them (dV for dO, dK for Q) have completed
+      // bounded-wait test: the CTA that claims work item 0 never issues the loads of that
+      // item's second iteration (global iteration held_g), so the waits run out
+      int held_g = -1;
       bool ok = true;
+      int g = 0;     // (query head, Q tile) iterations reached, over all items
+      int n_kv = 0;  // K/V tile pairs loaded
       int n_do = 0, n_q = 0;  // the dO and Q loads of iterations [0, n_do), [0, n_q) are issued
-      for (int i = 0; i < n_iter && ok; ++i) {
-        const int bi = i & 1, h = hk * p.group + i / per_head, m = m_lo + i % per_head;
-        const int q_y = VL ? sq.q0 + m * BM : m * BM, q_z = VL ? h : b * p.Hq + h;
-        if (i >= 2 && !(ok = mbar_wait<false>(bar(L::DO_FREE + bi), ((i - 2) >> 1) & 1, abort_flag, &g_status, lim)))
+      for (int r = 0; ok; ++r) {
+        const int slot = r & 1;
+        if (!(ok = mbar_wait<false>(bar(L::ITEM_EMPTY + slot), ((r >> 1) & 1) ^ 1, abort_flag, &g_status, lim)))
           break;
-        if (i != withheld) {
-          mbar_expect_tx(bar(L::DO_FULL + bi), L::TILE);
-          for (int rr = 0; rr < L::NREG; ++rr)
-            tma_load_3d(sb + L::DO_OFF + bi * L::TILE + rr * L::REGION, &tmdo, bar(L::DO_FULL + bi),
-                        rr * 64, q_y, q_z, pol_q);
-        }
-        n_do = i + 1;
-        if (i >= 2 && !(ok = mbar_wait<false>(bar(L::Q_FREE + bi), ((i - 2) >> 1) & 1, abort_flag, &g_status, lim)))
+        int w = atomicAdd(p.work_counter, 1);
+        if (w >= n_items) w = -1;
+        item_q[slot] = w;
+        mbar_arrive(bar(L::ITEM_FULL + slot));
+        if (w < 0) break;
+        const KVItem it = kv_item<VL>(p, n_kt, w);
+        if (it.n_iter == 0) continue;
+        // K and V, once the last item's final S^T and dP^T have completed
+        if (n_kv > 0 && !(ok = mbar_wait<false>(bar(L::KV_EMPTY), (n_kv - 1) & 1, abort_flag, &g_status, lim)))
           break;
-        if (i != withheld) {
-          mbar_expect_tx(bar(L::Q_FULL + bi), L::TILE);
-          for (int rr = 0; rr < L::NREG; ++rr)
-            tma_load_3d(sb + L::Q_OFF + bi * L::TILE + rr * L::REGION, &tmq, bar(L::Q_FULL + bi),
-                        rr * 64, q_y, q_z, pol_q);
+        const int kv_y = VL ? it.sq.k0 + it.n0 : it.n0, kv_z = VL ? it.hk : it.b * p.Hkv + it.hk;
+        mbar_expect_tx(bar(L::KV_FULL), 2 * L::TILE);
+        for (int rr = 0; rr < L::NREG; ++rr) {
+          tma_load_3d(sb + L::K_OFF + rr * L::REGION, &tmk, bar(L::KV_FULL), rr * 64, kv_y, kv_z, pol_kv);
+          tma_load_3d(sb + L::V_OFF + rr * L::REGION, &tmv, bar(L::KV_FULL), rr * 64, kv_y, kv_z, pol_kv);
         }
-        n_q = i + 1;
+        ++n_kv;
+        // iteration g's Q and dO go to buffer g & 1, once iteration g - 2's last products
+        // that read them (dV for dO, dK for Q) have completed
+        for (int i = 0; i < it.n_iter && ok; ++i, ++g) {
+          const int bi = g & 1, h = it.hk * p.group + i / it.per_head, m = it.m_lo + i % it.per_head;
+          const int q_y = VL ? it.sq.q0 + m * BM : m * BM, q_z = VL ? h : it.b * p.Hq + h;
+          const bool held = p.debug_fault == 3 && w == 0 && i == 1;
+          if (held) held_g = g;
+          if (g >= 2 &&
+              !(ok = mbar_wait<false>(bar(L::DO_FREE + bi), ((g - 2) >> 1) & 1, abort_flag, &g_status, lim)))
+            break;
+          if (!held) {
+            mbar_expect_tx(bar(L::DO_FULL + bi), L::TILE);
+            for (int rr = 0; rr < L::NREG; ++rr)
+              tma_load_3d(sb + L::DO_OFF + bi * L::TILE + rr * L::REGION, &tmdo, bar(L::DO_FULL + bi),
+                          rr * 64, q_y, q_z, pol_q);
+          }
+          n_do = g + 1;
+          if (g >= 2 &&
+              !(ok = mbar_wait<false>(bar(L::Q_FREE + bi), ((g - 2) >> 1) & 1, abort_flag, &g_status, lim)))
+            break;
+          if (!held) {
+            mbar_expect_tx(bar(L::Q_FULL + bi), L::TILE);
+            for (int rr = 0; rr < L::NREG; ++rr)
+              tma_load_3d(sb + L::Q_OFF + bi * L::TILE + rr * L::REGION, &tmq, bar(L::Q_FULL + bi),
+                          rr * 64, q_y, q_z, pol_q);
+          }
+          n_q = g + 1;
+        }
       }
-      // nothing may be in flight when the CTA exits: the last loads into each buffer
-      // (a withheld pair was never issued, and no later load of its buffer is reached)
-      drain_wait(bar(L::KV_FULL), 0, lim);
+      // nothing may be in flight when the CTA exits: the last load into each buffer (a
+      // buffer is reloaded only after its last load was consumed; a withheld pair was
+      // never issued, and no later load of its buffer is reached)
+      if (n_kv > 0) drain_wait(bar(L::KV_FULL), (n_kv - 1) & 1, lim);
       for (int i = max(0, n_do - 2); i < n_do; ++i)
-        if (i != withheld) drain_wait(bar(L::DO_FULL + (i & 1)), (i >> 1) & 1, lim);
+        if (i != held_g) drain_wait(bar(L::DO_FULL + (i & 1)), (i >> 1) & 1, lim);
       for (int i = max(0, n_q - 2); i < n_q; ++i)
-        if (i != withheld) drain_wait(bar(L::Q_FULL + (i & 1)), (i >> 1) & 1, lim);
+        if (i != held_g) drain_wait(bar(L::Q_FULL + (i & 1)), (i >> 1) & 1, lim);
     }
     __syncwarp();
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ MMAs (one thread)
-    if (lane == 0 && n_iter > 0) {
-      const uint64_t k_km = sdesc_sw128(sb + L::K_OFF, 16, 1024);
-      const uint64_t v_km = sdesc_sw128(sb + L::V_OFF, 16, 1024);
-      auto q_km = [&](int bi) { return sdesc_sw128(sb + L::Q_OFF + bi * L::TILE, 16, 1024); };
-      auto do_km = [&](int bi) { return sdesc_sw128(sb + L::DO_OFF + bi * L::TILE, 16, 1024); };
-      auto q_mn = [&](int bi) { return sdesc_sw128(sb + L::Q_OFF + bi * L::TILE, L::REGION, 1024); };
-      auto do_mn = [&](int bi) { return sdesc_sw128(sb + L::DO_OFF + bi * L::TILE, L::REGION, 1024); };
+    if (lane == 0) {
+      const uint32_t hi = desc_hi();
+      const uint32_t k_km = desc_km(sb + L::K_OFF), v_km = desc_km(sb + L::V_OFF);
+      const uint32_t q_km0 = desc_km(sb + L::Q_OFF), do_km0 = desc_km(sb + L::DO_OFF);
+      const uint32_t q_mn0 = desc_mn(sb + L::Q_OFF), do_mn0 = desc_mn(sb + L::DO_OFF);
+      constexpr uint32_t BUF = L::TILE >> 4;  // one Q or dO buffer in the address field
+      auto q_km = [&](int bi) { return q_km0 + bi * BUF; };
+      auto do_km = [&](int bi) { return do_km0 + bi * BUF; };
+      auto q_mn = [&](int bi) { return q_mn0 + bi * BUF; };
+      auto do_mn = [&](int bi) { return do_mn0 + bi * BUF; };
       auto wait = [&](int bar_i, int parity) -> bool {
         return mbar_wait<false>(bar(bar_i), parity & 1, abort_flag, &g_status, lim);
       };
-      // S^T(0), dP^T(0); then per iteration i: dV(i), S^T(i+1), dK(i), dP^T(i+1), so
-      // that the compute warps' P phase of i + 1 runs during dK(i), dP^T(i+1) and
-      // their dS phase of i during dV(i), S^T(i+1)
-      bool ok = wait(L::KV_FULL, 0) && wait(L::Q_FULL, 0);
-      if (ok) {
+      bool ok = true;
+      int g = 0;     // iterations issued, over all items
+      int n_it = 0;  // items with iterations
+      for (int r = 0; ok; ++r) {
+        const int slot = r & 1;
+        if (!(ok = wait(L::ITEM_FULL + slot, r >> 1))) break;
+        const int w = item_q[slot];
+        mbar_arrive(bar(L::ITEM_EMPTY + slot));
+        if (w < 0) break;
+        const int n = kv_item<VL>(p, n_kt, w).n_iter;
+        if (n == 0) continue;
+        // S^T(0), dP^T(0); then per iteration i: dV(i), S^T(i+1), dK(i), dP^T(i+1), so
+        // that the compute warps' P phase of i + 1 runs during dK(i), dP^T(i+1) and
+        // their dS phase of i during dV(i), S^T(i+1).  S^T(0) and dP^T(0) overwrite
+        // S^T and dP^T of the last item, read by its dV and dK, issued before them.
+        if (!(ok = wait(L::KV_FULL, n_it) && wait(L::Q_FULL + (g & 1), g >> 1))) break;
         tc_fence_after();
-        mma_kmajor<D, BF16>(tmem + C_S, k_km, q_km(0));
+        mma_kmajor<D, BF16>(tmem + C_S, k_km, q_km(g & 1), hi);
         umma_commit(bar(L::S_READY));
-        ok = wait(L::DO_FULL, 0);
-        if (ok) {
-          tc_fence_after();
-          mma_kmajor<D, BF16>(tmem + C_DP, v_km, do_km(0));
-          umma_commit(bar(L::DP_READY));
-        }
-      }
-      for (int i = 0; i < n_iter && ok; ++i) {
-        const int bi = i & 1, bn = bi ^ 1;
-        if (!(ok = wait(L::P_READY, i))) break;
+        if (!(ok = wait(L::DO_FULL + (g & 1), g >> 1))) break;
         tc_fence_after();
-        mma_tmem_a<D, BF16>(tmem + C_DV, tmem + C_S, do_mn(bi), i > 0);  // dV += P^T dO
-        umma_commit(bar(L::DO_FREE + bi));
-        if (i + 1 < n_iter) {
-          if (!(ok = wait(L::Q_FULL + bn, (i + 1) >> 1))) break;
+        mma_kmajor<D, BF16>(tmem + C_DP, v_km, do_km(g & 1), hi);
+        umma_commit(bar(L::DP_READY));
+        if (n == 1) umma_commit(bar(L::KV_EMPTY));  // the item's last readers of K and V
+        for (int i = 0; i < n && ok; ++i) {
+          const int gi = g + i, bi = gi & 1, bn = bi ^ 1;
+          if (!(ok = wait(L::P_READY, gi))) break;
+          // the item's first dV overwrites dV: the compute warps must have read the last one
+          if (i == 0 && n_it > 0 && !(ok = wait(L::ACC_FREE, n_it - 1))) break;
           tc_fence_after();
-          mma_kmajor<D, BF16>(tmem + C_S, k_km, q_km(bn));  // after dV read P^T there
-          umma_commit(bar(L::S_READY));
-        }
-        if (!(ok = wait(L::DS_READY, i))) break;
-        tc_fence_after();
-        mma_tmem_a<D, BF16>(tmem + C_DK, tmem + C_DP, q_mn(bi), i > 0);  // dK += dS^T Q
-        umma_commit(bar(L::Q_FREE + bi));
-        if (i + 1 < n_iter) {
-          if (!(ok = wait(L::DO_FULL + bn, (i + 1) >> 1))) break;
+          mma_tmem_a<D, BF16>(tmem + C_DV, tmem + C_S, do_mn(bi), hi, i > 0);  // dV += P^T dO
+          umma_commit(bar(L::DO_FREE + bi));
+          if (i + 1 < n) {
+            if (!(ok = wait(L::Q_FULL + bn, (gi + 1) >> 1))) break;
+            tc_fence_after();
+            mma_kmajor<D, BF16>(tmem + C_S, k_km, q_km(bn), hi);  // after dV read P^T there
+            umma_commit(bar(L::S_READY));
+          }
+          if (!(ok = wait(L::DS_READY, gi))) break;
           tc_fence_after();
-          mma_kmajor<D, BF16>(tmem + C_DP, v_km, do_km(bn));  // after dK read dS^T there
-          umma_commit(bar(L::DP_READY));
+          mma_tmem_a<D, BF16>(tmem + C_DK, tmem + C_DP, q_mn(bi), hi, i > 0);  // dK += dS^T Q
+          umma_commit(bar(L::Q_FREE + bi));
+          if (i + 1 < n) {
+            if (!(ok = wait(L::DO_FULL + bn, (gi + 1) >> 1))) break;
+            tc_fence_after();
+            mma_kmajor<D, BF16>(tmem + C_DP, v_km, do_km(bn), hi);  // after dK read dS^T there
+            umma_commit(bar(L::DP_READY));
+            if (i + 2 == n) umma_commit(bar(L::KV_EMPTY));
+          }
         }
+        if (!ok) break;
+        umma_commit(bar(L::DONE));  // this item's dK and dV are complete
+        g += n;
+        ++n_it;
       }
-      umma_commit(bar(L::DONE));  // dK and dV complete (also after an abort: a tracked commit)
-      umma_commit(bar(L::DRAIN));
+      umma_commit(bar(L::DRAIN));  // fires once every MMA issued above has completed
       drain_wait(bar(L::DRAIN), 0, lim);
     }
     __syncwarp();
@@ -404,102 +540,118 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int r = quarter * 32 + lane;
     const uint32_t lane_t = tmem + ((uint32_t)(quarter * 32) << 16);
     float* vec = reinterpret_cast<float*>(smem + L::VEC_OFF);  // [buffer][LSE_2, delta][BM]
-    const int key = n0 + r;
     const int c0 = half * 64;
     auto wait_warp = [&](uint32_t b_, uint32_t ph_) -> bool {
       return __all_sync(0xffffffffu, mbar_wait<false>(b_, ph_, abort_flag, &g_status, lim));
     };
-    // row r's LSE (half 0, log2 units) or delta (half 1) for iteration i, loaded one
-    // iteration ahead so its latency hides behind the current one
-    auto row_value = [&](int i) -> float {
-      const int hi = hk * p.group + i / per_head, qi = (m_lo + i % per_head) * BM + r;
-      if (qi >= sq.nq) return half == 0 ? INFINITY : 0.f;
-      const size_t idx = VL ? (size_t)hi * p.total_q + sq.q0 + qi : ((size_t)b * p.Hq + hi) * p.Sq + qi;
-      return half == 0 ? p.lse[idx] * 1.4426950408889634f : p.delta[idx];
-    };
-    float next_v = n_iter > 0 ? row_value(0) : 0.f;
     bool ok = true;
-    for (int it = 0; it < n_iter && ok; ++it) {
-      const int m0 = (m_lo + it % per_head) * BM;
-      // the row vectors of this Q tile, in buffer it & 1: every thread finished
-      // iteration it - 2's reads before it arrived on iteration it - 1's VEC_READY
-      float* v_lse = vec + (it & 1) * 2 * BM;
-      float* v_dl = v_lse + BM;
-      (half == 0 ? v_lse : v_dl)[r] = next_v;
-      mbar_arrive(bar(L::VEC_READY));
-      if (it + 1 < n_iter) next_v = row_value(it + 1);
-      if (!(ok = wait_warp(bar(L::VEC_READY), it & 1))) break;
-      // ---- P phase: P^T = 2^(S^T c - LSE_2) on the visible (key, query) pairs
-      if (!(ok = wait_warp(bar(L::S_READY), it & 1))) break;
-      tc_fence_after();
-      float pv[64];
-      {
-        uint32_t sr[64];
-        tmem_ld32(lane_t + C_S + c0, *reinterpret_cast<uint32_t(*)[32]>(sr));
-        tmem_ld32(lane_t + C_S + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
-        uint32_t pk[32];
-        // query columns [lo, hi) of this thread's 64 see key n0 + r; a tile whose every
-        // query sees every key (all but the window's edges and the ragged ends) needs no test
-        const int lo = p.win_right >= 0 ? key - dlen - p.win_right - m0 - c0 : 0;
-        int hi = key < sq.nk ? sq.nq - m0 - c0 : 0;
-        if (p.win_left >= 0) hi = min(hi, key - dlen + p.win_left - m0 - c0 + 1);
-        if (__all_sync(0xffffffffu, lo <= 0 && hi >= 64)) {
-#pragma unroll
-          for (int j = 0; j < 64; ++j) pv[j] = ex2(fmaf(__uint_as_float(sr[j]), p.c2, -v_lse[c0 + j]));
-        } else {
-#pragma unroll
-          for (int j = 0; j < 64; ++j)
-            pv[j] = (j >= lo && j < hi) ? ex2(fmaf(__uint_as_float(sr[j]), p.c2, -v_lse[c0 + j])) : 0.f;
-        }
-#pragma unroll
-        for (int j = 0; j < 32; ++j) pk[j] = pack2<BF16>(pv[2 * j], pv[2 * j + 1]);
-        tmem_st32(lane_t + C_S + c0, pk);  // P^T over the S^T columns this thread read
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(L::P_READY));
-      // ---- dS phase: dS^T = P^T (dP^T - delta)
-      if (!(ok = wait_warp(bar(L::DP_READY), it & 1))) break;
-      tc_fence_after();
-      {
-        uint32_t dr[64];
-        tmem_ld32(lane_t + C_DP + c0, *reinterpret_cast<uint32_t(*)[32]>(dr));
-        tmem_ld32(lane_t + C_DP + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(dr + 32));
-        uint32_t dk2[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float d0 = pv[2 * j] * (__uint_as_float(dr[2 * j]) - v_dl[c0 + 2 * j]);
-          const float d1 = pv[2 * j + 1] * (__uint_as_float(dr[2 * j + 1]) - v_dl[c0 + 2 * j + 1]);
-          dk2[j] = pack2<BF16>(d0, d1);
-        }
-        tmem_st32(lane_t + C_DP + c0, dk2);  // dS^T over the dP^T columns this thread read
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(L::DS_READY));
-    }
-    // this tile's dV rows (half 0) and dK rows (half 1); zero when no query sees the key
-    if (ok && (n_iter == 0 || wait_warp(bar(L::DONE), 0))) {
-      tc_fence_after();
+    int g = 0, n_it = 0;
+    for (int rq = 0; ok; ++rq) {
+      const int slot = rq & 1;
+      if (!(ok = wait_warp(bar(L::ITEM_FULL + slot), (rq >> 1) & 1))) break;
+      const int w = item_q[slot];
+      mbar_arrive(bar(L::ITEM_EMPTY + slot));
+      if (w < 0) break;
+      const KVItem it = kv_item<VL>(p, n_kt, w);
+      if (it.skip) continue;
+      const int key = it.n0 + r;
       const float f = half == 0 ? 1.f : p.scale;
       uint16_t* grad = half == 0 ? p.dv : p.dk;
-      uint4* row = reinterpret_cast<uint4*>(
-          VL ? grad + (size_t)(sq.k0 + key) * p.dk_rstride + (size_t)hk * D
-             : grad + (((size_t)b * p.Hkv + hk) * p.Skv + key) * D);
-      if (n_iter == 0) {
-        if (key < sq.nk)
-          for (int i = 0; i < D / 8; ++i) row[i] = make_uint4(0, 0, 0, 0);
-      } else {
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(lane_t + (half == 0 ? C_DV : C_DK) + 32 * c, v);
-          if (key < sq.nk) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) row[4 * c + i] = pack8<BF16>(v + 8 * i, f);
-          }
-        }
+      uint4* grow = reinterpret_cast<uint4*>(
+          VL ? grad + (size_t)(it.sq.k0 + key) * p.dk_rstride + (size_t)it.hk * D
+             : grad + (((size_t)it.b * p.Hkv + it.hk) * p.Skv + key) * D);
+      if (it.n_iter == 0) {  // no query sees these keys: dK = dV = 0
+        if (key < it.sq.nk)
+          for (int i = 0; i < D / 8; ++i) grow[i] = make_uint4(0, 0, 0, 0);
+        continue;
       }
+      // row r's LSE (half 0, log2 units) or delta (half 1) for iteration i, loaded one
+      // iteration ahead so its latency hides behind the current one
+      auto row_value = [&](int i) -> float {
+        const int hi = it.hk * p.group + i / it.per_head, qi = (it.m_lo + i % it.per_head) * BM + r;
+        if (qi >= it.sq.nq) return half == 0 ? INFINITY : 0.f;
+        const size_t idx =
+            VL ? (size_t)hi * p.total_q + it.sq.q0 + qi : ((size_t)it.b * p.Hq + hi) * p.Sq + qi;
+        return half == 0 ? p.lse[idx] * 1.4426950408889634f : p.delta[idx];
+      };
+      float next_v = row_value(0);
+      for (int i = 0; i < it.n_iter && ok; ++i) {
+        const int gi = g + i;
+        const int m0 = (it.m_lo + i % it.per_head) * BM;
+        // the row vectors of this Q tile, in buffer gi & 1: every thread finished
+        // iteration gi - 2's reads before it arrived on iteration gi - 1's VEC_READY
+        float* v_lse = vec + (gi & 1) * 2 * BM;
+        float* v_dl = v_lse + BM;
+        (half == 0 ? v_lse : v_dl)[r] = next_v;
+        mbar_arrive(bar(L::VEC_READY));
+        if (i + 1 < it.n_iter) next_v = row_value(i + 1);
+        if (!(ok = wait_warp(bar(L::VEC_READY), gi & 1))) break;
+        // ---- P phase: P^T = 2^(S^T c - LSE_2) on the visible (key, query) pairs
+        if (!(ok = wait_warp(bar(L::S_READY), gi & 1))) break;
+        tc_fence_after();
+        float pv[64];
+        {
+          uint32_t sr[64];
+          tmem_ld32(lane_t + C_S + c0, *reinterpret_cast<uint32_t(*)[32]>(sr));
+          tmem_ld32(lane_t + C_S + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+          uint32_t pk[32];
+          // query columns [lo, hi) of this thread's 64 see key n0 + r; a tile whose every
+          // query sees every key (all but the window's edges and the ragged ends) needs no test
+          const int lo = p.win_right >= 0 ? key - it.dlen - p.win_right - m0 - c0 : 0;
+          int hi = key < it.sq.nk ? it.sq.nq - m0 - c0 : 0;
+          if (p.win_left >= 0) hi = min(hi, key - it.dlen + p.win_left - m0 - c0 + 1);
+          if (__all_sync(0xffffffffu, lo <= 0 && hi >= 64)) {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) pv[j] = ex2(fmaf(__uint_as_float(sr[j]), p.c2, -v_lse[c0 + j]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 64; ++j)
+              pv[j] = (j >= lo && j < hi) ? ex2(fmaf(__uint_as_float(sr[j]), p.c2, -v_lse[c0 + j])) : 0.f;
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) pk[j] = pack2<BF16>(pv[2 * j], pv[2 * j + 1]);
+          tmem_st32(lane_t + C_S + c0, pk);  // P^T over the S^T columns this thread read
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(L::P_READY));
+        // ---- dS phase: dS^T = P^T (dP^T - delta)
+        if (!(ok = wait_warp(bar(L::DP_READY), gi & 1))) break;
+        tc_fence_after();
+        {
+          uint32_t dr[64];
+          tmem_ld32(lane_t + C_DP + c0, *reinterpret_cast<uint32_t(*)[32]>(dr));
+          tmem_ld32(lane_t + C_DP + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(dr + 32));
+          uint32_t dk2[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float d0 = pv[2 * j] * (__uint_as_float(dr[2 * j]) - v_dl[c0 + 2 * j]);
+            const float d1 = pv[2 * j + 1] * (__uint_as_float(dr[2 * j + 1]) - v_dl[c0 + 2 * j + 1]);
+            dk2[j] = pack2<BF16>(d0, d1);
+          }
+          tmem_st32(lane_t + C_DP + c0, dk2);  // dS^T over the dP^T columns this thread read
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(L::DS_READY));
+      }
+      if (!ok) break;
+      // this tile's dV rows (half 0) and dK rows (half 1): the whole row into registers,
+      // the accumulators handed back to the issuer, then rounded and stored
+      if (!(ok = wait_warp(bar(L::DONE), n_it & 1))) break;
+      tc_fence_after();
+      uint32_t v[D];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c)
+        tmem_ld32(lane_t + (half == 0 ? C_DV : C_DK) + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
+      tc_fence_before();
+      mbar_arrive(bar(L::ACC_FREE));
+      if (key < it.sq.nk) {
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i) grow[i] = pack8<BF16>(v + 8 * i, f);
+      }
+      g += it.n_iter;
+      ++n_it;
     }
   }
 
@@ -512,6 +664,11 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // ============================================================================ dQ
+// Persistent like the dK/dV kernel: work items (Q tile, query head, batch), the Q
+// tiles with the most keys first within each group of heads.  The K/V ring runs on
+// across items; the next item's Q and dO load once the current item's last S and dP
+// (their readers) complete, and its first dQ waits only for the compute warps to have
+// read the current dQ.
 template <int D, bool BF16, bool VL>
 __global__ void __launch_bounds__(THREADS, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -525,36 +682,31 @@ __global__ void __launch_bounds__(THREADS, 1)
   auto bar = [&](int i) -> uint32_t { return sb + L::BAR_OFF + 8u * i; };
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+  volatile int* item_q = reinterpret_cast<volatile int*>(misc + 2);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t lim = p.wait_limit_ns;
-
-  // CTA (m tile, query head, batch); the causal tiles with the most keys run first
   const int n_mt = (p.Sq + BM - 1) / BM;
-  const int m0 = (p.win_right >= 0 ? n_mt - 1 - (int)blockIdx.x : (int)blockIdx.x) * BM;
-  const int h = blockIdx.y, b = blockIdx.z;
-  const int hk = h / p.group;
-  const Seq sq = seq_of<VL>(p, b);
-  if (m0 >= sq.nq) return;  // past the sequence's queries (packed batches): nothing to do
-  const int dlen = sq.nk - sq.nq;
-  // the keys [k_lo, k_hi] some row of this tile sees, K/V tiles t_lo ... t_lo + n_kv - 1
-  const int last_row = min(m0 + BM, sq.nq) - 1;
-  int k_lo = 0, k_hi = sq.nk - 1;
-  if (p.win_right >= 0) k_hi = min(k_hi, last_row + dlen + p.win_right);
-  if (p.win_left >= 0) k_lo = max(0, m0 + dlen - p.win_left);
-  const int t_lo = k_lo / BN;
-  const int n_kv = k_lo <= k_hi ? k_hi / BN + 1 - t_lo : 0;
+  const int n_items = n_mt * p.Hq * p.B;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::QD_FULL), 1);
+    mbar_init(bar(L::QD_EMPTY), 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(bar(L::RING_FULL + s), 1);
       mbar_init(bar(L::RING_EMPTY + s), 1);
     }
     mbar_init(bar(L::S_READY), 1);
+    mbar_init(bar(L::S_READY + 1), 1);
     mbar_init(bar(L::DP_READY), 1);
     mbar_init(bar(L::DP_FREE), NCOMP);
     mbar_init(bar(L::DS_READY), NCOMP);
+    mbar_init(bar(L::DS_READY + 1), NCOMP);
     mbar_init(bar(L::DONE), 1);
+    mbar_init(bar(L::ACC_FREE), NCOMP);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(L::ITEM_FULL + i), 1);
+      mbar_init(bar(L::ITEM_EMPTY + i), 1 + NCOMP);  // the issuer and every compute thread
+    }
     mbar_init(bar(L::DRAIN), 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -567,92 +719,133 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
-  // TMEM columns: S of even K/V tiles at 0, of odd ones at 128 (dS over columns 0-31
+  // TMEM columns: S of even K/V steps at 0, of odd ones at 128 (dS over columns 0-31
   // and 64-95), dP at 256, dQ at 384
   constexpr uint32_t C_S = 0, C_DP = 256, C_DQ = 384;
 
   if (warp == LOAD_WARP) {
-    // ------------------------------------------------------------ loads (one thread)
-    if (lane == 0 && n_kv > 0) {
+    // ------------------------------------------------ work items and loads (one thread)
+    if (lane == 0) {
       prefetch_tmap(&tmq);
       prefetch_tmap(&tmk);
       prefetch_tmap(&tmv);
       prefetch_tmap(&tmdo);
       const uint64_t pol_q = policy_evict_first();
       const uint64_t pol_kv = policy_evict_last();
-      mbar_expect_tx(bar(L::QD_FULL), 2 * L::TILE);
-      const int q_y = VL ? sq.q0 + m0 : m0, q_z = VL ? h : b * p.Hq + h;
-      for (int rr = 0; rr < L::NREG; ++rr) {
-        tma_load_3d(sb + L::Q_OFF + rr * L::REGION, &tmq, bar(L::QD_FULL), rr * 64, q_y, q_z, pol_q);
-        tma_load_3d(sb + L::DO_OFF + rr * L::REGION, &tmdo, bar(L::QD_FULL), rr * 64, q_y, q_z, pol_q);
-      }
-      const int kv_y0 = (VL ? sq.k0 : 0) + t_lo * BN, kv_z = VL ? hk : b * p.Hkv + hk;
       bool ok = true;
-      int ld = 0;
-      for (; ld < 2 * n_kv && ok; ++ld) {  // K_0, V_0, K_1, V_1, ...
-        const int s = ld % NS;
-        if (ld >= NS && !(ok = mbar_wait<false>(bar(L::RING_EMPTY + s), ((ld / NS) - 1) & 1, abort_flag,
-                                         &g_status, lim)))
+      int n_qd = 0;  // Q/dO tile pairs loaded
+      int ld = 0;    // K/V ring loads issued, over all items
+      for (int r = 0; ok; ++r) {
+        const int slot = r & 1;
+        if (!(ok = mbar_wait<false>(bar(L::ITEM_EMPTY + slot), ((r >> 1) & 1) ^ 1, abort_flag, &g_status, lim)))
           break;
-        mbar_expect_tx(bar(L::RING_FULL + s), L::TILE);
-        const CUtensorMap* tm = (ld & 1) ? &tmv : &tmk;
-        for (int rr = 0; rr < L::NREG; ++rr)
-          tma_load_3d(sb + L::RING_OFF + s * L::TILE + rr * L::REGION, tm, bar(L::RING_FULL + s), rr * 64,
-                      kv_y0 + (ld >> 1) * BN, kv_z, pol_kv);
+        int w = atomicAdd(p.work_counter + 1, 1);
+        if (w >= n_items) w = -1;
+        item_q[slot] = w;
+        mbar_arrive(bar(L::ITEM_FULL + slot));
+        if (w < 0) break;
+        const QItem it = q_item<VL>(p, n_mt, w);
+        if (it.n_kv == 0) continue;
+        // Q and dO, once the last item's final S and dP have completed
+        if (n_qd > 0 && !(ok = mbar_wait<false>(bar(L::QD_EMPTY), (n_qd - 1) & 1, abort_flag, &g_status, lim)))
+          break;
+        const int q_y = VL ? it.sq.q0 + it.m0 : it.m0, q_z = VL ? it.h : it.b * p.Hq + it.h;
+        mbar_expect_tx(bar(L::QD_FULL), 2 * L::TILE);
+        for (int rr = 0; rr < L::NREG; ++rr) {
+          tma_load_3d(sb + L::Q_OFF + rr * L::REGION, &tmq, bar(L::QD_FULL), rr * 64, q_y, q_z, pol_q);
+          tma_load_3d(sb + L::DO_OFF + rr * L::REGION, &tmdo, bar(L::QD_FULL), rr * 64, q_y, q_z, pol_q);
+        }
+        ++n_qd;
+        const int hk = it.h / p.group;
+        const int kv_y0 = (VL ? it.sq.k0 : 0) + it.t_lo * BN, kv_z = VL ? hk : it.b * p.Hkv + hk;
+        for (int l = 0; l < 2 * it.n_kv && ok; ++l, ++ld) {  // V_0, K_0, V_1, K_1, ...
+          const int s = ld % NS;
+          if (ld >= NS && !(ok = mbar_wait<false>(bar(L::RING_EMPTY + s), ((ld / NS) - 1) & 1, abort_flag,
+                                                  &g_status, lim)))
+            break;
+          mbar_expect_tx(bar(L::RING_FULL + s), L::TILE);
+          const CUtensorMap* tm = (l & 1) ? &tmk : &tmv;
+          for (int rr = 0; rr < L::NREG; ++rr)
+            tma_load_3d(sb + L::RING_OFF + s * L::TILE + rr * L::REGION, tm, bar(L::RING_FULL + s), rr * 64,
+                        kv_y0 + (l >> 1) * BN, kv_z, pol_kv);
+        }
       }
-      drain_wait(bar(L::QD_FULL), 0, lim);
+      // the last Q/dO pair and the last NS ring loads may still be in flight
+      if (n_qd > 0) drain_wait(bar(L::QD_FULL), (n_qd - 1) & 1, lim);
       for (int l = max(0, ld - NS); l < ld; ++l) drain_wait(bar(L::RING_FULL + l % NS), (l / NS) & 1, lim);
     }
     __syncwarp();
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ MMAs (one thread)
-    if (lane == 0 && n_kv > 0) {
-      const uint64_t q_km = sdesc_sw128(sb + L::Q_OFF, 16, 1024);
-      const uint64_t do_km = sdesc_sw128(sb + L::DO_OFF, 16, 1024);
-      auto ring_km = [&](int ld) { return sdesc_sw128(sb + L::RING_OFF + (ld % NS) * L::TILE, 16, 1024); };
-      auto ring_mn = [&](int ld) {
-        return sdesc_sw128(sb + L::RING_OFF + (ld % NS) * L::TILE, L::REGION, 1024);
-      };
+    if (lane == 0) {
+      const uint32_t hi = desc_hi();
+      const uint32_t q_km = desc_km(sb + L::Q_OFF), do_km = desc_km(sb + L::DO_OFF);
+      const uint32_t ring_km0 = desc_km(sb + L::RING_OFF), ring_mn0 = desc_mn(sb + L::RING_OFF);
+      constexpr uint32_t SLOT = L::TILE >> 4;  // one ring slot in the address field
+      auto ring_km = [&](int l) { return ring_km0 + (uint32_t)(l % NS) * SLOT; };
+      auto ring_mn = [&](int l) { return ring_mn0 + (uint32_t)(l % NS) * SLOT; };
       auto wait = [&](int bar_i, int parity) -> bool {
         return mbar_wait<false>(bar(bar_i), parity & 1, abort_flag, &g_status, lim);
       };
-      auto ring_wait = [&](int ld) -> bool { return wait(L::RING_FULL + ld % NS, ld / NS); };
-      // S(0), dP(0); then per K/V tile j: S(j+1) into the other S buffer, dP(j+1) once
-      // the compute warps hold dP(j), dQ += dS(j) K(j) once they wrote dS(j)
-      bool ok = wait(L::QD_FULL, 0) && ring_wait(0);
-      if (ok) {
+      auto ring_wait = [&](int l) -> bool { return wait(L::RING_FULL + l % NS, l / NS); };
+      bool ok = true;
+      // step g reads ring loads 2g (V) and 2g + 1 (K); V is released once dP has read it,
+      // K once dQ has, so with NS = 5 both tiles of step g + 2 land while step g runs
+      int g = 0;     // K/V steps issued over all items
+      int n_it = 0;  // items with K/V steps
+      for (int r = 0; ok; ++r) {
+        const int slot = r & 1;
+        if (!(ok = wait(L::ITEM_FULL + slot, r >> 1))) break;
+        const int w = item_q[slot];
+        mbar_arrive(bar(L::ITEM_EMPTY + slot));
+        if (w < 0) break;
+        const int n = q_item<VL>(p, n_mt, w).n_kv;
+        if (n == 0) continue;
+        // S(0), dP(0); then per K/V step j: S(j+1) into the other S buffer, dP(j+1)
+        // once the compute warps hold dP(j), dQ += dS(j) K(j) once they wrote dS(j).
+        // S(0) goes to the buffer of step g, whose last dS was read by a dQ issued
+        // before; dP(0) waits until the compute warps hold the last item's final dP.
+        if (!(ok = wait(L::QD_FULL, n_it) && ring_wait(2 * g + 1))) break;
         tc_fence_after();
-        mma_kmajor<D, BF16>(tmem + C_S, q_km, ring_km(0));
-        umma_commit(bar(L::S_READY));
-        ok = ring_wait(1);
-        if (ok) {
-          tc_fence_after();
-          mma_kmajor<D, BF16>(tmem + C_DP, do_km, ring_km(1));
-          umma_commit(bar(L::DP_READY));
-        }
-      }
-      for (int j = 0; j < n_kv && ok; ++j) {
-        if (j + 1 < n_kv) {
-          if (!(ok = ring_wait(2 * j + 2))) break;
-          tc_fence_after();
-          // the other buffer held dS(j-1), read by dQ(j-1), issued before
-          mma_kmajor<D, BF16>(tmem + C_S + 128u * ((j + 1) & 1), q_km, ring_km(2 * j + 2));
-          umma_commit(bar(L::S_READY));
-        }
-        if (!(ok = wait(L::DP_FREE, j))) break;
-        if (j + 1 < n_kv) {
-          if (!(ok = ring_wait(2 * j + 3))) break;
-          tc_fence_after();
-          mma_kmajor<D, BF16>(tmem + C_DP, do_km, ring_km(2 * j + 3));
-          umma_commit(bar(L::DP_READY));
-        }
-        if (!(ok = wait(L::DS_READY, j))) break;
+        mma_kmajor<D, BF16>(tmem + C_S + 128u * (g & 1), q_km, ring_km(2 * g + 1), hi);
+        umma_commit(bar(L::S_READY + (g & 1)));
+        if (g > 0 && !(ok = wait(L::DP_FREE, g - 1))) break;
+        if (!(ok = ring_wait(2 * g))) break;
         tc_fence_after();
-        mma_tmem_a<D, BF16>(tmem + C_DQ, tmem + C_S + 128u * (j & 1), ring_mn(2 * j), j > 0);  // dQ += dS K
-        umma_commit(bar(L::RING_EMPTY + (2 * j) % NS));      // K(j): read by S(j) and dQ(j)
-        umma_commit(bar(L::RING_EMPTY + (2 * j + 1) % NS));  // V(j): read by dP(j)
+        mma_kmajor<D, BF16>(tmem + C_DP, do_km, ring_km(2 * g), hi);
+        umma_commit(bar(L::DP_READY));
+        umma_commit(bar(L::RING_EMPTY + (2 * g) % NS));  // V(0): read by dP(0)
+        if (n == 1) umma_commit(bar(L::QD_EMPTY));  // the item's last readers of Q and dO
+        for (int j = 0; j < n && ok; ++j) {
+          const int gj = g + j;
+          if (j + 1 < n) {
+            if (!(ok = ring_wait(2 * gj + 3))) break;
+            tc_fence_after();
+            // the other buffer held dS(gj - 1), read by dQ(gj - 1), issued before
+            mma_kmajor<D, BF16>(tmem + C_S + 128u * ((gj + 1) & 1), q_km, ring_km(2 * gj + 3), hi);
+            umma_commit(bar(L::S_READY + ((gj + 1) & 1)));
+          }
+          if (!(ok = wait(L::DP_FREE, gj))) break;
+          if (j + 1 < n) {
+            if (!(ok = ring_wait(2 * gj + 2))) break;
+            tc_fence_after();
+            mma_kmajor<D, BF16>(tmem + C_DP, do_km, ring_km(2 * gj + 2), hi);
+            umma_commit(bar(L::DP_READY));
+            umma_commit(bar(L::RING_EMPTY + (2 * gj + 2) % NS));  // V(j+1): read by dP(j+1)
+            if (j + 2 == n) umma_commit(bar(L::QD_EMPTY));
+          }
+          if (!(ok = wait(L::DS_READY + (gj & 1), gj >> 1))) break;
+          // the item's first dQ overwrites dQ: the compute warps must have read the last one
+          if (j == 0 && n_it > 0 && !(ok = wait(L::ACC_FREE, n_it - 1))) break;
+          tc_fence_after();
+          mma_tmem_a<D, BF16>(tmem + C_DQ, tmem + C_S + 128u * (gj & 1), ring_mn(2 * gj + 1), hi, j > 0);  // dQ += dS K
+          umma_commit(bar(L::RING_EMPTY + (2 * gj + 1) % NS));  // K(j): read by S(j) and dQ(j)
+        }
+        if (!ok) break;
+        umma_commit(bar(L::DONE));
+        g += n;
+        ++n_it;
       }
-      umma_commit(bar(L::DONE));
       umma_commit(bar(L::DRAIN));
       drain_wait(bar(L::DRAIN), 0, lim);
     }
@@ -662,66 +855,85 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int quarter = warp & 3, half = warp >> 2;
     const int r = quarter * 32 + lane;
     const uint32_t lane_t = tmem + ((uint32_t)(quarter * 32) << 16);
-    const int row = m0 + r;
     const int c0 = half * 64;  // this thread's 64 of a K/V tile's 128 keys
-    const bool live = row < sq.nq;
-    const size_t ridx = VL ? (size_t)h * p.total_q + sq.q0 + row : ((size_t)b * p.Hq + h) * p.Sq + row;
-    const float lse2 = live ? p.lse[ridx] * 1.4426950408889634f : INFINITY;
-    const float dlt = live ? p.delta[ridx] : 0.f;
-    // keys of this row: [key_lo, key_hi] (none for rows past the sequence)
-    int key_lo = 0, key_hi = live ? sq.nk - 1 : -1;
-    if (p.win_right >= 0) key_hi = min(key_hi, row + dlen + p.win_right);
-    if (p.win_left >= 0) key_lo = row + dlen - p.win_left;
     auto wait_warp = [&](uint32_t b_, uint32_t ph_) -> bool {
       return __all_sync(0xffffffffu, mbar_wait<false>(b_, ph_, abort_flag, &g_status, lim));
     };
     bool ok = true;
-    for (int j = 0; j < n_kv && ok; ++j) {
-      if (!(ok = wait_warp(bar(L::S_READY), j & 1))) break;
-      if (!(ok = wait_warp(bar(L::DP_READY), j & 1))) break;
-      tc_fence_after();
-      const uint32_t t_s = lane_t + C_S + 128u * (j & 1);
-      uint32_t sr[64], dr[64];
-      tmem_ld32(t_s + c0, *reinterpret_cast<uint32_t(*)[32]>(sr));
-      tmem_ld32(t_s + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
-      tmem_ld32(lane_t + C_DP + c0, *reinterpret_cast<uint32_t(*)[32]>(dr));
-      tmem_ld32(lane_t + C_DP + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(dr + 32));
-      tc_fence_before();
-      mbar_arrive(bar(L::DP_FREE));  // dP(j + 1) may overwrite dP(j)
-      // keys kb + u, ulo <= u < uhi, are visible to this row
-      const int kb = (t_lo + j) * BN + c0, ulo = key_lo - kb, uhi = key_hi + 1 - kb;
-      uint32_t pk[32];
-#pragma unroll
-      for (int u = 0; u < 32; ++u) {
-        const float p0 = (2 * u >= ulo && 2 * u < uhi) ? ex2(fmaf(__uint_as_float(sr[2 * u]), p.c2, -lse2)) : 0.f;
-        const float p1 = (2 * u + 1 >= ulo && 2 * u + 1 < uhi)
-                             ? ex2(fmaf(__uint_as_float(sr[2 * u + 1]), p.c2, -lse2)) : 0.f;
-        pk[u] = pack2<BF16>(p0 * (__uint_as_float(dr[2 * u]) - dlt), p1 * (__uint_as_float(dr[2 * u + 1]) - dlt));
-      }
-      tmem_st32(t_s + c0, pk);  // dS over the S columns this thread read
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(L::DS_READY));
-    }
-    // dQ = scale * (dS K) summed over the K/V tiles; rows that see no key get 0
-    if (ok && (n_kv == 0 || wait_warp(bar(L::DONE), 0))) {
-      tc_fence_after();
+    int g = 0, n_it = 0;
+    for (int rq = 0; ok; ++rq) {
+      const int slot = rq & 1;
+      if (!(ok = wait_warp(bar(L::ITEM_FULL + slot), (rq >> 1) & 1))) break;
+      const int w = item_q[slot];
+      mbar_arrive(bar(L::ITEM_EMPTY + slot));
+      if (w < 0) break;
+      const QItem it = q_item<VL>(p, n_mt, w);
+      if (it.skip) continue;
+      const int row = it.m0 + r;
+      const bool live = row < it.sq.nq;
+      const size_t ridx =
+          VL ? (size_t)it.h * p.total_q + it.sq.q0 + row : ((size_t)it.b * p.Hq + it.h) * p.Sq + row;
       uint4* dst = reinterpret_cast<uint4*>(
-          (VL ? p.dq + (size_t)(sq.q0 + row) * p.dq_rstride + (size_t)h * D : p.dq + ridx * D) + half * (D / 2));
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        uint32_t v[32];
-        if (n_kv > 0) {
-          tmem_ld32(lane_t + C_DQ + half * (D / 2) + 32 * c, v);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = 0u;
-        }
-        if (live) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dst[4 * c + i] = pack8<BF16>(v + 8 * i, p.scale);
-        }
+          (VL ? p.dq + (size_t)(it.sq.q0 + row) * p.dq_rstride + (size_t)it.h * D : p.dq + ridx * D) +
+          half * (D / 2));
+      if (it.n_kv == 0) {  // the rows see no key: dQ = 0
+        if (live)
+          for (int i = 0; i < D / 16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+        continue;
       }
+      const float lse2 = live ? p.lse[ridx] * 1.4426950408889634f : INFINITY;
+      const float dlt = live ? p.delta[ridx] : 0.f;
+      // keys of this row: [key_lo, key_hi] (none for rows past the sequence)
+      int key_lo = 0, key_hi = live ? it.sq.nk - 1 : -1;
+      if (p.win_right >= 0) key_hi = min(key_hi, row + it.dlen + p.win_right);
+      if (p.win_left >= 0) key_lo = row + it.dlen - p.win_left;
+      for (int j = 0; j < it.n_kv && ok; ++j) {
+        const int gj = g + j;
+        if (!(ok = wait_warp(bar(L::S_READY + (gj & 1)), (gj >> 1) & 1))) break;
+        if (!(ok = wait_warp(bar(L::DP_READY), gj & 1))) break;
+        tc_fence_after();
+        const uint32_t t_s = lane_t + C_S + 128u * (gj & 1);
+        uint32_t sr[64], dr[64];
+        tmem_ld32(t_s + c0, *reinterpret_cast<uint32_t(*)[32]>(sr));
+        tmem_ld32(t_s + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+        tmem_ld32(lane_t + C_DP + c0, *reinterpret_cast<uint32_t(*)[32]>(dr));
+        tmem_ld32(lane_t + C_DP + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(dr + 32));
+        tc_fence_before();
+        mbar_arrive(bar(L::DP_FREE));  // dP(j + 1) may overwrite dP(j)
+        // keys kb + u, ulo <= u < uhi, are visible to this row
+        const int kb = (it.t_lo + j) * BN + c0, ulo = key_lo - kb, uhi = key_hi + 1 - kb;
+        uint32_t pk[32];
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+          const float p0 =
+              (2 * u >= ulo && 2 * u < uhi) ? ex2(fmaf(__uint_as_float(sr[2 * u]), p.c2, -lse2)) : 0.f;
+          const float p1 = (2 * u + 1 >= ulo && 2 * u + 1 < uhi)
+                               ? ex2(fmaf(__uint_as_float(sr[2 * u + 1]), p.c2, -lse2)) : 0.f;
+          pk[u] = pack2<BF16>(p0 * (__uint_as_float(dr[2 * u]) - dlt),
+                              p1 * (__uint_as_float(dr[2 * u + 1]) - dlt));
+        }
+        tmem_st32(t_s + c0, pk);  // dS over the S columns this thread read
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(L::DS_READY + (gj & 1)));
+      }
+      if (!ok) break;
+      // dQ = scale * (dS K) summed over the K/V tiles: this thread's half of the row into
+      // registers, dQ handed back to the issuer, then rounded and stored
+      if (!(ok = wait_warp(bar(L::DONE), n_it & 1))) break;
+      tc_fence_after();
+      uint32_t v[D / 2];
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c)
+        tmem_ld32(lane_t + C_DQ + half * (D / 2) + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
+      tc_fence_before();
+      mbar_arrive(bar(L::ACC_FREE));
+      if (live) {
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i) dst[i] = pack8<BF16>(v + 8 * i, p.scale);
+      }
+      g += it.n_kv;
+      ++n_it;
     }
   }
 
@@ -812,29 +1024,28 @@ static cudaError_t launch_t(const BwdArgs& a, cudaStream_t stream) {
   p.dq_rstride = a.dq_rstride;
   p.dk_rstride = a.dk_rstride;
   const long long n_kt = (a.Skv + BN - 1) / BN, n_mt = (a.Sq + BM - 1) / BM;
+  // both persistent kernels claim work items from the two zeroed counters
+  p.work_counter = a.work_counter;
+  {
+    cudaError_t e = cudaMemsetAsync(a.work_counter, 0, 2 * sizeof(int), stream);
+    if (e != cudaSuccess) return e;
+  }
+  const int sms = a.num_sms > 0 ? a.num_sms : 1;
+  const int g = a.Hq / a.Hkv;
   if (n_kt > 0) {
     using L = KVLayout<D>;
     cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, BF16, VL>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
-    p.kv_slowest = 0;
-    if (!VL && a.win_left < 0) {
-      // the longest CTA (key tile 0) against an SM's share of all (query head, Q tile)
-      // iterations: above a fifth, start the long CTAs first
-      long long total = 0;
-      for (long long t = 0; t < n_kt; ++t) {
-        long long m_lo = 0;
-        if (a.causal) {
-          const long long lo = t * BN - (a.Skv - a.Sq) - (BM - 1);
-          m_lo = lo <= 0 ? 0 : ((lo + BM - 1) / BM < n_mt ? (lo + BM - 1) / BM : n_mt);
-        }
-        total += n_mt - m_lo;
-      }
-      total *= (long long)a.B * a.Hq;
-      const long long longest = n_mt * (a.Hq / a.Hkv);
-      p.kv_slowest = longest * 5 * (a.num_sms > 0 ? a.num_sms : 1) > total ? 1 : 0;
-    }
-    const dim3 grid = p.kv_slowest ? dim3(a.Hkv, a.B, (unsigned)n_kt) : dim3((unsigned)n_kt, a.Hkv, a.B);
+    // scheduling groups: as many (batch, KV head) planes as keep about 64 MB of their
+    // query heads' Q and dO in L2
+    const double qd_bytes = 4.0 * (double)(a.Sq > 0 ? a.Sq : 1) * D * g;
+    long long per = (long long)(64.0 * (1 << 20) / qd_bytes);
+    if (per < 1) per = 1;
+    if (per > (long long)a.B * a.Hkv) per = (long long)a.B * a.Hkv;
+    p.per_group = (int)per;
+    const long long n_items = n_kt * a.Hkv * a.B;
+    const int grid = (int)(n_items < sms ? n_items : sms);
     bwd_dkdv_kernel<D, BF16, VL><<<grid, THREADS, L::ALLOC, stream>>>(tq, tk, tv, tg, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -844,7 +1055,16 @@ static cudaError_t launch_t(const BwdArgs& a, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<D, BF16, VL>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
-    bwd_dq_kernel<D, BF16, VL><<<dim3((unsigned)n_mt, a.Hq, a.B), THREADS, L::ALLOC, stream>>>(tq, tk, tv, tg, p);
+    // scheduling groups: as many (batch, query head) planes as keep about 64 MB of
+    // their K and V in L2, rounded to whole GQA groups
+    const double kv_bytes = 4.0 * (double)(a.Skv > 0 ? a.Skv : 1) * D;
+    long long per = (long long)(64.0 * (1 << 20) / kv_bytes) * g;
+    if (per < g) per = g;
+    if (per > (long long)a.B * a.Hq) per = (long long)a.B * a.Hq;
+    p.per_group_q = (int)per;
+    const long long n_items = n_mt * a.Hq * a.B;
+    const int grid = (int)(n_items < sms ? n_items : sms);
+    bwd_dq_kernel<D, BF16, VL><<<grid, THREADS, L::ALLOC, stream>>>(tq, tk, tv, tg, p);
     return cudaGetLastError();
   }
   return cudaSuccess;

@@ -67,13 +67,14 @@ struct BwdArgs {
   void* dk;
   void* dv;
   float* delta;   // [B, Hq, Sq] fp32 workspace (the row terms)
+  int* work_counter;  // two ints of workspace: the persistent kernels' work-item counters
   int B, Hq, Hkv, Sq, Skv, D;
   int causal;
   float scale;
   int bf16;
   uint64_t wait_limit_ns;
-  int num_sms;  // multiprocessors of the device (CTA ordering)
-  int debug_fault;  // 3: CTA (0, 0, 0) withholds its second Q/dO tile pair (test only)
+  int num_sms;  // multiprocessors of the device (persistent grids)
+  int debug_fault;  // 3: the dK/dV CTA of work item 0 withholds its second Q/dO pair (test only)
   int win_left, win_right;  // sliding-window bounds, -1: none (causal: the right bound is 0)
   // token-major layouts (attn_bwd_varlen, attn_bwd_qkvpacked): vl = 1; q, o, dout, dq are
   // [tokens, Hq, D] and k, v, dk, dv [tokens, Hkv, D] with the token strides below

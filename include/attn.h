@@ -135,7 +135,8 @@ int attn_fwd_qkvpacked(const void* qkv, void* o, float* lse, int B, int S, int H
  * lse              device, [B, Hq, Sq] float32, the forward's (natural log).
  * o, lse must be attn_fwd's outputs for these q, k, v, causal and scale.
  * A workspace of attn_bwd_workspace_bytes(B, Hq, Sq, D) bytes (the fp32 row
- * terms) is taken from the library's stream-ordered pool.  No gradient is
+ * terms and the persistent kernels' two work counters) is taken from the
+ * library's stream-ordered pool.  No gradient is
  * accumulated with atomics: two calls give identical bits.
  * D 64 or 128; B, Hq, Hkv <= 65535; scale finite.  With Skv == 0, dq = 0.
  */
@@ -316,7 +317,8 @@ int attn_check_device_status(cudaStream_t stream);
  * run out: 1, attn_fwd withholds its first V tile; 2, the decode split kernel
  * (attn_decode, attn_decode_fused, attn_decode_paged, attn_decode_noalloc)
  * withholds the first V sub-tile of its CTA (0, 0, 0); 3, attn_bwd withholds
- * the second Q/dO tile pair of its CTA (0, 0, 0).  0 turns the fault off.
+ * the second Q/dO tile pair of its first work item (the dK/dV kernel's key tile
+ * 0 of the first head).  0 turns the fault off.
  * Returns ATTN_OK or ATTN_ERR_INVALID_ARG. */
 int attn_debug_set(int fault, unsigned wait_limit_us);
 
