@@ -66,7 +66,7 @@ def build(verbose: bool = False, force: bool = False, ptxas_info: bool = False) 
             if r.returncode != 0:
                 raise RuntimeError(f"nvcc failed: {' '.join(cmd)}")
     if force or jobs or _stale(LIB, objs):
-        cmd = [cc, *ARCH, "-shared", "-o", LIB, *objs]
+        cmd = [cc, *ARCH, "-shared", "-o", LIB, *objs, "-ldl"]  # NVTX loads its tool on demand
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             sys.stderr.write(r.stdout + r.stderr)

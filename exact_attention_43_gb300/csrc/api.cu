@@ -3,6 +3,8 @@
 #include "../../include/attn.h"
 #include "internal.h"
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <math.h>
 #include <mutex>
 
@@ -25,6 +27,17 @@ int g_num_sms[kMaxDevices];
 cudaMemPool_t g_pool[kMaxDevices];
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// An NVTX range named after the entry point around its validation and launches, so a
+// profiler's timeline shows which call enqueued which kernels (the llm.c attention page
+// wraps attention_forward and attention_backward the same way).  Without an attached
+// tool the push and pop return at once.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 int check_device(int* dev_out) {
   int dev = 0;
@@ -159,6 +172,7 @@ extern "C" {
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
              int Hkv, int Sq, int Skv, int D, int causal, float scale, int dtype,
              cudaStream_t stream) {
+  NvtxRange range_(__func__);
   if (B < 0 || Hq < 0 || Hkv < 0 || Sq < 0 || Skv < 0) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_UNSUPPORTED;
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
@@ -201,6 +215,7 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
                     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int B, int Hq, int Hkv,
                     int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int D, int causal,
                     int window_left, int window_right, float scale, int dtype, cudaStream_t stream) {
+  NvtxRange range_(__func__);
   if (B < 0 || Hq < 0 || Hkv < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 ||
       max_seqlen_k < 0)
     return ATTN_ERR_INVALID_ARG;
@@ -240,6 +255,7 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
 int attn_fwd_qkvpacked(const void* qkv, void* o, float* lse, int B, int S, int H, int D, int causal,
                        int window_left, int window_right, float scale, int dtype,
                        cudaStream_t stream) {
+  NvtxRange range_(__func__);
   if (B < 0 || S < 0 || H < 0) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_UNSUPPORTED;
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
@@ -327,6 +343,7 @@ size_t attn_bwd_workspace_bytes(int B, int Hq, int Sq, int D) {
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
              const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq, int Skv,
              int D, int causal, float scale, int dtype, cudaStream_t stream) {
+  NvtxRange range_(__func__);
   if (B < 0 || Hq < 0 || Hkv < 0 || Sq < 0 || Skv < 0) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_UNSUPPORTED;
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
@@ -382,6 +399,7 @@ int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, 
                     const int32_t* cu_seqlens_k, int B, int Hq, int Hkv, int total_q, int total_k,
                     int max_seqlen_q, int max_seqlen_k, int D, int causal, int window_left,
                     int window_right, float scale, int dtype, cudaStream_t stream) {
+  NvtxRange range_(__func__);
   if (B < 0 || Hq < 0 || Hkv < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 ||
       max_seqlen_k < 0)
     return ATTN_ERR_INVALID_ARG;
@@ -428,6 +446,7 @@ int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, 
 int attn_bwd_qkvpacked(const void* qkv, const void* o, const float* lse, const void* dout, void* dqkv,
                        int B, int S, int H, int D, int causal, int window_left, int window_right,
                        float scale, int dtype, cudaStream_t stream) {
+  NvtxRange range_(__func__);
   if (B < 0 || S < 0 || H < 0) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_UNSUPPORTED;
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
@@ -538,6 +557,7 @@ static int decode_contiguous_args(const void* q, const void* k_cache, const void
 int attn_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* seq_lens,
                 void* o, int B, int Hq, int Hkv, int max_S, int D, int num_splits, int dtype,
                 cudaStream_t stream) {
+  NvtxRange range_(__func__);
   ea::DecodeArgs a;
   bool empty;
   int st = decode_contiguous_args(q, k_cache, v_cache, seq_lens, o, B, Hq, Hkv, max_S, D,
@@ -552,6 +572,7 @@ int attn_decode(const void* q, const void* k_cache, const void* v_cache, const i
 int attn_decode_fused(const void* q, const void* k_cache, const void* v_cache,
                       const int32_t* seq_lens, void* o, int B, int Hq, int Hkv, int max_S, int D,
                       int num_splits, int dtype, cudaStream_t stream) {
+  NvtxRange range_(__func__);
   ea::DecodeArgs a;
   bool empty;
   int st = decode_contiguous_args(q, k_cache, v_cache, seq_lens, o, B, Hq, Hkv, max_S, D,
@@ -570,6 +591,7 @@ int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
                       const int32_t* block_table, const int32_t* seq_lens, void* o, int B, int Hq,
                       int Hkv, int num_pages, int page_size, int max_pages, int D, int num_splits,
                       int dtype, cudaStream_t stream) {
+  NvtxRange range_(__func__);
   if (B < 0 || Hq < 0 || Hkv < 0 || num_pages < 0 || page_size < 1 || max_pages < 0 || num_splits < 0)
     return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_UNSUPPORTED;
@@ -618,6 +640,7 @@ int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
 int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
                         const int32_t* seq_lens, void* o, int B, int Hq, int Hkv, int max_S, int D,
                         int num_splits, int dtype, cudaStream_t stream) {
+  NvtxRange range_(__func__);
   ea::DecodeArgs a;
   bool empty;
   int st = decode_contiguous_args(q, k_cache, v_cache, seq_lens, o, B, Hq, Hkv, max_S, D,

@@ -256,30 +256,57 @@ __device__ __forceinline__ uint4 pack8(const uint32_t* r, float f) {
                     pack2<BF16>(__uint_as_float(r[6]) * f, __uint_as_float(r[7]) * f));
 }
 
-// delta_i = sum_d dO_id O_id, one warp per row (rows of D contiguous elements).  With
-// hq_tm > 0 the rows are token-major ([tokens, hq_tm, D]) and the result goes to the
-// [Hq, total_q] layout of the LSE; otherwise to row order.
+// delta_i = sum_d dO_id O_id (rows of D contiguous elements).  D / 8 lanes share a row,
+// one 16-byte load of O and of dO each; a warp covers 256 / D rows per load and issues
+// the loads of DELTA_UNROLL such groups before reducing any, so enough bytes are in
+// flight to keep HBM busy.  With hq_tm > 0 the rows are token-major ([tokens, hq_tm, D])
+// and the result goes to the [Hq, total_q] layout of the LSE; otherwise to row order.
+constexpr int DELTA_UNROLL = 4;
+constexpr int DELTA_THREADS = 256;
+
+template <int D>
+constexpr int delta_rows_per_block() {
+  return (DELTA_THREADS / 32) * (256 / D) * DELTA_UNROLL;
+}
+
 template <int D, bool BF16>
-__global__ void __launch_bounds__(256) bwd_delta_kernel(const uint16_t* o, const uint16_t* dout,
-                                                        float* delta, long long rows, int hq_tm,
-                                                        long long total_q) {
-  constexpr int EPL = D / 32;  // elements per lane
-  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (row >= rows) return;
-  const int lane = threadIdx.x & 31;
-  const uint16_t* a = o + row * D + lane * EPL;
-  const uint16_t* g = dout + row * D + lane * EPL;
-  float s = 0.f;
+__global__ void __launch_bounds__(DELTA_THREADS) bwd_delta_kernel(const uint16_t* o, const uint16_t* dout,
+                                                                  float* delta, long long rows, int hq_tm,
+                                                                  long long total_q) {
+  constexpr int LPR = D / 8;          // lanes per row
+  constexpr int RPW = 32 / LPR;       // rows per warp per load
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sub = lane / LPR, part = lane % LPR;
+  const long long row0 = (long long)blockIdx.x * delta_rows_per_block<D>() + (long long)warp * RPW * DELTA_UNROLL;
+  uint4 a[DELTA_UNROLL], g[DELTA_UNROLL];
 #pragma unroll
-  for (int e = 0; e < EPL; e += 2) {
-    const float2 x = unpack2<BF16>(*reinterpret_cast<const uint32_t*>(a + e));
-    const float2 y = unpack2<BF16>(*reinterpret_cast<const uint32_t*>(g + e));
-    s = fmaf(x.x, y.x, s);
-    s = fmaf(x.y, y.y, s);
+  for (int u = 0; u < DELTA_UNROLL; ++u) {
+    const long long row = row0 + u * RPW + sub;
+    if (row < rows) {
+      a[u] = reinterpret_cast<const uint4*>(o + row * D)[part];
+      g[u] = reinterpret_cast<const uint4*>(dout + row * D)[part];
+    } else {
+      a[u] = make_uint4(0, 0, 0, 0);
+      g[u] = make_uint4(0, 0, 0, 0);
+    }
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-  if (lane == 0) delta[hq_tm > 0 ? (row % hq_tm) * total_q + row / hq_tm : row] = s;
+  for (int u = 0; u < DELTA_UNROLL; ++u) {
+    const uint32_t* x = reinterpret_cast<const uint32_t*>(&a[u]);
+    const uint32_t* y = reinterpret_cast<const uint32_t*>(&g[u]);
+    float s = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 xv = unpack2<BF16>(x[e]);
+      const float2 yv = unpack2<BF16>(y[e]);
+      s = fmaf(xv.x, yv.x, s);
+      s = fmaf(xv.y, yv.y, s);
+    }
+#pragma unroll
+    for (int off = LPR / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    const long long row = row0 + u * RPW + sub;
+    if (part == 0 && row < rows) delta[hq_tm > 0 ? (row % hq_tm) * total_q + row / hq_tm : row] = s;
+  }
 }
 
 // Shared-memory descriptors of 128-byte-swizzled tiles as two 32-bit halves: the high
@@ -966,7 +993,8 @@ static cudaError_t launch_t(const BwdArgs& a, cudaStream_t stream) {
   // row terms: one per (query token, head) in either layout
   const long long rows = VL ? (long long)a.total_q * a.Hq : (long long)a.B * a.Hq * a.Sq;
   if (rows > 0) {
-    bwd_delta_kernel<D, BF16><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
+    constexpr int RB = delta_rows_per_block<D>();
+    bwd_delta_kernel<D, BF16><<<(unsigned)((rows + RB - 1) / RB), DELTA_THREADS, 0, stream>>>(
         static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.delta, rows,
         VL ? a.Hq : 0, (long long)a.total_q);
     cudaError_t e = cudaGetLastError();
