@@ -12,24 +12,28 @@
 // GB300 design, three kernels and no atomics (every gradient is reproducible bit
 // for bit):
 //  * a prep kernel forms the row term delta_i = sum_d dO_id O_id;
-//  * the dK/dV kernel keeps one 128-key tile of one KV head per CTA: K and V stay
+//  * both product kernels are persistent (one CTA per SM claiming work items from a
+//    counter) with four roles: a loader thread, an MMA-issuing thread, eight compute
+//    warps (two threads per TMEM lane, 64 columns each) and an epilogue warpgroup
+//    that reads the finished accumulators, hands them back and stores them while the
+//    compute warps start the next item;
+//  * the dK/dV kernel's work item is one 128-key tile of one KV head: K and V stay
 //    in shared memory, and dK, dV accumulate in TMEM over every query head of the
 //    GQA group and every Q tile that sees the keys (causal tiles that see none are
-//    skipped).  Per Q tile one thread issues S^T = K Q^T and dP^T = V dO^T into two
-//    TMEM regions, then dV += P^T dO and dK += dS^T Q with A read from TMEM.  Eight
-//    compute warps (two threads per key row, 64 queries each; TMEM lane = key)
-//    work in two phases, P^T = 2^(S^T c - LSE_2) and then dS^T = P^T (dP^T - delta),
-//    each written back over the columns it came from as 16-bit; the MMAs are
-//    ordered dV(i), S^T(i+1), dK(i), dP^T(i+1), so each phase runs while the
-//    tensor core works on two products of the tile before or after it;
-//  * the dQ kernel keeps one 128-row Q tile (and its dO) per CTA and streams the
-//    K/V tiles it sees through a 4-stage ring, like the forward: S = Q K^T (two
-//    TMEM buffers, so the next S is computed while this one is used), dP = dO V^T,
-//    dS = P (dP - delta) written over S as 16-bit, dQ += dS K accumulated in TMEM
-//    and stored once.  Recomputing S and dP costs two more products per (Q tile,
-//    KV tile) than one kernel that adds dQ into memory from the dK/dV kernel, but
-//    the eight compute warps then overlap the tensor core instead of waiting on
-//    it, and dQ needs no fp32 atomics.
+//    skipped).  Per Q tile the issuer puts S^T = K Q^T and dP^T = V dO^T into two
+//    TMEM regions, then dV += P^T dO and dK += dS^T Q with A read from TMEM.  The
+//    compute warps work in two phases, P^T = 2^(S^T c - LSE_2) and then
+//    dS^T = P^T (dP^T - delta), each written back over the columns it came from as
+//    16-bit; the MMAs are ordered dV(i), S^T(i+1), dK(i), dP^T(i+1), so each phase
+//    runs while the tensor core works on two products of the tile before or after it;
+//  * the dQ kernel's work item is one 128-row Q tile (and its dO): it streams the
+//    K/V tiles it sees through a 5-slot ring, V before K, like the forward:
+//    S = Q K^T (two TMEM buffers, so the next S is computed while this one is used),
+//    dP = dO V^T, dS = P (dP - delta) written over S as 16-bit, dQ += dS K
+//    accumulated in TMEM and stored once.  Recomputing S and dP costs two more
+//    products per (Q tile, KV tile) than one kernel that adds dQ into memory from the
+//    dK/dV kernel, but the compute warps then overlap the tensor core instead of
+//    waiting on it, and dQ needs no fp32 atomics.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -42,10 +46,15 @@ __device__ unsigned g_status;
 
 constexpr int BM = 128;        // queries per Q tile
 constexpr int BN = 128;        // keys per K/V tile (= TMEM lanes in the dK/dV kernel)
-constexpr int THREADS = 320;   // warps 0-7 compute, warp 8 loads, warp 9 issues the MMAs
-constexpr int LOAD_WARP = 8;
-constexpr int MMA_WARP = 9;
+// Warps 0-7 compute, 8-11 the epilogue (reads the accumulators, hands them back, rounds
+// and stores), warp 12 loads, warp 13 issues the MMAs (14, 15 idle: setmaxnreg works on
+// whole warpgroups).
+constexpr int THREADS = 512;
+constexpr int EPI_WARP = 8;
+constexpr int LOAD_WARP = 12;
+constexpr int MMA_WARP = 13;
 constexpr int NCOMP = 256;     // compute threads: warps w and w + 4 share TMEM lanes 32 (w mod 4) ...
+constexpr int NEPI = 128;      // epilogue threads: one accumulator row (TMEM lane) each
 constexpr int NS = 5;          // dQ kernel: K/V ring stages (two and a half K/V steps)
 constexpr uint32_t TMEM_COLS = 512;
 
@@ -384,7 +393,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(bar(L::Q_FREE + i), 1);
       mbar_init(bar(L::DO_FREE + i), 1);
       mbar_init(bar(L::ITEM_FULL + i), 1);
-      mbar_init(bar(L::ITEM_EMPTY + i), 1 + NCOMP);  // the issuer and every compute thread
+      mbar_init(bar(L::ITEM_EMPTY + i), 1 + NCOMP + NEPI);  // issuer, compute and epilogue threads
     }
     mbar_init(bar(L::S_READY), 1);
     mbar_init(bar(L::DP_READY), 1);
@@ -392,7 +401,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(bar(L::DS_READY), NCOMP);
     mbar_init(bar(L::VEC_READY), NCOMP);
     mbar_init(bar(L::DONE), 1);
-    mbar_init(bar(L::ACC_FREE), NCOMP);
+    mbar_init(bar(L::ACC_FREE), NEPI);
     mbar_init(bar(L::DRAIN), 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -408,158 +417,163 @@ __global__ void __launch_bounds__(THREADS, 1)
   // TMEM columns: S^T (P^T over columns 0-31 and 64-95) at 0, dP^T (dS^T likewise)
   // at 128, dV at 256, dK at 384
   constexpr uint32_t C_S = 0, C_DP = 128, C_DV = 256, C_DK = 384;
-
-  if (warp == LOAD_WARP) {
-    // ------------------------------------------------ work items and loads (one thread)
-    if (lane == 0) {
-      prefetch_tmap(&tmq);
-      prefetch_tmap(&tmk);
-      prefetch_tmap(&tmv);
-      prefetch_tmap(&tmdo);
-      const uint64_t pol_kv = policy_evict_first();
-      const uint64_t pol_q = policy_evict_last();
-      // bounded-wait test: the CTA that claims work item 0 never issues the loads of that
-      // item's second iteration (global iteration held_g), so the waits run out
-      int held_g = -1;
-      bool ok = true;
-      int g = 0;     // (query head, Q tile) iterations reached, over all items
-      int n_kv = 0;  // K/V tile pairs loaded
-      int n_do = 0, n_q = 0;  // the dO and Q loads of iterations [0, n_do), [0, n_q) are issued
-      for (int r = 0; ok; ++r) {
-        const int slot = r & 1;
-        if (!(ok = mbar_wait<false>(bar(L::ITEM_EMPTY + slot), ((r >> 1) & 1) ^ 1, abort_flag, &g_status, lim)))
-          break;
-        int w = atomicAdd(p.work_counter, 1);
-        if (w >= n_items) w = -1;
-        item_q[slot] = w;
-        mbar_arrive(bar(L::ITEM_FULL + slot));
-        if (w < 0) break;
-        const KVItem it = kv_item<VL>(p, n_kt, w);
-        if (it.n_iter == 0) continue;
-        // K and V, once the last item's final S^T and dP^T have completed
-        if (n_kv > 0 && !(ok = mbar_wait<false>(bar(L::KV_EMPTY), (n_kv - 1) & 1, abort_flag, &g_status, lim)))
-          break;
-        const int kv_y = VL ? it.sq.k0 + it.n0 : it.n0, kv_z = VL ? it.hk : it.b * p.Hkv + it.hk;
-        mbar_expect_tx(bar(L::KV_FULL), 2 * L::TILE);
-        for (int rr = 0; rr < L::NREG; ++rr) {
-          tma_load_3d(sb + L::K_OFF + rr * L::REGION, &tmk, bar(L::KV_FULL), rr * 64, kv_y, kv_z, pol_kv);
-          tma_load_3d(sb + L::V_OFF + rr * L::REGION, &tmv, bar(L::KV_FULL), rr * 64, kv_y, kv_z, pol_kv);
-        }
-        ++n_kv;
-        // iteration g's Q and dO go to buffer g & 1, once iteration g - 2's last products
-        // that read them (dV for dO, dK for Q) have completed
-        for (int i = 0; i < it.n_iter && ok; ++i, ++g) {
-          const int bi = g & 1, h = it.hk * p.group + i / it.per_head, m = it.m_lo + i % it.per_head;
-          const int q_y = VL ? it.sq.q0 + m * BM : m * BM, q_z = VL ? h : it.b * p.Hq + h;
-          const bool held = p.debug_fault == 3 && w == 0 && i == 1;
-          if (held) held_g = g;
-          if (g >= 2 &&
-              !(ok = mbar_wait<false>(bar(L::DO_FREE + bi), ((g - 2) >> 1) & 1, abort_flag, &g_status, lim)))
+  // one branch per warpgroup, each opening with its register limit: 256 compute threads
+  // x 176 + 128 epilogue x 80 + 128 (loads, MMAs, two idle warps) x 80 = 512 x 128
+  if (warp >= LOAD_WARP) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 80;" ::: "memory");
+    if (warp == LOAD_WARP) {
+      // ------------------------------------------------ work items and loads (one thread)
+      if (lane == 0) {
+        prefetch_tmap(&tmq);
+        prefetch_tmap(&tmk);
+        prefetch_tmap(&tmv);
+        prefetch_tmap(&tmdo);
+        const uint64_t pol_kv = policy_evict_first();
+        const uint64_t pol_q = policy_evict_last();
+        // bounded-wait test: the CTA that claims work item 0 never issues the loads of that
+        // item's second iteration (global iteration held_g), so the waits run out
+        int held_g = -1;
+        bool ok = true;
+        int g = 0;     // (query head, Q tile) iterations reached, over all items
+        int n_kv = 0;  // K/V tile pairs loaded
+        int n_do = 0, n_q = 0;  // the dO and Q loads of iterations [0, n_do), [0, n_q) are issued
+        for (int r = 0; ok; ++r) {
+          const int slot = r & 1;
+          if (!(ok = mbar_wait<false>(bar(L::ITEM_EMPTY + slot), ((r >> 1) & 1) ^ 1, abort_flag, &g_status, lim)))
             break;
-          if (!held) {
-            mbar_expect_tx(bar(L::DO_FULL + bi), L::TILE);
-            for (int rr = 0; rr < L::NREG; ++rr)
-              tma_load_3d(sb + L::DO_OFF + bi * L::TILE + rr * L::REGION, &tmdo, bar(L::DO_FULL + bi),
-                          rr * 64, q_y, q_z, pol_q);
-          }
-          n_do = g + 1;
-          if (g >= 2 &&
-              !(ok = mbar_wait<false>(bar(L::Q_FREE + bi), ((g - 2) >> 1) & 1, abort_flag, &g_status, lim)))
+          int w = atomicAdd(p.work_counter, 1);
+          if (w >= n_items) w = -1;
+          item_q[slot] = w;
+          mbar_arrive(bar(L::ITEM_FULL + slot));
+          if (w < 0) break;
+          const KVItem it = kv_item<VL>(p, n_kt, w);
+          if (it.n_iter == 0) continue;
+          // K and V, once the last item's final S^T and dP^T have completed
+          if (n_kv > 0 && !(ok = mbar_wait<false>(bar(L::KV_EMPTY), (n_kv - 1) & 1, abort_flag, &g_status, lim)))
             break;
-          if (!held) {
-            mbar_expect_tx(bar(L::Q_FULL + bi), L::TILE);
-            for (int rr = 0; rr < L::NREG; ++rr)
-              tma_load_3d(sb + L::Q_OFF + bi * L::TILE + rr * L::REGION, &tmq, bar(L::Q_FULL + bi),
-                          rr * 64, q_y, q_z, pol_q);
+          const int kv_y = VL ? it.sq.k0 + it.n0 : it.n0, kv_z = VL ? it.hk : it.b * p.Hkv + it.hk;
+          mbar_expect_tx(bar(L::KV_FULL), 2 * L::TILE);
+          for (int rr = 0; rr < L::NREG; ++rr) {
+            tma_load_3d(sb + L::K_OFF + rr * L::REGION, &tmk, bar(L::KV_FULL), rr * 64, kv_y, kv_z, pol_kv);
+            tma_load_3d(sb + L::V_OFF + rr * L::REGION, &tmv, bar(L::KV_FULL), rr * 64, kv_y, kv_z, pol_kv);
           }
-          n_q = g + 1;
-        }
-      }
-      // nothing may be in flight when the CTA exits: the last load into each buffer (a
-      // buffer is reloaded only after its last load was consumed; a withheld pair was
-      // never issued, and no later load of its buffer is reached)
-      if (n_kv > 0) drain_wait(bar(L::KV_FULL), (n_kv - 1) & 1, lim);
-      for (int i = max(0, n_do - 2); i < n_do; ++i)
-        if (i != held_g) drain_wait(bar(L::DO_FULL + (i & 1)), (i >> 1) & 1, lim);
-      for (int i = max(0, n_q - 2); i < n_q; ++i)
-        if (i != held_g) drain_wait(bar(L::Q_FULL + (i & 1)), (i >> 1) & 1, lim);
-    }
-    __syncwarp();
-  } else if (warp == MMA_WARP) {
-    // ------------------------------------------------------------ MMAs (one thread)
-    if (lane == 0) {
-      const uint32_t hi = desc_hi();
-      const uint32_t k_km = desc_km(sb + L::K_OFF), v_km = desc_km(sb + L::V_OFF);
-      const uint32_t q_km0 = desc_km(sb + L::Q_OFF), do_km0 = desc_km(sb + L::DO_OFF);
-      const uint32_t q_mn0 = desc_mn(sb + L::Q_OFF), do_mn0 = desc_mn(sb + L::DO_OFF);
-      constexpr uint32_t BUF = L::TILE >> 4;  // one Q or dO buffer in the address field
-      auto q_km = [&](int bi) { return q_km0 + bi * BUF; };
-      auto do_km = [&](int bi) { return do_km0 + bi * BUF; };
-      auto q_mn = [&](int bi) { return q_mn0 + bi * BUF; };
-      auto do_mn = [&](int bi) { return do_mn0 + bi * BUF; };
-      auto wait = [&](int bar_i, int parity) -> bool {
-        return mbar_wait<false>(bar(bar_i), parity & 1, abort_flag, &g_status, lim);
-      };
-      bool ok = true;
-      int g = 0;     // iterations issued, over all items
-      int n_it = 0;  // items with iterations
-      for (int r = 0; ok; ++r) {
-        const int slot = r & 1;
-        if (!(ok = wait(L::ITEM_FULL + slot, r >> 1))) break;
-        const int w = item_q[slot];
-        mbar_arrive(bar(L::ITEM_EMPTY + slot));
-        if (w < 0) break;
-        const int n = kv_item<VL>(p, n_kt, w).n_iter;
-        if (n == 0) continue;
-        // S^T(0), dP^T(0); then per iteration i: dV(i), S^T(i+1), dK(i), dP^T(i+1), so
-        // that the compute warps' P phase of i + 1 runs during dK(i), dP^T(i+1) and
-        // their dS phase of i during dV(i), S^T(i+1).  S^T(0) and dP^T(0) overwrite
-        // S^T and dP^T of the last item, read by its dV and dK, issued before them.
-        if (!(ok = wait(L::KV_FULL, n_it) && wait(L::Q_FULL + (g & 1), g >> 1))) break;
-        tc_fence_after();
-        mma_kmajor<D, BF16>(tmem + C_S, k_km, q_km(g & 1), hi);
-        umma_commit(bar(L::S_READY));
-        if (!(ok = wait(L::DO_FULL + (g & 1), g >> 1))) break;
-        tc_fence_after();
-        mma_kmajor<D, BF16>(tmem + C_DP, v_km, do_km(g & 1), hi);
-        umma_commit(bar(L::DP_READY));
-        if (n == 1) umma_commit(bar(L::KV_EMPTY));  // the item's last readers of K and V
-        for (int i = 0; i < n && ok; ++i) {
-          const int gi = g + i, bi = gi & 1, bn = bi ^ 1;
-          if (!(ok = wait(L::P_READY, gi))) break;
-          // the item's first dV overwrites dV: the compute warps must have read the last one
-          if (i == 0 && n_it > 0 && !(ok = wait(L::ACC_FREE, n_it - 1))) break;
-          tc_fence_after();
-          mma_tmem_a<D, BF16>(tmem + C_DV, tmem + C_S, do_mn(bi), hi, i > 0);  // dV += P^T dO
-          umma_commit(bar(L::DO_FREE + bi));
-          if (i + 1 < n) {
-            if (!(ok = wait(L::Q_FULL + bn, (gi + 1) >> 1))) break;
-            tc_fence_after();
-            mma_kmajor<D, BF16>(tmem + C_S, k_km, q_km(bn), hi);  // after dV read P^T there
-            umma_commit(bar(L::S_READY));
-          }
-          if (!(ok = wait(L::DS_READY, gi))) break;
-          tc_fence_after();
-          mma_tmem_a<D, BF16>(tmem + C_DK, tmem + C_DP, q_mn(bi), hi, i > 0);  // dK += dS^T Q
-          umma_commit(bar(L::Q_FREE + bi));
-          if (i + 1 < n) {
-            if (!(ok = wait(L::DO_FULL + bn, (gi + 1) >> 1))) break;
-            tc_fence_after();
-            mma_kmajor<D, BF16>(tmem + C_DP, v_km, do_km(bn), hi);  // after dK read dS^T there
-            umma_commit(bar(L::DP_READY));
-            if (i + 2 == n) umma_commit(bar(L::KV_EMPTY));
+          ++n_kv;
+          // iteration g's Q and dO go to buffer g & 1, once iteration g - 2's last products
+          // that read them (dV for dO, dK for Q) have completed
+          for (int i = 0; i < it.n_iter && ok; ++i, ++g) {
+            const int bi = g & 1, h = it.hk * p.group + i / it.per_head, m = it.m_lo + i % it.per_head;
+            const int q_y = VL ? it.sq.q0 + m * BM : m * BM, q_z = VL ? h : it.b * p.Hq + h;
+            const bool held = p.debug_fault == 3 && w == 0 && i == 1;
+            if (held) held_g = g;
+            if (g >= 2 &&
+                !(ok = mbar_wait<false>(bar(L::DO_FREE + bi), ((g - 2) >> 1) & 1, abort_flag, &g_status, lim)))
+              break;
+            if (!held) {
+              mbar_expect_tx(bar(L::DO_FULL + bi), L::TILE);
+              for (int rr = 0; rr < L::NREG; ++rr)
+                tma_load_3d(sb + L::DO_OFF + bi * L::TILE + rr * L::REGION, &tmdo, bar(L::DO_FULL + bi),
+                            rr * 64, q_y, q_z, pol_q);
+            }
+            n_do = g + 1;
+            if (g >= 2 &&
+                !(ok = mbar_wait<false>(bar(L::Q_FREE + bi), ((g - 2) >> 1) & 1, abort_flag, &g_status, lim)))
+              break;
+            if (!held) {
+              mbar_expect_tx(bar(L::Q_FULL + bi), L::TILE);
+              for (int rr = 0; rr < L::NREG; ++rr)
+                tma_load_3d(sb + L::Q_OFF + bi * L::TILE + rr * L::REGION, &tmq, bar(L::Q_FULL + bi),
+                            rr * 64, q_y, q_z, pol_q);
+            }
+            n_q = g + 1;
           }
         }
-        if (!ok) break;
-        umma_commit(bar(L::DONE));  // this item's dK and dV are complete
-        g += n;
-        ++n_it;
+        // nothing may be in flight when the CTA exits: the last load into each buffer (a
+        // buffer is reloaded only after its last load was consumed; a withheld pair was
+        // never issued, and no later load of its buffer is reached)
+        if (n_kv > 0) drain_wait(bar(L::KV_FULL), (n_kv - 1) & 1, lim);
+        for (int i = max(0, n_do - 2); i < n_do; ++i)
+          if (i != held_g) drain_wait(bar(L::DO_FULL + (i & 1)), (i >> 1) & 1, lim);
+        for (int i = max(0, n_q - 2); i < n_q; ++i)
+          if (i != held_g) drain_wait(bar(L::Q_FULL + (i & 1)), (i >> 1) & 1, lim);
       }
-      umma_commit(bar(L::DRAIN));  // fires once every MMA issued above has completed
-      drain_wait(bar(L::DRAIN), 0, lim);
+      __syncwarp();
+    } else if (warp == MMA_WARP) {
+      // ------------------------------------------------------------ MMAs (one thread)
+      if (lane == 0) {
+        const uint32_t hi = desc_hi();
+        const uint32_t k_km = desc_km(sb + L::K_OFF), v_km = desc_km(sb + L::V_OFF);
+        const uint32_t q_km0 = desc_km(sb + L::Q_OFF), do_km0 = desc_km(sb + L::DO_OFF);
+        const uint32_t q_mn0 = desc_mn(sb + L::Q_OFF), do_mn0 = desc_mn(sb + L::DO_OFF);
+        constexpr uint32_t BUF = L::TILE >> 4;  // one Q or dO buffer in the address field
+        auto q_km = [&](int bi) { return q_km0 + bi * BUF; };
+        auto do_km = [&](int bi) { return do_km0 + bi * BUF; };
+        auto q_mn = [&](int bi) { return q_mn0 + bi * BUF; };
+        auto do_mn = [&](int bi) { return do_mn0 + bi * BUF; };
+        auto wait = [&](int bar_i, int parity) -> bool {
+          return mbar_wait<false>(bar(bar_i), parity & 1, abort_flag, &g_status, lim);
+        };
+        bool ok = true;
+        int g = 0;     // iterations issued, over all items
+        int n_it = 0;  // items with iterations
+        for (int r = 0; ok; ++r) {
+          const int slot = r & 1;
+          if (!(ok = wait(L::ITEM_FULL + slot, r >> 1))) break;
+          const int w = item_q[slot];
+          mbar_arrive(bar(L::ITEM_EMPTY + slot));
+          if (w < 0) break;
+          const int n = kv_item<VL>(p, n_kt, w).n_iter;
+          if (n == 0) continue;
+          // S^T(0), dP^T(0); then per iteration i: dV(i), S^T(i+1), dK(i), dP^T(i+1), so
+          // that the compute warps' P phase of i + 1 runs during dK(i), dP^T(i+1) and
+          // their dS phase of i during dV(i), S^T(i+1).  S^T(0) and dP^T(0) overwrite
+          // S^T and dP^T of the last item, read by its dV and dK, issued before them.
+          if (!(ok = wait(L::KV_FULL, n_it) && wait(L::Q_FULL + (g & 1), g >> 1))) break;
+          tc_fence_after();
+          mma_kmajor<D, BF16>(tmem + C_S, k_km, q_km(g & 1), hi);
+          umma_commit(bar(L::S_READY));
+          if (!(ok = wait(L::DO_FULL + (g & 1), g >> 1))) break;
+          tc_fence_after();
+          mma_kmajor<D, BF16>(tmem + C_DP, v_km, do_km(g & 1), hi);
+          umma_commit(bar(L::DP_READY));
+          if (n == 1) umma_commit(bar(L::KV_EMPTY));  // the item's last readers of K and V
+          for (int i = 0; i < n && ok; ++i) {
+            const int gi = g + i, bi = gi & 1, bn = bi ^ 1;
+            if (!(ok = wait(L::P_READY, gi))) break;
+            // the item's first dV overwrites dV: the compute warps must have read the last one
+            if (i == 0 && n_it > 0 && !(ok = wait(L::ACC_FREE, n_it - 1))) break;
+            tc_fence_after();
+            mma_tmem_a<D, BF16>(tmem + C_DV, tmem + C_S, do_mn(bi), hi, i > 0);  // dV += P^T dO
+            umma_commit(bar(L::DO_FREE + bi));
+            if (i + 1 < n) {
+              if (!(ok = wait(L::Q_FULL + bn, (gi + 1) >> 1))) break;
+              tc_fence_after();
+              mma_kmajor<D, BF16>(tmem + C_S, k_km, q_km(bn), hi);  // after dV read P^T there
+              umma_commit(bar(L::S_READY));
+            }
+            if (!(ok = wait(L::DS_READY, gi))) break;
+            tc_fence_after();
+            mma_tmem_a<D, BF16>(tmem + C_DK, tmem + C_DP, q_mn(bi), hi, i > 0);  // dK += dS^T Q
+            umma_commit(bar(L::Q_FREE + bi));
+            if (i + 1 < n) {
+              if (!(ok = wait(L::DO_FULL + bn, (gi + 1) >> 1))) break;
+              tc_fence_after();
+              mma_kmajor<D, BF16>(tmem + C_DP, v_km, do_km(bn), hi);  // after dK read dS^T there
+              umma_commit(bar(L::DP_READY));
+              if (i + 2 == n) umma_commit(bar(L::KV_EMPTY));
+            }
+          }
+          if (!ok) break;
+          umma_commit(bar(L::DONE));  // this item's dK and dV are complete
+          g += n;
+          ++n_it;
+        }
+        umma_commit(bar(L::DRAIN));  // fires once every MMA issued above has completed
+        drain_wait(bar(L::DRAIN), 0, lim);
+      }
+      __syncwarp();
     }
-    __syncwarp();
-  } else if (warp < 8) {
+  } else if (warp < EPI_WARP) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 176;" ::: "memory");
     // ------------------------------------------------ compute warps: two threads per key row
     // TMEM lane r: key n0 + r; warps w and w + 4 share the lanes of quarter w and
     // take queries [0, 64) and [64, 128) of each Q tile
@@ -571,8 +585,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     auto wait_warp = [&](uint32_t b_, uint32_t ph_) -> bool {
       return __all_sync(0xffffffffu, mbar_wait<false>(b_, ph_, abort_flag, &g_status, lim));
     };
+    // row r's LSE (half 0, log2 units) or delta (half 1) for iteration i of item t, loaded
+    // one iteration ahead so its latency hides behind the current one
+    auto row_value = [&](const KVItem& t, int i) -> float {
+      const int hi = t.hk * p.group + i / t.per_head, qi = (t.m_lo + i % t.per_head) * BM + r;
+      if (qi >= t.sq.nq) return half == 0 ? INFINITY : 0.f;
+      const size_t idx = VL ? (size_t)hi * p.total_q + t.sq.q0 + qi : ((size_t)t.b * p.Hq + hi) * p.Sq + qi;
+      return half == 0 ? p.lse[idx] * 1.4426950408889634f : p.delta[idx];
+    };
     bool ok = true;
-    int g = 0, n_it = 0;
+    int g = 0;
     for (int rq = 0; ok; ++rq) {
       const int slot = rq & 1;
       if (!(ok = wait_warp(bar(L::ITEM_FULL + slot), (rq >> 1) & 1))) break;
@@ -580,28 +602,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_arrive(bar(L::ITEM_EMPTY + slot));
       if (w < 0) break;
       const KVItem it = kv_item<VL>(p, n_kt, w);
-      if (it.skip) continue;
+      if (it.n_iter == 0) continue;  // skipped, or zero rows written by the epilogue warps
       const int key = it.n0 + r;
-      const float f = half == 0 ? 1.f : p.scale;
-      uint16_t* grad = half == 0 ? p.dv : p.dk;
-      uint4* grow = reinterpret_cast<uint4*>(
-          VL ? grad + (size_t)(it.sq.k0 + key) * p.dk_rstride + (size_t)it.hk * D
-             : grad + (((size_t)it.b * p.Hkv + it.hk) * p.Skv + key) * D);
-      if (it.n_iter == 0) {  // no query sees these keys: dK = dV = 0
-        if (key < it.sq.nk)
-          for (int i = 0; i < D / 8; ++i) grow[i] = make_uint4(0, 0, 0, 0);
-        continue;
-      }
-      // row r's LSE (half 0, log2 units) or delta (half 1) for iteration i, loaded one
-      // iteration ahead so its latency hides behind the current one
-      auto row_value = [&](int i) -> float {
-        const int hi = it.hk * p.group + i / it.per_head, qi = (it.m_lo + i % it.per_head) * BM + r;
-        if (qi >= it.sq.nq) return half == 0 ? INFINITY : 0.f;
-        const size_t idx =
-            VL ? (size_t)hi * p.total_q + it.sq.q0 + qi : ((size_t)it.b * p.Hq + hi) * p.Sq + qi;
-        return half == 0 ? p.lse[idx] * 1.4426950408889634f : p.delta[idx];
-      };
-      float next_v = row_value(0);
+      float next_v = row_value(it, 0);
       for (int i = 0; i < it.n_iter && ok; ++i) {
         const int gi = g + i;
         const int m0 = (it.m_lo + i % it.per_head) * BM;
@@ -611,7 +614,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         float* v_dl = v_lse + BM;
         (half == 0 ? v_lse : v_dl)[r] = next_v;
         mbar_arrive(bar(L::VEC_READY));
-        if (i + 1 < it.n_iter) next_v = row_value(i + 1);
+        if (i + 1 < it.n_iter) next_v = row_value(it, i + 1);
         if (!(ok = wait_warp(bar(L::VEC_READY), gi & 1))) break;
         // ---- P phase: P^T = 2^(S^T c - LSE_2) on the visible (key, query) pairs
         if (!(ok = wait_warp(bar(L::S_READY), gi & 1))) break;
@@ -663,25 +666,60 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_arrive(bar(L::DS_READY));
       }
       if (!ok) break;
-      // this tile's dV rows (half 0) and dK rows (half 1): the whole row into registers,
-      // the accumulators handed back to the issuer, then rounded and stored
+      g += it.n_iter;
+    }
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 80;" ::: "memory");
+    // ------------------------------------------------ epilogue: one key row (TMEM lane) per thread
+    // Once the item's last dK product completes, dV and dK of row r go from TMEM into
+    // registers 32 columns at a time; after the last load the accumulators are handed
+    // back (ACC_FREE) and the rows are rounded and stored, off the compute warps' path.
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_t = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    auto wait_warp = [&](uint32_t b_, uint32_t ph_) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait<false>(b_, ph_, abort_flag, &g_status, lim));
+    };
+    bool ok = true;
+    int n_it = 0;
+    for (int rq = 0; ok; ++rq) {
+      const int slot = rq & 1;
+      if (!(ok = wait_warp(bar(L::ITEM_FULL + slot), (rq >> 1) & 1))) break;
+      const int w = item_q[slot];
+      mbar_arrive(bar(L::ITEM_EMPTY + slot));
+      if (w < 0) break;
+      const KVItem it = kv_item<VL>(p, n_kt, w);
+      if (it.skip) continue;
+      const int key = it.n0 + r;
+      const size_t off = VL ? (size_t)(it.sq.k0 + key) * p.dk_rstride + (size_t)it.hk * D
+                            : (((size_t)it.b * p.Hkv + it.hk) * p.Skv + key) * D;
+      uint4* dv_row = reinterpret_cast<uint4*>(p.dv + off);
+      uint4* dk_row = reinterpret_cast<uint4*>(p.dk + off);
+      if (it.n_iter == 0) {  // no query sees these keys: dK = dV = 0
+        if (key < it.sq.nk)
+          for (int i = 0; i < D / 8; ++i) dv_row[i] = dk_row[i] = make_uint4(0, 0, 0, 0);
+        continue;
+      }
       if (!(ok = wait_warp(bar(L::DONE), n_it & 1))) break;
       tc_fence_after();
-      uint32_t v[D];
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c)
-        tmem_ld32(lane_t + (half == 0 ? C_DV : C_DK) + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
-      tc_fence_before();
-      mbar_arrive(bar(L::ACC_FREE));
-      if (key < it.sq.nk) {
+      for (int c = 0; c < 2 * (D / 32); ++c) {  // dV's D columns, then dK's
+        const bool is_dk = c >= D / 32;
+        uint32_t v[32];
+        tmem_ld32(lane_t + (is_dk ? C_DK : C_DV) + 32 * (c % (D / 32)), v);
+        if (c == 2 * (D / 32) - 1) {  // both rows are in registers or stored: hand TMEM back
+          tc_fence_before();
+          mbar_arrive(bar(L::ACC_FREE));
+        }
+        if (key < it.sq.nk) {
+          uint4* dst = (is_dk ? dk_row : dv_row) + 4 * (c % (D / 32));
+          const float f = is_dk ? p.scale : 1.f;
 #pragma unroll
-        for (int i = 0; i < D / 8; ++i) grow[i] = pack8<BF16>(v + 8 * i, f);
+          for (int i = 0; i < 4; ++i) dst[i] = pack8<BF16>(v + 8 * i, f);
+        }
       }
-      g += it.n_iter;
       ++n_it;
     }
   }
-
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -729,10 +767,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(bar(L::DS_READY), NCOMP);
     mbar_init(bar(L::DS_READY + 1), NCOMP);
     mbar_init(bar(L::DONE), 1);
-    mbar_init(bar(L::ACC_FREE), NCOMP);
+    mbar_init(bar(L::ACC_FREE), NEPI);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(L::ITEM_FULL + i), 1);
-      mbar_init(bar(L::ITEM_EMPTY + i), 1 + NCOMP);  // the issuer and every compute thread
+      mbar_init(bar(L::ITEM_EMPTY + i), 1 + NCOMP + NEPI);  // issuer, compute and epilogue threads
     }
     mbar_init(bar(L::DRAIN), 1);
     *abort_flag = 0;
@@ -749,135 +787,140 @@ __global__ void __launch_bounds__(THREADS, 1)
   // TMEM columns: S of even K/V steps at 0, of odd ones at 128 (dS over columns 0-31
   // and 64-95), dP at 256, dQ at 384
   constexpr uint32_t C_S = 0, C_DP = 256, C_DQ = 384;
-
-  if (warp == LOAD_WARP) {
-    // ------------------------------------------------ work items and loads (one thread)
-    if (lane == 0) {
-      prefetch_tmap(&tmq);
-      prefetch_tmap(&tmk);
-      prefetch_tmap(&tmv);
-      prefetch_tmap(&tmdo);
-      const uint64_t pol_q = policy_evict_first();
-      const uint64_t pol_kv = policy_evict_last();
-      bool ok = true;
-      int n_qd = 0;  // Q/dO tile pairs loaded
-      int ld = 0;    // K/V ring loads issued, over all items
-      for (int r = 0; ok; ++r) {
-        const int slot = r & 1;
-        if (!(ok = mbar_wait<false>(bar(L::ITEM_EMPTY + slot), ((r >> 1) & 1) ^ 1, abort_flag, &g_status, lim)))
-          break;
-        int w = atomicAdd(p.work_counter + 1, 1);
-        if (w >= n_items) w = -1;
-        item_q[slot] = w;
-        mbar_arrive(bar(L::ITEM_FULL + slot));
-        if (w < 0) break;
-        const QItem it = q_item<VL>(p, n_mt, w);
-        if (it.n_kv == 0) continue;
-        // Q and dO, once the last item's final S and dP have completed
-        if (n_qd > 0 && !(ok = mbar_wait<false>(bar(L::QD_EMPTY), (n_qd - 1) & 1, abort_flag, &g_status, lim)))
-          break;
-        const int q_y = VL ? it.sq.q0 + it.m0 : it.m0, q_z = VL ? it.h : it.b * p.Hq + it.h;
-        mbar_expect_tx(bar(L::QD_FULL), 2 * L::TILE);
-        for (int rr = 0; rr < L::NREG; ++rr) {
-          tma_load_3d(sb + L::Q_OFF + rr * L::REGION, &tmq, bar(L::QD_FULL), rr * 64, q_y, q_z, pol_q);
-          tma_load_3d(sb + L::DO_OFF + rr * L::REGION, &tmdo, bar(L::QD_FULL), rr * 64, q_y, q_z, pol_q);
-        }
-        ++n_qd;
-        const int hk = it.h / p.group;
-        const int kv_y0 = (VL ? it.sq.k0 : 0) + it.t_lo * BN, kv_z = VL ? hk : it.b * p.Hkv + hk;
-        for (int l = 0; l < 2 * it.n_kv && ok; ++l, ++ld) {  // V_0, K_0, V_1, K_1, ...
-          const int s = ld % NS;
-          if (ld >= NS && !(ok = mbar_wait<false>(bar(L::RING_EMPTY + s), ((ld / NS) - 1) & 1, abort_flag,
-                                                  &g_status, lim)))
+  // one branch per warpgroup, each opening with its register limit: 256 compute threads
+  // x 176 + 128 epilogue x 80 + 128 (loads, MMAs, two idle warps) x 80 = 512 x 128
+  if (warp >= LOAD_WARP) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 80;" ::: "memory");
+    if (warp == LOAD_WARP) {
+      // ------------------------------------------------ work items and loads (one thread)
+      if (lane == 0) {
+        prefetch_tmap(&tmq);
+        prefetch_tmap(&tmk);
+        prefetch_tmap(&tmv);
+        prefetch_tmap(&tmdo);
+        const uint64_t pol_q = policy_evict_first();
+        const uint64_t pol_kv = policy_evict_last();
+        bool ok = true;
+        int n_qd = 0;  // Q/dO tile pairs loaded
+        int ld = 0;    // K/V ring loads issued, over all items
+        for (int r = 0; ok; ++r) {
+          const int slot = r & 1;
+          if (!(ok = mbar_wait<false>(bar(L::ITEM_EMPTY + slot), ((r >> 1) & 1) ^ 1, abort_flag, &g_status, lim)))
             break;
-          mbar_expect_tx(bar(L::RING_FULL + s), L::TILE);
-          const CUtensorMap* tm = (l & 1) ? &tmk : &tmv;
-          for (int rr = 0; rr < L::NREG; ++rr)
-            tma_load_3d(sb + L::RING_OFF + s * L::TILE + rr * L::REGION, tm, bar(L::RING_FULL + s), rr * 64,
-                        kv_y0 + (l >> 1) * BN, kv_z, pol_kv);
+          int w = atomicAdd(p.work_counter + 1, 1);
+          if (w >= n_items) w = -1;
+          item_q[slot] = w;
+          mbar_arrive(bar(L::ITEM_FULL + slot));
+          if (w < 0) break;
+          const QItem it = q_item<VL>(p, n_mt, w);
+          if (it.n_kv == 0) continue;
+          // Q and dO, once the last item's final S and dP have completed
+          if (n_qd > 0 && !(ok = mbar_wait<false>(bar(L::QD_EMPTY), (n_qd - 1) & 1, abort_flag, &g_status, lim)))
+            break;
+          const int q_y = VL ? it.sq.q0 + it.m0 : it.m0, q_z = VL ? it.h : it.b * p.Hq + it.h;
+          mbar_expect_tx(bar(L::QD_FULL), 2 * L::TILE);
+          for (int rr = 0; rr < L::NREG; ++rr) {
+            tma_load_3d(sb + L::Q_OFF + rr * L::REGION, &tmq, bar(L::QD_FULL), rr * 64, q_y, q_z, pol_q);
+            tma_load_3d(sb + L::DO_OFF + rr * L::REGION, &tmdo, bar(L::QD_FULL), rr * 64, q_y, q_z, pol_q);
+          }
+          ++n_qd;
+          const int hk = it.h / p.group;
+          const int kv_y0 = (VL ? it.sq.k0 : 0) + it.t_lo * BN, kv_z = VL ? hk : it.b * p.Hkv + hk;
+          for (int l = 0; l < 2 * it.n_kv && ok; ++l, ++ld) {  // V_0, K_0, V_1, K_1, ...
+            const int s = ld % NS;
+            if (ld >= NS && !(ok = mbar_wait<false>(bar(L::RING_EMPTY + s), ((ld / NS) - 1) & 1, abort_flag,
+                                                    &g_status, lim)))
+              break;
+            mbar_expect_tx(bar(L::RING_FULL + s), L::TILE);
+            const CUtensorMap* tm = (l & 1) ? &tmk : &tmv;
+            for (int rr = 0; rr < L::NREG; ++rr)
+              tma_load_3d(sb + L::RING_OFF + s * L::TILE + rr * L::REGION, tm, bar(L::RING_FULL + s), rr * 64,
+                          kv_y0 + (l >> 1) * BN, kv_z, pol_kv);
+          }
         }
+        // the last Q/dO pair and the last NS ring loads may still be in flight
+        if (n_qd > 0) drain_wait(bar(L::QD_FULL), (n_qd - 1) & 1, lim);
+        for (int l = max(0, ld - NS); l < ld; ++l) drain_wait(bar(L::RING_FULL + l % NS), (l / NS) & 1, lim);
       }
-      // the last Q/dO pair and the last NS ring loads may still be in flight
-      if (n_qd > 0) drain_wait(bar(L::QD_FULL), (n_qd - 1) & 1, lim);
-      for (int l = max(0, ld - NS); l < ld; ++l) drain_wait(bar(L::RING_FULL + l % NS), (l / NS) & 1, lim);
-    }
-    __syncwarp();
-  } else if (warp == MMA_WARP) {
-    // ------------------------------------------------------------ MMAs (one thread)
-    if (lane == 0) {
-      const uint32_t hi = desc_hi();
-      const uint32_t q_km = desc_km(sb + L::Q_OFF), do_km = desc_km(sb + L::DO_OFF);
-      const uint32_t ring_km0 = desc_km(sb + L::RING_OFF), ring_mn0 = desc_mn(sb + L::RING_OFF);
-      constexpr uint32_t SLOT = L::TILE >> 4;  // one ring slot in the address field
-      auto ring_km = [&](int l) { return ring_km0 + (uint32_t)(l % NS) * SLOT; };
-      auto ring_mn = [&](int l) { return ring_mn0 + (uint32_t)(l % NS) * SLOT; };
-      auto wait = [&](int bar_i, int parity) -> bool {
-        return mbar_wait<false>(bar(bar_i), parity & 1, abort_flag, &g_status, lim);
-      };
-      auto ring_wait = [&](int l) -> bool { return wait(L::RING_FULL + l % NS, l / NS); };
-      bool ok = true;
-      // step g reads ring loads 2g (V) and 2g + 1 (K); V is released once dP has read it,
-      // K once dQ has, so with NS = 5 both tiles of step g + 2 land while step g runs
-      int g = 0;     // K/V steps issued over all items
-      int n_it = 0;  // items with K/V steps
-      for (int r = 0; ok; ++r) {
-        const int slot = r & 1;
-        if (!(ok = wait(L::ITEM_FULL + slot, r >> 1))) break;
-        const int w = item_q[slot];
-        mbar_arrive(bar(L::ITEM_EMPTY + slot));
-        if (w < 0) break;
-        const int n = q_item<VL>(p, n_mt, w).n_kv;
-        if (n == 0) continue;
-        // S(0), dP(0); then per K/V step j: S(j+1) into the other S buffer, dP(j+1)
-        // once the compute warps hold dP(j), dQ += dS(j) K(j) once they wrote dS(j).
-        // S(0) goes to the buffer of step g, whose last dS was read by a dQ issued
-        // before; dP(0) waits until the compute warps hold the last item's final dP.
-        if (!(ok = wait(L::QD_FULL, n_it) && ring_wait(2 * g + 1))) break;
-        tc_fence_after();
-        mma_kmajor<D, BF16>(tmem + C_S + 128u * (g & 1), q_km, ring_km(2 * g + 1), hi);
-        umma_commit(bar(L::S_READY + (g & 1)));
-        if (g > 0 && !(ok = wait(L::DP_FREE, g - 1))) break;
-        if (!(ok = ring_wait(2 * g))) break;
-        tc_fence_after();
-        mma_kmajor<D, BF16>(tmem + C_DP, do_km, ring_km(2 * g), hi);
-        umma_commit(bar(L::DP_READY));
-        umma_commit(bar(L::RING_EMPTY + (2 * g) % NS));  // V(0): read by dP(0)
-        if (n == 1) umma_commit(bar(L::QD_EMPTY));  // the item's last readers of Q and dO
-        for (int j = 0; j < n && ok; ++j) {
-          const int gj = g + j;
-          if (j + 1 < n) {
-            if (!(ok = ring_wait(2 * gj + 3))) break;
-            tc_fence_after();
-            // the other buffer held dS(gj - 1), read by dQ(gj - 1), issued before
-            mma_kmajor<D, BF16>(tmem + C_S + 128u * ((gj + 1) & 1), q_km, ring_km(2 * gj + 3), hi);
-            umma_commit(bar(L::S_READY + ((gj + 1) & 1)));
-          }
-          if (!(ok = wait(L::DP_FREE, gj))) break;
-          if (j + 1 < n) {
-            if (!(ok = ring_wait(2 * gj + 2))) break;
-            tc_fence_after();
-            mma_kmajor<D, BF16>(tmem + C_DP, do_km, ring_km(2 * gj + 2), hi);
-            umma_commit(bar(L::DP_READY));
-            umma_commit(bar(L::RING_EMPTY + (2 * gj + 2) % NS));  // V(j+1): read by dP(j+1)
-            if (j + 2 == n) umma_commit(bar(L::QD_EMPTY));
-          }
-          if (!(ok = wait(L::DS_READY + (gj & 1), gj >> 1))) break;
-          // the item's first dQ overwrites dQ: the compute warps must have read the last one
-          if (j == 0 && n_it > 0 && !(ok = wait(L::ACC_FREE, n_it - 1))) break;
+      __syncwarp();
+    } else if (warp == MMA_WARP) {
+      // ------------------------------------------------------------ MMAs (one thread)
+      if (lane == 0) {
+        const uint32_t hi = desc_hi();
+        const uint32_t q_km = desc_km(sb + L::Q_OFF), do_km = desc_km(sb + L::DO_OFF);
+        const uint32_t ring_km0 = desc_km(sb + L::RING_OFF), ring_mn0 = desc_mn(sb + L::RING_OFF);
+        constexpr uint32_t SLOT = L::TILE >> 4;  // one ring slot in the address field
+        auto ring_km = [&](int l) { return ring_km0 + (uint32_t)(l % NS) * SLOT; };
+        auto ring_mn = [&](int l) { return ring_mn0 + (uint32_t)(l % NS) * SLOT; };
+        auto wait = [&](int bar_i, int parity) -> bool {
+          return mbar_wait<false>(bar(bar_i), parity & 1, abort_flag, &g_status, lim);
+        };
+        auto ring_wait = [&](int l) -> bool { return wait(L::RING_FULL + l % NS, l / NS); };
+        bool ok = true;
+        // step g reads ring loads 2g (V) and 2g + 1 (K); V is released once dP has read it,
+        // K once dQ has, so with NS = 5 both tiles of step g + 2 land while step g runs
+        int g = 0;     // K/V steps issued over all items
+        int n_it = 0;  // items with K/V steps
+        for (int r = 0; ok; ++r) {
+          const int slot = r & 1;
+          if (!(ok = wait(L::ITEM_FULL + slot, r >> 1))) break;
+          const int w = item_q[slot];
+          mbar_arrive(bar(L::ITEM_EMPTY + slot));
+          if (w < 0) break;
+          const int n = q_item<VL>(p, n_mt, w).n_kv;
+          if (n == 0) continue;
+          // S(0), dP(0); then per K/V step j: S(j+1) into the other S buffer, dP(j+1)
+          // once the compute warps hold dP(j), dQ += dS(j) K(j) once they wrote dS(j).
+          // S(0) goes to the buffer of step g, whose last dS was read by a dQ issued
+          // before; dP(0) waits until the compute warps hold the last item's final dP.
+          if (!(ok = wait(L::QD_FULL, n_it) && ring_wait(2 * g + 1))) break;
           tc_fence_after();
-          mma_tmem_a<D, BF16>(tmem + C_DQ, tmem + C_S + 128u * (gj & 1), ring_mn(2 * gj + 1), hi, j > 0);  // dQ += dS K
-          umma_commit(bar(L::RING_EMPTY + (2 * gj + 1) % NS));  // K(j): read by S(j) and dQ(j)
+          mma_kmajor<D, BF16>(tmem + C_S + 128u * (g & 1), q_km, ring_km(2 * g + 1), hi);
+          umma_commit(bar(L::S_READY + (g & 1)));
+          if (g > 0 && !(ok = wait(L::DP_FREE, g - 1))) break;
+          if (!(ok = ring_wait(2 * g))) break;
+          tc_fence_after();
+          mma_kmajor<D, BF16>(tmem + C_DP, do_km, ring_km(2 * g), hi);
+          umma_commit(bar(L::DP_READY));
+          umma_commit(bar(L::RING_EMPTY + (2 * g) % NS));  // V(0): read by dP(0)
+          if (n == 1) umma_commit(bar(L::QD_EMPTY));  // the item's last readers of Q and dO
+          for (int j = 0; j < n && ok; ++j) {
+            const int gj = g + j;
+            if (j + 1 < n) {
+              if (!(ok = ring_wait(2 * gj + 3))) break;
+              tc_fence_after();
+              // the other buffer held dS(gj - 1), read by dQ(gj - 1), issued before
+              mma_kmajor<D, BF16>(tmem + C_S + 128u * ((gj + 1) & 1), q_km, ring_km(2 * gj + 3), hi);
+              umma_commit(bar(L::S_READY + ((gj + 1) & 1)));
+            }
+            if (!(ok = wait(L::DP_FREE, gj))) break;
+            if (j + 1 < n) {
+              if (!(ok = ring_wait(2 * gj + 2))) break;
+              tc_fence_after();
+              mma_kmajor<D, BF16>(tmem + C_DP, do_km, ring_km(2 * gj + 2), hi);
+              umma_commit(bar(L::DP_READY));
+              umma_commit(bar(L::RING_EMPTY + (2 * gj + 2) % NS));  // V(j+1): read by dP(j+1)
+              if (j + 2 == n) umma_commit(bar(L::QD_EMPTY));
+            }
+            if (!(ok = wait(L::DS_READY + (gj & 1), gj >> 1))) break;
+            // the item's first dQ overwrites dQ: the compute warps must have read the last one
+            if (j == 0 && n_it > 0 && !(ok = wait(L::ACC_FREE, n_it - 1))) break;
+            tc_fence_after();
+            mma_tmem_a<D, BF16>(tmem + C_DQ, tmem + C_S + 128u * (gj & 1), ring_mn(2 * gj + 1), hi, j > 0);  // dQ += dS K
+            umma_commit(bar(L::RING_EMPTY + (2 * gj + 1) % NS));  // K(j): read by S(j) and dQ(j)
+          }
+          if (!ok) break;
+          umma_commit(bar(L::DONE));
+          g += n;
+          ++n_it;
         }
-        if (!ok) break;
-        umma_commit(bar(L::DONE));
-        g += n;
-        ++n_it;
+        umma_commit(bar(L::DRAIN));
+        drain_wait(bar(L::DRAIN), 0, lim);
       }
-      umma_commit(bar(L::DRAIN));
-      drain_wait(bar(L::DRAIN), 0, lim);
+      __syncwarp();
     }
-    __syncwarp();
-  } else if (warp < 8) {
+  } else if (warp < EPI_WARP) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 176;" ::: "memory");
     // ------------------------------------------------ compute warps: two threads per query row
     const int quarter = warp & 3, half = warp >> 2;
     const int r = quarter * 32 + lane;
@@ -887,7 +930,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       return __all_sync(0xffffffffu, mbar_wait<false>(b_, ph_, abort_flag, &g_status, lim));
     };
     bool ok = true;
-    int g = 0, n_it = 0;
+    int g = 0;
     for (int rq = 0; ok; ++rq) {
       const int slot = rq & 1;
       if (!(ok = wait_warp(bar(L::ITEM_FULL + slot), (rq >> 1) & 1))) break;
@@ -895,19 +938,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_arrive(bar(L::ITEM_EMPTY + slot));
       if (w < 0) break;
       const QItem it = q_item<VL>(p, n_mt, w);
-      if (it.skip) continue;
+      if (it.n_kv == 0) continue;  // skipped, or zero rows written by the epilogue warps
       const int row = it.m0 + r;
       const bool live = row < it.sq.nq;
       const size_t ridx =
           VL ? (size_t)it.h * p.total_q + it.sq.q0 + row : ((size_t)it.b * p.Hq + it.h) * p.Sq + row;
-      uint4* dst = reinterpret_cast<uint4*>(
-          (VL ? p.dq + (size_t)(it.sq.q0 + row) * p.dq_rstride + (size_t)it.h * D : p.dq + ridx * D) +
-          half * (D / 2));
-      if (it.n_kv == 0) {  // the rows see no key: dQ = 0
-        if (live)
-          for (int i = 0; i < D / 16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
-        continue;
-      }
       const float lse2 = live ? p.lse[ridx] * 1.4426950408889634f : INFINITY;
       const float dlt = live ? p.delta[ridx] : 0.f;
       // keys of this row: [key_lo, key_hi] (none for rows past the sequence)
@@ -945,25 +980,57 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_arrive(bar(L::DS_READY + (gj & 1)));
       }
       if (!ok) break;
-      // dQ = scale * (dS K) summed over the K/V tiles: this thread's half of the row into
-      // registers, dQ handed back to the issuer, then rounded and stored
+      g += it.n_kv;
+    }
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 80;" ::: "memory");
+    // ------------------------------------------------ epilogue: one query row (TMEM lane) per thread
+    // Once the item's last dQ product completes, the row goes from TMEM into registers
+    // 32 columns at a time; after the last load dQ is handed back (ACC_FREE), and the
+    // row is scaled, rounded and stored, off the compute warps' path.
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_t = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    auto wait_warp = [&](uint32_t b_, uint32_t ph_) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait<false>(b_, ph_, abort_flag, &g_status, lim));
+    };
+    bool ok = true;
+    int n_it = 0;
+    for (int rq = 0; ok; ++rq) {
+      const int slot = rq & 1;
+      if (!(ok = wait_warp(bar(L::ITEM_FULL + slot), (rq >> 1) & 1))) break;
+      const int w = item_q[slot];
+      mbar_arrive(bar(L::ITEM_EMPTY + slot));
+      if (w < 0) break;
+      const QItem it = q_item<VL>(p, n_mt, w);
+      if (it.skip) continue;
+      const int row = it.m0 + r;
+      const bool live = row < it.sq.nq;
+      uint4* dst = reinterpret_cast<uint4*>(
+          VL ? p.dq + (size_t)(it.sq.q0 + row) * p.dq_rstride + (size_t)it.h * D
+             : p.dq + (((size_t)it.b * p.Hq + it.h) * p.Sq + row) * D);
+      if (it.n_kv == 0) {  // the rows see no key: dQ = 0
+        if (live)
+          for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+        continue;
+      }
       if (!(ok = wait_warp(bar(L::DONE), n_it & 1))) break;
       tc_fence_after();
-      uint32_t v[D / 2];
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c)
-        tmem_ld32(lane_t + C_DQ + half * (D / 2) + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
-      tc_fence_before();
-      mbar_arrive(bar(L::ACC_FREE));
-      if (live) {
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(lane_t + C_DQ + 32 * c, v);
+        if (c == D / 32 - 1) {  // the whole row is in registers or stored: hand dQ back
+          tc_fence_before();
+          mbar_arrive(bar(L::ACC_FREE));
+        }
+        if (live) {
 #pragma unroll
-        for (int i = 0; i < D / 16; ++i) dst[i] = pack8<BF16>(v + 8 * i, p.scale);
+          for (int i = 0; i < 4; ++i) dst[4 * c + i] = pack8<BF16>(v + 8 * i, p.scale);
+        }
       }
-      g += it.n_kv;
       ++n_it;
     }
   }
-
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
