@@ -84,6 +84,7 @@ struct Params {
   const int32_t* cu_k;
   int total_q, total_k;
   long long dq_rstride, dk_rstride;
+  int st32;  // dq, dk, dv and their row strides are 32-byte aligned: 32-byte stores
 };
 
 // Query and key tokens of one sequence (the token-major layouts), or the dense
@@ -263,6 +264,27 @@ __device__ __forceinline__ uint4 pack8(const uint32_t* r, float f) {
                     pack2<BF16>(__uint_as_float(r[2]) * f, __uint_as_float(r[3]) * f),
                     pack2<BF16>(__uint_as_float(r[4]) * f, __uint_as_float(r[5]) * f),
                     pack2<BF16>(__uint_as_float(r[6]) * f, __uint_as_float(r[7]) * f));
+}
+
+// 32 consecutive fp32 values of a TMEM row, times f, as 16-bit values at dst (64 bytes):
+// two 32-byte stores, each a whole sector, when dst is 32-byte aligned, else four
+// 16-byte ones.
+template <bool BF16>
+__device__ __forceinline__ void store_row32(void* dst, const uint32_t (&v)[32], float f, bool st32) {
+  if (st32) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t pk[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        pk[i] = pack2<BF16>(__uint_as_float(v[16 * h + 2 * i]) * f, __uint_as_float(v[16 * h + 2 * i + 1]) * f);
+      st_global_v8(static_cast<char*>(dst) + 32 * h, pk);
+    }
+  } else {
+    uint4* d = static_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d[i] = pack8<BF16>(v + 8 * i, f);
+  }
 }
 
 // delta_i = sum_d dO_id O_id (rows of D contiguous elements).  D / 8 lanes share a row,
@@ -711,10 +733,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_arrive(bar(L::ACC_FREE));
         }
         if (key < it.sq.nk) {
-          uint4* dst = (is_dk ? dk_row : dv_row) + 4 * (c % (D / 32));
-          const float f = is_dk ? p.scale : 1.f;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = pack8<BF16>(v + 8 * i, f);
+          store_row32<BF16>((is_dk ? dk_row : dv_row) + 4 * (c % (D / 32)), v, is_dk ? p.scale : 1.f, p.st32);
         }
       }
       ++n_it;
@@ -1023,10 +1042,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_fence_before();
           mbar_arrive(bar(L::ACC_FREE));
         }
-        if (live) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dst[4 * c + i] = pack8<BF16>(v + 8 * i, p.scale);
-        }
+        if (live) store_row32<BF16>(dst + 4 * c, v, p.scale, p.st32);
       }
       ++n_it;
     }
@@ -1118,6 +1134,9 @@ static cudaError_t launch_t(const BwdArgs& a, cudaStream_t stream) {
   p.total_k = a.total_k;
   p.dq_rstride = a.dq_rstride;
   p.dk_rstride = a.dk_rstride;
+  p.st32 = (reinterpret_cast<uintptr_t>(a.dq) | reinterpret_cast<uintptr_t>(a.dk) |
+            reinterpret_cast<uintptr_t>(a.dv)) % 32 == 0 &&
+           (a.dq_rstride * 2) % 32 == 0 && (a.dk_rstride * 2) % 32 == 0;
   const long long n_kt = (a.Skv + BN - 1) / BN, n_mt = (a.Sq + BM - 1) / BM;
   // both persistent kernels claim work items from the two zeroed counters
   p.work_counter = a.work_counter;
