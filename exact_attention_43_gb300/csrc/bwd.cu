@@ -435,6 +435,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the dQ kernel reads nothing this one writes: it may take each SM this grid leaves
+  griddep_launch_dependents();
   const uint32_t tmem = misc[0];
   // TMEM columns: S^T (P^T over columns 0-31 and 64-95) at 0, dP^T (dS^T likewise)
   // at 128, dV at 256, dK at 384
@@ -1053,6 +1055,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
+  // launched to overlap the dK/dV kernel's last items: complete only after it has, so
+  // that work ordered after this kernel also sees dK and dV
+  griddep_wait();
 }
 
 // 3-D tensor map over 16-bit elements: D contiguous, then n1 rows s1 elements apart,
@@ -1178,8 +1183,19 @@ static cudaError_t launch_t(const BwdArgs& a, cudaStream_t stream) {
     p.per_group_q = (int)per;
     const long long n_items = n_mt * a.Hq * a.B;
     const int grid = (int)(n_items < sms ? n_items : sms);
-    bwd_dq_kernel<D, BF16, VL><<<grid, THREADS, L::ALLOC, stream>>>(tq, tk, tv, tg, p);
-    return cudaGetLastError();
+    // After the dK/dV kernel its CTAs start on the SMs that kernel's CTAs leave, while
+    // its last items run (programmatic stream serialization; it signals at its start).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = L::ALLOC;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = n_kt > 0 ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, bwd_dq_kernel<D, BF16, VL>, tq, tk, tv, tg, p);
   }
   return cudaSuccess;
 }
