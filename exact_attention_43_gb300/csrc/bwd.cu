@@ -309,6 +309,7 @@ __global__ void __launch_bounds__(DELTA_THREADS) bwd_delta_kernel(const uint16_t
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = lane / LPR, part = lane % LPR;
   const long long row0 = (long long)blockIdx.x * delta_rows_per_block<D>() + (long long)warp * RPW * DELTA_UNROLL;
+  griddep_launch_dependents();  // the dK/dV kernel may start setting up on SMs this grid leaves
   uint4 a[DELTA_UNROLL], g[DELTA_UNROLL];
 #pragma unroll
   for (int u = 0; u < DELTA_UNROLL; ++u) {
@@ -435,8 +436,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // the dQ kernel reads nothing this one writes: it may take each SM this grid leaves
-  griddep_launch_dependents();
   const uint32_t tmem = misc[0];
   // TMEM columns: S^T (P^T over columns 0-31 and 64-95) at 0, dP^T (dS^T likewise)
   // at 128, dV at 256, dK at 384
@@ -617,6 +616,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       const size_t idx = VL ? (size_t)hi * p.total_q + t.sq.q0 + qi : ((size_t)t.b * p.Hq + hi) * p.Sq + qi;
       return half == 0 ? p.lse[idx] * 1.4426950408889634f : p.delta[idx];
     };
+    // The row terms come from the kernel before this one, which this one was launched to
+    // overlap: wait for its completion; then the dQ kernel, which reads them too and
+    // nothing this one writes, may take each SM this grid leaves.
+    griddep_wait();
+    griddep_launch_dependents();
     bool ok = true;
     int g = 0;
     for (int rq = 0; ok; ++rq) {
@@ -1080,6 +1084,10 @@ template <int D, bool BF16, bool VL>
 static cudaError_t launch_t(const BwdArgs& a, cudaStream_t stream) {
   // row terms: one per (query token, head) in either layout
   const long long rows = VL ? (long long)a.total_q * a.Hq : (long long)a.B * a.Hq * a.Sq;
+  {
+    cudaError_t e = cudaMemsetAsync(a.work_counter, 0, 2 * sizeof(int), stream);
+    if (e != cudaSuccess) return e;
+  }
   if (rows > 0) {
     constexpr int RB = delta_rows_per_block<D>();
     bwd_delta_kernel<D, BF16><<<(unsigned)((rows + RB - 1) / RB), DELTA_THREADS, 0, stream>>>(
@@ -1143,12 +1151,9 @@ static cudaError_t launch_t(const BwdArgs& a, cudaStream_t stream) {
             reinterpret_cast<uintptr_t>(a.dv)) % 32 == 0 &&
            (a.dq_rstride * 2) % 32 == 0 && (a.dk_rstride * 2) % 32 == 0;
   const long long n_kt = (a.Skv + BN - 1) / BN, n_mt = (a.Sq + BM - 1) / BM;
-  // both persistent kernels claim work items from the two zeroed counters
+  // both persistent kernels claim work items from the two counters, zeroed before the
+  // row terms kernel
   p.work_counter = a.work_counter;
-  {
-    cudaError_t e = cudaMemsetAsync(a.work_counter, 0, 2 * sizeof(int), stream);
-    if (e != cudaSuccess) return e;
-  }
   const int sms = a.num_sms > 0 ? a.num_sms : 1;
   const int g = a.Hq / a.Hkv;
   if (n_kt > 0) {
@@ -1165,8 +1170,19 @@ static cudaError_t launch_t(const BwdArgs& a, cudaStream_t stream) {
     p.per_group = (int)per;
     const long long n_items = n_kt * a.Hkv * a.B;
     const int grid = (int)(n_items < sms ? n_items : sms);
-    bwd_dkdv_kernel<D, BF16, VL><<<grid, THREADS, L::ALLOC, stream>>>(tq, tk, tv, tg, p);
-    e = cudaGetLastError();
+    // after the row terms kernel, its CTAs set up on the SMs that kernel's CTAs leave
+    // (programmatic stream serialization; the compute warps wait for its completion)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = L::ALLOC;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = rows > 0 ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, bwd_dkdv_kernel<D, BF16, VL>, tq, tk, tv, tg, p);
     if (e != cudaSuccess) return e;
   }
   if (n_mt > 0 && rows > 0) {
