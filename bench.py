@@ -26,7 +26,11 @@ Inputs are resident in HBM when the timed region starts; the e2e figure
 repeats the step from pinned host buffers with the copies inside its timed
 region: every prefill's Q, K, V, the decode queries, the valid prefix
 (seq_lens rows) of every (sequence, KV head) of the K and V caches, and
-seq_lens in; every O, LSE and the decode output back.  The backward (attn_bwd)
+seq_lens in; every O, LSE and the decode output back.  The copies overlap the
+computation as a serving loop would: a leg's inputs go over on a copy stream while
+the legs before it compute, and its results come back on another stream while the
+legs after it compute; a step ends when its last result is on the host.  The
+backward (attn_bwd)
 of the three prefill workloads is timed after the step, in a loop of its own,
 and reported under "backward"; it is not part of the metric.
 """
@@ -410,21 +414,55 @@ def main():
         h2d += 2 * sum(n for _, _, n in kv_prefix) * hdk.shape[3] * hdk.element_size()
         d2h += hdo.numel() * hdo.element_size()
 
-        def e2e_step():
-            for (name, w, q, k, v, o, lse), (hq, hk, hv, ho, hl) in zip(fwd_legs, host_fwd):
+        # Copies overlap compute: each leg's inputs go over on a copy stream as soon as
+        # that leg's previous computation has read its buffers, the legs compute in order
+        # on the compute stream once their inputs are in, and each leg's results come
+        # back on a third stream; a step ends when its last results are on the host.
+        h2d_stream = torch.cuda.Stream(device=dev)
+        d2h_stream = torch.cuda.Stream(device=dev)
+        freed = [torch.cuda.Event() for _ in range(n_legs)]  # leg i read its inputs
+
+        def leg_h2d(i):
+            if i < len(fwd_legs):
+                _, _, q, k, v, _, _ = fwd_legs[i]
+                hq, hk, hv, _, _ = host_fwd[i]
                 q.copy_(hq, non_blocking=True)
                 k.copy_(hk, non_blocking=True)
                 v.copy_(hv, non_blocking=True)
-                ea.attn_fwd(q, k, v, causal=True, scale=w.scale, out=o, lse=lse, stream=stream)
+            else:
+                dq.copy_(hdq, non_blocking=True)
+                for b, h, n in kv_prefix:
+                    dk[b, h, :n].copy_(hdk[b, h, :n], non_blocking=True)
+                    dv[b, h, :n].copy_(hdv[b, h, :n], non_blocking=True)
+                lens_d.copy_(hlens, non_blocking=True)
+
+        def leg_d2h(i):
+            if i < len(fwd_legs):
+                _, _, _, _, _, o, lse = fwd_legs[i]
+                _, _, _, ho, hl = host_fwd[i]
                 ho.copy_(o, non_blocking=True)
                 hl.copy_(lse, non_blocking=True)
-            dq.copy_(hdq, non_blocking=True)
-            for b, h, n in kv_prefix:
-                dk[b, h, :n].copy_(hdk[b, h, :n], non_blocking=True)
-                dv[b, h, :n].copy_(hdv[b, h, :n], non_blocking=True)
-            lens_d.copy_(hlens, non_blocking=True)
-            ea.attn_decode(dq, dk, dv, lens_d, num_splits=dw.num_splits, out=do, stream=stream)
-            hdo.copy_(do, non_blocking=True)
+            else:
+                hdo.copy_(do, non_blocking=True)
+
+        def e2e_step():
+            h2d_stream.wait_stream(stream)  # nothing of this step starts before it
+            ready = []
+            with torch.cuda.stream(h2d_stream):
+                for i in range(n_legs):
+                    h2d_stream.wait_event(freed[i])
+                    leg_h2d(i)
+                    ev_i = torch.cuda.Event()
+                    ev_i.record(h2d_stream)
+                    ready.append(ev_i)
+            for i in range(n_legs):
+                stream.wait_event(ready[i])
+                run_leg(i)
+                freed[i].record(stream)
+                d2h_stream.wait_event(freed[i])
+                with torch.cuda.stream(d2h_stream):
+                    leg_d2h(i)
+            stream.wait_stream(d2h_stream)
 
         e2e_step()
         torch.cuda.synchronize()
