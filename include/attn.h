@@ -6,7 +6,9 @@
  * device.  Work is enqueued asynchronously on the caller's CUDA stream; the
  * library keeps no pointer after a call returns and the caller owns every
  * buffer.  All tensors are dense, row-major, with the head dimension
- * innermost.
+ * innermost.  Workspaces are allocated and freed on the caller's stream, so a
+ * call may be captured into a CUDA graph (the backward's kernels are chained by
+ * programmatic launches, recorded as programmatic edges).
  *
  * Sources of what is computed (page title and the part of the page):
  *   - abaddon 0.2.0-rc.2, src/cuda_inference/kernels/attention.rs: module doc
