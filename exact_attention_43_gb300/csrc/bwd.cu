@@ -33,7 +33,10 @@
 //    accumulated in TMEM and stored once.  Recomputing S and dP costs two more
 //    products per (Q tile, KV tile) than one kernel that adds dQ into memory from the
 //    dK/dV kernel, but the compute warps then overlap the tensor core instead of
-//    waiting on it, and dQ needs no fp32 atomics.
+//    waiting on it, and dQ needs no fp32 atomics;
+//  * the three kernels are chained by programmatic launches: the dK/dV kernel sets up
+//    while the prep kernel's last CTAs run, and the dQ kernel, which reads nothing the
+//    dK/dV kernel writes, takes each SM the dK/dV kernel's last items leave.
 #include "internal.h"
 #include "ptx.cuh"
 
