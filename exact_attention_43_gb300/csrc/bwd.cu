@@ -990,17 +990,29 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_ld32(lane_t + C_DP + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(dr + 32));
         tc_fence_before();
         mbar_arrive(bar(L::DP_FREE));  // dP(j + 1) may overwrite dP(j)
-        // keys kb + u, ulo <= u < uhi, are visible to this row
+        // keys kb + u, ulo <= u < uhi, are visible to this row; a tile whose every key
+        // is visible to the whole warp's rows (all but the diagonal, the window's edges
+        // and the ragged ends) needs no test
         const int kb = (it.t_lo + j) * BN + c0, ulo = key_lo - kb, uhi = key_hi + 1 - kb;
         uint32_t pk[32];
+        if (__all_sync(0xffffffffu, ulo <= 0 && uhi >= 64)) {
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-          const float p0 =
-              (2 * u >= ulo && 2 * u < uhi) ? ex2(fmaf(__uint_as_float(sr[2 * u]), p.c2, -lse2)) : 0.f;
-          const float p1 = (2 * u + 1 >= ulo && 2 * u + 1 < uhi)
-                               ? ex2(fmaf(__uint_as_float(sr[2 * u + 1]), p.c2, -lse2)) : 0.f;
-          pk[u] = pack2<BF16>(p0 * (__uint_as_float(dr[2 * u]) - dlt),
-                              p1 * (__uint_as_float(dr[2 * u + 1]) - dlt));
+          for (int u = 0; u < 32; ++u) {
+            const float p0 = ex2(fmaf(__uint_as_float(sr[2 * u]), p.c2, -lse2));
+            const float p1 = ex2(fmaf(__uint_as_float(sr[2 * u + 1]), p.c2, -lse2));
+            pk[u] = pack2<BF16>(p0 * (__uint_as_float(dr[2 * u]) - dlt),
+                                p1 * (__uint_as_float(dr[2 * u + 1]) - dlt));
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < 32; ++u) {
+            const float p0 =
+                (2 * u >= ulo && 2 * u < uhi) ? ex2(fmaf(__uint_as_float(sr[2 * u]), p.c2, -lse2)) : 0.f;
+            const float p1 = (2 * u + 1 >= ulo && 2 * u + 1 < uhi)
+                                 ? ex2(fmaf(__uint_as_float(sr[2 * u + 1]), p.c2, -lse2)) : 0.f;
+            pk[u] = pack2<BF16>(p0 * (__uint_as_float(dr[2 * u]) - dlt),
+                                p1 * (__uint_as_float(dr[2 * u + 1]) - dlt));
+          }
         }
         tmem_st32(t_s + c0, pk);  // dS over the S columns this thread read
         tmem_wait_st();
