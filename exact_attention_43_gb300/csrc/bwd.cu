@@ -269,6 +269,13 @@ __device__ __forceinline__ uint4 pack8(const uint32_t* r, float f) {
                     pack2<BF16>(__uint_as_float(r[6]) * f, __uint_as_float(r[7]) * f));
 }
 
+// a * b on both lanes of two packed f32 values (sm_100 and later: one instruction).
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // 32 consecutive fp32 values of a TMEM row, times f, as 16-bit values at dst (64 bytes):
 // two 32-byte stores, each a whole sector, when dst is 32-byte aligned, else four
 // 16-byte ones.
@@ -611,13 +618,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     auto wait_warp = [&](uint32_t b_, uint32_t ph_) -> bool {
       return __all_sync(0xffffffffu, mbar_wait<false>(b_, ph_, abort_flag, &g_status, lim));
     };
-    // row r's LSE (half 0, log2 units) or delta (half 1) for iteration i of item t, loaded
-    // one iteration ahead so its latency hides behind the current one
+    // row r's negated LSE (half 0, log2 units) or negated delta (half 1) for iteration i
+    // of item t, loaded one iteration ahead so its latency hides behind the current one
+    // (negated, so that both enter the packed f32x2 forms below as addends)
     auto row_value = [&](const KVItem& t, int i) -> float {
       const int hi = t.hk * p.group + i / t.per_head, qi = (t.m_lo + i % t.per_head) * BM + r;
-      if (qi >= t.sq.nq) return half == 0 ? INFINITY : 0.f;
+      if (qi >= t.sq.nq) return half == 0 ? -INFINITY : -0.f;
       const size_t idx = VL ? (size_t)hi * p.total_q + t.sq.q0 + qi : ((size_t)t.b * p.Hq + hi) * p.Sq + qi;
-      return half == 0 ? p.lse[idx] * 1.4426950408889634f : p.delta[idx];
+      return half == 0 ? -(p.lse[idx] * 1.4426950408889634f) : -p.delta[idx];
     };
     // The row terms come from the kernel before this one, which this one was launched to
     // overlap: wait for its completion; then the dQ kernel, which reads them too and
@@ -639,11 +647,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int i = 0; i < it.n_iter && ok; ++i) {
         const int gi = g + i;
         const int m0 = (it.m_lo + i % it.per_head) * BM;
-        // the row vectors of this Q tile, in buffer gi & 1: every thread finished
-        // iteration gi - 2's reads before it arrived on iteration gi - 1's VEC_READY
-        float* v_lse = vec + (gi & 1) * 2 * BM;
-        float* v_dl = v_lse + BM;
-        (half == 0 ? v_lse : v_dl)[r] = next_v;
+        // the row vectors of this Q tile (-LSE_2, -delta), in buffer gi & 1: every thread
+        // finished iteration gi - 2's reads before it arrived on iteration gi - 1's VEC_READY
+        float* v_nl = vec + (gi & 1) * 2 * BM;
+        float* v_nd = v_nl + BM;
+        (half == 0 ? v_nl : v_nd)[r] = next_v;
         mbar_arrive(bar(L::VEC_READY));
         if (i + 1 < it.n_iter) next_v = row_value(it, i + 1);
         if (!(ok = wait_warp(bar(L::VEC_READY), gi & 1))) break;
@@ -662,12 +670,21 @@ __global__ void __launch_bounds__(THREADS, 1)
           int hi = key < it.sq.nk ? it.sq.nq - m0 - c0 : 0;
           if (p.win_left >= 0) hi = min(hi, key - it.dlen + p.win_left - m0 - c0 + 1);
           if (__all_sync(0xffffffffu, lo <= 0 && hi >= 64)) {
+            // two query columns per packed f32x2 FMA (the same rounding as one fmaf each)
+            const uint64_t c2p = f2_pack(p.c2, p.c2);
+            const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(v_nl + c0);
 #pragma unroll
-            for (int j = 0; j < 64; ++j) pv[j] = ex2(fmaf(__uint_as_float(sr[j]), p.c2, -v_lse[c0 + j]));
+            for (int j = 0; j < 32; ++j) {
+              float a0, a1;
+              f2_unpack(fma2(f2_pack(__uint_as_float(sr[2 * j]), __uint_as_float(sr[2 * j + 1])), c2p, nl2[j]),
+                        a0, a1);
+              pv[2 * j] = ex2(a0);
+              pv[2 * j + 1] = ex2(a1);
+            }
           } else {
 #pragma unroll
             for (int j = 0; j < 64; ++j)
-              pv[j] = (j >= lo && j < hi) ? ex2(fmaf(__uint_as_float(sr[j]), p.c2, -v_lse[c0 + j])) : 0.f;
+              pv[j] = (j >= lo && j < hi) ? ex2(fmaf(__uint_as_float(sr[j]), p.c2, v_nl[c0 + j])) : 0.f;
           }
 #pragma unroll
           for (int j = 0; j < 32; ++j) pk[j] = pack2<BF16>(pv[2 * j], pv[2 * j + 1]);
@@ -684,10 +701,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_ld32(lane_t + C_DP + c0, *reinterpret_cast<uint32_t(*)[32]>(dr));
           tmem_ld32(lane_t + C_DP + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(dr + 32));
           uint32_t dk2[32];
+          const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(v_nd + c0);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float d0 = pv[2 * j] * (__uint_as_float(dr[2 * j]) - v_dl[c0 + 2 * j]);
-            const float d1 = pv[2 * j + 1] * (__uint_as_float(dr[2 * j + 1]) - v_dl[c0 + 2 * j + 1]);
+          for (int j = 0; j < 32; ++j) {  // P (dP - delta), two query columns per packed op
+            float d0, d1;
+            const uint64_t dd = add2(f2_pack(__uint_as_float(dr[2 * j]), __uint_as_float(dr[2 * j + 1])), nd2[j]);
+            f2_unpack(mul2(f2_pack(pv[2 * j], pv[2 * j + 1]), dd), d0, d1);
             dk2[j] = pack2<BF16>(d0, d1);
           }
           tmem_st32(lane_t + C_DP + c0, dk2);  // dS^T over the dP^T columns this thread read
@@ -996,12 +1015,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int kb = (it.t_lo + j) * BN + c0, ulo = key_lo - kb, uhi = key_hi + 1 - kb;
         uint32_t pk[32];
         if (__all_sync(0xffffffffu, ulo <= 0 && uhi >= 64)) {
+          // both columns of a pair in one packed f32x2 operation (same roundings)
+          const uint64_t c2p = f2_pack(p.c2, p.c2), nl = f2_pack(-lse2, -lse2), nd = f2_pack(-dlt, -dlt);
 #pragma unroll
           for (int u = 0; u < 32; ++u) {
-            const float p0 = ex2(fmaf(__uint_as_float(sr[2 * u]), p.c2, -lse2));
-            const float p1 = ex2(fmaf(__uint_as_float(sr[2 * u + 1]), p.c2, -lse2));
-            pk[u] = pack2<BF16>(p0 * (__uint_as_float(dr[2 * u]) - dlt),
-                                p1 * (__uint_as_float(dr[2 * u + 1]) - dlt));
+            float a0, a1, d0, d1;
+            f2_unpack(fma2(f2_pack(__uint_as_float(sr[2 * u]), __uint_as_float(sr[2 * u + 1])), c2p, nl), a0, a1);
+            const uint64_t dd = add2(f2_pack(__uint_as_float(dr[2 * u]), __uint_as_float(dr[2 * u + 1])), nd);
+            f2_unpack(mul2(f2_pack(ex2(a0), ex2(a1)), dd), d0, d1);
+            pk[u] = pack2<BF16>(d0, d1);
           }
         } else {
 #pragma unroll
