@@ -269,6 +269,33 @@ __device__ __forceinline__ uint4 pack8(const uint32_t* r, float f) {
                     pack2<BF16>(__uint_as_float(r[6]) * f, __uint_as_float(r[7]) * f));
 }
 
+// Two 64-column pieces of this thread's TMEM lane (32x32b shape) at taddr_a and taddr_b,
+// issued back to back and waited for once.
+__device__ __forceinline__ void tmem_ld64_ab(uint32_t taddr_a, uint32_t taddr_b, uint32_t (&r)[128]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%128];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, %80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95, %96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, %111, %112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127}, [%129];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]),
+        "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]),
+        "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]),
+        "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]),
+        "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]),
+        "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]),
+        "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]),
+        "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]),
+        "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
+      : "r"(taddr_a), "r"(taddr_b)
+      : "memory");
+}
+
 // a * b on both lanes of two packed f32 values (sm_100 and later: one instruction).
 __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
   uint64_t d;
@@ -661,8 +688,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         float pv[64];
         {
           uint32_t sr[64];
-          tmem_ld32(lane_t + C_S + c0, *reinterpret_cast<uint32_t(*)[32]>(sr));
-          tmem_ld32(lane_t + C_S + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+          tmem_ld64(lane_t + C_S + c0, sr);  // one TMEM round trip
           uint32_t pk[32];
           // query columns [lo, hi) of this thread's 64 see key n0 + r; a tile whose every
           // query sees every key (all but the window's edges and the ragged ends) needs no test
@@ -698,8 +724,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         {
           uint32_t dr[64];
-          tmem_ld32(lane_t + C_DP + c0, *reinterpret_cast<uint32_t(*)[32]>(dr));
-          tmem_ld32(lane_t + C_DP + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(dr + 32));
+          tmem_ld64(lane_t + C_DP + c0, dr);  // one TMEM round trip
           uint32_t dk2[32];
           const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(v_nd + c0);
 #pragma unroll
@@ -1002,11 +1027,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!(ok = wait_warp(bar(L::DP_READY), gj & 1))) break;
         tc_fence_after();
         const uint32_t t_s = lane_t + C_S + 128u * (gj & 1);
-        uint32_t sr[64], dr[64];
-        tmem_ld32(t_s + c0, *reinterpret_cast<uint32_t(*)[32]>(sr));
-        tmem_ld32(t_s + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
-        tmem_ld32(lane_t + C_DP + c0, *reinterpret_cast<uint32_t(*)[32]>(dr));
-        tmem_ld32(lane_t + C_DP + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(dr + 32));
+        uint32_t sd[128];  // S in [0, 64), dP in [64, 128): one TMEM round trip
+        tmem_ld64_ab(t_s + c0, lane_t + C_DP + c0, sd);
+        const uint32_t* sr = sd;
+        const uint32_t* dr = sd + 64;
         tc_fence_before();
         mbar_arrive(bar(L::DP_FREE));  // dP(j + 1) may overwrite dP(j)
         // keys kb + u, ulo <= u < uhi, are visible to this row; a tile whose every key
