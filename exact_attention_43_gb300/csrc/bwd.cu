@@ -708,9 +708,16 @@ __global__ void __launch_bounds__(THREADS, 1)
               pv[2 * j + 1] = ex2(a1);
             }
           } else {
+            const uint64_t c2p = f2_pack(p.c2, p.c2);
+            const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(v_nl + c0);
 #pragma unroll
-            for (int j = 0; j < 64; ++j)
-              pv[j] = (j >= lo && j < hi) ? ex2(fmaf(__uint_as_float(sr[j]), p.c2, v_nl[c0 + j])) : 0.f;
+            for (int j = 0; j < 32; ++j) {
+              float a0, a1;
+              f2_unpack(fma2(f2_pack(__uint_as_float(sr[2 * j]), __uint_as_float(sr[2 * j + 1])), c2p, nl2[j]),
+                        a0, a1);
+              pv[2 * j] = (2 * j >= lo && 2 * j < hi) ? ex2(a0) : 0.f;
+              pv[2 * j + 1] = (2 * j + 1 >= lo && 2 * j + 1 < hi) ? ex2(a1) : 0.f;
+            }
           }
 #pragma unroll
           for (int j = 0; j < 32; ++j) pk[j] = pack2<BF16>(pv[2 * j], pv[2 * j + 1]);
@@ -1050,14 +1057,16 @@ __global__ void __launch_bounds__(THREADS, 1)
             pk[u] = pack2<BF16>(d0, d1);
           }
         } else {
+          const uint64_t c2p = f2_pack(p.c2, p.c2), nl = f2_pack(-lse2, -lse2), nd = f2_pack(-dlt, -dlt);
 #pragma unroll
           for (int u = 0; u < 32; ++u) {
-            const float p0 =
-                (2 * u >= ulo && 2 * u < uhi) ? ex2(fmaf(__uint_as_float(sr[2 * u]), p.c2, -lse2)) : 0.f;
-            const float p1 = (2 * u + 1 >= ulo && 2 * u + 1 < uhi)
-                                 ? ex2(fmaf(__uint_as_float(sr[2 * u + 1]), p.c2, -lse2)) : 0.f;
-            pk[u] = pack2<BF16>(p0 * (__uint_as_float(dr[2 * u]) - dlt),
-                                p1 * (__uint_as_float(dr[2 * u + 1]) - dlt));
+            float a0, a1, d0, d1;
+            f2_unpack(fma2(f2_pack(__uint_as_float(sr[2 * u]), __uint_as_float(sr[2 * u + 1])), c2p, nl), a0, a1);
+            const float p0 = (2 * u >= ulo && 2 * u < uhi) ? ex2(a0) : 0.f;
+            const float p1 = (2 * u + 1 >= ulo && 2 * u + 1 < uhi) ? ex2(a1) : 0.f;
+            const uint64_t dd = add2(f2_pack(__uint_as_float(dr[2 * u]), __uint_as_float(dr[2 * u + 1])), nd);
+            f2_unpack(mul2(f2_pack(p0, p1), dd), d0, d1);
+            pk[u] = pack2<BF16>(d0, d1);
           }
         }
         tmem_st32(t_s + c0, pk);  // dS over the S columns this thread read
