@@ -269,31 +269,48 @@ __device__ __forceinline__ uint4 pack8(const uint32_t* r, float f) {
                     pack2<BF16>(__uint_as_float(r[6]) * f, __uint_as_float(r[7]) * f));
 }
 
-// Two 64-column pieces of this thread's TMEM lane (32x32b shape) at taddr_a and taddr_b,
-// issued back to back and waited for once.
-__device__ __forceinline__ void tmem_ld64_ab(uint32_t taddr_a, uint32_t taddr_b, uint32_t (&r)[128]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%128];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, %80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95, %96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, %111, %112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127}, [%129];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+// 32 consecutive 32-bit TMEM columns of this thread's lane (32x32b shape), issued and not
+// waited for: the registers are valid only after tmem_wait_ld_regs on them.
+__device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
         "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
         "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
-        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
-        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
-        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
-        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]),
-        "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]),
-        "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]),
-        "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]),
-        "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]),
-        "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]),
-        "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]),
-        "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]),
-        "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
-      : "r"(taddr_a), "r"(taddr_b)
-      : "memory");
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+               : "r"(taddr)
+               : "memory");
+}
+
+// Wait for this thread's TMEM loads; the registers pass through the statement, so no use
+// of them can be scheduled above it.
+__device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+        "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]),
+        "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+        "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&a)[32], uint32_t (&b)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]),
+        "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]), "+r"(a[14]), "+r"(a[15]),
+        "+r"(a[16]), "+r"(a[17]), "+r"(a[18]), "+r"(a[19]), "+r"(a[20]), "+r"(a[21]), "+r"(a[22]), "+r"(a[23]),
+        "+r"(a[24]), "+r"(a[25]), "+r"(a[26]), "+r"(a[27]), "+r"(a[28]), "+r"(a[29]), "+r"(a[30]), "+r"(a[31]),
+        "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]), "+r"(b[5]), "+r"(b[6]), "+r"(b[7]),
+        "+r"(b[8]), "+r"(b[9]), "+r"(b[10]), "+r"(b[11]), "+r"(b[12]), "+r"(b[13]), "+r"(b[14]), "+r"(b[15]),
+        "+r"(b[16]), "+r"(b[17]), "+r"(b[18]), "+r"(b[19]), "+r"(b[20]), "+r"(b[21]), "+r"(b[22]), "+r"(b[23]),
+        "+r"(b[24]), "+r"(b[25]), "+r"(b[26]), "+r"(b[27]), "+r"(b[28]), "+r"(b[29]), "+r"(b[30]), "+r"(b[31])
+               :
+               : "memory");
+}
+
+// 16 consecutive 32-bit TMEM columns of this thread's lane (not waited for).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
+               ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+               : "memory");
 }
 
 // a * b on both lanes of two packed f32 values (sm_100 and later: one instruction).
@@ -687,41 +704,45 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         float pv[64];
         {
-          uint32_t sr[64];
-          tmem_ld64(lane_t + C_S + c0, sr);  // one TMEM round trip
-          uint32_t pk[32];
+          // the two 32-column halves of this thread's S^T: the second loads while the
+          // first is turned into P^T and stored
+          uint32_t sa[32], sb[32];
+          tmem_ld32_issue(lane_t + C_S + c0, sa);
+          tmem_wait_ld_regs(sa);
+          tmem_ld32_issue(lane_t + C_S + c0 + 32, sb);
           // query columns [lo, hi) of this thread's 64 see key n0 + r; a tile whose every
           // query sees every key (all but the window's edges and the ragged ends) needs no test
           const int lo = p.win_right >= 0 ? key - it.dlen - p.win_right - m0 - c0 : 0;
           int hi = key < it.sq.nk ? it.sq.nq - m0 - c0 : 0;
           if (p.win_left >= 0) hi = min(hi, key - it.dlen + p.win_left - m0 - c0 + 1);
-          if (__all_sync(0xffffffffu, lo <= 0 && hi >= 64)) {
-            // two query columns per packed f32x2 FMA (the same rounding as one fmaf each)
-            const uint64_t c2p = f2_pack(p.c2, p.c2);
-            const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(v_nl + c0);
+          const bool all_visible = __all_sync(0xffffffffu, lo <= 0 && hi >= 64);
+          // two query columns per packed f32x2 FMA (the same rounding as one fmaf each)
+          const uint64_t c2p = f2_pack(p.c2, p.c2);
+          const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(v_nl + c0);
+          auto p_half = [&](const uint32_t(&sx)[32], int h, bool masked) {
+            uint32_t pk[16];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
+            for (int j = 0; j < 16; ++j) {
+              const int c = 32 * h + 2 * j;
               float a0, a1;
-              f2_unpack(fma2(f2_pack(__uint_as_float(sr[2 * j]), __uint_as_float(sr[2 * j + 1])), c2p, nl2[j]),
+              f2_unpack(fma2(f2_pack(__uint_as_float(sx[2 * j]), __uint_as_float(sx[2 * j + 1])), c2p,
+                             nl2[16 * h + j]),
                         a0, a1);
-              pv[2 * j] = ex2(a0);
-              pv[2 * j + 1] = ex2(a1);
+              pv[c] = (!masked || (c >= lo && c < hi)) ? ex2(a0) : 0.f;
+              pv[c + 1] = (!masked || (c + 1 >= lo && c + 1 < hi)) ? ex2(a1) : 0.f;
+              pk[j] = pack2<BF16>(pv[c], pv[c + 1]);
             }
+            tmem_st16(lane_t + C_S + c0 + 16 * h, pk);  // P^T over S^T columns already read
+          };
+          if (all_visible) {
+            p_half(sa, 0, false);
+            tmem_wait_ld_regs(sb);
+            p_half(sb, 1, false);
           } else {
-            const uint64_t c2p = f2_pack(p.c2, p.c2);
-            const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(v_nl + c0);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              float a0, a1;
-              f2_unpack(fma2(f2_pack(__uint_as_float(sr[2 * j]), __uint_as_float(sr[2 * j + 1])), c2p, nl2[j]),
-                        a0, a1);
-              pv[2 * j] = (2 * j >= lo && 2 * j < hi) ? ex2(a0) : 0.f;
-              pv[2 * j + 1] = (2 * j + 1 >= lo && 2 * j + 1 < hi) ? ex2(a1) : 0.f;
-            }
+            p_half(sa, 0, true);
+            tmem_wait_ld_regs(sb);
+            p_half(sb, 1, true);
           }
-#pragma unroll
-          for (int j = 0; j < 32; ++j) pk[j] = pack2<BF16>(pv[2 * j], pv[2 * j + 1]);
-          tmem_st32(lane_t + C_S + c0, pk);  // P^T over the S^T columns this thread read
         }
         tmem_wait_st();
         tc_fence_before();
@@ -730,18 +751,27 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!(ok = wait_warp(bar(L::DP_READY), gi & 1))) break;
         tc_fence_after();
         {
-          uint32_t dr[64];
-          tmem_ld64(lane_t + C_DP + c0, dr);  // one TMEM round trip
-          uint32_t dk2[32];
+          uint32_t da[32], db[32];
+          tmem_ld32_issue(lane_t + C_DP + c0, da);
+          tmem_wait_ld_regs(da);
+          tmem_ld32_issue(lane_t + C_DP + c0 + 32, db);
           const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(v_nd + c0);
+          auto ds_half = [&](const uint32_t(&dx)[32], int h) {  // P (dP - delta), packed pairs
+            uint32_t dk2[16];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {  // P (dP - delta), two query columns per packed op
-            float d0, d1;
-            const uint64_t dd = add2(f2_pack(__uint_as_float(dr[2 * j]), __uint_as_float(dr[2 * j + 1])), nd2[j]);
-            f2_unpack(mul2(f2_pack(pv[2 * j], pv[2 * j + 1]), dd), d0, d1);
-            dk2[j] = pack2<BF16>(d0, d1);
-          }
-          tmem_st32(lane_t + C_DP + c0, dk2);  // dS^T over the dP^T columns this thread read
+            for (int j = 0; j < 16; ++j) {
+              const int c = 32 * h + 2 * j;
+              float d0, d1;
+              const uint64_t dd =
+                  add2(f2_pack(__uint_as_float(dx[2 * j]), __uint_as_float(dx[2 * j + 1])), nd2[16 * h + j]);
+              f2_unpack(mul2(f2_pack(pv[c], pv[c + 1]), dd), d0, d1);
+              dk2[j] = pack2<BF16>(d0, d1);
+            }
+            tmem_st16(lane_t + C_DP + c0 + 16 * h, dk2);  // dS^T over dP^T columns already read
+          };
+          ds_half(da, 0);
+          tmem_wait_ld_regs(db);
+          ds_half(db, 1);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -1034,42 +1064,43 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!(ok = wait_warp(bar(L::DP_READY), gj & 1))) break;
         tc_fence_after();
         const uint32_t t_s = lane_t + C_S + 128u * (gj & 1);
-        uint32_t sd[128];  // S in [0, 64), dP in [64, 128): one TMEM round trip
-        tmem_ld64_ab(t_s + c0, lane_t + C_DP + c0, sd);
-        const uint32_t* sr = sd;
-        const uint32_t* dr = sd + 64;
-        tc_fence_before();
-        mbar_arrive(bar(L::DP_FREE));  // dP(j + 1) may overwrite dP(j)
+        // the two 32-column halves of this thread's S and dP: the second pair loads while
+        // the first is turned into dS and stored
+        uint32_t s_a[32], d_a[32], s_b[32], d_b[32];
+        tmem_ld32_issue(t_s + c0, s_a);
+        tmem_ld32_issue(lane_t + C_DP + c0, d_a);
+        tmem_wait_ld_regs(s_a, d_a);
+        tmem_ld32_issue(t_s + c0 + 32, s_b);
+        tmem_ld32_issue(lane_t + C_DP + c0 + 32, d_b);
         // keys kb + u, ulo <= u < uhi, are visible to this row; a tile whose every key
         // is visible to the whole warp's rows (all but the diagonal, the window's edges
         // and the ragged ends) needs no test
         const int kb = (it.t_lo + j) * BN + c0, ulo = key_lo - kb, uhi = key_hi + 1 - kb;
-        uint32_t pk[32];
-        if (__all_sync(0xffffffffu, ulo <= 0 && uhi >= 64)) {
-          // both columns of a pair in one packed f32x2 operation (same roundings)
-          const uint64_t c2p = f2_pack(p.c2, p.c2), nl = f2_pack(-lse2, -lse2), nd = f2_pack(-dlt, -dlt);
+        const bool all_visible = __all_sync(0xffffffffu, ulo <= 0 && uhi >= 64);
+        // both columns of a pair in one packed f32x2 operation (same roundings)
+        const uint64_t c2p = f2_pack(p.c2, p.c2), nl = f2_pack(-lse2, -lse2), nd = f2_pack(-dlt, -dlt);
+        auto ds_half = [&](const uint32_t(&sx)[32], const uint32_t(&dx)[32], int h, bool masked) {
+          uint32_t pk[16];
 #pragma unroll
-          for (int u = 0; u < 32; ++u) {
+          for (int u = 0; u < 16; ++u) {
+            const int c = 32 * h + 2 * u;
             float a0, a1, d0, d1;
-            f2_unpack(fma2(f2_pack(__uint_as_float(sr[2 * u]), __uint_as_float(sr[2 * u + 1])), c2p, nl), a0, a1);
-            const uint64_t dd = add2(f2_pack(__uint_as_float(dr[2 * u]), __uint_as_float(dr[2 * u + 1])), nd);
-            f2_unpack(mul2(f2_pack(ex2(a0), ex2(a1)), dd), d0, d1);
-            pk[u] = pack2<BF16>(d0, d1);
-          }
-        } else {
-          const uint64_t c2p = f2_pack(p.c2, p.c2), nl = f2_pack(-lse2, -lse2), nd = f2_pack(-dlt, -dlt);
-#pragma unroll
-          for (int u = 0; u < 32; ++u) {
-            float a0, a1, d0, d1;
-            f2_unpack(fma2(f2_pack(__uint_as_float(sr[2 * u]), __uint_as_float(sr[2 * u + 1])), c2p, nl), a0, a1);
-            const float p0 = (2 * u >= ulo && 2 * u < uhi) ? ex2(a0) : 0.f;
-            const float p1 = (2 * u + 1 >= ulo && 2 * u + 1 < uhi) ? ex2(a1) : 0.f;
-            const uint64_t dd = add2(f2_pack(__uint_as_float(dr[2 * u]), __uint_as_float(dr[2 * u + 1])), nd);
+            f2_unpack(fma2(f2_pack(__uint_as_float(sx[2 * u]), __uint_as_float(sx[2 * u + 1])), c2p, nl), a0, a1);
+            const float p0 = (!masked || (c >= ulo && c < uhi)) ? ex2(a0) : 0.f;
+            const float p1 = (!masked || (c + 1 >= ulo && c + 1 < uhi)) ? ex2(a1) : 0.f;
+            const uint64_t dd = add2(f2_pack(__uint_as_float(dx[2 * u]), __uint_as_float(dx[2 * u + 1])), nd);
             f2_unpack(mul2(f2_pack(p0, p1), dd), d0, d1);
             pk[u] = pack2<BF16>(d0, d1);
           }
-        }
-        tmem_st32(t_s + c0, pk);  // dS over the S columns this thread read
+          tmem_st16(t_s + c0 + 16 * h, pk);  // dS over S columns already read
+        };
+        if (all_visible) ds_half(s_a, d_a, 0, false);
+        else ds_half(s_a, d_a, 0, true);
+        tmem_wait_ld_regs(s_b, d_b);
+        tc_fence_before();
+        mbar_arrive(bar(L::DP_FREE));  // dP(j + 1) may overwrite dP(j)
+        if (all_visible) ds_half(s_b, d_b, 1, false);
+        else ds_half(s_b, d_b, 1, true);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(L::DS_READY + (gj & 1)));
