@@ -537,8 +537,9 @@ __global__ void __launch_bounds__(THREADS, 1)
           ++n_kv;
           // iteration g's Q and dO go to buffer g & 1, once iteration g - 2's last products
           // that read them (dV for dO, dK for Q) have completed
-          for (int i = 0; i < it.n_iter && ok; ++i, ++g) {
-            const int bi = g & 1, h = it.hk * p.group + i / it.per_head, m = it.m_lo + i % it.per_head;
+          for (int i = 0, h = it.hk * p.group, m = it.m_lo; i < it.n_iter && ok;
+               ++i, ++g, h += (m + 1 == it.m_lo + it.per_head), m = (m + 1 == it.m_lo + it.per_head) ? it.m_lo : m + 1) {
+            const int bi = g & 1;  // query head h, Q tile m
             const int q_y = VL ? it.sq.q0 + m * BM : m * BM, q_z = VL ? h : it.b * p.Hq + h;
             const bool held = p.debug_fault == 3 && w == 0 && i == 1;
             if (held) held_g = g;
@@ -665,8 +666,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     // row r's negated LSE (half 0, log2 units) or negated delta (half 1) for iteration i
     // of item t, loaded one iteration ahead so its latency hides behind the current one
     // (negated, so that both enter the packed f32x2 forms below as addends)
-    auto row_value = [&](const KVItem& t, int i) -> float {
-      const int hi = t.hk * p.group + i / t.per_head, qi = (t.m_lo + i % t.per_head) * BM + r;
+    auto row_value = [&](const KVItem& t, int hh, int mm) -> float {  // query head hk G + hh, Q tile mm
+      const int hi = t.hk * p.group + hh, qi = mm * BM + r;
       if (qi >= t.sq.nq) return half == 0 ? -INFINITY : -0.f;
       const size_t idx = VL ? (size_t)hi * p.total_q + t.sq.q0 + qi : ((size_t)t.b * p.Hq + hi) * p.Sq + qi;
       return half == 0 ? -(p.lse[idx] * 1.4426950408889634f) : -p.delta[idx];
@@ -687,17 +688,25 @@ __global__ void __launch_bounds__(THREADS, 1)
       const KVItem it = kv_item<VL>(p, n_kt, w);
       if (it.n_iter == 0) continue;  // skipped, or zero rows written by the epilogue warps
       const int key = it.n0 + r;
-      float next_v = row_value(it, 0);
+      // iteration i is query head hk G + i / per_head, Q tile m_lo + i % per_head: kept
+      // as counters (this one's and the next's) rather than divided out every iteration
+      int m_i = it.m_lo, h_n = 0, m_n = it.m_lo;
+      float next_v = row_value(it, 0, it.m_lo);
       for (int i = 0; i < it.n_iter && ok; ++i) {
         const int gi = g + i;
-        const int m0 = (it.m_lo + i % it.per_head) * BM;
+        const int m0 = m_i * BM;
+        if (++m_n == it.m_lo + it.per_head) {  // the next iteration's (head, tile)
+          m_n = it.m_lo;
+          ++h_n;
+        }
         // the row vectors of this Q tile (-LSE_2, -delta), in buffer gi & 1: every thread
         // finished iteration gi - 2's reads before it arrived on iteration gi - 1's VEC_READY
         float* v_nl = vec + (gi & 1) * 2 * BM;
         float* v_nd = v_nl + BM;
         (half == 0 ? v_nl : v_nd)[r] = next_v;
         mbar_arrive(bar(L::VEC_READY));
-        if (i + 1 < it.n_iter) next_v = row_value(it, i + 1);
+        if (i + 1 < it.n_iter) next_v = row_value(it, h_n, m_n);
+        m_i = m_n;
         if (!(ok = wait_warp(bar(L::VEC_READY), gi & 1))) break;
         // ---- P phase: P^T = 2^(S^T c - LSE_2) on the visible (key, query) pairs
         if (!(ok = wait_warp(bar(L::S_READY), gi & 1))) break;
