@@ -1310,7 +1310,8 @@ static cudaError_t launch_t(const BwdArgs& a, cudaStream_t stream) {
     const long long n_items = n_mt * a.Hq * a.B;
     const int grid = (int)(n_items < sms ? n_items : sms);
     // After the dK/dV kernel its CTAs start on the SMs that kernel's CTAs leave, while
-    // its last items run (programmatic stream serialization; it signals at its start).
+    // its last items run (programmatic stream serialization; that kernel signals once
+    // its compute warps have seen the row terms complete).
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(THREADS);
