@@ -407,16 +407,116 @@ __device__ __forceinline__ uint32_t desc_mn(uint32_t saddr) {
   return (uint32_t)sdesc_sw128(saddr, 128 * 128, 1024);
 }
 
+// The eight MMAs of a 128-deep product in one statement: one predicate for the first
+// (accumulate or not), a constant true one for the rest, the operand addresses stepped
+// by immediates, so the issuing thread spends as few instructions as possible between
+// products (it blocks on the tensor core's queue, and what it does in between shows).
+// K-major A and B in shared memory (D = 128: two 64-column regions of 4 steps each).
+__device__ __forceinline__ void mma8_ss(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi, uint32_t idesc,
+                                        uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 da, db;\n\t.reg .b32 ta, tb;\n\t"
+      "setp.ne.b32 p0, %5, 0;\n\t"
+      "setp.eq.b32 p1, 0, 0;\n\t"
+      "mov.b64 da, {%1, %3};\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p0;\n\t"
+      "add.u32 ta, %1, 2;\n\t"
+      "add.u32 tb, %2, 2;\n\t"
+      "mov.b64 da, {ta, %3};\n\t"
+      "mov.b64 db, {tb, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p1;\n\t"
+      "add.u32 ta, %1, 4;\n\t"
+      "add.u32 tb, %2, 4;\n\t"
+      "mov.b64 da, {ta, %3};\n\t"
+      "mov.b64 db, {tb, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p1;\n\t"
+      "add.u32 ta, %1, 6;\n\t"
+      "add.u32 tb, %2, 6;\n\t"
+      "mov.b64 da, {ta, %3};\n\t"
+      "mov.b64 db, {tb, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p1;\n\t"
+      "add.u32 ta, %1, 1024;\n\t"
+      "add.u32 tb, %2, 1024;\n\t"
+      "mov.b64 da, {ta, %3};\n\t"
+      "mov.b64 db, {tb, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p1;\n\t"
+      "add.u32 ta, %1, 1026;\n\t"
+      "add.u32 tb, %2, 1026;\n\t"
+      "mov.b64 da, {ta, %3};\n\t"
+      "mov.b64 db, {tb, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p1;\n\t"
+      "add.u32 ta, %1, 1028;\n\t"
+      "add.u32 tb, %2, 1028;\n\t"
+      "mov.b64 da, {ta, %3};\n\t"
+      "mov.b64 db, {tb, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p1;\n\t"
+      "add.u32 ta, %1, 1030;\n\t"
+      "add.u32 tb, %2, 1030;\n\t"
+      "mov.b64 da, {ta, %3};\n\t"
+      "mov.b64 db, {tb, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p1;\n\t"
+      "}" ::"r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+// A (128 x 128, two 16-bit values per column) in TMEM in the split layout of the
+// compute threads (K-rows 0-63 at columns 0-31, 64-127 at 64-95), B MN-major in
+// shared memory (16 K-rows = 2048 bytes a step).
+__device__ __forceinline__ void mma8_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi, uint32_t idesc,
+                                        uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 db;\n\t.reg .b32 ta, tb;\n\t"
+      "setp.ne.b32 p0, %5, 0;\n\t"
+      "setp.eq.b32 p1, 0, 0;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p0;\n\t"
+      "add.u32 ta, %1, 8;\n\t"
+      "add.u32 tb, %2, 128;\n\t"
+      "mov.b64 db, {tb, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
+      "add.u32 ta, %1, 16;\n\t"
+      "add.u32 tb, %2, 256;\n\t"
+      "mov.b64 db, {tb, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
+      "add.u32 ta, %1, 24;\n\t"
+      "add.u32 tb, %2, 384;\n\t"
+      "mov.b64 db, {tb, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
+      "add.u32 ta, %1, 64;\n\t"
+      "add.u32 tb, %2, 512;\n\t"
+      "mov.b64 db, {tb, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
+      "add.u32 ta, %1, 72;\n\t"
+      "add.u32 tb, %2, 640;\n\t"
+      "mov.b64 db, {tb, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
+      "add.u32 ta, %1, 80;\n\t"
+      "add.u32 tb, %2, 768;\n\t"
+      "mov.b64 db, {tb, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
+      "add.u32 ta, %1, 88;\n\t"
+      "add.u32 tb, %2, 896;\n\t"
+      "mov.b64 db, {tb, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p1;\n\t"
+      "}" ::"r"(d_tmem), "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
 // S-like product D[tmem] = A B^T over the head dimension, both operands K-major
 // 128 x D tiles in shared memory (16 columns = 32 bytes of a 128-byte swizzled row).
 template <int D, bool BF16>
 __device__ __forceinline__ void mma_kmajor(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi) {
   constexpr uint32_t idesc = umma_idesc_f16(BF16, 128, 128, false, false);
   constexpr int REGION = 128 * 128;
+  if constexpr (D == 128) {
+    mma8_ss(d_tmem, a_lo, b_lo, hi, idesc, 0u);
+  } else {
 #pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = ((kk >> 2) * REGION + (kk & 3) * 32) >> 4;
-    umma_ss_lo(d_tmem, a_lo + off, hi, b_lo + off, hi, idesc, kk > 0 ? 1u : 0u);
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t off = ((kk >> 2) * REGION + (kk & 3) * 32) >> 4;
+      umma_ss_lo(d_tmem, a_lo + off, hi, b_lo + off, hi, idesc, kk > 0 ? 1u : 0u);
+    }
   }
 }
 
@@ -430,10 +530,7 @@ template <int D, bool BF16>
 __device__ __forceinline__ void mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
                                            bool acc) {
   constexpr uint32_t idesc = umma_idesc_f16(BF16, 128, D, false, true);
-#pragma unroll
-  for (int kk = 0; kk < 128 / 16; ++kk)
-    umma_ts_lo(d_tmem, a_tmem + kk * 8 + (kk >= 4 ? 32 : 0), b_lo + kk * 128, hi, idesc,
-               (acc || kk > 0) ? 1u : 0u);
+  mma8_ts(d_tmem, a_tmem, b_lo, hi, idesc, acc ? 1u : 0u);
 }
 
 // ============================================================================ dK, dV
