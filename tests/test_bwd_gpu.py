@@ -137,3 +137,31 @@ def test_bwd_deterministic():
     torch.cuda.synchronize()
     for x, y in zip(a, b):
         assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+
+
+def test_bwd_gradients_only_16_byte_aligned():
+    """The C ABI promises 16-byte alignment only: gradients that are not 32-byte aligned
+    take 16-byte row stores (the check is on the host, per call) and must hold the same
+    bits as 32-byte-aligned ones; nothing outside them is written."""
+    import exact_attention_43_gb300 as ea
+
+    q, k, v = wl.fwd_inputs(1, 4, 2, 300, 300, 128, seed=4400, device="cuda")
+    do = wl.normal((1, 4, 300, 128), seed=4401, device="cuda")
+    o, lse = ea.attn_fwd(q, k, v, causal=True)
+    ref = ea.attn_bwd(q, k, v, o, lse, do, causal=True)
+
+    def offset_view(like):
+        n = like.numel()
+        buf = torch.full((n + 16,), float("nan"), dtype=like.dtype, device="cuda")
+        view = buf[8:8 + n].view(tuple(like.shape))
+        assert view.data_ptr() % 32 == 16
+        return buf, view
+
+    (bq, dq), (bk, dk), (bv, dv) = offset_view(q), offset_view(k), offset_view(v)
+    ea.attn_bwd(q, k, v, o, lse, do, causal=True, dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    assert ea.check_device_status() == 0
+    for buf, got, want, n in ((bq, dq, ref[0], q.numel()), (bk, dk, ref[1], k.numel()),
+                              (bv, dv, ref[2], v.numel())):
+        assert bool(torch.isnan(buf[:8].float()).all()) and bool(torch.isnan(buf[8 + n:].float()).all())
+        assert torch.equal(got.view(torch.int16), want.view(torch.int16))
