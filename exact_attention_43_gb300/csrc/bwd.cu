@@ -1065,12 +1065,26 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t q_km = desc_km(sb + L::Q_OFF), do_km = desc_km(sb + L::DO_OFF);
         const uint32_t ring_km0 = desc_km(sb + L::RING_OFF), ring_mn0 = desc_mn(sb + L::RING_OFF);
         constexpr uint32_t SLOT = L::TILE >> 4;  // one ring slot in the address field
-        auto ring_km = [&](int l) { return ring_km0 + (uint32_t)(l % NS) * SLOT; };
-        auto ring_mn = [&](int l) { return ring_mn0 + (uint32_t)(l % NS) * SLOT; };
         auto wait = [&](int bar_i, int parity) -> bool {
           return mbar_wait<false>(bar(bar_i), parity & 1, abort_flag, &g_status, lim);
         };
-        auto ring_wait = [&](int l) -> bool { return wait(L::RING_FULL + l % NS, l / NS); };
+        // a ring load as its slot and the parity of its use of the slot, stepped rather than
+        // divided out per product (the issuing thread's instructions between products show)
+        struct RingPos {
+          int s, ph;
+        };
+        auto ring_pos = [&](int l) { return RingPos{l % NS, (l / NS) & 1}; };
+        auto ring_next = [&](RingPos a, int k) {  // load index + k, 0 < k < NS
+          a.s += k;
+          if (a.s >= NS) {
+            a.s -= NS;
+            a.ph ^= 1;
+          }
+          return a;
+        };
+        auto ring_km = [&](RingPos a) { return ring_km0 + (uint32_t)a.s * SLOT; };
+        auto ring_mn = [&](RingPos a) { return ring_mn0 + (uint32_t)a.s * SLOT; };
+        auto ring_wait = [&](RingPos a) -> bool { return wait(L::RING_FULL + a.s, a.ph); };
         bool ok = true;
         // step g reads ring loads 2g (V) and 2g + 1 (K); V is released once dP has read it,
         // K once dQ has, so with NS = 5 both tiles of step g + 2 land while step g runs
@@ -1088,41 +1102,45 @@ __global__ void __launch_bounds__(THREADS, 1)
           // once the compute warps hold dP(j), dQ += dS(j) K(j) once they wrote dS(j).
           // S(0) goes to the buffer of step g, whose last dS was read by a dQ issued
           // before; dP(0) waits until the compute warps hold the last item's final dP.
-          if (!(ok = wait(L::QD_FULL, n_it) && ring_wait(2 * g + 1))) break;
+          RingPos kp = ring_pos(2 * g + 1);        // K of the current step (load 2 gj + 1)
+          const RingPos vp0 = ring_pos(2 * g);     // V(0)
+          if (!(ok = wait(L::QD_FULL, n_it) && ring_wait(kp))) break;
           tc_fence_after();
-          mma_kmajor<D, BF16>(tmem + C_S + 128u * (g & 1), q_km, ring_km(2 * g + 1), hi);
+          mma_kmajor<D, BF16>(tmem + C_S + 128u * (g & 1), q_km, ring_km(kp), hi);
           umma_commit(bar(L::S_READY + (g & 1)));
           if (g > 0 && !(ok = wait(L::DP_FREE, g - 1))) break;
-          if (!(ok = ring_wait(2 * g))) break;
+          if (!(ok = ring_wait(vp0))) break;
           tc_fence_after();
-          mma_kmajor<D, BF16>(tmem + C_DP, do_km, ring_km(2 * g), hi);
+          mma_kmajor<D, BF16>(tmem + C_DP, do_km, ring_km(vp0), hi);
           umma_commit(bar(L::DP_READY));
-          umma_commit(bar(L::RING_EMPTY + (2 * g) % NS));  // V(0): read by dP(0)
+          umma_commit(bar(L::RING_EMPTY + vp0.s));  // V(0): read by dP(0)
           if (n == 1) umma_commit(bar(L::QD_EMPTY));  // the item's last readers of Q and dO
           for (int j = 0; j < n && ok; ++j) {
             const int gj = g + j;
+            const RingPos vn = ring_next(kp, 1), kn = ring_next(kp, 2);  // V(j+1), K(j+1)
             if (j + 1 < n) {
-              if (!(ok = ring_wait(2 * gj + 3))) break;
+              if (!(ok = ring_wait(kn))) break;
               tc_fence_after();
               // the other buffer held dS(gj - 1), read by dQ(gj - 1), issued before
-              mma_kmajor<D, BF16>(tmem + C_S + 128u * ((gj + 1) & 1), q_km, ring_km(2 * gj + 3), hi);
+              mma_kmajor<D, BF16>(tmem + C_S + 128u * ((gj + 1) & 1), q_km, ring_km(kn), hi);
               umma_commit(bar(L::S_READY + ((gj + 1) & 1)));
             }
             if (!(ok = wait(L::DP_FREE, gj))) break;
             if (j + 1 < n) {
-              if (!(ok = ring_wait(2 * gj + 2))) break;
+              if (!(ok = ring_wait(vn))) break;
               tc_fence_after();
-              mma_kmajor<D, BF16>(tmem + C_DP, do_km, ring_km(2 * gj + 2), hi);
+              mma_kmajor<D, BF16>(tmem + C_DP, do_km, ring_km(vn), hi);
               umma_commit(bar(L::DP_READY));
-              umma_commit(bar(L::RING_EMPTY + (2 * gj + 2) % NS));  // V(j+1): read by dP(j+1)
+              umma_commit(bar(L::RING_EMPTY + vn.s));  // V(j+1): read by dP(j+1)
               if (j + 2 == n) umma_commit(bar(L::QD_EMPTY));
             }
             if (!(ok = wait(L::DS_READY + (gj & 1), gj >> 1))) break;
             // the item's first dQ overwrites dQ: the compute warps must have read the last one
             if (j == 0 && n_it > 0 && !(ok = wait(L::ACC_FREE, n_it - 1))) break;
             tc_fence_after();
-            mma_tmem_a<D, BF16>(tmem + C_DQ, tmem + C_S + 128u * (gj & 1), ring_mn(2 * gj + 1), hi, j > 0);  // dQ += dS K
-            umma_commit(bar(L::RING_EMPTY + (2 * gj + 1) % NS));  // K(j): read by S(j) and dQ(j)
+            mma_tmem_a<D, BF16>(tmem + C_DQ, tmem + C_S + 128u * (gj & 1), ring_mn(kp), hi, j > 0);  // dQ += dS K
+            umma_commit(bar(L::RING_EMPTY + kp.s));  // K(j): read by S(j) and dQ(j)
+            kp = kn;
           }
           if (!ok) break;
           umma_commit(bar(L::DONE));
