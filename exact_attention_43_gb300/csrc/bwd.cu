@@ -156,13 +156,13 @@ struct QLayout {
   static constexpr int RING_OFF = 2 * TILE;
   static constexpr int BAR_OFF = RING_OFF + NS * TILE;
   enum {
-    // S_READY + b, DS_READY + b: S, dS of a step in TMEM buffer b.  One barrier per
-    // buffer: S of the next step is issued before the compute warps wait for this one
-    // (at an item's start even two), and they may write dS of the next step before the
-    // issuer waits for this one; a barrier must never complete two phases ahead of a
-    // waiter, and the step after next needs a hand-off from the waiter first.
-    QD_FULL, QD_EMPTY, RING_FULL, RING_EMPTY = RING_FULL + NS, S_READY = RING_EMPTY + NS,
-    DP_READY = S_READY + 2, DP_FREE, DS_READY, DONE = DS_READY + 2, ACC_FREE, ITEM_FULL,
+    // DS_READY + b: dS of a step in TMEM buffer b.  One barrier per buffer: the compute
+    // warps may write dS of the next step before the issuer waits for this one; a
+    // barrier must never complete two phases ahead of a waiter, and the step after next
+    // needs a hand-off from the waiter first.  S has no barrier of its own: a step's S is
+    // issued before its dP by the same thread, so DP_READY's commit covers both.
+    QD_FULL, QD_EMPTY, RING_FULL, RING_EMPTY = RING_FULL + NS, DP_READY = RING_EMPTY + NS,
+    DP_FREE, DS_READY, DONE = DS_READY + 2, ACC_FREE, ITEM_FULL,
     ITEM_EMPTY = ITEM_FULL + 2, DRAIN = ITEM_EMPTY + 2, NUM_BARS
   };
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;  // as KVLayout
@@ -975,8 +975,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(bar(L::RING_FULL + s), 1);
       mbar_init(bar(L::RING_EMPTY + s), 1);
     }
-    mbar_init(bar(L::S_READY), 1);
-    mbar_init(bar(L::S_READY + 1), 1);
     mbar_init(bar(L::DP_READY), 1);
     mbar_init(bar(L::DP_FREE), NCOMP);
     mbar_init(bar(L::DS_READY), NCOMP);
@@ -1107,7 +1105,6 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (!(ok = wait(L::QD_FULL, n_it) && ring_wait(kp))) break;
           tc_fence_after();
           mma_kmajor<D, BF16>(tmem + C_S + 128u * (g & 1), q_km, ring_km(kp), hi);
-          umma_commit(bar(L::S_READY + (g & 1)));
           if (g > 0 && !(ok = wait(L::DP_FREE, g - 1))) break;
           if (!(ok = ring_wait(vp0))) break;
           tc_fence_after();
@@ -1123,7 +1120,6 @@ __global__ void __launch_bounds__(THREADS, 1)
               tc_fence_after();
               // the other buffer held dS(gj - 1), read by dQ(gj - 1), issued before
               mma_kmajor<D, BF16>(tmem + C_S + 128u * ((gj + 1) & 1), q_km, ring_km(kn), hi);
-              umma_commit(bar(L::S_READY + ((gj + 1) & 1)));
             }
             if (!(ok = wait(L::DP_FREE, gj))) break;
             if (j + 1 < n) {
@@ -1184,8 +1180,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (p.win_left >= 0) key_lo = row + it.dlen - p.win_left;
       for (int j = 0; j < it.n_kv && ok; ++j) {
         const int gj = g + j;
-        if (!(ok = wait_warp(bar(L::S_READY + (gj & 1)), (gj >> 1) & 1))) break;
-        if (!(ok = wait_warp(bar(L::DP_READY), gj & 1))) break;
+        if (!(ok = wait_warp(bar(L::DP_READY), gj & 1))) break;  // S of this step, then its dP
         tc_fence_after();
         const uint32_t t_s = lane_t + C_S + 128u * (gj & 1);
         // the two 32-column halves of this thread's S and dP: the second pair loads while
