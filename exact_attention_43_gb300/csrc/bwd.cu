@@ -161,7 +161,10 @@ struct QLayout {
     // barrier must never complete two phases ahead of a waiter, and the step after next
     // needs a hand-off from the waiter first.  S has no barrier of its own: a step's S is
     // issued before its dP by the same thread, so DP_READY's commit covers both.
-    QD_FULL, QD_EMPTY, RING_FULL, RING_EMPTY = RING_FULL + NS, DP_READY = RING_EMPTY + NS,
+    // RING_FREE + (q & 3): ring loads 2q - 1 and 2q (K of step q - 1, V of step q) may be
+    // overwritten, one commit for both; the loader waits for q in order, and q + 4 cannot
+    // complete before load 2q + 8 is issued, so no waiter sees a barrier two phases on.
+    QD_FULL, QD_EMPTY, RING_FULL, RING_FREE = RING_FULL + NS, DP_READY = RING_FREE + 4,
     DP_FREE, DS_READY, DONE = DS_READY + 2, ACC_FREE, ITEM_FULL,
     ITEM_EMPTY = ITEM_FULL + 2, DRAIN = ITEM_EMPTY + 2, NUM_BARS
   };
@@ -973,8 +976,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(bar(L::QD_EMPTY), 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(bar(L::RING_FULL + s), 1);
-      mbar_init(bar(L::RING_EMPTY + s), 1);
     }
+    for (int q = 0; q < 4; ++q) mbar_init(bar(L::RING_FREE + q), 1);
     mbar_init(bar(L::DP_READY), 1);
     mbar_init(bar(L::DP_FREE), NCOMP);
     mbar_init(bar(L::DS_READY), NCOMP);
@@ -1041,8 +1044,9 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int kv_y0 = (VL ? it.sq.k0 : 0) + it.t_lo * BN, kv_z = VL ? hk : it.b * p.Hkv + hk;
           for (int l = 0; l < 2 * it.n_kv && ok; ++l, ++ld) {  // V_0, K_0, V_1, K_1, ...
             const int s = ld % NS;
-            if (ld >= NS && !(ok = mbar_wait<false>(bar(L::RING_EMPTY + s), ((ld / NS) - 1) & 1, abort_flag,
-                                                    &g_status, lim)))
+            const int q = (ld - NS + 1) >> 1;  // the release that covers load ld - NS
+            if (ld >= NS &&
+                !(ok = mbar_wait<false>(bar(L::RING_FREE + (q & 3)), (q >> 2) & 1, abort_flag, &g_status, lim)))
               break;
             mbar_expect_tx(bar(L::RING_FULL + s), L::TILE);
             const CUtensorMap* tm = (l & 1) ? &tmk : &tmv;
@@ -1084,8 +1088,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         auto ring_mn = [&](RingPos a) { return ring_mn0 + (uint32_t)a.s * SLOT; };
         auto ring_wait = [&](RingPos a) -> bool { return wait(L::RING_FULL + a.s, a.ph); };
         bool ok = true;
-        // step g reads ring loads 2g (V) and 2g + 1 (K); V is released once dP has read it,
-        // K once dQ has, so with NS = 5 both tiles of step g + 2 land while step g runs
+        // step g reads ring loads 2g (V) and 2g + 1 (K); K(g) and V(g + 1) are released
+        // together once dQ(g) has read K(g) (dP(g + 1), which reads V(g + 1), is issued
+        // before it), so with NS = 5 both tiles of step g + 2 land while step g runs
         int g = 0;     // K/V steps issued over all items
         int n_it = 0;  // items with K/V steps
         for (int r = 0; ok; ++r) {
@@ -1110,7 +1115,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_fence_after();
           mma_kmajor<D, BF16>(tmem + C_DP, do_km, ring_km(vp0), hi);
           umma_commit(bar(L::DP_READY));
-          umma_commit(bar(L::RING_EMPTY + vp0.s));  // V(0): read by dP(0)
+          umma_commit(bar(L::RING_FREE + (g & 3)));  // V(0), and K of the step before (its dQ came first)
           if (n == 1) umma_commit(bar(L::QD_EMPTY));  // the item's last readers of Q and dO
           for (int j = 0; j < n && ok; ++j) {
             const int gj = g + j;
@@ -1127,7 +1132,6 @@ __global__ void __launch_bounds__(THREADS, 1)
               tc_fence_after();
               mma_kmajor<D, BF16>(tmem + C_DP, do_km, ring_km(vn), hi);
               umma_commit(bar(L::DP_READY));
-              umma_commit(bar(L::RING_EMPTY + vn.s));  // V(j+1): read by dP(j+1)
               if (j + 2 == n) umma_commit(bar(L::QD_EMPTY));
             }
             if (!(ok = wait(L::DS_READY + (gj & 1), gj >> 1))) break;
@@ -1135,7 +1139,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (j == 0 && n_it > 0 && !(ok = wait(L::ACC_FREE, n_it - 1))) break;
             tc_fence_after();
             mma_tmem_a<D, BF16>(tmem + C_DQ, tmem + C_S + 128u * (gj & 1), ring_mn(kp), hi, j > 0);  // dQ += dS K
-            umma_commit(bar(L::RING_EMPTY + kp.s));  // K(j): read by S(j) and dQ(j)
+            // K(j), read by S(j) and dQ(j), and V(j+1), read by dP(j+1) issued before; at
+            // the item's last step the next item's first dP releases them
+            if (j + 1 < n) umma_commit(bar(L::RING_FREE + ((gj + 1) & 3)));
             kp = kn;
           }
           if (!ok) break;
