@@ -132,8 +132,7 @@ struct KVLayout {
   static constexpr int VEC_OFF = 6 * TILE;  // [2 buffers][LSE_2, delta][BM] of the Q tile
   static constexpr int BAR_OFF = VEC_OFF + 2 * 2 * BM * 4;
   enum {
-    KV_FULL, KV_EMPTY, Q_FULL, DO_FULL = Q_FULL + 2, Q_FREE = DO_FULL + 2, DO_FREE = Q_FREE + 2,
-    S_READY = DO_FREE + 2, DP_READY, P_READY, DS_READY, VEC_READY, DONE, ACC_FREE, ITEM_FULL,
+    KV_FULL, KV_EMPTY, Q_FULL, DO_FULL = Q_FULL + 2, QD_FREE = DO_FULL + 2, S_READY = QD_FREE + 2, DP_READY, P_READY, DS_READY, VEC_READY, DONE, ACC_FREE, ITEM_FULL,
     ITEM_EMPTY = ITEM_FULL + 2, DRAIN = ITEM_EMPTY + 2, NUM_BARS
   };
   // [0] TMEM base, [1] abort flag, [2], [3] the two queued work items
@@ -567,8 +566,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(L::Q_FULL + i), 1);
       mbar_init(bar(L::DO_FULL + i), 1);
-      mbar_init(bar(L::Q_FREE + i), 1);
-      mbar_init(bar(L::DO_FREE + i), 1);
+      mbar_init(bar(L::QD_FREE + i), 1);
       mbar_init(bar(L::ITEM_FULL + i), 1);
       mbar_init(bar(L::ITEM_EMPTY + i), 1 + NCOMP + NEPI);  // issuer, compute and epilogue threads
     }
@@ -635,8 +633,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             tma_load_3d(sb + L::V_OFF + rr * L::REGION, &tmv, bar(L::KV_FULL), rr * 64, kv_y, kv_z, pol_kv);
           }
           ++n_kv;
-          // iteration g's Q and dO go to buffer g & 1, once iteration g - 2's last products
-          // that read them (dV for dO, dK for Q) have completed
+          // iteration g's Q and dO go to buffer g & 1, once iteration g - 2's dK, the last
+          // product to read either (after its dV), has completed; Q first, as S^T needs it first
           for (int i = 0, h = it.hk * p.group, m = it.m_lo; i < it.n_iter && ok;
                ++i, ++g, h += (m + 1 == it.m_lo + it.per_head), m = (m + 1 == it.m_lo + it.per_head) ? it.m_lo : m + 1) {
             const int bi = g & 1;  // query head h, Q tile m
@@ -644,25 +642,19 @@ __global__ void __launch_bounds__(THREADS, 1)
             const bool held = p.debug_fault == 3 && w == 0 && i == 1;
             if (held) held_g = g;
             if (g >= 2 &&
-                !(ok = mbar_wait<false>(bar(L::DO_FREE + bi), ((g - 2) >> 1) & 1, abort_flag, &g_status, lim)))
-              break;
-            if (!held) {
-              mbar_expect_tx(bar(L::DO_FULL + bi), L::TILE);
-              for (int rr = 0; rr < L::NREG; ++rr)
-                tma_load_3d(sb + L::DO_OFF + bi * L::TILE + rr * L::REGION, &tmdo, bar(L::DO_FULL + bi),
-                            rr * 64, q_y, q_z, pol_q);
-            }
-            n_do = g + 1;
-            if (g >= 2 &&
-                !(ok = mbar_wait<false>(bar(L::Q_FREE + bi), ((g - 2) >> 1) & 1, abort_flag, &g_status, lim)))
+                !(ok = mbar_wait<false>(bar(L::QD_FREE + bi), ((g - 2) >> 1) & 1, abort_flag, &g_status, lim)))
               break;
             if (!held) {
               mbar_expect_tx(bar(L::Q_FULL + bi), L::TILE);
               for (int rr = 0; rr < L::NREG; ++rr)
                 tma_load_3d(sb + L::Q_OFF + bi * L::TILE + rr * L::REGION, &tmq, bar(L::Q_FULL + bi),
                             rr * 64, q_y, q_z, pol_q);
+              mbar_expect_tx(bar(L::DO_FULL + bi), L::TILE);
+              for (int rr = 0; rr < L::NREG; ++rr)
+                tma_load_3d(sb + L::DO_OFF + bi * L::TILE + rr * L::REGION, &tmdo, bar(L::DO_FULL + bi),
+                            rr * 64, q_y, q_z, pol_q);
             }
-            n_q = g + 1;
+            n_q = n_do = g + 1;
           }
         }
         // nothing may be in flight when the CTA exits: the last load into each buffer (a
@@ -721,7 +713,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (i == 0 && n_it > 0 && !(ok = wait(L::ACC_FREE, n_it - 1))) break;
             tc_fence_after();
             mma_tmem_a<D, BF16>(tmem + C_DV, tmem + C_S, do_mn(bi), hi, i > 0);  // dV += P^T dO
-            umma_commit(bar(L::DO_FREE + bi));
             if (i + 1 < n) {
               if (!(ok = wait(L::Q_FULL + bn, (gi + 1) >> 1))) break;
               tc_fence_after();
@@ -731,7 +722,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!(ok = wait(L::DS_READY, gi))) break;
             tc_fence_after();
             mma_tmem_a<D, BF16>(tmem + C_DK, tmem + C_DP, q_mn(bi), hi, i > 0);  // dK += dS^T Q
-            umma_commit(bar(L::Q_FREE + bi));
+            umma_commit(bar(L::QD_FREE + bi));  // Q and dO of iteration i: dK reads last
             if (i + 1 < n) {
               if (!(ok = wait(L::DO_FULL + bn, (gi + 1) >> 1))) break;
               tc_fence_after();
